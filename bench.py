@@ -1,0 +1,322 @@
+#!/usr/bin/env python3
+"""Benchmark: one Muon step with Gram Newton-Schulz over a batch of 24 bf16 matrices
+1024 x 4096 (dense-MLP projections, alpha = 4), i.e. momentum EMA (mu = 0.95), Frobenius
+normalisation, Gram NS (T = 5, fixed quintic, restart after iteration 2) and the weight
+update (lr = 0.02), all in libgns kernels on one GPU per process.
+
+Prints ONE JSON line (rank 0). `value` is whole-job matrices/s with inputs resident in HBM;
+`e2e` is the same metric with the gradient copied in from pinned host memory and the
+updated weights copied back every step; `roofline` rates the dominant kernel (the
+tcgen05 GEMM) from CUDA events recorded around each of its launches in an instrumented
+repeat of the timed loop; `cpu_baseline` times the fp64 CPU oracle on a bounded sample.
+
+`--impl reference` times the CPU oracle itself (the only reference there is) with the same
+metric and unit, each step one matrix of the workload.
+
+Multi-GPU (torchrun): replicas only — every rank runs the same workload on its own GPU;
+there is no data-path collective. Timing is barrier-bracketed and the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Gram-NS orthogonalized matrices/s and TFLOP/s vs BF16 tensor peak (α=4, T=5)"
+UNIT = "matrices/s"
+COUNT, ROWS, COLS = 24, 1024, 4096
+LR, MU = 0.02, 0.95
+WORKLOAD = "muon_step bf16 24 x 1024x4096 (alpha=4): momentum 0.95, Gram NS T=5 fixed quintic restart@2, lr 0.02"
+
+
+def alg_flops_per_matrix(n=ROWS, m=COLS):
+    """(14 + 6 alpha) n^3: Gram NS with one restart (Dion3 sec. 4.1 + 4.2), symmetric
+    products counted as n^3 (sec. 2.3)."""
+    alpha = m / n
+    return (14 + 6 * alpha) * n ** 3
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d.get("bf16_tflops", 1900.0), d.get("bf16_tflops_sustained", 1700.0), d.get("hbm_gbs", 6800.0), "measured"
+    return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------------------------------
+# clocks during the timed region
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index=0):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        sm_sorted = sorted(sm)
+        return {"sm_mhz": sm_sorted[len(sm_sorted) // 2] if sm_sorted else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------------------
+# CPU oracle timing
+
+def time_oracle(n_matrices, seed=1):
+    import numpy as np
+    from matrix_orthogonalizing_optimizer_gb300 import inputs
+    from oracle import muon as omuon
+    s = 1.0 / np.sqrt(COLS)
+    mats = []
+    for i in range(n_matrices):
+        W = inputs.round_to_bf16_bits(inputs.gaussian(seed, (ROWS, COLS), s, stream=10 * i))
+        G = inputs.round_to_bf16_bits(inputs.gaussian(seed, (ROWS, COLS), s, stream=10 * i + 1))
+        M = inputs.round_to_bf16_bits(inputs.gaussian(seed, (ROWS, COLS), s, stream=10 * i + 2))
+        mats.append((W, G, M))
+    t0 = time.perf_counter()
+    for (W, G, M) in mats:
+        omuon.muon_step(W, G, M, lr=LR, mu=MU)
+    return time.perf_counter() - t0
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    for _ in range(args.warmup):
+        time_oracle(1)
+    total = 0.0
+    for _ in range(args.steps):
+        total += time_oracle(1)
+    v = args.steps / total
+    sample = "1 of the 24 matrices per step (fp64 numpy oracle: momentum, Gram NS restart@2, update)"
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1000.0 * total / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------------------
+# GPU arm
+
+def run_ours(args, rank, world, dist):
+    import ctypes
+
+    import torch
+
+    import matrix_orthogonalizing_optimizer_gb300 as gns
+    from matrix_orthogonalizing_optimizer_gb300 import _lib
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    lib = _lib.load()
+
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1234 + rank)
+    s = 1.0 / COLS ** 0.5
+
+    def randn():
+        return (torch.randn((COUNT, ROWS, COLS), generator=gen, device=dev, dtype=torch.float32) * s).to(torch.bfloat16)
+
+    W = randn()
+    M = torch.zeros((COUNT, ROWS, COLS), dtype=torch.bfloat16, device=dev)
+    G1, G2, G = randn(), randn(), randn()
+    ns = gns.NsParams()
+    ws = gns.alloc_workspace(gns.workspace_size(_lib.GNS_OP_MUON_STEP, M, ns), dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(g):
+        gns.muon_step(W, g, M, lr=LR, momentum=MU, ns=ns, workspace=ws, status=status, stream=stream)
+
+    # the configuration's two earlier synthetic gradient steps, then warm-up on G
+    step(G1)
+    step(G2)
+    for _ in range(args.warmup):
+        step(G)
+    torch.cuda.synchronize()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    def max_over_ranks(x):
+        if dist is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    # ---- timed region: inputs resident in HBM ----
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.2)
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    lib.gns_profile_set(None, 0)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step(G)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    n_gemm, n_all = ctypes.c_int(0), ctypes.c_int(0)
+    lib.gns_profile_query(ctypes.byref(n_gemm), ctypes.byref(n_all))
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps)
+    value = world * COUNT / (ms / 1000.0)
+    tflops = world * COUNT * alg_flops_per_matrix() / (ms / 1000.0) / 1e12
+
+    # ---- instrumented repeat: CUDA events around every GEMM launch (same stream) ----
+    per_step = n_gemm.value // max(args.steps, 1)
+    cap = per_step * args.steps
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * cap)]
+    handles = (ctypes.c_void_p * (2 * cap))(*[ctypes.c_void_p(e.cuda_event) for e in evs])
+    torch.cuda.synchronize()
+    lib.gns_profile_set(handles, cap)
+    for _ in range(args.steps):
+        step(G)
+    torch.cuda.synchronize()
+    lib.gns_profile_set(None, 0)
+    gemm_ms = sum(evs[2 * i].elapsed_time(evs[2 * i + 1]) for i in range(cap)) / args.steps
+    gemm_launch_ms = gemm_ms / max(per_step, 1)
+    flops_per_launch = COUNT * alg_flops_per_matrix() / max(per_step, 1)
+    achieved = flops_per_launch / (gemm_launch_ms / 1000.0) / 1e12
+    peak_burst, peak_sus, _, peak_src = load_peaks()
+
+    # ---- end to end: gradient in from pinned host memory, weights back, every step ----
+    G_host = G.cpu().pin_memory()
+    W_host = torch.empty_like(W, device="cpu").pin_memory()
+    G_dev = torch.empty_like(G)
+    torch.cuda.synchronize()
+    barrier()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(3, min(args.steps, 20))
+    f0.record(stream)
+    for _ in range(e2e_steps):
+        G_dev.copy_(G_host, non_blocking=True)
+        step(G_dev)
+        W_host.copy_(W, non_blocking=True)
+    f1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = max_over_ranks(f0.elapsed_time(f1) / e2e_steps)
+    bytes_step = COUNT * ROWS * COLS * 2
+
+    st = int(status.item())
+    if rank != 0:
+        return 0
+    cpu = None
+    if not args.no_cpu_baseline:
+        n_cpu = 2
+        t = time_oracle(n_cpu)
+        cpu = {"value": n_cpu / t, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"{n_cpu} of the 24 matrices, full Muon step in the fp64 numpy oracle "
+                         f"({t:.1f} s)"}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "matrices": COUNT, "rows": ROWS, "cols": COLS,
+                   "l2": "inputs larger than L2 (W, G, M: 604 MB per rank)", "parallelism": f"replicas x{world}"},
+        "tflops": tflops, "tflops_frac_of_peak": tflops / peak_burst,
+        "e2e": {"value": world * COUNT / (e2e_ms / 1000.0), "unit": UNIT, "h2d_bytes_per_step": bytes_step,
+                "d2h_bytes_per_step": bytes_step},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_burst, "unit": "TFLOP/s",
+                     "frac": achieved / peak_burst, "traffic": None,
+                     "kernel": "gns::tc::gemm_kernel (tcgen05 bf16 GEMM, all 17 launches of a step)",
+                     "peak_kind": f"dense bf16 burst, {peak_src}",
+                     "frac_of_sustained": achieved / peak_sus,
+                     "gemm_ms_per_step": gemm_ms, "gemm_launches_per_step": per_step},
+        "gpu_launches": n_all.value,
+        "device_status": st,
+        "clocks": clk,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        backend = "nccl" if (args.impl == "ours" and torch.cuda.is_available()) else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        tdist.init_process_group(backend=backend)
+        dist = tdist
+    try:
+        if args.impl == "reference":
+            return run_reference(args, rank, world)
+        return run_ours(args, rank, world, dist)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,209 @@
+"""Python API over libgns with the C ABI's names. PyTorch supplies device memory and the
+stream; every step of the computation runs in the library's CUDA kernels.
+
+Tensors are CUDA tensors of dtype bfloat16 (hot path) or float32 (validation path), 2-D
+(one matrix) or 3-D (a batch of same-shape matrices, the megabatch of Dion3 sec. 7), with a
+contiguous last dimension, 16-byte aligned rows (ld a multiple of 16 bytes) and 16-byte
+aligned storage.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+from dataclasses import dataclass
+from typing import Iterable, List, Optional, Sequence
+
+import torch
+
+from . import _lib
+from ._lib import GnsBatch, GnsMuonParams, GnsNsParams, check, load
+
+# Fixed quintic of "Scaling Muon for Diffusion Transformers", appendix D.3.
+QUINTIC_FIXED = ((3.4445, -4.7750, 2.0315),) * 5
+
+
+@dataclass
+class NsParams:
+    """Newton-Schulz schedule (T = len(coeffs)); restarts = iterations after which Gram NS
+    restarts (Dion3 Algorithm 3: after iteration 2)."""
+    coeffs: Sequence = QUINTIC_FIXED
+    restarts: Sequence[int] = (2,)
+    eps: float = 1e-7
+
+    def c_struct(self) -> GnsNsParams:
+        p = GnsNsParams()
+        p.T = len(self.coeffs)
+        if not 1 <= p.T <= _lib.GNS_MAX_T:
+            raise ValueError("T must be in [1, 16]")
+        for t, (a, b, c) in enumerate(self.coeffs):
+            p.a[t], p.b[t], p.c[t] = float(a), float(b), float(c)
+        mask = 0
+        for r in self.restarts:
+            mask |= 1 << int(r)
+        p.restart_mask = mask
+        p.eps = float(self.eps)
+        return p
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return _lib.GNS_BF16
+    if t.dtype == torch.float32:
+        return _lib.GNS_F32
+    raise TypeError(f"unsupported dtype {t.dtype}: bfloat16 or float32")
+
+
+def batch_of(t: torch.Tensor) -> GnsBatch:
+    """gns_batch describing a 2-D or 3-D CUDA tensor (no copy)."""
+    if not t.is_cuda:
+        raise ValueError("tensors must live on a CUDA device")
+    if t.dim() == 2:
+        t3 = t.unsqueeze(0)
+    elif t.dim() == 3:
+        t3 = t
+    else:
+        raise ValueError("tensors must be 2-D or 3-D")
+    if t3.stride(2) != 1:
+        raise ValueError("the last dimension must be contiguous")
+    b = GnsBatch()
+    b.ptr = t3.data_ptr()
+    b.count, b.rows, b.cols = t3.shape
+    # a single row has no row stride of its own: any ld >= cols that keeps rows aligned
+    b.ld = t3.stride(1) if t3.shape[1] > 1 else ((b.cols + 7) // 8) * 8
+    b.stride = t3.stride(0) if t3.shape[0] > 1 else b.rows * b.ld
+    return b
+
+
+def _batches(ts: Iterable[torch.Tensor]):
+    ts = list(ts)
+    arr = (GnsBatch * len(ts))(*[batch_of(t) for t in ts])
+    return arr, ts
+
+
+def _stream_ptr(stream: Optional[torch.cuda.Stream], device) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return s.cuda_stream
+
+
+def _as_list(x) -> List[torch.Tensor]:
+    return [x] if isinstance(x, torch.Tensor) else list(x)
+
+
+def workspace_size(op: int, xs, ns: Optional[NsParams] = None, frac: float = 1.0, dtype=None) -> int:
+    xs = _as_list(xs)
+    arr, _ = _batches(xs)
+    dt = _dtype_code(xs[0]) if dtype is None else dtype
+    nsp = (ns or NsParams()).c_struct()
+    mp = GnsMuonParams(0.0, 0.0, 0.0, 1.0, float(frac))
+    n = load().gns_workspace_size(op, arr, len(xs), dt, ctypes.byref(nsp), ctypes.byref(mp))
+    if n == 0:
+        raise _lib.GnsError(f"workspace_size: {_lib.last_error()}")
+    return int(n)
+
+
+def alloc_workspace(nbytes: int, device) -> torch.Tensor:
+    """A 256-byte aligned device buffer of at least nbytes (torch allocations are)."""
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def _status_ptr(status: Optional[torch.Tensor]) -> Optional[int]:
+    if status is None:
+        return None
+    if status.dtype != torch.int32 or not status.is_cuda:
+        raise ValueError("status must be a CUDA int32 tensor")
+    return status.data_ptr()
+
+
+def _ns_common(fn_name: str, op: int, xs, outs, ns, workspace, status, stream):
+    xs = _as_list(xs)
+    outs = [torch.empty_like(x) for x in xs] if outs is None else _as_list(outs)
+    ns = ns or NsParams()
+    need = workspace_size(op, xs, ns)
+    ws = workspace if workspace is not None else alloc_workspace(need, xs[0].device)
+    xa, _ = _batches(xs)
+    oa, _ = _batches(outs)
+    nsp = ns.c_struct()
+    fn = getattr(load(), fn_name)
+    rc = fn(xa, oa, len(xs), _dtype_code(xs[0]), ctypes.byref(nsp), ws.data_ptr(), ws.numel(),
+            _status_ptr(status), _stream_ptr(stream, xs[0].device))
+    check(rc, fn_name)
+    return outs
+
+
+def gram_ns_batched(xs, outs=None, ns: Optional[NsParams] = None, workspace=None, status=None, stream=None):
+    """Gram Newton-Schulz (Dion3 Algorithm 3) of every matrix in xs (tensor or list of
+    tensors, one per shape group); returns the list of outputs."""
+    return _ns_common("gns_gram_ns_batched", _lib.GNS_OP_GRAM_NS, xs, outs, ns, workspace, status, stream)
+
+
+def ns_standard_batched(xs, outs=None, ns: Optional[NsParams] = None, workspace=None, status=None, stream=None):
+    """Standard Newton-Schulz (Dion3 Algorithm 1 with symmetric products)."""
+    return _ns_common("gns_ns_standard_batched", _lib.GNS_OP_NS_STANDARD, xs, outs, ns, workspace, status, stream)
+
+
+def sym_gemm_xxt(x: torch.Tensor, c: torch.Tensor, alpha: float = 1.0, beta: float = 0.0, status=None, stream=None):
+    xb, cb = batch_of(x), batch_of(c)
+    rc = load().gns_sym_gemm_xxt(ctypes.byref(xb), ctypes.byref(cb), float(alpha), float(beta), _dtype_code(x),
+                                 _status_ptr(status), _stream_ptr(stream, x.device))
+    check(rc, "gns_sym_gemm_xxt")
+    return c
+
+
+def sym_gemm(a: torch.Tensor, b: torch.Tensor, c: Optional[torch.Tensor], d: torch.Tensor, alpha: float = 1.0,
+             beta: float = 0.0, status=None, stream=None):
+    ab, bb, db = batch_of(a), batch_of(b), batch_of(d)
+    cb = batch_of(c) if c is not None else None
+    rc = load().gns_sym_gemm(ctypes.byref(ab), ctypes.byref(bb), ctypes.byref(cb) if cb is not None else None,
+                             ctypes.byref(db), float(alpha), float(beta), _dtype_code(a), _status_ptr(status),
+                             _stream_ptr(stream, a.device))
+    check(rc, "gns_sym_gemm")
+    return d
+
+
+def sym_poly_update(R, Q, Z, RZ, q_scratch, a: float, b: float, c: float, q_is_identity: bool, skip_r: bool,
+                    status=None, stream=None):
+    bs = [batch_of(t) for t in (R, Q, Z, RZ)]
+    qs = batch_of(q_scratch) if q_scratch is not None else None
+    rc = load().gns_sym_poly_update(*[ctypes.byref(x) for x in bs], ctypes.byref(qs) if qs is not None else None,
+                                    float(a), float(b), float(c), int(bool(q_is_identity)), int(bool(skip_r)),
+                                    _dtype_code(R), _status_ptr(status), _stream_ptr(stream, R.device))
+    check(rc, "gns_sym_poly_update")
+
+
+def muon_step(W, G, M, lr: float, momentum: float = 0.95, weight_decay: float = 0.0, scale: float = 1.0,
+              frac: float = 1.0, ns: Optional[NsParams] = None, workspace=None, status=None, stream=None):
+    """One Muon step (frac = 1) or Dion3 fractional update (frac < 1), in place on W and M."""
+    Ws, Gs, Ms = _as_list(W), _as_list(G), _as_list(M)
+    ns = ns or NsParams()
+    need = workspace_size(_lib.GNS_OP_MUON_STEP, Ms, ns, frac=frac)
+    ws = workspace if workspace is not None else alloc_workspace(need, Ms[0].device)
+    wa, _ = _batches(Ws)
+    ga, _ = _batches(Gs)
+    ma, _ = _batches(Ms)
+    nsp = ns.c_struct()
+    mp = GnsMuonParams(float(lr), float(momentum), float(weight_decay), float(scale), float(frac))
+    rc = load().gns_muon_step(wa, ga, ma, len(Ms), ctypes.byref(mp), ctypes.byref(nsp), ws.data_ptr(), ws.numel(),
+                              _status_ptr(status), _stream_ptr(stream, Ms[0].device))
+    check(rc, "gns_muon_step")
+
+
+def frac_row_select(m: torch.Tensor, k: int, idx: Optional[torch.Tensor] = None, gathered=None, workspace=None,
+                    stream=None):
+    """Exact-l1 top-k rows (columns of a tall matrix) of every matrix of m; returns idx."""
+    mb = batch_of(m)
+    count = mb.count
+    if idx is None:
+        idx = torch.empty((count, k), dtype=torch.int32, device=m.device)
+    need = workspace_size(_lib.GNS_OP_FRAC_SELECT, [m])
+    ws = workspace if workspace is not None else alloc_workspace(need, m.device)
+    gb = batch_of(gathered) if gathered is not None else None
+    rc = load().gns_frac_row_select(ctypes.byref(mb), int(k), idx.data_ptr(),
+                                    ctypes.byref(gb) if gb is not None else None, ws.data_ptr(), ws.numel(),
+                                    _stream_ptr(stream, m.device))
+    check(rc, "gns_frac_row_select")
+    return idx
+
+
+def frac_k(frac: float, n: int) -> int:
+    """k = ceil(f n) of Dion3 Algorithm 4, clamped to [1, n]."""
+    return max(1, min(n, int(math.ceil(frac * n - 1e-9))))

@@ -1,0 +1,683 @@
+// HBM-bound kernels of libgns: momentum update with fused Frobenius statistics, norm
+// finalisation, exact l1 selection keys, top-k row selection, row gather / scatter /
+// decay, and small batched copies.
+//
+// Reductions are deterministic: every matrix is split into a fixed number of parts
+// (NPART), each part reduced by one block in a fixed order, and the parts summed in a
+// fixed order. Selection keys are exact integers, so their reduction order cannot matter.
+#include <algorithm>
+
+#include "common.cuh"
+#include "elementwise.h"
+
+namespace gns {
+
+// ---------------------------------------------------------------------------------------
+// block reduction helpers
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Sum over a block of 256 threads in a fixed order (warp shuffles, then warp 0).
+__device__ float block_sum_256(float v) {
+  __shared__ float ws[8];
+  v = warp_sum(v);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) ws[w] = v;
+  __syncthreads();
+  float t = 0.f;
+  if (w == 0) {
+    t = l < 8 ? ws[l] : 0.f;
+    t = warp_sum(t);
+  }
+  return t;  // valid in thread 0
+}
+
+template <typename T>
+__device__ __forceinline__ float to_f(T v);
+template <>
+__device__ __forceinline__ float to_f<float>(float v) {
+  return v;
+}
+template <>
+__device__ __forceinline__ float to_f<bf16>(bf16 v) {
+  return __bfloat162float(v);
+}
+
+// ---------------------------------------------------------------------------------------
+// sum of squares per matrix (read only), partials[b * npart + part]
+
+template <typename T>
+__global__ void sumsq_kernel(const T* X, long long ld, long long stride, int rows, int cols, int npart,
+                             float* partials) {
+  const int b = blockIdx.y, part = blockIdx.x;
+  const int rp = (rows + npart - 1) / npart;
+  const int r0 = part * rp, r1 = min(rows, r0 + rp);
+  const T* Xb = X + (long long)b * stride;
+  float acc = 0.f;
+  for (int r = r0; r < r1; ++r) {
+    const T* row = Xb + (long long)r * ld;
+    for (int c = threadIdx.x; c < cols; c += blockDim.x) {
+      const float v = to_f(row[c]);
+      acc = fmaf(v, v, acc);
+    }
+  }
+  const float s = block_sum_256(acc);
+  if (threadIdx.x == 0) partials[(long long)b * npart + part] = s;
+}
+
+// ---------------------------------------------------------------------------------------
+// momentum: M <- mu * M + G (mode 0; fp32 product, fp32 sum, one bf16 rounding) or
+// M <- M + G (mode 1), with the sum of squares of the stored new M in partials (when set).
+
+__device__ __forceinline__ float mom(float m, float g, float mu, int mode) {
+  return mode == 0 ? __fadd_rn(__fmul_rn(mu, m), g) : __fadd_rn(m, g);
+}
+
+__global__ void momentum_kernel(bf16* M, long long ldm, long long sm, const bf16* G, long long ldg, long long sg,
+                                int rows, int cols, float mu, int mode, int npart, float* partials) {
+  const int b = blockIdx.y, part = blockIdx.x;
+  const int rp = (rows + npart - 1) / npart;
+  const int r0 = part * rp, r1 = min(rows, r0 + rp);
+  bf16* Mb = M + (long long)b * sm;
+  const bf16* Gb = G + (long long)b * sg;
+  float acc = 0.f;
+  const int cvec = cols & ~7;
+  for (int r = r0; r < r1; ++r) {
+    bf16* mr = Mb + (long long)r * ldm;
+    const bf16* gr = Gb + (long long)r * ldg;
+    for (int c = threadIdx.x * 8; c < cvec; c += blockDim.x * 8) {
+      uint4 mv = *reinterpret_cast<const uint4*>(mr + c);
+      const uint4 gv = *reinterpret_cast<const uint4*>(gr + c);
+      bf16* me = reinterpret_cast<bf16*>(&mv);
+      const bf16* ge = reinterpret_cast<const bf16*>(&gv);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const bf16 nv = f_to_bf16(mom(bf16_to_f(me[e]), bf16_to_f(ge[e]), mu, mode));
+        me[e] = nv;
+        const float f = bf16_to_f(nv);
+        acc = fmaf(f, f, acc);
+      }
+      *reinterpret_cast<uint4*>(mr + c) = mv;
+    }
+    for (int c = cvec + threadIdx.x; c < cols; c += blockDim.x) {
+      const bf16 nv = f_to_bf16(mom(bf16_to_f(mr[c]), bf16_to_f(gr[c]), mu, mode));
+      mr[c] = nv;
+      const float f = bf16_to_f(nv);
+      acc = fmaf(f, f, acc);
+    }
+  }
+  if (partials) {
+    const float s = block_sum_256(acc);
+    if (threadIdx.x == 0) partials[(long long)b * npart + part] = s;
+  }
+}
+
+// inv[b] = 1 / (sqrt(sum of partials) + eps), partials summed in order in fp64.
+__global__ void finalize_norm_kernel(const float* partials, int npart, int count, float eps, float* inv) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= count) return;
+  double s = 0.0;
+  for (int p = 0; p < npart; ++p) s += (double)partials[(long long)b * npart + p];
+  inv[b] = (float)(1.0 / (sqrt(s) + (double)eps));
+}
+
+// ---------------------------------------------------------------------------------------
+// exact l1 keys. A finite bf16 value with exponent field E and fraction f has magnitude
+// mant * 2^(e-1) units of 2^-133, mant = (E ? 128 + f : f), e = max(E, 1). The key is the
+// exact sum, kept as KEY_DIGITS base-2^32 digits; a thread accumulates digit sums in
+// 64-bit registers (digit d = (e-1) >> 5 receives mant << ((e-1) & 31)) and carries them
+// into canonical 32-bit digits before adding them into the row's key with integer atomics
+// (order-independent). Rows with an Inf/NaN are flagged in nf.
+
+struct KeyAcc {
+  uint64_t acc[8];
+  uint64_t cur;
+  uint32_t dcur;
+  bool nonfinite;
+  __device__ void init() {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0;
+    cur = 0;
+    dcur = 0;
+    nonfinite = false;
+  }
+  __device__ __forceinline__ void flush() {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (dcur == (uint32_t)i) acc[i] += cur;
+    cur = 0;
+  }
+  __device__ __forceinline__ void add(uint16_t bits) {
+    const uint32_t E = (bits >> 7) & 0xFFu;
+    if (E == 0xFFu) {
+      nonfinite = true;
+      return;
+    }
+    const uint32_t f = bits & 0x7Fu;
+    const uint32_t mant = E ? (f | 0x80u) : f;
+    if (!mant) return;
+    const uint32_t ee = E ? E - 1u : 0u;
+    const uint32_t d = ee >> 5;
+    const uint64_t v = static_cast<uint64_t>(mant) << (ee & 31u);
+    if (d != dcur) {
+      flush();
+      dcur = d;
+    }
+    cur += v;
+  }
+  // canonical digits (each < 2^32) of this thread's partial sum
+  __device__ void digits(uint32_t (&dg)[KEY_DIGITS]) {
+    flush();
+    uint64_t carry = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint64_t t = acc[i] + carry;
+      dg[i] = static_cast<uint32_t>(t);
+      carry = t >> 32;
+    }
+    dg[8] = static_cast<uint32_t>(carry);
+    dg[9] = static_cast<uint32_t>(carry >> 32);
+  }
+};
+
+// Rows of the (non-transposed) matrix: M <- M + G and the key of each row. One warp per
+// row; per-lane digits are summed across the warp (each sum < 2^37) and stored.
+__global__ void frac_add_keys_rows_kernel(bf16* M, long long ldm, long long sm, const bf16* G, long long ldg,
+                                          long long sg, int rows, int cols, int count, unsigned long long* keys,
+                                          int* nf) {
+  const int warps_per_block = blockDim.x >> 5;
+  const long long gw = (long long)blockIdx.x * warps_per_block + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (gw >= (long long)rows * count) return;
+  const int b = (int)(gw / rows), r = (int)(gw % rows);
+  bf16* mr = M + (long long)b * sm + (long long)r * ldm;
+  const bf16* gr = G + (long long)b * sg + (long long)r * ldg;
+  KeyAcc ka;
+  ka.init();
+  const int cvec = cols & ~7;
+  for (int c = lane * 8; c < cvec; c += 32 * 8) {
+    uint4 mv = *reinterpret_cast<const uint4*>(mr + c);
+    const uint4 gv = *reinterpret_cast<const uint4*>(gr + c);
+    bf16* me = reinterpret_cast<bf16*>(&mv);
+    const bf16* ge = reinterpret_cast<const bf16*>(&gv);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      me[e] = f_to_bf16(__fadd_rn(bf16_to_f(me[e]), bf16_to_f(ge[e])));
+      ka.add(__bfloat16_as_ushort(me[e]));
+    }
+    *reinterpret_cast<uint4*>(mr + c) = mv;
+  }
+  for (int c = cvec + lane; c < cols; c += 32) {
+    const bf16 nv = f_to_bf16(__fadd_rn(bf16_to_f(mr[c]), bf16_to_f(gr[c])));
+    mr[c] = nv;
+    ka.add(__bfloat16_as_ushort(nv));
+  }
+  uint32_t dg[KEY_DIGITS];
+  ka.digits(dg);
+  unsigned long long* kr = keys + ((long long)b * rows + r) * KEY_DIGITS;
+  const unsigned any_nf = __any_sync(0xffffffffu, ka.nonfinite);
+#pragma unroll
+  for (int i = 0; i < KEY_DIGITS; ++i) {
+    unsigned long long s = dg[i];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) kr[i] = s;
+  }
+  if (lane == 0) nf[(long long)b * rows + r] = any_nf ? 1 : 0;
+}
+
+// Columns of the matrix (rows of its transpose): M <- M + G elementwise and the key of
+// every column, one thread per column over a chunk of rows, digits added with atomics.
+// keys / nf must be zero on entry.
+__global__ void frac_add_keys_cols_kernel(bf16* M, long long ldm, long long sm, const bf16* G, long long ldg,
+                                          long long sg, int rows, int cols, int rows_per_chunk,
+                                          unsigned long long* keys, int* nf) {
+  const int b = blockIdx.z;
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= cols) return;
+  const int r0 = blockIdx.y * rows_per_chunk, r1 = min(rows, r0 + rows_per_chunk);
+  bf16* Mb = M + (long long)b * sm;
+  const bf16* Gb = G + (long long)b * sg;
+  KeyAcc ka;
+  ka.init();
+  for (int r = r0; r < r1; ++r) {
+    const bf16 nv = f_to_bf16(__fadd_rn(bf16_to_f(Mb[(long long)r * ldm + c]), bf16_to_f(Gb[(long long)r * ldg + c])));
+    Mb[(long long)r * ldm + c] = nv;
+    ka.add(__bfloat16_as_ushort(nv));
+  }
+  uint32_t dg[KEY_DIGITS];
+  ka.digits(dg);
+  unsigned long long* kc = keys + ((long long)b * cols + c) * KEY_DIGITS;
+#pragma unroll
+  for (int i = 0; i < KEY_DIGITS; ++i)
+    if (dg[i]) atomicAdd(kc + i, (unsigned long long)dg[i]);
+  if (ka.nonfinite) atomicOr(nf + (long long)b * cols + c, 1);
+}
+
+// Keys of the rows (trans = 0) or columns (trans = 1) of M, without updating M.
+__global__ void keys_only_kernel(const bf16* M, long long ldm, long long sm, int rows, int cols, int trans,
+                                 int rows_per_chunk, unsigned long long* keys, int* nf) {
+  const int b = blockIdx.z;
+  const bf16* Mb = M + (long long)b * sm;
+  KeyAcc ka;
+  ka.init();
+  int key_index, nkeys;
+  if (!trans) {
+    // one thread per (row, column chunk): columns [c0, c1)
+    const int r = blockIdx.y;
+    const int c0 = (blockIdx.x * blockDim.x + threadIdx.x) * rows_per_chunk;
+    if (c0 >= cols) return;
+    const int c1 = min(cols, c0 + rows_per_chunk);
+    for (int c = c0; c < c1; ++c) ka.add(__bfloat16_as_ushort(Mb[(long long)r * ldm + c]));
+    key_index = r;
+    nkeys = rows;
+  } else {
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= cols) return;
+    const int r0 = blockIdx.y * rows_per_chunk, r1 = min(rows, r0 + rows_per_chunk);
+    for (int r = r0; r < r1; ++r) ka.add(__bfloat16_as_ushort(Mb[(long long)r * ldm + c]));
+    key_index = c;
+    nkeys = cols;
+  }
+  uint32_t dg[KEY_DIGITS];
+  ka.digits(dg);
+  unsigned long long* kk = keys + ((long long)b * nkeys + key_index) * KEY_DIGITS;
+#pragma unroll
+  for (int i = 0; i < KEY_DIGITS; ++i)
+    if (dg[i]) atomicAdd(kk + i, (unsigned long long)dg[i]);
+  if (ka.nonfinite) atomicOr(nf + (long long)b * nkeys + key_index, 1);
+}
+
+// ---------------------------------------------------------------------------------------
+// top-k selection per matrix (one block of 1024 threads each): exact radix select over
+// the KEY_DIGITS*4 bytes of the keys from the most significant byte down; keys equal to
+// the k-th largest go to the lowest indices; the k indices are written ascending.
+
+__device__ int block_exclusive_scan_1024(int v, int* total) {
+  __shared__ int wsum[32];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  __syncthreads();
+  if (lane == 31) wsum[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    int s = wsum[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    wsum[lane] = s;  // inclusive
+  }
+  __syncthreads();
+  const int base = w ? wsum[w - 1] : 0;
+  *total = wsum[31];
+  return base + x - v;
+}
+
+__global__ void __launch_bounds__(1024) select_topk_kernel(unsigned long long* keys, const int* nf, int n, int k,
+                                                           int* idx) {
+  extern __shared__ uint8_t st[];  // n states: 0 candidate, 1 selected, 2 rejected
+  __shared__ unsigned hist[256];
+  __shared__ int sh_T, sh_kleft, sh_cnt;
+  const int b = blockIdx.x;
+  unsigned long long* K = keys + (long long)b * n * KEY_DIGITS;
+  const int* F = nf + (long long)b * n;
+  // canonicalise digits (carry propagation); non-finite rows get the key 2^319
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    unsigned long long* kr = K + (long long)i * KEY_DIGITS;
+    if (F[i]) {
+      for (int d = 0; d < KEY_DIGITS; ++d) kr[d] = 0;
+      kr[KEY_DIGITS - 1] = 0x80000000ull;
+    } else {
+      unsigned long long carry = 0;
+      for (int d = 0; d < KEY_DIGITS; ++d) {
+        const unsigned long long t = kr[d] + carry;
+        kr[d] = t & 0xFFFFFFFFull;
+        carry = t >> 32;
+      }
+    }
+    st[i] = 0;
+  }
+  int kleft = k;
+  __syncthreads();
+  for (int p = KEY_DIGITS * 4 - 1; p >= 0; --p) {
+    for (int h = threadIdx.x; h < 256; h += blockDim.x) hist[h] = 0;
+    __syncthreads();
+    const int dg = p >> 2, sh = (p & 3) * 8;
+    for (int i = threadIdx.x; i < n; i += blockDim.x)
+      if (st[i] == 0) atomicAdd(&hist[(K[(long long)i * KEY_DIGITS + dg] >> sh) & 0xFF], 1u);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int cum = 0, T = 0;
+      for (int bk = 255; bk >= 0; --bk) {
+        if (cum + (int)hist[bk] >= kleft) {
+          T = bk;
+          break;
+        }
+        cum += (int)hist[bk];
+      }
+      sh_T = T;
+      sh_kleft = kleft - cum;
+      sh_cnt = (int)hist[T];
+    }
+    __syncthreads();
+    const unsigned T = (unsigned)sh_T;
+    for (int i = threadIdx.x; i < n; i += blockDim.x)
+      if (st[i] == 0) {
+        const unsigned by = (unsigned)((K[(long long)i * KEY_DIGITS + dg] >> sh) & 0xFF);
+        st[i] = by > T ? 1 : (by < T ? 2 : 0);
+      }
+    kleft = sh_kleft;
+    const int cnt = sh_cnt;
+    __syncthreads();
+    if (cnt == kleft) break;  // every remaining candidate is selected
+  }
+  // remaining candidates hold equal keys: the kleft lowest indices are selected
+  const int seg = (n + blockDim.x - 1) / blockDim.x;
+  const int i0 = min(n, (int)threadIdx.x * seg), i1 = min(n, i0 + seg);
+  int c = 0;
+  for (int i = i0; i < i1; ++i) c += st[i] == 0;
+  int tot;
+  int rank = block_exclusive_scan_1024(c, &tot);
+  for (int i = i0; i < i1; ++i)
+    if (st[i] == 0) {
+      st[i] = rank < kleft ? 1 : 2;
+      ++rank;
+    }
+  __syncthreads();
+  c = 0;
+  for (int i = i0; i < i1; ++i) c += st[i] == 1;
+  int pos = block_exclusive_scan_1024(c, &tot);
+  int* out = idx + (long long)b * k;
+  for (int i = i0; i < i1; ++i)
+    if (st[i] == 1) {
+      if (pos < k) out[pos] = i;
+      ++pos;
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// gathers, decays, copies
+
+// X[b][i][:] = M[b][idx[b*k + i]][:] (rows), with sum-of-squares partials of X.
+__global__ void gather_rows_kernel(const bf16* M, long long ldm, long long sm, const int* idx, int k, int cols,
+                                   bf16* X, long long ldx, long long sx, int npart, float* partials) {
+  const int b = blockIdx.y, part = blockIdx.x;
+  const int rp = (k + npart - 1) / npart;
+  const int i0 = part * rp, i1 = min(k, i0 + rp);
+  float acc = 0.f;
+  for (int i = i0; i < i1; ++i) {
+    const int r = idx[(long long)b * k + i];
+    const bf16* src = M + (long long)b * sm + (long long)r * ldm;
+    bf16* dst = X + (long long)b * sx + (long long)i * ldx;
+    for (int c = threadIdx.x; c < cols; c += blockDim.x) {
+      const bf16 v = src[c];
+      dst[c] = v;
+      const float f = bf16_to_f(v);
+      acc = fmaf(f, f, acc);
+    }
+  }
+  const float s = block_sum_256(acc);
+  if (threadIdx.x == 0) partials[(long long)b * npart + part] = s;
+}
+
+// X[b][i][j] = M[b][j][idx[b*k + i]] (columns of M become rows of X); 32 x 32 tiles.
+__global__ void gather_cols_kernel(const bf16* M, long long ldm, long long sm, const int* idx, int k, int rows,
+                                   bf16* X, long long ldx, long long sx) {
+  __shared__ bf16 tile[32][33];
+  const int b = blockIdx.z;
+  const int i0 = blockIdx.x * 32, j0 = blockIdx.y * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
+  for (int jj = ty; jj < 32; jj += 8) {
+    const int j = j0 + jj, i = i0 + tx;
+    bf16 v = f_to_bf16(0.f);
+    if (j < rows && i < k) v = M[(long long)b * sm + (long long)j * ldm + idx[(long long)b * k + i]];
+    tile[jj][tx] = v;
+  }
+  __syncthreads();
+  for (int ii = ty; ii < 32; ii += 8) {
+    const int i = i0 + ii, j = j0 + tx;
+    if (i < k && j < rows) X[(long long)b * sx + (long long)i * ldx + j] = tile[tx][ii];
+  }
+}
+
+// M[b][idx[i]][:] <- bf16(mu * M) (trans = 0) or M[b][:][idx[i]] (trans = 1).
+__global__ void decay_selected_kernel(bf16* M, long long ldm, long long sm, const int* idx, int k, int len,
+                                      int trans, float mu) {
+  const int b = blockIdx.z;
+  const int i = blockIdx.y;
+  const int sel = idx[(long long)b * k + i];
+  bf16* Mb = M + (long long)b * sm;
+  for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < len; j += gridDim.x * blockDim.x) {
+    bf16* p = trans ? Mb + (long long)j * ldm + sel : Mb + (long long)sel * ldm + j;
+    *p = f_to_bf16(__fmul_rn(mu, bf16_to_f(*p)));
+  }
+}
+
+// Rows (trans = 0) or columns (trans = 1) of W that are NOT in idx get W <- bf16(factor W).
+__global__ void scale_unselected_kernel(bf16* W, long long ldw, long long sw, int rows, int cols, const int* idx,
+                                        int k, int trans, float factor) {
+  const int b = blockIdx.z;
+  const int* sel = idx + (long long)b * k;
+  bf16* Wb = W + (long long)b * sw;
+  const long long total = (long long)rows * cols;
+  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (long long)gridDim.x * blockDim.x) {
+    const int r = (int)(e / cols), c = (int)(e % cols);
+    const int key = trans ? c : r;
+    int lo = 0, hi = k;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (sel[mid] < key) lo = mid + 1; else hi = mid;
+    }
+    if (lo < k && sel[lo] == key) continue;
+    bf16* p = Wb + (long long)r * ldw + c;
+    *p = f_to_bf16(__fmul_rn(factor, bf16_to_f(*p)));
+  }
+}
+
+// W <- beta * W + alpha * Y (same shape), fp32 arithmetic, one rounding.
+template <typename T>
+__global__ void axpby_kernel(T* W, long long ldw, long long sw, const T* Y, long long ldy, long long sy, int rows,
+                             int cols, float alpha, float beta) {
+  const int b = blockIdx.z;
+  const long long total = (long long)rows * cols;
+  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (long long)gridDim.x * blockDim.x) {
+    const int r = (int)(e / cols), c = (int)(e % cols);
+    T* p = W + (long long)b * sw + (long long)r * ldw + c;
+    const float y = to_f(Y[(long long)b * sy + (long long)r * ldy + c]);
+    const float o = fmaf(alpha, y, beta * to_f(*p));
+    if constexpr (sizeof(T) == 2) *p = f_to_bf16(o); else *p = o;
+  }
+}
+
+template <typename T>
+__global__ void copy_kernel(T* D, long long ldd, long long sd, const T* S, long long lds, long long ss, int rows,
+                            int cols) {
+  const int b = blockIdx.z;
+  const long long total = (long long)rows * cols;
+  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (long long)gridDim.x * blockDim.x) {
+    const int r = (int)(e / cols), c = (int)(e % cols);
+    D[(long long)b * sd + (long long)r * ldd + c] = S[(long long)b * ss + (long long)r * lds + c];
+  }
+}
+
+// ---------------------------------------------------------------------------------------
+// launchers
+
+static cudaStream_t S(void* s) { return static_cast<cudaStream_t>(s); }
+
+static int check_launch(const char* what, std::string* err) {
+  profile_count_launch();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    *err = std::string(what) + ": " + cudaGetErrorString(e);
+    return GNS_ERR_CUDA;
+  }
+  return GNS_OK;
+}
+
+static unsigned grid_1d(long long work, int threads) {
+  long long g = (work + threads - 1) / threads;
+  const long long cap = (long long)device_sm_count() * 16;
+  if (g > cap) g = cap;
+  if (g < 1) g = 1;
+  return (unsigned)g;
+}
+
+int launch_sumsq(gns_dtype dt, const MatRef& X, int64_t count, float* partials, void* stream, std::string* err) {
+  dim3 grid(NPART, (unsigned)count);
+  if (dt == GNS_BF16)
+    sumsq_kernel<bf16><<<grid, 256, 0, S(stream)>>>(static_cast<const bf16*>(X.ptr), X.ld, X.stride, (int)X.rows,
+                                                   (int)X.cols, NPART, partials);
+  else
+    sumsq_kernel<float><<<grid, 256, 0, S(stream)>>>(static_cast<const float*>(X.ptr), X.ld, X.stride, (int)X.rows,
+                                                    (int)X.cols, NPART, partials);
+  return check_launch("sumsq", err);
+}
+
+int launch_momentum(const MatRef& M, const MatRef& G, int64_t count, float mu, int mode, float* partials,
+                    void* stream, std::string* err) {
+  dim3 grid(NPART, (unsigned)count);
+  momentum_kernel<<<grid, 256, 0, S(stream)>>>(static_cast<bf16*>(M.ptr), M.ld, M.stride,
+                                               static_cast<const bf16*>(G.ptr), G.ld, G.stride, (int)M.rows,
+                                               (int)M.cols, mu, mode, NPART, partials);
+  return check_launch("momentum", err);
+}
+
+int launch_finalize_norm(const float* partials, int64_t count, float eps, float* inv, void* stream, std::string* err) {
+  finalize_norm_kernel<<<(unsigned)((count + 127) / 128), 128, 0, S(stream)>>>(partials, NPART, (int)count, eps, inv);
+  return check_launch("finalize_norm", err);
+}
+
+int launch_frac_add_keys(const MatRef& M, const MatRef& G, int64_t count, int trans, unsigned long long* keys,
+                         int* nf, void* stream, std::string* err) {
+  if (!trans) {
+    const long long rows_total = M.rows * count;
+    const unsigned blocks = (unsigned)((rows_total + 7) / 8);
+    frac_add_keys_rows_kernel<<<blocks, 256, 0, S(stream)>>>(static_cast<bf16*>(M.ptr), M.ld, M.stride,
+                                                             static_cast<const bf16*>(G.ptr), G.ld, G.stride,
+                                                             (int)M.rows, (int)M.cols, (int)count, keys, nf);
+  } else {
+    cudaMemsetAsync(keys, 0, sizeof(unsigned long long) * KEY_DIGITS * M.cols * count, S(stream));
+    cudaMemsetAsync(nf, 0, sizeof(int) * M.cols * count, S(stream));
+    const int rpc = 256;
+    dim3 grid((unsigned)((M.cols + 255) / 256), (unsigned)((M.rows + rpc - 1) / rpc), (unsigned)count);
+    frac_add_keys_cols_kernel<<<grid, 256, 0, S(stream)>>>(static_cast<bf16*>(M.ptr), M.ld, M.stride,
+                                                           static_cast<const bf16*>(G.ptr), G.ld, G.stride,
+                                                           (int)M.rows, (int)M.cols, rpc, keys, nf);
+  }
+  return check_launch("frac_add_keys", err);
+}
+
+int launch_keys_only(const MatRef& M, int64_t count, int trans, unsigned long long* keys, int* nf, void* stream,
+                     std::string* err) {
+  const int64_t nkeys = trans ? M.cols : M.rows;
+  cudaMemsetAsync(keys, 0, sizeof(unsigned long long) * KEY_DIGITS * nkeys * count, S(stream));
+  cudaMemsetAsync(nf, 0, sizeof(int) * nkeys * count, S(stream));
+  const int chunk = 256;
+  if (!trans) {
+    dim3 grid((unsigned)((M.cols + (long long)chunk * 64 - 1) / ((long long)chunk * 64)), (unsigned)M.rows,
+              (unsigned)count);
+    keys_only_kernel<<<grid, 64, 0, S(stream)>>>(static_cast<const bf16*>(M.ptr), M.ld, M.stride, (int)M.rows,
+                                                 (int)M.cols, 0, chunk, keys, nf);
+  } else {
+    dim3 grid((unsigned)((M.cols + 255) / 256), (unsigned)((M.rows + chunk - 1) / chunk), (unsigned)count);
+    keys_only_kernel<<<grid, 256, 0, S(stream)>>>(static_cast<const bf16*>(M.ptr), M.ld, M.stride, (int)M.rows,
+                                                  (int)M.cols, 1, chunk, keys, nf);
+  }
+  return check_launch("keys", err);
+}
+
+int launch_select_topk(unsigned long long* keys, const int* nf, int64_t n, int64_t k, int64_t count, int* idx,
+                       void* stream, std::string* err) {
+  if (n > MAX_SELECT_N) {
+    *err = "selection dimension exceeds the supported maximum";
+    return GNS_ERR_UNSUPPORTED;
+  }
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(select_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, MAX_SELECT_N);
+    attr = true;
+  }
+  select_topk_kernel<<<(unsigned)count, 1024, (size_t)n, S(stream)>>>(keys, nf, (int)n, (int)k, idx);
+  return check_launch("select_topk", err);
+}
+
+int launch_gather(const MatRef& M, int64_t count, int trans, const int* idx, int64_t k, const MatRef& X,
+                  float* partials, void* stream, std::string* err) {
+  if (!trans) {
+    dim3 grid(NPART, (unsigned)count);
+    gather_rows_kernel<<<grid, 256, 0, S(stream)>>>(static_cast<const bf16*>(M.ptr), M.ld, M.stride, idx, (int)k,
+                                                    (int)M.cols, static_cast<bf16*>(X.ptr), X.ld, X.stride, NPART,
+                                                    partials);
+  } else {
+    dim3 grid((unsigned)((k + 31) / 32), (unsigned)((M.rows + 31) / 32), (unsigned)count);
+    gather_cols_kernel<<<grid, 256, 0, S(stream)>>>(static_cast<const bf16*>(M.ptr), M.ld, M.stride, idx, (int)k,
+                                                    (int)M.rows, static_cast<bf16*>(X.ptr), X.ld, X.stride);
+    if (partials) {
+      MatRef xs = X;
+      xs.rows = k;
+      xs.cols = M.rows;
+      int rc = launch_sumsq(GNS_BF16, xs, count, partials, stream, err);
+      if (rc) return rc;
+    }
+  }
+  return check_launch("gather", err);
+}
+
+int launch_decay_selected(const MatRef& M, int64_t count, int trans, const int* idx, int64_t k, float mu,
+                          void* stream, std::string* err) {
+  const int64_t len = trans ? M.rows : M.cols;
+  dim3 grid((unsigned)std::min<int64_t>((len + 255) / 256, 64), (unsigned)k, (unsigned)count);
+  decay_selected_kernel<<<grid, 256, 0, S(stream)>>>(static_cast<bf16*>(M.ptr), M.ld, M.stride, idx, (int)k, (int)len,
+                                                     trans, mu);
+  return check_launch("decay_selected", err);
+}
+
+int launch_scale_unselected(const MatRef& W, int64_t count, int trans, const int* idx, int64_t k, float factor,
+                            void* stream, std::string* err) {
+  dim3 grid(grid_1d(W.rows * W.cols, 256), 1, (unsigned)count);
+  scale_unselected_kernel<<<grid, 256, 0, S(stream)>>>(static_cast<bf16*>(W.ptr), W.ld, W.stride, (int)W.rows,
+                                                       (int)W.cols, idx, (int)k, trans, factor);
+  return check_launch("scale_unselected", err);
+}
+
+int launch_axpby(gns_dtype dt, const MatRef& W, const MatRef& Y, int64_t count, float alpha, float beta, void* stream,
+                 std::string* err) {
+  dim3 grid(grid_1d(W.rows * W.cols, 256), 1, (unsigned)count);
+  if (dt == GNS_BF16)
+    axpby_kernel<bf16><<<grid, 256, 0, S(stream)>>>(static_cast<bf16*>(W.ptr), W.ld, W.stride,
+                                                   static_cast<const bf16*>(Y.ptr), Y.ld, Y.stride, (int)W.rows,
+                                                   (int)W.cols, alpha, beta);
+  else
+    axpby_kernel<float><<<grid, 256, 0, S(stream)>>>(static_cast<float*>(W.ptr), W.ld, W.stride,
+                                                    static_cast<const float*>(Y.ptr), Y.ld, Y.stride, (int)W.rows,
+                                                    (int)W.cols, alpha, beta);
+  return check_launch("axpby", err);
+}
+
+int launch_copy(gns_dtype dt, const MatRef& D, const MatRef& Sr, int64_t count, void* stream, std::string* err) {
+  dim3 grid(grid_1d(D.rows * D.cols, 256), 1, (unsigned)count);
+  if (dt == GNS_BF16)
+    copy_kernel<bf16><<<grid, 256, 0, S(stream)>>>(static_cast<bf16*>(D.ptr), D.ld, D.stride,
+                                                  static_cast<const bf16*>(Sr.ptr), Sr.ld, Sr.stride, (int)D.rows,
+                                                  (int)D.cols);
+  else
+    copy_kernel<float><<<grid, 256, 0, S(stream)>>>(static_cast<float*>(D.ptr), D.ld, D.stride,
+                                                   static_cast<const float*>(Sr.ptr), Sr.ld, Sr.stride, (int)D.rows,
+                                                   (int)D.cols);
+  return check_launch("copy", err);
+}
+
+}  // namespace gns

@@ -1,0 +1,76 @@
+// Internal interface of the batched GEMM launchers of libgns (not part of the C ABI).
+//
+// Every product in the library has the form
+//     D = alpha' * (A (x) B) + beta' * C          (per matrix b of a batch)
+// with (A (x) B)[i][j] = sum_k A(i,k) B(j,k), i < M, j < N, k < K, where
+//     A(i,k) = a_mn ? A[k][i] : A[i][k]      (physical row-major matrices)
+//     B(j,k) = b_mn ? B[k][j] : B[j][k]
+// so an ordinary product A * Bmat is b_mn = 1 with B = Bmat, and X X^T is A = B = X with
+// a_mn = b_mn = 0. alpha' = alpha * scale[b]^alpha_pow, beta' = beta * scale[b]^beta_pow.
+// C and D are read / written at (i, j) (or at (j, i) when c_trans / d_trans), with the
+// row index i replaced by row_map[b * row_map_stride + i] when row_map is set.
+// sym: M == N and only tiles with tile_row <= tile_col are computed; each off-diagonal tile
+// is also written to its mirrored position (j, i); diagonal tiles are written once.
+// D2 (optional, same layout as D): D + gamma * I on the diagonal entries i == j < diag_limit.
+#pragma once
+
+#include <stdint.h>
+
+#include <string>
+
+#include "../../include/gns.h"
+
+namespace gns {
+
+struct MatRef {
+  void* ptr = nullptr;  // element (0,0) of matrix 0
+  int64_t ld = 0;       // elements between rows
+  int64_t stride = 0;   // elements between matrices
+  int64_t rows = 0;     // physical rows
+  int64_t cols = 0;     // physical cols
+};
+
+struct GemmOp {
+  MatRef A;
+  int a_mn = 0;
+  MatRef B;
+  int b_mn = 0;
+  int64_t M = 0, N = 0, K = 0, batch = 0;
+  int sym = 0;
+  float alpha = 1.f, beta = 0.f, gamma = 0.f;
+  int alpha_pow = 0, beta_pow = 0;
+  const float* scale = nullptr;
+  MatRef C;
+  int c_trans = 0;
+  MatRef D;
+  int d_trans = 0;
+  MatRef D2;
+  int64_t diag_limit = 0;
+  const int32_t* row_map = nullptr;
+  int64_t row_map_stride = 0;
+  int check_finite = 0;
+};
+
+// Enqueues all ops as one launch (ops must be mutually independent). Returns GNS_OK or an
+// error status with *err set.
+int gemm_launch_bf16(const GemmOp* ops, int nops, int32_t* dev_status, void* stream, std::string* err);
+int gemm_launch_f32(const GemmOp* ops, int nops, int32_t* dev_status, void* stream, std::string* err);
+
+// Instrumentation (gns_profile_set): event records around GEMM launches, launch counts.
+void profile_gemm_begin(void* stream);
+void profile_gemm_end(void* stream);
+void profile_count_launch();
+
+inline int gemm_launch(gns_dtype dt, const GemmOp* ops, int nops, int32_t* dev_status, void* stream,
+                       std::string* err) {
+  profile_gemm_begin(stream);
+  const int rc = dt == GNS_BF16 ? gemm_launch_bf16(ops, nops, dev_status, stream, err)
+                                : gemm_launch_f32(ops, nops, dev_status, stream, err);
+  profile_gemm_end(stream);
+  return rc;
+}
+
+// Number of SMs of the current device (cached per device).
+int device_sm_count();
+
+}  // namespace gns

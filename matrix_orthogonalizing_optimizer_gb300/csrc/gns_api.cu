@@ -1,0 +1,830 @@
+// C ABI of libgns (include/gns.h): argument validation, workspace planning and the stage
+// sequences of standard and Gram Newton-Schulz, the Muon step and the Dion3 fractional
+// update, expressed as batched GEMM launches (gemm_tc.cu / gemm_simt.cu) and HBM-bound
+// kernels (elementwise.cu). No host synchronisation and no device allocation happen here.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/gns.h"
+#include "elementwise.h"
+#include "gemm.h"
+
+namespace gns {
+
+static thread_local std::string g_err;
+
+static int fail(int code, const std::string& msg) {
+  g_err = msg;
+  return code;
+}
+
+static int64_t round_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
+
+// ---------------------------------------------------------------------------------------
+// instrumentation (gns_profile_set / gns_profile_query)
+
+struct ProfileState {
+  void** events = nullptr;
+  int capacity = 0;
+  int gemm = 0;
+  int all = 0;
+};
+static thread_local ProfileState g_prof;
+
+void profile_gemm_begin(void* stream) {
+  if (g_prof.events && g_prof.gemm < g_prof.capacity)
+    cudaEventRecord(static_cast<cudaEvent_t>(g_prof.events[2 * g_prof.gemm]), static_cast<cudaStream_t>(stream));
+}
+
+void profile_gemm_end(void* stream) {
+  if (g_prof.events && g_prof.gemm < g_prof.capacity)
+    cudaEventRecord(static_cast<cudaEvent_t>(g_prof.events[2 * g_prof.gemm + 1]), static_cast<cudaStream_t>(stream));
+  ++g_prof.gemm;
+  ++g_prof.all;
+}
+
+void profile_count_launch() { ++g_prof.all; }
+
+constexpr int64_t PAD = 128;  // padding of the n x n workspace matrices (tile size)
+
+// ---------------------------------------------------------------------------------------
+// workspace arena: the same planning code computes sizes (base == nullptr) and pointers
+
+struct Arena {
+  uint8_t* base = nullptr;
+  size_t off = 0;
+  void* take(size_t bytes) {
+    off = (size_t)round_up((int64_t)off, 256);
+    void* p = base ? base + off : nullptr;
+    off += bytes;
+    return p;
+  }
+};
+
+// A workspace batch of `count` matrices with `rows_alloc` allocated rows, of which `rows`
+// are valid: tensor maps and epilogues see `rows`, so the rows beyond read as zero.
+static MatRef ws_mat(Arena& a, int64_t count, int64_t rows_alloc, int64_t rows, int64_t cols, int64_t ld,
+                     size_t es) {
+  MatRef m;
+  m.rows = rows;
+  m.cols = cols;
+  m.ld = ld;
+  m.stride = rows_alloc * ld;
+  m.ptr = a.take((size_t)(count * m.stride) * es);
+  return m;
+}
+
+static MatRef to_ref(const gns_batch& b) {
+  MatRef m;
+  m.ptr = b.ptr;
+  m.ld = b.ld;
+  m.stride = b.count > 1 ? b.stride : b.rows * b.ld;
+  m.rows = b.rows;
+  m.cols = b.cols;
+  return m;
+}
+
+// ---------------------------------------------------------------------------------------
+// validation
+
+static size_t elem_size(gns_dtype dt) { return dt == GNS_BF16 ? 2 : 4; }
+
+static int check_batch(const gns_batch* b, gns_dtype dt, const char* name) {
+  if (!b) return fail(GNS_ERR_INVALID, std::string(name) + ": null batch descriptor");
+  const int64_t al = dt == GNS_BF16 ? 8 : 4;
+  if (!b->ptr) return fail(GNS_ERR_INVALID, std::string(name) + ": null data pointer");
+  if (b->count < 1 || b->rows < 1 || b->cols < 1)
+    return fail(GNS_ERR_INVALID, std::string(name) + ": count, rows and cols must be >= 1");
+  if (b->rows > (1 << 30) || b->cols > (1 << 30) || b->count > (1 << 24))
+    return fail(GNS_ERR_INVALID, std::string(name) + ": dimension too large");
+  if (b->ld < b->cols) return fail(GNS_ERR_INVALID, std::string(name) + ": ld < cols");
+  if (b->ld % al) return fail(GNS_ERR_UNSUPPORTED, std::string(name) + ": ld must be a multiple of 16 bytes");
+  if (reinterpret_cast<uintptr_t>(b->ptr) % 16)
+    return fail(GNS_ERR_UNSUPPORTED, std::string(name) + ": pointer must be 16-byte aligned");
+  if (b->count > 1) {
+    if (b->stride % al) return fail(GNS_ERR_UNSUPPORTED, std::string(name) + ": stride must be a multiple of 16 bytes");
+    if (b->stride < b->rows * b->ld) return fail(GNS_ERR_INVALID, std::string(name) + ": stride < rows * ld");
+  }
+  return GNS_OK;
+}
+
+static int check_ns(const gns_ns_params* ns) {
+  if (!ns) return fail(GNS_ERR_INVALID, "null ns params");
+  if (ns->T < 1 || ns->T > GNS_MAX_T) return fail(GNS_ERR_INVALID, "T must be in [1, 16]");
+  const uint32_t allowed = ns->T >= 2 ? (((1u << ns->T) - 1u) & ~1u) : 0u;
+  if (ns->restart_mask & ~allowed)
+    return fail(GNS_ERR_INVALID, "restart_mask bits must lie in [1, T-1] (restart after iteration i)");
+  if (!(ns->eps >= 0.f) || !std::isfinite(ns->eps)) return fail(GNS_ERR_INVALID, "eps must be finite and >= 0");
+  for (int t = 0; t < ns->T; ++t)
+    if (!std::isfinite(ns->a[t]) || !std::isfinite(ns->b[t]) || !std::isfinite(ns->c[t]))
+      return fail(GNS_ERR_INVALID, "coefficients must be finite");
+  return GNS_OK;
+}
+
+static bool same_shape(const gns_batch& a, const gns_batch& b) {
+  return a.count == b.count && a.rows == b.rows && a.cols == b.cols;
+}
+
+// ---------------------------------------------------------------------------------------
+// the oriented matrix X (n x m, n <= m) that one group orthogonalizes
+
+struct Src {
+  MatRef mat;        // physical storage
+  int trans = 0;     // X = mat^T
+  bool user = true;  // scaled by inv (user data) or already normalised (workspace)
+};
+
+// X as the A operand (or B operand of X X^T): X(i,k)
+static void as_rows(const Src& s, MatRef* m, int* mn) {
+  *m = s.mat;
+  *mn = s.trans;
+}
+// X as the B operand of Q X: B(j,k) = X[k][j]
+static void as_right(const Src& s, MatRef* m, int* mn) {
+  *m = s.mat;
+  *mn = s.trans ? 0 : 1;
+}
+
+// Final write: D = alpha' (Q X) + beta C with C = D (when has_c), optional row map.
+struct Final {
+  MatRef D;
+  int d_trans = 0;
+  float alpha = 1.f;
+  float beta = 0.f;
+  bool has_c = false;
+  const int32_t* row_map = nullptr;
+  int64_t rms = 0;
+  int check_finite = 1;
+};
+
+struct GramBufs {
+  float* partials = nullptr;
+  float* inv = nullptr;
+  MatRef R, Z, RZ, Q[2], X[2];
+  int64_t np = 0;
+};
+
+struct StdBufs {
+  float* partials = nullptr;
+  float* inv = nullptr;
+  MatRef A, Bm, X[2];
+  int64_t np = 0;
+};
+
+static int popcount32(uint32_t v) {
+  int c = 0;
+  while (v) {
+    c += v & 1u;
+    v >>= 1;
+  }
+  return c;
+}
+
+static void plan_gram(Arena& a, int64_t B, int64_t n, int64_t m, gns_dtype dt, const gns_ns_params* ns, GramBufs* g,
+                      bool with_norm) {
+  const size_t es = elem_size(dt);
+  g->np = round_up(n, PAD);
+  const int64_t ldx = round_up(m, 8);
+  if (with_norm) {
+    g->partials = static_cast<float*>(a.take(sizeof(float) * NPART * B));
+    g->inv = static_cast<float*>(a.take(sizeof(float) * B));
+  }
+  g->R = ws_mat(a, B, g->np, g->np, g->np, g->np, es);
+  g->Z = ws_mat(a, B, g->np, g->np, g->np, g->np, es);
+  g->RZ = ws_mat(a, B, g->np, g->np, g->np, g->np, es);
+  g->Q[0] = ws_mat(a, B, g->np, g->np, g->np, g->np, es);
+  g->Q[1] = ws_mat(a, B, g->np, g->np, g->np, g->np, es);
+  const int nr = popcount32(ns->restart_mask);
+  for (int i = 0; i < std::min(nr, 2); ++i) {
+    g->X[i] = ws_mat(a, B, g->np, n, m, ldx, es);
+  }
+}
+
+static void plan_std(Arena& a, int64_t B, int64_t n, int64_t m, gns_dtype dt, StdBufs* s, bool with_norm) {
+  const size_t es = elem_size(dt);
+  s->np = round_up(n, PAD);
+  const int64_t ldx = round_up(m, 8);
+  if (with_norm) {
+    s->partials = static_cast<float*>(a.take(sizeof(float) * NPART * B));
+    s->inv = static_cast<float*>(a.take(sizeof(float) * B));
+  }
+  s->A = ws_mat(a, B, s->np, s->np, s->np, s->np, es);
+  s->Bm = ws_mat(a, B, s->np, s->np, s->np, s->np, es);
+  s->X[0] = ws_mat(a, B, s->np, n, m, ldx, es);
+  s->X[1] = ws_mat(a, B, s->np, n, m, ldx, es);
+}
+
+static GemmOp sym_op(const MatRef& A, int a_mn, const MatRef& Bm, int b_mn, int64_t K, int64_t np, int64_t B,
+                     float alpha, int alpha_pow, const float* scale, const MatRef* C, float beta, const MatRef& D) {
+  GemmOp o;
+  o.A = A;
+  o.a_mn = a_mn;
+  o.B = Bm;
+  o.b_mn = b_mn;
+  o.M = o.N = np;
+  o.K = K;
+  o.batch = B;
+  o.sym = 1;
+  o.alpha = alpha;
+  o.alpha_pow = alpha_pow;
+  o.scale = scale;
+  if (C) {
+    o.C = *C;
+    o.beta = beta;
+  }
+  o.D = D;
+  return o;
+}
+
+// Dion3 Algorithm 3 on one group (B matrices, oriented X = n x m). inv: per-matrix
+// 1/(||X||_F + eps) already computed on the stream.
+static int run_gram(gns_dtype dt, const Src& src, int64_t B, int64_t n, int64_t m, const gns_ns_params* ns,
+                    const GramBufs& g, const float* inv, const Final& fin, int32_t* st, void* stream) {
+  std::string err;
+  const int64_t np = g.np;
+  auto launch = [&](const GemmOp* ops, int nops) -> int {
+    int rc = gemm_launch(dt, ops, nops, st, stream, &err);
+    return rc ? fail(rc, err) : GNS_OK;
+  };
+  int rc;
+  Src X = src;
+  // R_0 = X X^T (scaled by inv^2), Algorithm 3 line 4
+  {
+    MatRef xa;
+    int mn;
+    as_rows(X, &xa, &mn);
+    GemmOp o = sym_op(xa, mn, xa, mn, m, np, B, 1.f, 2, inv, nullptr, 0.f, g.R);
+    if ((rc = launch(&o, 1))) return rc;
+  }
+  bool q_id = true;
+  int qc = 0;
+  int nx = 0;
+  const int T = ns->T;
+  for (int t = 1; t <= T; ++t) {
+    const float a = ns->a[t - 1], b = ns->b[t - 1], c = ns->c[t - 1];
+    if (t > 1 && ((ns->restart_mask >> (t - 1)) & 1u)) {
+      // restart (lines 7-11): X <- Q X; R <- X X^T; Q <- I
+      MatRef xb;
+      int bmn;
+      as_right(X, &xb, &bmn);
+      GemmOp o;
+      o.A = g.Q[qc];
+      o.a_mn = 0;
+      o.B = xb;
+      o.b_mn = bmn;
+      o.M = n;
+      o.N = m;
+      o.K = np;
+      o.batch = B;
+      o.alpha = 1.f;
+      o.alpha_pow = X.user ? 1 : 0;
+      o.scale = inv;
+      MatRef xd = g.X[nx & 1];
+      o.D = xd;
+      if ((rc = launch(&o, 1))) return rc;
+      ++nx;
+      X.mat = xd;
+      X.trans = 0;
+      X.user = false;
+      GemmOp r = sym_op(xd, 0, xd, 0, m, np, B, 1.f, 0, nullptr, nullptr, 0.f, g.R);
+      if ((rc = launch(&r, 1))) return rc;
+      q_id = true;
+    }
+    // line 12: Z = b R + c R^2 (a_t I is never added to Z, appendix B.2.3)
+    GemmOp oz = sym_op(g.R, 0, g.R, 1, np, np, B, c, 0, nullptr, &g.R, b, g.Z);
+    if (q_id) {
+      // line 13 with Q_{t-1} = I: Q_t = Z_t + a_t I, written by the same launch
+      oz.D2 = g.Q[qc];
+      oz.gamma = a;
+      oz.diag_limit = n;
+    }
+    if ((rc = launch(&oz, 1))) return rc;
+    const bool r_needed = t < T && !((ns->restart_mask >> t) & 1u);
+    GemmOp ops[2];
+    int nops = 0;
+    if (!q_id) {
+      // line 13: Q_t = Q_{t-1} Z_t + a_t Q_{t-1}
+      ops[nops++] = sym_op(g.Q[qc], 0, g.Z, 1, np, np, B, 1.f, 0, nullptr, &g.Q[qc], a, g.Q[1 - qc]);
+    }
+    if (r_needed) {
+      // line 14: RZ_t = R_{t-1} Z_t + a_t R_{t-1}
+      ops[nops++] = sym_op(g.R, 0, g.Z, 1, np, np, B, 1.f, 0, nullptr, &g.R, a, g.RZ);
+    }
+    if (nops && (rc = launch(ops, nops))) return rc;
+    if (!q_id) qc = 1 - qc;
+    if (r_needed) {
+      // line 15: R_t = Z_t RZ_t + a_t RZ_t
+      GemmOp orr = sym_op(g.Z, 0, g.RZ, 1, np, np, B, 1.f, 0, nullptr, &g.RZ, a, g.R);
+      if ((rc = launch(&orr, 1))) return rc;
+    }
+    q_id = false;
+  }
+  // line 17: X <- Q_T X, written (or added) to the final destination
+  {
+    MatRef xb;
+    int bmn;
+    as_right(X, &xb, &bmn);
+    GemmOp o;
+    o.A = g.Q[qc];
+    o.a_mn = 0;
+    o.B = xb;
+    o.b_mn = bmn;
+    o.M = n;
+    o.N = m;
+    o.K = np;
+    o.batch = B;
+    o.alpha = fin.alpha;
+    o.alpha_pow = X.user ? 1 : 0;
+    o.scale = inv;
+    o.D = fin.D;
+    o.d_trans = fin.d_trans;
+    if (fin.has_c) {
+      o.C = fin.D;
+      o.c_trans = fin.d_trans;
+      o.beta = fin.beta;
+    }
+    o.row_map = fin.row_map;
+    o.row_map_stride = fin.rms;
+    o.check_finite = fin.check_finite;
+    if ((rc = launch(&o, 1))) return rc;
+  }
+  return GNS_OK;
+}
+
+// Dion3 Algorithm 1 with symmetric products (sec. 2.3). Writes X_T to fin.D (direct mode,
+// fin.has_c must be false) or, when to_ws, leaves it in the returned workspace buffer.
+static int run_std(gns_dtype dt, const Src& src, int64_t B, int64_t n, int64_t m, const gns_ns_params* ns,
+                   const StdBufs& s, const float* inv, const Final* fin, MatRef* result, int32_t* st, void* stream) {
+  std::string err;
+  const int64_t np = s.np;
+  auto launch = [&](const GemmOp* ops, int nops) -> int {
+    int rc = gemm_launch(dt, ops, nops, st, stream, &err);
+    return rc ? fail(rc, err) : GNS_OK;
+  };
+  int rc;
+  Src X = src;
+  for (int t = 1; t <= ns->T; ++t) {
+    const float a = ns->a[t - 1], b = ns->b[t - 1], c = ns->c[t - 1];
+    const int sp = X.user ? 1 : 0;
+    MatRef xa;
+    int amn;
+    as_rows(X, &xa, &amn);
+    // A = X X^T
+    GemmOp oa = sym_op(xa, amn, xa, amn, m, np, B, 1.f, 2 * sp, inv, nullptr, 0.f, s.A);
+    if ((rc = launch(&oa, 1))) return rc;
+    // B = b A + c A^2
+    GemmOp ob = sym_op(s.A, 0, s.A, 1, np, np, B, c, 0, nullptr, &s.A, b, s.Bm);
+    if ((rc = launch(&ob, 1))) return rc;
+    // X <- a X + B X
+    MatRef xb;
+    int bmn;
+    as_right(X, &xb, &bmn);
+    GemmOp ox;
+    ox.A = s.Bm;
+    ox.a_mn = 0;
+    ox.B = xb;
+    ox.b_mn = bmn;
+    ox.K = np;
+    ox.batch = B;
+    ox.alpha = 1.f;
+    ox.alpha_pow = sp;
+    ox.scale = inv;
+    ox.C = X.mat;
+    ox.c_trans = X.trans;
+    ox.beta = a;
+    ox.beta_pow = sp;
+    const bool last = t == ns->T;
+    if (last && fin) {
+      ox.M = n;
+      ox.N = m;
+      ox.D = fin->D;
+      ox.d_trans = fin->d_trans;
+      ox.check_finite = fin->check_finite;
+    } else {
+      ox.M = n;
+      ox.N = m;
+      ox.D = s.X[(t - 1) & 1];
+      ox.check_finite = last;
+    }
+    if ((rc = launch(&ox, 1))) return rc;
+    X.mat = ox.D;
+    X.trans = 0;
+    X.user = false;
+    if (last && result) *result = ox.D;
+  }
+  return GNS_OK;
+}
+
+// ---------------------------------------------------------------------------------------
+// per-op planning shared by sizing and execution
+
+struct GroupShape {
+  int64_t B, rows, cols, n, m;
+  int trans;
+};
+
+static GroupShape shape_of(const gns_batch& x) {
+  GroupShape g;
+  g.B = x.count;
+  g.rows = x.rows;
+  g.cols = x.cols;
+  g.trans = x.rows > x.cols;
+  g.n = std::min(x.rows, x.cols);
+  g.m = std::max(x.rows, x.cols);
+  return g;
+}
+
+static int64_t frac_k(float frac, int64_t n) {
+  int64_t k = (int64_t)std::ceil((double)frac * (double)n - 1e-9);
+  return std::max<int64_t>(1, std::min<int64_t>(k, n));
+}
+
+}  // namespace gns
+
+using namespace gns;
+
+extern "C" {
+
+int gns_version(void) { return GNS_VERSION; }
+
+int gns_profile_set(void** events, int capacity) {
+  if (events && capacity < 0) return fail(GNS_ERR_INVALID, "negative capacity");
+  g_prof.events = events;
+  g_prof.capacity = events ? capacity : 0;
+  g_prof.gemm = 0;
+  g_prof.all = 0;
+  return GNS_OK;
+}
+
+int gns_profile_query(int* gemm_launches, int* all_launches) {
+  if (gemm_launches) *gemm_launches = g_prof.gemm;
+  if (all_launches) *all_launches = g_prof.all;
+  return GNS_OK;
+}
+
+const char* gns_status_string(int s) {
+  switch (s) {
+    case GNS_OK: return "GNS_OK";
+    case GNS_ERR_INVALID: return "GNS_ERR_INVALID";
+    case GNS_ERR_UNSUPPORTED: return "GNS_ERR_UNSUPPORTED";
+    case GNS_ERR_WORKSPACE: return "GNS_ERR_WORKSPACE";
+    case GNS_ERR_CUDA: return "GNS_ERR_CUDA";
+    default: return "GNS_UNKNOWN_STATUS";
+  }
+}
+
+int gns_last_error(char* buf, size_t len) {
+  if (buf && len) {
+    const size_t n = std::min(len - 1, g_err.size());
+    memcpy(buf, g_err.data(), n);
+    buf[n] = 0;
+  }
+  return (int)g_err.size();
+}
+
+void gns_ns_params_default(gns_ns_params* p) {
+  if (!p) return;
+  memset(p, 0, sizeof(*p));
+  p->T = 5;
+  for (int t = 0; t < 5; ++t) {
+    p->a[t] = 3.4445f;
+    p->b[t] = -4.7750f;
+    p->c[t] = 2.0315f;
+  }
+  p->restart_mask = 1u << 2;
+  p->eps = 1e-7f;
+}
+
+static int plan_op(gns_op op, const gns_batch* x, int ngroups, gns_dtype dt, const gns_ns_params* ns,
+                   const gns_muon_params* mp, Arena& a) {
+  if (!x || ngroups < 1) return fail(GNS_ERR_INVALID, "need at least one batch");
+  if (dt != GNS_BF16 && dt != GNS_F32) return fail(GNS_ERR_INVALID, "unknown dtype");
+  if (op != GNS_OP_FRAC_SELECT) {
+    int rc = check_ns(ns);
+    if (rc) return rc;
+  }
+  for (int gi = 0; gi < ngroups; ++gi) {
+    int rc = check_batch(&x[gi], dt, "x");
+    if (rc) return rc;
+    GroupShape s = shape_of(x[gi]);
+    if (op == GNS_OP_GRAM_NS) {
+      if (s.n == s.m) {
+        StdBufs sb;
+        plan_std(a, s.B, s.n, s.m, dt, &sb, true);
+      } else {
+        GramBufs gb;
+        plan_gram(a, s.B, s.n, s.m, dt, ns, &gb, true);
+      }
+    } else if (op == GNS_OP_NS_STANDARD) {
+      StdBufs sb;
+      plan_std(a, s.B, s.n, s.m, dt, &sb, true);
+    } else if (op == GNS_OP_MUON_STEP) {
+      if (!mp) return fail(GNS_ERR_INVALID, "null muon params");
+      if (mp->frac >= 1.f) {
+        if (s.n == s.m) {
+          StdBufs sb;
+          plan_std(a, s.B, s.n, s.m, dt, &sb, true);
+        } else {
+          GramBufs gb;
+          plan_gram(a, s.B, s.n, s.m, dt, ns, &gb, true);
+        }
+      } else {
+        const int64_t k = frac_k(mp->frac, s.n);
+        a.take(sizeof(unsigned long long) * KEY_DIGITS * s.n * s.B);
+        a.take(sizeof(int) * s.n * s.B);
+        a.take(sizeof(int) * k * s.B);
+        a.take(sizeof(uint16_t) * (size_t)(s.B * round_up(k, PAD) * round_up(s.m, 8)));
+        GramBufs gb;
+        plan_gram(a, s.B, k, s.m, dt, ns, &gb, true);
+      }
+    } else if (op == GNS_OP_FRAC_SELECT) {
+      a.take(sizeof(unsigned long long) * KEY_DIGITS * s.n * s.B);
+      a.take(sizeof(int) * s.n * s.B);
+      a.take(sizeof(float) * NPART * s.B);
+    } else {
+      return fail(GNS_ERR_INVALID, "unknown op");
+    }
+  }
+  return GNS_OK;
+}
+
+size_t gns_workspace_size(gns_op op, const gns_batch* x, int ngroups, gns_dtype dtype, const gns_ns_params* ns,
+                          const gns_muon_params* muon) {
+  Arena a;
+  if (plan_op(op, x, ngroups, dtype, ns, muon, a)) return 0;
+  return a.off + 256;
+}
+
+static int check_ws(void* ws, size_t ws_bytes, size_t need) {
+  if (need && !ws) return fail(GNS_ERR_WORKSPACE, "null workspace");
+  if (reinterpret_cast<uintptr_t>(ws) % 256) return fail(GNS_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  if (ws_bytes < need)
+    return fail(GNS_ERR_WORKSPACE, "workspace too small: need " + std::to_string(need) + " bytes");
+  return GNS_OK;
+}
+
+static int ns_common(bool gram, const gns_batch* x, const gns_batch* out, int ngroups, gns_dtype dt,
+                     const gns_ns_params* ns, void* ws, size_t ws_bytes, int32_t* st, void* stream) {
+  if (!out) return fail(GNS_ERR_INVALID, "null out");
+  const gns_op op = gram ? GNS_OP_GRAM_NS : GNS_OP_NS_STANDARD;
+  size_t need = gns_workspace_size(op, x, ngroups, dt, ns, nullptr);
+  if (!need) return GNS_ERR_INVALID;
+  int rc = check_ws(ws, ws_bytes, need);
+  if (rc) return rc;
+  for (int gi = 0; gi < ngroups; ++gi) {
+    if ((rc = check_batch(&out[gi], dt, "out"))) return rc;
+    if (!same_shape(x[gi], out[gi])) return fail(GNS_ERR_INVALID, "out must have the shape of x");
+    if (x[gi].ptr == out[gi].ptr) return fail(GNS_ERR_INVALID, "out may not alias x");
+  }
+  Arena a;
+  a.base = static_cast<uint8_t*>(ws);
+  std::string err;
+  for (int gi = 0; gi < ngroups; ++gi) {
+    GroupShape s = shape_of(x[gi]);
+    Src src;
+    src.mat = to_ref(x[gi]);
+    src.trans = s.trans;
+    Final fin;
+    fin.D = to_ref(out[gi]);
+    fin.d_trans = s.trans;
+    if (gram && s.n != s.m) {
+      GramBufs gb;
+      plan_gram(a, s.B, s.n, s.m, dt, ns, &gb, true);
+      if ((rc = launch_sumsq(dt, src.mat, s.B, gb.partials, stream, &err))) return fail(rc, err);
+      if ((rc = launch_finalize_norm(gb.partials, s.B, ns->eps, gb.inv, stream, &err))) return fail(rc, err);
+      if ((rc = run_gram(dt, src, s.B, s.n, s.m, ns, gb, gb.inv, fin, st, stream))) return rc;
+    } else {
+      StdBufs sb;
+      plan_std(a, s.B, s.n, s.m, dt, &sb, true);
+      if ((rc = launch_sumsq(dt, src.mat, s.B, sb.partials, stream, &err))) return fail(rc, err);
+      if ((rc = launch_finalize_norm(sb.partials, s.B, ns->eps, sb.inv, stream, &err))) return fail(rc, err);
+      if ((rc = run_std(dt, src, s.B, s.n, s.m, ns, sb, sb.inv, &fin, nullptr, st, stream))) return rc;
+    }
+  }
+  return GNS_OK;
+}
+
+int gns_gram_ns_batched(const gns_batch* x, const gns_batch* out, int ngroups, gns_dtype dtype,
+                        const gns_ns_params* ns, void* ws, size_t ws_bytes, int32_t* dev_status, void* stream) {
+  return ns_common(true, x, out, ngroups, dtype, ns, ws, ws_bytes, dev_status, stream);
+}
+
+int gns_ns_standard_batched(const gns_batch* x, const gns_batch* out, int ngroups, gns_dtype dtype,
+                            const gns_ns_params* ns, void* ws, size_t ws_bytes, int32_t* dev_status, void* stream) {
+  return ns_common(false, x, out, ngroups, dtype, ns, ws, ws_bytes, dev_status, stream);
+}
+
+int gns_sym_gemm_xxt(const gns_batch* x, const gns_batch* c, float alpha, float beta, gns_dtype dt,
+                     int32_t* dev_status, void* stream) {
+  int rc;
+  if ((rc = check_batch(x, dt, "x")) || (rc = check_batch(c, dt, "c"))) return rc;
+  if (c->count != x->count || c->rows != x->rows || c->cols != x->rows)
+    return fail(GNS_ERR_INVALID, "c must be count x rows x rows of x");
+  if (x->ptr == c->ptr) return fail(GNS_ERR_INVALID, "c may not alias x");
+  MatRef xm = to_ref(*x), cm = to_ref(*c);
+  GemmOp o = sym_op(xm, 0, xm, 0, x->cols, x->rows, x->count, alpha, 0, nullptr, beta != 0.f ? &cm : nullptr, beta, cm);
+  std::string err;
+  rc = gemm_launch(dt, &o, 1, dev_status, stream, &err);
+  return rc ? fail(rc, err) : GNS_OK;
+}
+
+int gns_sym_gemm(const gns_batch* a, const gns_batch* b, const gns_batch* c, const gns_batch* d, float alpha,
+                 float beta, gns_dtype dt, int32_t* dev_status, void* stream) {
+  int rc;
+  if ((rc = check_batch(a, dt, "a")) || (rc = check_batch(b, dt, "b")) || (rc = check_batch(d, dt, "d"))) return rc;
+  const int64_t n = a->rows;
+  if (a->cols != n || b->rows != n || b->cols != n || d->rows != n || d->cols != n || b->count != a->count ||
+      d->count != a->count)
+    return fail(GNS_ERR_INVALID, "a, b, d must be count x n x n");
+  if (beta != 0.f) {
+    if (!c) return fail(GNS_ERR_INVALID, "c is required when beta != 0");
+    if ((rc = check_batch(c, dt, "c"))) return rc;
+    if (!same_shape(*c, *d)) return fail(GNS_ERR_INVALID, "c must have the shape of d");
+  }
+  if (d->ptr == a->ptr || d->ptr == b->ptr) return fail(GNS_ERR_INVALID, "d may not alias a or b");
+  MatRef am = to_ref(*a), bm = to_ref(*b), dm = to_ref(*d);
+  MatRef cm;
+  if (beta != 0.f) cm = to_ref(*c);
+  GemmOp o = sym_op(am, 0, bm, 1, n, n, a->count, alpha, 0, nullptr, beta != 0.f ? &cm : nullptr, beta, dm);
+  std::string err;
+  rc = gemm_launch(dt, &o, 1, dev_status, stream, &err);
+  return rc ? fail(rc, err) : GNS_OK;
+}
+
+int gns_sym_poly_update(const gns_batch* R, const gns_batch* Q, const gns_batch* Z, const gns_batch* RZ,
+                        const gns_batch* q_scratch, float a, float b, float c, int q_is_identity, int skip_r,
+                        gns_dtype dt, int32_t* dev_status, void* stream) {
+  int rc;
+  if ((rc = check_batch(R, dt, "R")) || (rc = check_batch(Q, dt, "Q")) || (rc = check_batch(Z, dt, "Z")) ||
+      (rc = check_batch(RZ, dt, "RZ")))
+    return rc;
+  const int64_t n = R->rows;
+  if (R->cols != n || !same_shape(*R, *Q) || !same_shape(*R, *Z) || !same_shape(*R, *RZ))
+    return fail(GNS_ERR_INVALID, "R, Q, Z, RZ must be count x n x n");
+  if (!q_is_identity) {
+    if ((rc = check_batch(q_scratch, dt, "q_scratch"))) return rc;
+    if (!same_shape(*R, *q_scratch)) return fail(GNS_ERR_INVALID, "q_scratch must be count x n x n");
+  }
+  const int64_t B = R->count;
+  MatRef r = to_ref(*R), q = to_ref(*Q), z = to_ref(*Z), rz = to_ref(*RZ);
+  std::string err;
+  GemmOp oz = sym_op(r, 0, r, 1, n, n, B, c, 0, nullptr, &r, b, z);
+  if (q_is_identity) {
+    oz.D2 = q;
+    oz.gamma = a;
+    oz.diag_limit = n;
+  }
+  if ((rc = gemm_launch(dt, &oz, 1, dev_status, stream, &err))) return fail(rc, err);
+  GemmOp ops[2];
+  int nops = 0;
+  MatRef qs;
+  if (!q_is_identity) {
+    qs = to_ref(*q_scratch);
+    ops[nops++] = sym_op(q, 0, z, 1, n, n, B, 1.f, 0, nullptr, &q, a, qs);
+  }
+  if (!skip_r) ops[nops++] = sym_op(r, 0, z, 1, n, n, B, 1.f, 0, nullptr, &r, a, rz);
+  if (nops && (rc = gemm_launch(dt, ops, nops, dev_status, stream, &err))) return fail(rc, err);
+  if (!q_is_identity && (rc = launch_copy(dt, q, qs, B, stream, &err))) return fail(rc, err);
+  if (!skip_r) {
+    GemmOp orr = sym_op(z, 0, rz, 1, n, n, B, 1.f, 0, nullptr, &rz, a, r);
+    if ((rc = gemm_launch(dt, &orr, 1, dev_status, stream, &err))) return fail(rc, err);
+  }
+  return GNS_OK;
+}
+
+int gns_muon_step(const gns_batch* W, const gns_batch* G, const gns_batch* M, int ngroups,
+                  const gns_muon_params* mp, const gns_ns_params* ns, void* ws, size_t ws_bytes,
+                  int32_t* dev_status, void* stream) {
+  if (!W || !G || !M || !mp) return fail(GNS_ERR_INVALID, "null argument");
+  if (!(mp->frac > 0.f) || mp->frac > 1.f) return fail(GNS_ERR_INVALID, "frac must be in (0, 1]");
+  if (!std::isfinite(mp->lr) || !std::isfinite(mp->momentum) || !std::isfinite(mp->weight_decay) ||
+      !std::isfinite(mp->scale))
+    return fail(GNS_ERR_INVALID, "muon params must be finite");
+  int rc;
+  for (int gi = 0; gi < ngroups; ++gi) {
+    if ((rc = check_batch(&W[gi], GNS_BF16, "W")) || (rc = check_batch(&G[gi], GNS_BF16, "G")) ||
+        (rc = check_batch(&M[gi], GNS_BF16, "M")))
+      return rc;
+    if (!same_shape(W[gi], G[gi]) || !same_shape(W[gi], M[gi]))
+      return fail(GNS_ERR_INVALID, "W, G, M must have equal shapes");
+    if (W[gi].ptr == G[gi].ptr || W[gi].ptr == M[gi].ptr || G[gi].ptr == M[gi].ptr)
+      return fail(GNS_ERR_INVALID, "W, G, M may not alias");
+  }
+  size_t need = gns_workspace_size(GNS_OP_MUON_STEP, M, ngroups, GNS_BF16, ns, mp);
+  if (!need) return GNS_ERR_INVALID;
+  if ((rc = check_ws(ws, ws_bytes, need))) return rc;
+  Arena a;
+  a.base = static_cast<uint8_t*>(ws);
+  std::string err;
+  const float lr = mp->lr, mu = mp->momentum;
+  const float decay = 1.f - mp->lr * mp->weight_decay;
+  for (int gi = 0; gi < ngroups; ++gi) {
+    GroupShape s = shape_of(M[gi]);
+    MatRef mm = to_ref(M[gi]), gm = to_ref(G[gi]), wm = to_ref(W[gi]);
+    if (mp->frac >= 1.f) {
+      // Muon, eq. (1): M <- mu M + G; W <- (1 - lr wd) W - lr scale polar(M)
+      Src src;
+      src.mat = mm;
+      src.trans = s.trans;
+      if (s.n == s.m) {
+        StdBufs sb;
+        plan_std(a, s.B, s.n, s.m, GNS_BF16, &sb, true);
+        if ((rc = launch_momentum(mm, gm, s.B, mu, 0, sb.partials, stream, &err))) return fail(rc, err);
+        if ((rc = launch_finalize_norm(sb.partials, s.B, ns->eps, sb.inv, stream, &err))) return fail(rc, err);
+        MatRef xt;
+        if ((rc = run_std(GNS_BF16, src, s.B, s.n, s.m, ns, sb, sb.inv, nullptr, &xt, dev_status, stream)))
+          return rc;
+        MatRef xv = xt;
+        xv.rows = s.n;
+        if ((rc = launch_axpby(GNS_BF16, wm, xv, s.B, -lr * mp->scale, decay, stream, &err))) return fail(rc, err);
+      } else {
+        GramBufs gb;
+        plan_gram(a, s.B, s.n, s.m, GNS_BF16, ns, &gb, true);
+        if ((rc = launch_momentum(mm, gm, s.B, mu, 0, gb.partials, stream, &err))) return fail(rc, err);
+        if ((rc = launch_finalize_norm(gb.partials, s.B, ns->eps, gb.inv, stream, &err))) return fail(rc, err);
+        Final fin;
+        fin.D = wm;
+        fin.d_trans = s.trans;
+        fin.alpha = -lr * mp->scale;
+        fin.beta = decay;
+        fin.has_c = true;
+        if ((rc = run_gram(GNS_BF16, src, s.B, s.n, s.m, ns, gb, gb.inv, fin, dev_status, stream))) return rc;
+      }
+    } else {
+      // Dion3 Algorithm 4 (Muon flavour)
+      const int64_t k = frac_k(mp->frac, s.n);
+      auto* keys = static_cast<unsigned long long*>(a.take(sizeof(unsigned long long) * KEY_DIGITS * s.n * s.B));
+      auto* nf = static_cast<int*>(a.take(sizeof(int) * s.n * s.B));
+      auto* idx = static_cast<int*>(a.take(sizeof(int) * k * s.B));
+      MatRef xs;
+      xs.rows = k;
+      xs.cols = s.m;
+      xs.ld = round_up(s.m, 8);
+      xs.stride = round_up(k, PAD) * xs.ld;
+      xs.ptr = a.take(sizeof(uint16_t) * (size_t)(s.B * xs.stride));
+      GramBufs gb;
+      plan_gram(a, s.B, k, s.m, GNS_BF16, ns, &gb, true);
+      // line 2: M <- M + G, with the exact l1 keys of the oriented rows
+      if ((rc = launch_frac_add_keys(mm, gm, s.B, s.trans, keys, nf, stream, &err))) return fail(rc, err);
+      // line 3: selection
+      if ((rc = launch_select_topk(keys, nf, s.n, k, s.B, idx, stream, &err))) return fail(rc, err);
+      // gather M[S, :] and its Frobenius norm
+      if ((rc = launch_gather(mm, s.B, s.trans, idx, k, xs, gb.partials, stream, &err))) return fail(rc, err);
+      if ((rc = launch_finalize_norm(gb.partials, s.B, ns->eps, gb.inv, stream, &err))) return fail(rc, err);
+      // line 8 on the rows that are not updated below
+      if (decay != 1.f && (rc = launch_scale_unselected(wm, s.B, s.trans, idx, k, decay, stream, &err)))
+        return fail(rc, err);
+      // lines 4, 8, 9: O = polar(M[S]); W[S] <- (1 - lr wd) W[S] - lr scale O
+      Src src;
+      src.mat = xs;
+      src.trans = 0;
+      Final fin;
+      fin.D = wm;
+      fin.d_trans = s.trans;
+      fin.alpha = -lr * mp->scale;
+      fin.beta = decay;
+      fin.has_c = true;
+      fin.row_map = idx;
+      fin.rms = k;
+      if ((rc = run_gram(GNS_BF16, src, s.B, k, s.m, ns, gb, gb.inv, fin, dev_status, stream))) return rc;
+      // line 10: error feedback
+      if ((rc = launch_decay_selected(mm, s.B, s.trans, idx, k, mu, stream, &err))) return fail(rc, err);
+    }
+  }
+  return GNS_OK;
+}
+
+int gns_frac_row_select(const gns_batch* m, int k, int32_t* idx, const gns_batch* gathered, void* ws,
+                        size_t ws_bytes, void* stream) {
+  int rc;
+  if ((rc = check_batch(m, GNS_BF16, "m"))) return rc;
+  if (!idx) return fail(GNS_ERR_INVALID, "null idx");
+  GroupShape s = shape_of(*m);
+  if (k < 1 || k > s.n) return fail(GNS_ERR_INVALID, "k must be in [1, min(rows, cols)]");
+  size_t need = gns_workspace_size(GNS_OP_FRAC_SELECT, m, 1, GNS_BF16, nullptr, nullptr);
+  if ((rc = check_ws(ws, ws_bytes, need))) return rc;
+  if (gathered) {
+    if ((rc = check_batch(gathered, GNS_BF16, "gathered"))) return rc;
+    if (gathered->count != s.B || gathered->rows != k || gathered->cols != s.m)
+      return fail(GNS_ERR_INVALID, "gathered must be count x k x max(rows, cols)");
+  }
+  Arena a;
+  a.base = static_cast<uint8_t*>(ws);
+  auto* keys = static_cast<unsigned long long*>(a.take(sizeof(unsigned long long) * KEY_DIGITS * s.n * s.B));
+  auto* nf = static_cast<int*>(a.take(sizeof(int) * s.n * s.B));
+  auto* partials = static_cast<float*>(a.take(sizeof(float) * NPART * s.B));
+  std::string err;
+  MatRef mm = to_ref(*m);
+  if ((rc = launch_keys_only(mm, s.B, s.trans, keys, nf, stream, &err))) return fail(rc, err);
+  if ((rc = launch_select_topk(keys, nf, s.n, k, s.B, idx, stream, &err))) return fail(rc, err);
+  if (gathered && (rc = launch_gather(mm, s.B, s.trans, idx, k, to_ref(*gathered), partials, stream, &err)))
+    return fail(rc, err);
+  return GNS_OK;
+}
+
+}  // extern "C"

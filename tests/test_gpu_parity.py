@@ -1,0 +1,375 @@
+"""GPU parity: every entry point of the C ABI against the CPU fp64 oracle (or, for single
+products, against the product written out in numpy fp64), on seeded inputs.
+
+Tolerances (relative Frobenius error unless stated):
+  * bf16 Gram / standard Newton-Schulz and Muon output: 2e-2;
+  * fp32 validation path: 1e-4;
+  * single bf16 products: 1e-2 (one bf16 rounding of the output, 2^-9 relative, plus fp32
+    accumulation);
+  * momentum, selection and error-feedback decay: bit-exact;
+  * weights after the update: |W_gpu - W_oracle| beyond half a bf16 ulp of the stored
+    weight, in Frobenius norm, at most 2e-2 of the oracle's update lr * scale * O.
+"""
+import numpy as np
+import pytest
+
+from matrix_orthogonalizing_optimizer_gb300 import inputs
+from oracle import muon as omuon
+from oracle import newton_schulz as ons
+from util import bf16_input, bf16_ulp, bits_to_torch, rel_fro, torch_to_bits, torch_to_f64
+
+torch = pytest.importorskip("torch")
+gns = pytest.importorskip("matrix_orthogonalizing_optimizer_gb300")
+
+pytestmark = pytest.mark.gpu
+
+TOL_BF16 = 2e-2
+TOL_F32 = 1e-4
+TOL_PRODUCT = 1e-2
+
+
+def _orth_oracle(X):
+    """Algorithm 3 (or Algorithm 1 for square) on one matrix of any orientation."""
+    return omuon.orthogonalize(X)
+
+
+def _square_oracle(X):
+    return ons.ns_standard(X, ons.QUINTIC_FIXED)
+
+
+def _status():
+    return torch.zeros(1, dtype=torch.int32, device="cuda")
+
+
+# ---------------------------------------------------------------------------------------
+# symmetric products
+
+@pytest.mark.parametrize("count,n,K", [(1, 128, 64), (3, 200, 328), (2, 257, 1000), (1, 8, 24), (2, 384, 512)])
+def test_sym_gemm_xxt_bf16(count, n, K):
+    bits, x = bf16_input(1, (count, n, K), 1.0 / np.sqrt(K))
+    xt = bits_to_torch(bits)
+    c = torch.full((count, n, n), float("nan"), dtype=torch.bfloat16, device="cuda")
+    gns.sym_gemm_xxt(xt, c, alpha=1.5)
+    torch.cuda.synchronize()
+    got = torch_to_f64(c)
+    for b in range(count):
+        assert rel_fro(got[b], 1.5 * x[b] @ x[b].T) < TOL_PRODUCT
+    cb = torch_to_bits(c)
+    assert np.array_equal(cb, np.swapaxes(cb, 1, 2)), "mirrored output must be exactly symmetric"
+
+
+def test_sym_gemm_xxt_beta_bf16():
+    count, n, K = 2, 300, 500
+    bits, x = bf16_input(2, (count, n, K), 1.0 / np.sqrt(K))
+    s_bits, s = bf16_input(3, (count, n, n))
+    s_sym = inputs.round_to_bf16_bits(0.5 * (s + np.swapaxes(s, 1, 2)))
+    c = bits_to_torch(s_sym)
+    c0 = torch_to_f64(c)
+    gns.sym_gemm_xxt(bits_to_torch(bits), c, alpha=0.5, beta=-2.0)
+    torch.cuda.synchronize()
+    got = torch_to_f64(c)
+    for b in range(count):
+        assert rel_fro(got[b], 0.5 * x[b] @ x[b].T - 2.0 * c0[b]) < TOL_PRODUCT
+
+
+@pytest.mark.parametrize("count,n", [(2, 128), (3, 300), (1, 520)])
+def test_sym_gemm_bf16(count, n):
+    # A and B commute (polynomials of one symmetric S), so A B and C are symmetric
+    _, s = bf16_input(4, (count, n, n), 1.0 / np.sqrt(n))
+    S = 0.5 * (s + np.swapaxes(s, 1, 2))
+    A = inputs.bf16_round(S)
+    B = inputs.bf16_round(S @ S + 0.3 * S)
+    C = inputs.bf16_round(S @ S)
+    at, bt, ct = (bits_to_torch(inputs.round_to_bf16_bits(v)) for v in (A, B, C))
+    d = torch.empty_like(at)
+    gns.sym_gemm(at, bt, ct, d, alpha=2.0, beta=0.7)
+    torch.cuda.synchronize()
+    got = torch_to_f64(d)
+    for b in range(count):
+        assert rel_fro(got[b], 2.0 * A[b] @ B[b] + 0.7 * C[b]) < TOL_PRODUCT
+    # in place on C (d aliases c), beta = 0 without c
+    gns.sym_gemm(at, bt, ct, ct, alpha=1.0, beta=1.0)
+    d2 = torch.empty_like(at)
+    gns.sym_gemm(at, bt, None, d2, alpha=1.0, beta=0.0)
+    torch.cuda.synchronize()
+    for b in range(count):
+        assert rel_fro(torch_to_f64(ct)[b], A[b] @ B[b] + C[b]) < TOL_PRODUCT
+        assert rel_fro(torch_to_f64(d2)[b], A[b] @ B[b]) < TOL_PRODUCT
+
+
+@pytest.mark.parametrize("n,K", [(64, 100), (200, 333)])
+def test_sym_gemm_xxt_f32(n, K):
+    x = inputs.gaussian(5, (2, n, K)).astype(np.float32)
+    xt = torch.from_numpy(x).cuda()
+    c = torch.empty((2, n, n), dtype=torch.float32, device="cuda")
+    gns.sym_gemm_xxt(xt, c)
+    torch.cuda.synchronize()
+    got = c.cpu().numpy().astype(np.float64)
+    for b in range(2):
+        assert rel_fro(got[b], x[b].astype(np.float64) @ x[b].T.astype(np.float64)) < 1e-6
+
+
+# ---------------------------------------------------------------------------------------
+# one iteration of Algorithm 3 (lines 12-15)
+
+@pytest.mark.parametrize("q_is_identity,skip_r", [(True, False), (False, False), (False, True)])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_sym_poly_update(q_is_identity, skip_r, dtype):
+    n, count = 200, 2
+    a, b, c = ons.QUINTIC_FIXED[0]
+    X = inputs.gaussian(6, (count, n, 3 * n))
+    X = X / np.linalg.norm(X, axis=(1, 2), keepdims=True)
+    R0 = X @ np.swapaxes(X, 1, 2)
+    Q0 = np.eye(n)[None] + 0.1 * R0
+    if dtype == "bf16":
+        R0, Q0 = inputs.bf16_round(R0), inputs.bf16_round(Q0)
+        mk = lambda v: bits_to_torch(inputs.round_to_bf16_bits(v))
+        tol = TOL_PRODUCT * 2
+    else:
+        mk = lambda v: torch.from_numpy(v.astype(np.float32)).cuda()
+        R0 = R0.astype(np.float32).astype(np.float64)
+        Q0 = Q0.astype(np.float32).astype(np.float64)
+        tol = 1e-5
+    R, Q = mk(R0), mk(Q0)
+    Z, RZ, QS = torch.empty_like(R), torch.empty_like(R), torch.empty_like(R)
+    gns.sym_poly_update(R, Q, Z, RZ, QS, a, b, c, q_is_identity, skip_r)
+    torch.cuda.synchronize()
+    I = np.eye(n)
+    for k in range(count):
+        Zr = b * R0[k] + c * R0[k] @ R0[k]
+        Qr = Zr + a * I if q_is_identity else Q0[k] @ Zr + a * Q0[k]
+        assert rel_fro(torch_to_f64(Z)[k], Zr) < tol
+        assert rel_fro(torch_to_f64(Q)[k], Qr) < tol
+        if not skip_r:
+            RZr = R0[k] @ Zr + a * R0[k]
+            Rr = Zr @ RZr + a * RZr
+            assert rel_fro(torch_to_f64(RZ)[k], RZr) < tol
+            assert rel_fro(torch_to_f64(R)[k], Rr) < tol
+
+
+# ---------------------------------------------------------------------------------------
+# full Newton-Schulz
+
+SHAPES_BF16 = [(4, 128, 512), (3, 200, 800), (2, 512, 300), (2, 1024, 4096), (1, 1, 40), (2, 96, 2000),
+               (3, 136, 136)]
+
+
+@pytest.mark.parametrize("count,rows,cols", SHAPES_BF16)
+def test_gram_ns_bf16(count, rows, cols):
+    bits, x = bf16_input(7, (count, rows, cols))
+    xt = bits_to_torch(bits)
+    st = _status()
+    out = gns.gram_ns_batched(xt, status=st)[0]
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    got = torch_to_f64(out)
+    for b in range(count):
+        want = _square_oracle(x[b]) if rows == cols else _orth_oracle(x[b])
+        assert rel_fro(got[b], want) < TOL_BF16, (b, rel_fro(got[b], want))
+
+
+@pytest.mark.parametrize("count,rows,cols", [(2, 128, 512), (2, 300, 200), (1, 256, 256)])
+def test_ns_standard_bf16(count, rows, cols):
+    bits, x = bf16_input(8, (count, rows, cols))
+    out = gns.ns_standard_batched(bits_to_torch(bits))[0]
+    torch.cuda.synchronize()
+    got = torch_to_f64(out)
+    for b in range(count):
+        X = x[b].T if rows > cols else x[b]
+        want = ons.ns_standard(X, ons.QUINTIC_FIXED)
+        want = want.T if rows > cols else want
+        assert rel_fro(got[b], want) < TOL_BF16
+
+
+def test_c1_fp32_validation_path():
+    """128 x 512 fp32, N(0,1), Gram NS with restart after 2 vs the oracle, and vs standard NS."""
+    x = inputs.gaussian(1, (1, 128, 512)).astype(np.float32)
+    xt = torch.from_numpy(x).cuda()
+    g = gns.gram_ns_batched(xt)[0]
+    s = gns.ns_standard_batched(xt)[0]
+    torch.cuda.synchronize()
+    X = x[0].astype(np.float64)
+    want = ons.gram_ns_stabilized(X, ons.QUINTIC_FIXED, restarts=(2,))
+    assert rel_fro(g.cpu().numpy()[0], want) < TOL_F32
+    assert rel_fro(s.cpu().numpy()[0], ons.ns_standard(X, ons.QUINTIC_FIXED)) < TOL_F32
+
+
+@pytest.mark.parametrize("count,rows,cols", [(2, 100, 260), (1, 300, 129), (2, 64, 64)])
+def test_gram_ns_f32_ragged(count, rows, cols):
+    x = inputs.gaussian(9, (count, rows, cols)).astype(np.float32)
+    out = gns.gram_ns_batched(torch.from_numpy(x).cuda())[0]
+    torch.cuda.synchronize()
+    got = out.cpu().numpy().astype(np.float64)
+    for b in range(count):
+        X = x[b].astype(np.float64)
+        want = _square_oracle(X) if rows == cols else _orth_oracle(X)
+        assert rel_fro(got[b], want) < TOL_F32
+
+
+def test_gram_ns_multiple_groups_and_schedules():
+    b1, x1 = bf16_input(10, (2, 128, 384))
+    b2, x2 = bf16_input(11, (3, 640, 160))
+    outs = gns.gram_ns_batched([bits_to_torch(b1), bits_to_torch(b2)])
+    torch.cuda.synchronize()
+    for got, x in ((outs[0], x1), (outs[1], x2)):
+        g = torch_to_f64(got)
+        for b in range(x.shape[0]):
+            assert rel_fro(g[b], _orth_oracle(x[b])) < TOL_BF16
+    # classic coefficients, 8 iterations, restarts after 2 and 5 (two restarts)
+    C = ons.CLASSIC[:1] * 8
+    ns = gns.NsParams(coeffs=C, restarts=(2, 5))
+    out = gns.gram_ns_batched(bits_to_torch(b1), ns=ns)[0]
+    torch.cuda.synchronize()
+    g = torch_to_f64(out)
+    for b in range(2):
+        assert rel_fro(g[b], ons.gram_ns_stabilized(x1[b], C, restarts=(2, 5))) < TOL_BF16
+    # no restart at all
+    out = gns.gram_ns_batched(bits_to_torch(b1), ns=gns.NsParams(restarts=()))[0]
+    torch.cuda.synchronize()
+    g = torch_to_f64(out)
+    for b in range(2):
+        assert rel_fro(g[b], ons.gram_ns_stabilized(x1[b], ons.QUINTIC_FIXED, restarts=())) < TOL_BF16
+
+
+def test_degenerate_inputs():
+    # zero matrix: eps keeps the result finite and zero
+    z = torch.zeros((2, 128, 256), dtype=torch.bfloat16, device="cuda")
+    st = _status()
+    out = gns.gram_ns_batched(z, status=st)[0]
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and torch.count_nonzero(out).item() == 0
+    # a single row: output = phi(sigma) x / |x|
+    bits, x = bf16_input(12, (1, 1, 4096))
+    out = gns.gram_ns_batched(bits_to_torch(bits))[0]
+    torch.cuda.synchronize()
+    assert rel_fro(torch_to_f64(out)[0], _orth_oracle(x[0])) < TOL_BF16
+    # a non-finite input is reported in the status word
+    bad = bits_to_torch(bits).clone()
+    bad[0, 0, 5] = float("inf")
+    st = _status()
+    gns.gram_ns_batched(bad, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & 1
+
+
+def test_argument_errors():
+    x = torch.zeros((2, 64, 100), dtype=torch.bfloat16, device="cuda")  # ld 100: not 16-byte rows
+    with pytest.raises(Exception, match="16 bytes"):
+        gns.gram_ns_batched(x)
+    y = torch.zeros((2, 64, 128), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(Exception, match="T must be"):
+        gns.gram_ns_batched(y, ns=gns.NsParams(coeffs=[(1.0, 0.0, 0.0)] * 17))
+    with pytest.raises(Exception, match="restart_mask"):
+        gns.gram_ns_batched(y, ns=gns.NsParams(restarts=(5,)))
+    with pytest.raises(Exception, match="workspace"):
+        gns.gram_ns_batched(y, workspace=torch.empty(1024, dtype=torch.uint8, device="cuda"))
+
+
+# ---------------------------------------------------------------------------------------
+# Muon step and Dion3 fractional update
+
+def _w_update_ok(W_gpu, W_or, dW_or, tol=TOL_BF16):
+    half_ulp = 0.5 * bf16_ulp(np.maximum(np.abs(W_or), np.abs(W_gpu)))
+    excess = np.maximum(np.abs(W_gpu - W_or) - half_ulp, 0.0)
+    return np.linalg.norm(excess) <= tol * np.linalg.norm(dW_or), np.linalg.norm(excess) / np.linalg.norm(dW_or)
+
+
+@pytest.mark.parametrize("count,rows,cols", [(3, 256, 1024), (2, 700, 200), (2, 384, 384)])
+def test_muon_step_dense(count, rows, cols):
+    Wb, W = bf16_input(13, (count, rows, cols), 1.0 / np.sqrt(cols))
+    Gb, _ = bf16_input(14, (count, rows, cols), 1.0 / np.sqrt(cols))
+    Mb, _ = bf16_input(15, (count, rows, cols), 1.0 / np.sqrt(cols))
+    Wt, Gt, Mt = bits_to_torch(Wb), bits_to_torch(Gb), bits_to_torch(Mb)
+    gns.muon_step(Wt, Gt, Mt, lr=0.02, momentum=0.95, weight_decay=0.1, scale=1.5)
+    torch.cuda.synchronize()
+    Mg, Wg = torch_to_bits(Mt), torch_to_f64(Wt)
+    for b in range(count):
+        W_or, M_or, O = omuon.muon_step(Wb[b], Gb[b], Mb[b], lr=0.02, mu=0.95, weight_decay=0.1, scale=1.5)
+        if rows == cols:
+            O = _square_oracle(omuon.bf16_decode(M_or))
+            W_or = (1 - 0.02 * 0.1) * W[b] - 0.02 * 1.5 * O
+        assert np.array_equal(Mg[b], M_or), "momentum must match bit for bit"
+        ok, err = _w_update_ok(Wg[b], W_or, 0.02 * 1.5 * O)
+        assert ok, err
+
+
+def _frac_case(seed, count, rows, cols, frac, ties=False):
+    Wb, W = bf16_input(seed, (count, rows, cols), 1.0 / np.sqrt(cols))
+    Gb, _ = bf16_input(seed + 1, (count, rows, cols), 1.0 / np.sqrt(cols))
+    Mb, _ = bf16_input(seed + 2, (count, rows, cols), 1.0 / np.sqrt(cols))
+    if ties:
+        # duplicate rows (or columns) of M + G so that equal keys compete for the last slots
+        if rows <= cols:
+            Mb[:, 5] = Mb[:, 1]; Gb[:, 5] = Gb[:, 1]; Mb[:, 9] = Mb[:, 1]; Gb[:, 9] = Gb[:, 1]
+        else:
+            Mb[:, :, 5] = Mb[:, :, 1]; Gb[:, :, 5] = Gb[:, :, 1]
+    return Wb, Gb, Mb
+
+
+@pytest.mark.parametrize("count,rows,cols,frac", [(2, 256, 1024, 0.25), (2, 300, 900, 0.5), (2, 640, 192, 0.25),
+                                                  (1, 64, 512, 1.0 / 64)])
+def test_frac_step(count, rows, cols, frac):
+    Wb, Gb, Mb = _frac_case(20, count, rows, cols, frac, ties=True)
+    Wt, Gt, Mt = bits_to_torch(Wb), bits_to_torch(Gb), bits_to_torch(Mb)
+    gns.muon_step(Wt, Gt, Mt, lr=0.02, momentum=0.95, frac=frac)
+    torch.cuda.synchronize()
+    Mg, Wg = torch_to_bits(Mt), torch_to_f64(Wt)
+    for b in range(count):
+        W_or, M_or, S, O = omuon.frac_step(Wb[b], Gb[b], Mb[b], frac, lr=0.02, mu=0.95)
+        assert np.array_equal(Mg[b], M_or), "selection and error feedback must match bit for bit"
+        dW = np.zeros_like(W_or)
+        if rows <= cols:
+            dW[S] = 0.02 * O
+        else:
+            dW[:, S] = 0.02 * O.T
+        ok, err = _w_update_ok(Wg[b], W_or, dW)
+        assert ok, err
+
+
+@pytest.mark.parametrize("rows,cols,k", [(256, 1024, 64), (300, 500, 1), (300, 500, 300), (600, 160, 40)])
+def test_frac_row_select_exact(rows, cols, k):
+    count = 3
+    bits, _ = bf16_input(30, (count, rows, cols))
+    # planted ties, subnormals and a non-finite row
+    if rows <= cols:
+        bits[:, 7] = bits[:, 3]
+        bits[:, 11] = bits[:, 3]
+        bits[0, 20, :8] = np.array([1, 2, 3, 0x80, 0x8001, 0x7F7F, 0x0080, 0x0001], dtype=np.uint16)
+        bits[1, 42, 17] = 0x7F80
+    else:
+        bits[:, :, 7] = bits[:, :, 3]
+        bits[1, 17, 42] = 0x7FC0
+    m = bits_to_torch(bits)
+    idx = gns.frac_row_select(m, k)
+    gath = torch.empty((count, k, max(rows, cols)), dtype=torch.bfloat16, device="cuda")
+    idx2 = gns.frac_row_select(m, k, gathered=gath)
+    torch.cuda.synchronize()
+    got = idx.cpu().numpy()
+    assert np.array_equal(got, idx2.cpu().numpy())
+    for b in range(count):
+        X = bits[b] if rows <= cols else np.ascontiguousarray(bits[b].T)
+        S = omuon.top_k_rows(omuon.l1_keys_exact(X), k)
+        assert np.array_equal(got[b], S)
+        assert np.array_equal(torch_to_bits(gath)[b], X[S])
+
+
+# ---------------------------------------------------------------------------------------
+# full-size workload: 24 x 1024 x 4096 Muon step (every matrix checked)
+
+def test_full_size_dense_muon_24x1024x4096():
+    count, rows, cols = 24, 1024, 4096
+    s = 1.0 / np.sqrt(cols)
+    Wb = inputs.round_to_bf16_bits(inputs.gaussian(100, (count, rows, cols), s, stream=0))
+    Gb = inputs.round_to_bf16_bits(inputs.gaussian(100, (count, rows, cols), s, stream=3))
+    Mb = inputs.round_to_bf16_bits(inputs.gaussian(100, (count, rows, cols), s, stream=4))
+    Wt, Gt, Mt = bits_to_torch(Wb), bits_to_torch(Gb), bits_to_torch(Mb)
+    st = _status()
+    gns.muon_step(Wt, Gt, Mt, lr=0.02, momentum=0.95, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    Mg, Wg = torch_to_bits(Mt), torch_to_f64(Wt)
+    for b in range(count):
+        W_or, M_or, O = omuon.muon_step(Wb[b], Gb[b], Mb[b], lr=0.02, mu=0.95)
+        assert np.array_equal(Mg[b], M_or)
+        ok, err = _w_update_ok(Wg[b], W_or, 0.02 * O)
+        assert ok, (b, err)
