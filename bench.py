@@ -224,6 +224,8 @@ def run_ours(args, rank, world, dist):
     per_step = n_gemm.value // max(args.steps, 1)
     cap = per_step * args.steps
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * cap)]
+    for e in evs:  # torch creates the CUDA event on first record
+        e.record(stream)
     handles = (ctypes.c_void_p * (2 * cap))(*[ctypes.c_void_p(e.cuda_event) for e in evs])
     torch.cuda.synchronize()
     lib.gns_profile_set(handles, cap)

@@ -11,6 +11,7 @@ from .api import (  # noqa: F401
     QUINTIC_FIXED,
     alloc_workspace,
     batch_of,
+    empty_padded,
     frac_k,
     frac_row_select,
     gram_ns_batched,
@@ -23,6 +24,6 @@ from .api import (  # noqa: F401
 )
 
 __all__ = [
-    "NsParams", "QUINTIC_FIXED", "alloc_workspace", "batch_of", "frac_k", "frac_row_select", "gram_ns_batched",
+    "NsParams", "QUINTIC_FIXED", "alloc_workspace", "batch_of", "empty_padded", "frac_k", "frac_row_select", "gram_ns_batched",
     "muon_step", "ns_standard_batched", "sym_gemm", "sym_gemm_xxt", "sym_poly_update", "workspace_size",
 ]

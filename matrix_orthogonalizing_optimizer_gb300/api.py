@@ -74,6 +74,15 @@ def batch_of(t: torch.Tensor) -> GnsBatch:
     return b
 
 
+def empty_padded(shape, dtype, device) -> torch.Tensor:
+    """Uninitialised tensor of `shape` whose rows start on 16-byte boundaries (the last
+    dimension is padded in storage, the returned view has the requested shape)."""
+    *lead, cols = shape
+    al = 16 // torch.empty((), dtype=dtype).element_size()
+    ld = (cols + al - 1) // al * al
+    return torch.empty((*lead, ld), dtype=dtype, device=device)[..., :cols]
+
+
 def _batches(ts: Iterable[torch.Tensor]):
     ts = list(ts)
     arr = (GnsBatch * len(ts))(*[batch_of(t) for t in ts])
@@ -116,7 +125,7 @@ def _status_ptr(status: Optional[torch.Tensor]) -> Optional[int]:
 
 def _ns_common(fn_name: str, op: int, xs, outs, ns, workspace, status, stream):
     xs = _as_list(xs)
-    outs = [torch.empty_like(x) for x in xs] if outs is None else _as_list(outs)
+    outs = [empty_padded(x.shape, x.dtype, x.device) for x in xs] if outs is None else _as_list(outs)
     ns = ns or NsParams()
     need = workspace_size(op, xs, ns)
     ws = workspace if workspace is not None else alloc_workspace(need, xs[0].device)
@@ -194,6 +203,8 @@ def frac_row_select(m: torch.Tensor, k: int, idx: Optional[torch.Tensor] = None,
     count = mb.count
     if idx is None:
         idx = torch.empty((count, k), dtype=torch.int32, device=m.device)
+    if idx.dtype != torch.int32 or not idx.is_contiguous() or idx.numel() < count * k:
+        raise ValueError("idx must be a contiguous int32 tensor of count * k entries")
     need = workspace_size(_lib.GNS_OP_FRAC_SELECT, [m])
     ws = workspace if workspace is not None else alloc_workspace(need, m.device)
     gb = batch_of(gathered) if gathered is not None else None

@@ -39,7 +39,8 @@ constexpr int NUM_THREADS = 192;
 constexpr int MAX_PROB = 4;
 constexpr int TMEM_COLS = 256;                       // two 128-column fp32 accumulators
 constexpr int BAR_BYTES = 256;
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 2 * STAGING_BYTES + BAR_BYTES;
+constexpr int DIAG_BYTES = TM * 4;                   // fp32 diagonal of a tile (for D2)
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 2 * STAGING_BYTES + BAR_BYTES + DIAG_BYTES;
 
 struct Problem {
   CUtensorMap tmA;
@@ -144,10 +145,12 @@ __device__ void coop_load(bf16* S, const bf16* G, long long ld, long long sb, in
   }
 }
 
-// Inverse of coop_load; also writes D2 = value + gamma on global diagonal entries
-// (gi == gj < diag_limit) when D2 is set (D2 uses the same row mapping as D).
+// Inverse of coop_load; also writes D2 = D + gamma I when D2 is set (same row mapping as
+// D): off the diagonal D2 takes the stored value, on the global diagonal (gi == gj <
+// diag_limit) it takes dg[u], the fp32 diagonal plus gamma rounded once (appendix B.2.3:
+// adding a_t I to an already rounded Z loses a_t's precision).
 __device__ void coop_store(const bf16* S, bf16* G, long long ld, long long sb, bf16* G2, long long ld2,
-                           long long sb2, float gamma, int diag_limit, int b, int trans, int m0, int n0, int M,
+                           long long sb2, const float* dg, int diag_limit, int b, int trans, int m0, int n0, int M,
                            int N, const int* row_map, long long rms, int et) {
   const int ew = et >> 5, lane = et & 31;
   bf16* Gb = G + (long long)b * sb;
@@ -173,7 +176,7 @@ __device__ void coop_store(const bf16* S, bf16* G, long long ld, long long sb, b
         uint2 q = pk;
         bf16* qv = reinterpret_cast<bf16*>(&q);
         for (int e = 0; e < 4; ++e)
-          if (gi == gj + e && gi < diag_limit) qv[e] = f_to_bf16(bf16_to_f(pv[e]) + gamma);
+          if (gi == gj + e && gi < diag_limit) qv[e] = f_to_bf16(dg[u]);
         if (gj + 3 < N) {
           *reinterpret_cast<uint2*>(G2b + ro2 + gj) = q;
         } else {
@@ -208,6 +211,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
   uint64_t* tfull = bars + 2 * STAGES;
   uint64_t* tempty = tfull + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  float* diag = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES + 2 * STAGING_BYTES + BAR_BYTES);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* epi_flag = abort_flag + 1;
 
@@ -346,6 +350,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
       tc_fence_after();
       const bool inplace = !has_c || (pr.c_trans == pr.d_trans);
       bf16* SD = inplace ? S0 : S1;
+      const bool want_diag = pr.D2 != nullptr && c.tm == c.tn;
+      float dv = 0.f;
       bool bad = false;
 #pragma unroll 1
       for (int ch = 0; ch < TN / 32; ++ch) {
@@ -378,6 +384,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
 #pragma unroll
           for (int j = 0; j < 32; ++j) bad |= !isfinite(o[j]);
         }
+        if (want_diag && (r >> 5) == ch) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j == (r & 31)) dv = o[j];
+        }
         if (!pr.d_trans) {
           uint4* dst = reinterpret_cast<uint4*>(SD + r * SPITCH + ch * 32);
 #pragma unroll
@@ -397,14 +408,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
           for (int j = 0; j < 32; ++j) S1[(ch * 32 + j) * SPITCH + r] = f_to_bf16(o[j]);
         }
       }
+      if (want_diag) diag[r] = dv + pr.gamma;
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
       if (bad) set_status(P.status, GNS_DEVST_NONFINITE);
       named_bar_sync(1, 128);
-      coop_store(SD, pr.D, pr.ldd, pr.sd, pr.D2, pr.ld2, pr.s2, pr.gamma, pr.diag_limit, c.b, pr.d_trans, m0, n0,
+      coop_store(SD, pr.D, pr.ldd, pr.sd, pr.D2, pr.ld2, pr.s2, diag, pr.diag_limit, c.b, pr.d_trans, m0, n0,
                  pr.M, pr.N, pr.row_map, pr.rm_stride, et);
       if (mirror)
-        coop_store(S1, pr.D, pr.ldd, pr.sd, pr.D2, pr.ld2, pr.s2, pr.gamma, pr.diag_limit, c.b, 0, n0, m0, pr.N,
+        coop_store(S1, pr.D, pr.ldd, pr.sd, pr.D2, pr.ld2, pr.s2, diag, pr.diag_limit, c.b, 0, n0, m0, pr.N,
                    pr.M, nullptr, 0, et);
       named_bar_sync(1, 128);
     }

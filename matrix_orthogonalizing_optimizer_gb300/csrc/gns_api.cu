@@ -36,14 +36,19 @@ struct ProfileState {
 };
 static thread_local ProfileState g_prof;
 
+// A failed event record (e.g. an invalid handle) is cleared so it cannot surface as the
+// error of a later launch; instrumentation never fails a computation.
+static void record_event(void* ev, void* stream) {
+  if (cudaEventRecord(static_cast<cudaEvent_t>(ev), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    (void)cudaGetLastError();
+}
+
 void profile_gemm_begin(void* stream) {
-  if (g_prof.events && g_prof.gemm < g_prof.capacity)
-    cudaEventRecord(static_cast<cudaEvent_t>(g_prof.events[2 * g_prof.gemm]), static_cast<cudaStream_t>(stream));
+  if (g_prof.events && g_prof.gemm < g_prof.capacity) record_event(g_prof.events[2 * g_prof.gemm], stream);
 }
 
 void profile_gemm_end(void* stream) {
-  if (g_prof.events && g_prof.gemm < g_prof.capacity)
-    cudaEventRecord(static_cast<cudaEvent_t>(g_prof.events[2 * g_prof.gemm + 1]), static_cast<cudaStream_t>(stream));
+  if (g_prof.events && g_prof.gemm < g_prof.capacity) record_event(g_prof.events[2 * g_prof.gemm + 1], stream);
   ++g_prof.gemm;
   ++g_prof.all;
 }

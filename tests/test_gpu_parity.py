@@ -16,7 +16,7 @@ import pytest
 from matrix_orthogonalizing_optimizer_gb300 import inputs
 from oracle import muon as omuon
 from oracle import newton_schulz as ons
-from util import bf16_input, bf16_ulp, bits_to_torch, rel_fro, torch_to_bits, torch_to_f64
+from util import bf16_input, bf16_ulp, bits_to_torch, empty_like_padded, padded_copy, rel_fro, torch_to_bits, torch_to_f64
 
 torch = pytest.importorskip("torch")
 gns = pytest.importorskip("matrix_orthogonalizing_optimizer_gb300")
@@ -26,6 +26,11 @@ pytestmark = pytest.mark.gpu
 TOL_BF16 = 2e-2
 TOL_F32 = 1e-4
 TOL_PRODUCT = 1e-2
+# Rank-1 input (every singular value at 1 after normalisation): each stored bf16 Z_t =
+# b R + c R^2 (|Z| ~ 2.74 at r = 1) carries a 2^-9 relative rounding that the a_t term
+# cancels down to |h(1)| ~ 0.70, i.e. x3.9, about 0.76% per Q update; five updates bound
+# the error by ~3.8%. Measured: 2.7-2.8%.
+TOL_BF16_RANK1 = 4e-2
 
 
 def _orth_oracle(X):
@@ -48,7 +53,7 @@ def _status():
 def test_sym_gemm_xxt_bf16(count, n, K):
     bits, x = bf16_input(1, (count, n, K), 1.0 / np.sqrt(K))
     xt = bits_to_torch(bits)
-    c = torch.full((count, n, n), float("nan"), dtype=torch.bfloat16, device="cuda")
+    c = empty_like_padded(torch.empty((count, n, n), dtype=torch.bfloat16, device="cuda"), fill=float("nan"))
     gns.sym_gemm_xxt(xt, c, alpha=1.5)
     torch.cuda.synchronize()
     got = torch_to_f64(c)
@@ -81,7 +86,7 @@ def test_sym_gemm_bf16(count, n):
     B = inputs.bf16_round(S @ S + 0.3 * S)
     C = inputs.bf16_round(S @ S)
     at, bt, ct = (bits_to_torch(inputs.round_to_bf16_bits(v)) for v in (A, B, C))
-    d = torch.empty_like(at)
+    d = empty_like_padded(at)
     gns.sym_gemm(at, bt, ct, d, alpha=2.0, beta=0.7)
     torch.cuda.synchronize()
     got = torch_to_f64(d)
@@ -89,7 +94,7 @@ def test_sym_gemm_bf16(count, n):
         assert rel_fro(got[b], 2.0 * A[b] @ B[b] + 0.7 * C[b]) < TOL_PRODUCT
     # in place on C (d aliases c), beta = 0 without c
     gns.sym_gemm(at, bt, ct, ct, alpha=1.0, beta=1.0)
-    d2 = torch.empty_like(at)
+    d2 = empty_like_padded(at)
     gns.sym_gemm(at, bt, None, d2, alpha=1.0, beta=0.0)
     torch.cuda.synchronize()
     for b in range(count):
@@ -100,8 +105,8 @@ def test_sym_gemm_bf16(count, n):
 @pytest.mark.parametrize("n,K", [(64, 100), (200, 333)])
 def test_sym_gemm_xxt_f32(n, K):
     x = inputs.gaussian(5, (2, n, K)).astype(np.float32)
-    xt = torch.from_numpy(x).cuda()
-    c = torch.empty((2, n, n), dtype=torch.float32, device="cuda")
+    xt = padded_copy(torch.from_numpy(x).cuda())
+    c = empty_like_padded(torch.empty((2, n, n), dtype=torch.float32, device="cuda"))
     gns.sym_gemm_xxt(xt, c)
     torch.cuda.synchronize()
     got = c.cpu().numpy().astype(np.float64)
@@ -126,12 +131,12 @@ def test_sym_poly_update(q_is_identity, skip_r, dtype):
         mk = lambda v: bits_to_torch(inputs.round_to_bf16_bits(v))
         tol = TOL_PRODUCT * 2
     else:
-        mk = lambda v: torch.from_numpy(v.astype(np.float32)).cuda()
+        mk = lambda v: padded_copy(torch.from_numpy(v.astype(np.float32)).cuda())
         R0 = R0.astype(np.float32).astype(np.float64)
         Q0 = Q0.astype(np.float32).astype(np.float64)
         tol = 1e-5
     R, Q = mk(R0), mk(Q0)
-    Z, RZ, QS = torch.empty_like(R), torch.empty_like(R), torch.empty_like(R)
+    Z, RZ, QS = empty_like_padded(R), empty_like_padded(R), empty_like_padded(R)
     gns.sym_poly_update(R, Q, Z, RZ, QS, a, b, c, q_is_identity, skip_r)
     torch.cuda.synchronize()
     I = np.eye(n)
@@ -163,9 +168,10 @@ def test_gram_ns_bf16(count, rows, cols):
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     got = torch_to_f64(out)
+    tol = TOL_BF16_RANK1 if min(rows, cols) == 1 else TOL_BF16
     for b in range(count):
         want = _square_oracle(x[b]) if rows == cols else _orth_oracle(x[b])
-        assert rel_fro(got[b], want) < TOL_BF16, (b, rel_fro(got[b], want))
+        assert rel_fro(got[b], want) < tol, (b, rel_fro(got[b], want))
 
 
 @pytest.mark.parametrize("count,rows,cols", [(2, 128, 512), (2, 300, 200), (1, 256, 256)])
@@ -197,7 +203,7 @@ def test_c1_fp32_validation_path():
 @pytest.mark.parametrize("count,rows,cols", [(2, 100, 260), (1, 300, 129), (2, 64, 64)])
 def test_gram_ns_f32_ragged(count, rows, cols):
     x = inputs.gaussian(9, (count, rows, cols)).astype(np.float32)
-    out = gns.gram_ns_batched(torch.from_numpy(x).cuda())[0]
+    out = gns.gram_ns_batched(padded_copy(torch.from_numpy(x).cuda()))[0]
     torch.cuda.synchronize()
     got = out.cpu().numpy().astype(np.float64)
     for b in range(count):
@@ -242,7 +248,7 @@ def test_degenerate_inputs():
     bits, x = bf16_input(12, (1, 1, 4096))
     out = gns.gram_ns_batched(bits_to_torch(bits))[0]
     torch.cuda.synchronize()
-    assert rel_fro(torch_to_f64(out)[0], _orth_oracle(x[0])) < TOL_BF16
+    assert rel_fro(torch_to_f64(out)[0], _orth_oracle(x[0])) < TOL_BF16_RANK1
     # a non-finite input is reported in the status word
     bad = bits_to_torch(bits).clone()
     bad[0, 0, 5] = float("inf")
@@ -341,7 +347,7 @@ def test_frac_row_select_exact(rows, cols, k):
         bits[1, 17, 42] = 0x7FC0
     m = bits_to_torch(bits)
     idx = gns.frac_row_select(m, k)
-    gath = torch.empty((count, k, max(rows, cols)), dtype=torch.bfloat16, device="cuda")
+    gath = empty_like_padded(torch.empty((count, k, max(rows, cols)), dtype=torch.bfloat16, device="cuda"))
     idx2 = gns.frac_row_select(m, k, gathered=gath)
     torch.cuda.synchronize()
     got = idx.cpu().numpy()

@@ -11,8 +11,35 @@ def rel_fro(a, b):
 
 
 def bits_to_torch(bits, device="cuda"):
+    """bf16 tensor of the given bits; rows padded in storage to 16 bytes when needed."""
     import torch
-    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+    return padded_copy(t)
+
+
+def padded_copy(t):
+    """Copy of t whose rows start on 16-byte boundaries (storage padded, view unpadded)."""
+    import torch
+    cols = t.shape[-1]
+    al = 16 // t.element_size()
+    if cols % al == 0:
+        return t
+    ld = (cols + al - 1) // al * al
+    buf = torch.zeros((*t.shape[:-1], ld), dtype=t.dtype, device=t.device)
+    v = buf[..., :cols]
+    v.copy_(t)
+    return v
+
+
+def empty_like_padded(t, fill=None):
+    import torch
+    cols = t.shape[-1]
+    al = 16 // t.element_size()
+    ld = (cols + al - 1) // al * al
+    buf = torch.empty((*t.shape[:-1], ld), dtype=t.dtype, device=t.device)
+    if fill is not None:
+        buf.fill_(fill)
+    return buf[..., :cols]
 
 
 def torch_to_bits(t):
