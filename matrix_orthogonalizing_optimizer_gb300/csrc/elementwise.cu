@@ -486,6 +486,30 @@ __global__ void scale_unselected_kernel(bf16* W, long long ldw, long long sw, in
   }
 }
 
+// Selected rows of W (or columns, trans = 1) take beta * W + alpha * O:
+// W[idx[i]][j] (trans: W[j][idx[i]]) for O[i][j], i < k, j < len; fp32 arithmetic, one
+// rounding (the weight update of Dion3 sec. 6 on the selected rows only).
+__global__ void scatter_update_kernel(bf16* W, long long ldw, long long sw, const bf16* O, long long ldo,
+                                      long long so, const int* idx, int k, int len, int trans, float alpha,
+                                      float beta) {
+  const int b = blockIdx.z;
+  const long long total = (long long)k * len;
+  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (long long)gridDim.x * blockDim.x) {
+    int i, j;
+    if (!trans) {
+      i = (int)(e / len);
+      j = (int)(e % len);
+    } else {
+      j = (int)(e / k);
+      i = (int)(e % k);
+    }
+    const int sel = idx[(long long)b * k + i];
+    bf16* p = W + (long long)b * sw + (trans ? (long long)j * ldw + sel : (long long)sel * ldw + j);
+    const float o = bf16_to_f(O[(long long)b * so + (long long)i * ldo + j]);
+    *p = f_to_bf16(fmaf(alpha, o, beta * bf16_to_f(*p)));
+  }
+}
+
 // W <- beta * W + alpha * Y (same shape), fp32 arithmetic, one rounding.
 template <typename T>
 __global__ void axpby_kernel(T* W, long long ldw, long long sw, const T* Y, long long ldy, long long sy, int rows,
@@ -651,6 +675,16 @@ int launch_scale_unselected(const MatRef& W, int64_t count, int trans, const int
   scale_unselected_kernel<<<grid, 256, 0, S(stream)>>>(static_cast<bf16*>(W.ptr), W.ld, W.stride, (int)W.rows,
                                                        (int)W.cols, idx, (int)k, trans, factor);
   return check_launch("scale_unselected", err);
+}
+
+int launch_scatter_update(const MatRef& W, const MatRef& O, int64_t count, int trans, const int* idx, int64_t k,
+                          float alpha, float beta, void* stream, std::string* err) {
+  const int64_t len = O.cols;
+  dim3 grid(grid_1d(k * len, 256), 1, (unsigned)count);
+  scatter_update_kernel<<<grid, 256, 0, S(stream)>>>(static_cast<bf16*>(W.ptr), W.ld, W.stride,
+                                                     static_cast<const bf16*>(O.ptr), O.ld, O.stride, idx, (int)k,
+                                                     (int)len, trans, alpha, beta);
+  return check_launch("scatter_update", err);
 }
 
 int launch_axpby(gns_dtype dt, const MatRef& W, const MatRef& Y, int64_t count, float alpha, float beta, void* stream,

@@ -29,6 +29,8 @@ int launch_decay_selected(const MatRef& M, int64_t count, int trans, const int* 
                           void* stream, std::string* err);
 int launch_scale_unselected(const MatRef& W, int64_t count, int trans, const int* idx, int64_t k, float factor,
                             void* stream, std::string* err);
+int launch_scatter_update(const MatRef& W, const MatRef& O, int64_t count, int trans, const int* idx, int64_t k,
+                          float alpha, float beta, void* stream, std::string* err);
 int launch_axpby(gns_dtype dt, const MatRef& W, const MatRef& Y, int64_t count, float alpha, float beta, void* stream,
                  std::string* err);
 int launch_copy(gns_dtype dt, const MatRef& D, const MatRef& S, int64_t count, void* stream, std::string* err);

@@ -1,24 +1,27 @@
 // Batched bf16 GEMM on the 5th-generation tensor cores (tcgen05 + TMEM + TMA), sm_103a.
 //
-// One persistent CTA per SM walks a list of 128 x 128 output tiles (all tiles of a
-// rectangular product, or the upper-triangle tiles of a symmetric one: Dion3 sec. 5
-// "Triangular Scheduler"). Warp roles:
-//   warp 0    TMA producer: 64-wide K slices of A and B into a 4-stage shared-memory ring
-//             (128-byte swizzle; K-major operands as one 128x64 box, MN-major ones as two
-//             64x64 boxes), completion on per-stage mbarriers.
-//   warp 1    TMEM allocator and MMA issuer: one thread issues tcgen05.mma (M=128, N=128,
-//             K=16, bf16 in, fp32 accumulate) into one of two TMEM accumulators, so the
-//             epilogue of tile i overlaps the main loop of tile i+1 (Dion3 appendix C.1).
-//   warps 2-5 epilogue: tcgen05.ld of the accumulator (thread = tile row), alpha/beta
-//             combination with the C tile staged in shared memory, store through shared
-//             staging with coalesced global writes; symmetric tiles are also written
-//             transposed to the mirrored position, diagonal tiles once (Dion3 sec. 5
-//             "Writing to the Transposed Tile", appendix C.1).
+// A cluster of two CTAs (a CTA pair on neighbouring SMs) computes one 256 x 256 output
+// tile with 2-CTA MMAs (tcgen05.mma.cta_group::2, M = 256, N = 256, K = 16): each CTA
+// stages its 128 rows of A and its 128 columns of B, and holds its 128 x 256 half of the
+// fp32 accumulator in its own tensor memory (Dion3 appendix C.1: 256 x 256 cluster tiles,
+// 2-CTA collaboration, two accumulators so the epilogue overlaps the next main loop).
+// Persistent pairs walk a list of tiles: every tile of a rectangular product, or the
+// upper-triangle tiles of a symmetric one (Dion3 sec. 5, "Triangular Scheduler").
+//
+// Warp roles in each CTA:
+//   warp 0    TMA producer: 64-wide K slices into a 4-stage ring (128-byte swizzle; a
+//             K-major operand is one 128 x 64 box, an MN-major one two 64 x 64 boxes);
+//             completion is signalled on the leader CTA's stage barrier.
+//   warp 1    TMEM allocation (both CTAs) and, in the leader CTA, the MMA issuer.
+//   warps 2-5 epilogue: tcgen05.ld of the accumulator (thread = row), alpha/beta with the
+//             C tile (TMA-loaded), result staged in 128-byte-swizzled shared memory and
+//             written with TMA stores in 64-column chunks; off-diagonal tiles of symmetric
+//             products are also stored transposed at the mirrored position, diagonal tiles
+//             once (Dion3 sec. 5 "Writing to the Transposed Tile", appendix C.1).
 #include <cudaTypedefs.h>
 
 #include <algorithm>
 #include <mutex>
-#include <vector>
 
 #include "common.cuh"
 #include "gemm.h"
@@ -27,43 +30,42 @@ namespace gns {
 
 namespace tc {
 
-constexpr int TM = 128;
-constexpr int TN = 128;
-constexpr int TK = 64;
+constexpr int TM = 128;                          // accumulator rows per CTA (256 per pair)
+constexpr int TN = 256;                          // tile columns
+constexpr int BN = 128;                          // B columns staged per CTA
+constexpr int TK = 64;                           // K slice per stage
 constexpr int STAGES = 4;
-constexpr int A_BYTES = TM * TK * 2;                 // 16 KiB
-constexpr int STAGE_BYTES = (TM + TN) * TK * 2;      // 32 KiB
-constexpr int SPITCH = TN + 8;                       // staging row pitch (elements)
-constexpr int STAGING_BYTES = TM * SPITCH * 2;       // 34816
+constexpr int A_BYTES = TM * TK * 2;             // 16 KiB
+constexpr int STAGE_BYTES = (TM + BN) * TK * 2;  // 32 KiB per CTA
+constexpr int CHUNK = 64;                        // epilogue columns per chunk
+constexpr int NCHUNK = TN / CHUNK;
+constexpr int BOX_BYTES = 64 * 64 * 2;           // one 64 x 64 bf16 box, 128-byte swizzle
+constexpr int CHUNK_BYTES = 2 * BOX_BYTES;       // 128 x 64 (or 64 x 128) elements
 constexpr int NUM_THREADS = 192;
 constexpr int MAX_PROB = 4;
-constexpr int TMEM_COLS = 256;                       // two 128-column fp32 accumulators
-constexpr int BAR_BYTES = 256;
-constexpr int DIAG_BYTES = TM * 4;                   // fp32 diagonal of a tile (for D2)
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 2 * STAGING_BYTES + BAR_BYTES + DIAG_BYTES;
+constexpr int TMEM_COLS = 512;                   // two 256-column fp32 accumulators
+constexpr int OFF_SC = STAGES * STAGE_BYTES;     // C chunk
+constexpr int OFF_SD = OFF_SC + CHUNK_BYTES;     // 2 output chunks
+constexpr int OFF_SM = OFF_SD + 2 * CHUNK_BYTES; // 2 mirrored chunks
+constexpr int OFF_BAR = OFF_SM + 2 * CHUNK_BYTES;
+constexpr int BAR_BYTES = 512;
+constexpr int SMEM_BYTES = 1024 + OFF_BAR + BAR_BYTES;
 
 struct Problem {
   CUtensorMap tmA;
   CUtensorMap tmB;
+  CUtensorMap tmC;
+  CUtensorMap tmD;
+  CUtensorMap tmD2;
   int a_mn, b_mn;
-  int M, N;
   int kblocks;
   int tiles_m, tiles_n, sym;
   int tile_begin, tiles_per_mat;
   float alpha, beta, gamma;
   int alpha_pow, beta_pow;
   const float* scale;
-  const bf16* C;
-  long long ldc, sc;
-  int c_trans;
-  bf16* D;
-  long long ldd, sd;
-  int d_trans;
-  bf16* D2;
-  long long ld2, s2;
+  int has_c, c_trans, d_trans, has_d2;
   int diag_limit;
-  const int* row_map;
-  long long rm_stride;
   int check_finite;
 };
 
@@ -75,7 +77,7 @@ struct Params {
 };
 
 struct TileCoord {
-  int p, b, tm, tn;
+  int p, b, I, J;
 };
 
 __device__ __forceinline__ TileCoord decode_tile(const Params& P, int tile) {
@@ -93,130 +95,76 @@ __device__ __forceinline__ TileCoord decode_tile(const Params& P, int tile) {
       t -= pr.tiles_m - i;
       ++i;
     }
-    tc.tm = i;
-    tc.tn = i + t;
+    tc.I = i;
+    tc.J = i + t;
   } else {
-    tc.tm = t / pr.tiles_n;
-    tc.tn = t - tc.tm * pr.tiles_n;
+    tc.I = t / pr.tiles_n;
+    tc.J = t - tc.I * pr.tiles_n;
   }
   return tc;
 }
 
 __device__ __forceinline__ float powi(float s, int p) { return p == 0 ? 1.f : (p == 1 ? s : s * s); }
 
-// Staging block S (128 x 128, pitch SPITCH) <-> global matrix G of batch entry b:
-//   trans = 0: S[u][v] = G[pi(m0+u)][n0+v]   (valid when m0+u < M and n0+v < N)
-//   trans = 1: S[u][v] = G[n0+u][pi(m0+v)]   (valid when n0+u < N and m0+v < M)
-// pi(i) = row_map ? row_map[b*rms + i] : i. Out-of-range elements load as 0 and are not stored.
-__device__ void coop_load(bf16* S, const bf16* G, long long ld, long long sb, int b, int trans, int m0, int n0,
-                          int M, int N, const int* row_map, long long rms, int et) {
-  const int ew = et >> 5, lane = et & 31;
-  const bf16* Gb = G + (long long)b * sb;
-  const int v0 = lane * 4;
-  for (int u = ew; u < TM; u += 4) {
-    uint2 pk = make_uint2(0u, 0u);
-    bf16* pv = reinterpret_cast<bf16*>(&pk);
-    if (!trans) {
-      const int gi = m0 + u;
-      const int gj = n0 + v0;
-      if (gi < M) {
-        const long long ro = (long long)(row_map ? row_map[(long long)b * rms + gi] : gi) * ld;
-        if (gj + 3 < N) {
-          pk = *reinterpret_cast<const uint2*>(Gb + ro + gj);
-        } else {
-          for (int e = 0; e < 4; ++e)
-            if (gj + e < N) pv[e] = Gb[ro + gj + e];
-        }
-      }
-    } else {
-      const int gj = n0 + u;
-      const int gi = m0 + v0;
-      if (gj < N) {
-        const long long ro = (long long)gj * ld;
-        if (!row_map && gi + 3 < M) {
-          pk = *reinterpret_cast<const uint2*>(Gb + ro + gi);
-        } else {
-          for (int e = 0; e < 4; ++e)
-            if (gi + e < M) pv[e] = Gb[ro + (row_map ? row_map[(long long)b * rms + gi + e] : gi + e)];
-        }
-      }
-    }
-    *reinterpret_cast<uint2*>(S + u * SPITCH + v0) = pk;
+// Byte offset of element (tile row r in [0,128), chunk column c in [0,64)) in a staged chunk:
+// "direct" keeps the tile's orientation (two 64-row boxes), "transposed" stores the chunk as
+// its transpose (64 rows x 128 columns, two 64-column boxes). Both follow the 128-byte
+// swizzle of the TMA boxes: 16-byte unit u of box row y lives at unit u ^ (y & 7).
+__device__ __forceinline__ uint32_t off_direct(int r, int c) {
+  const int y = r & 63;
+  return (uint32_t)((r >> 6) * BOX_BYTES + y * 128 + (((c >> 3) ^ (y & 7)) << 4) + ((c & 7) << 1));
+}
+__device__ __forceinline__ uint32_t off_trans(int r, int c) {
+  const int x = r & 63;
+  return (uint32_t)((r >> 6) * BOX_BYTES + c * 128 + (((x >> 3) ^ (c & 7)) << 4) + ((x & 7) << 1));
+}
+
+// The two 64 x 64 boxes of one chunk: rows [row0, row0+128) x cols [col0, col0+64) of the
+// matrix (trans = 0), or rows [col0, col0+64) x cols [row0, row0+128) (trans = 1).
+__device__ __forceinline__ void chunk_load(uint8_t* s, const CUtensorMap* map, uint64_t* bar, int trans, int row0,
+                                           int col0, int b) {
+  if (!trans) {
+    tma_load_3d(s, map, bar, col0, row0, b);
+    tma_load_3d(s + BOX_BYTES, map, bar, col0, row0 + 64, b);
+  } else {
+    tma_load_3d(s, map, bar, row0, col0, b);
+    tma_load_3d(s + BOX_BYTES, map, bar, row0 + 64, col0, b);
+  }
+}
+__device__ __forceinline__ void chunk_store(const uint8_t* s, const CUtensorMap* map, int trans, int row0, int col0,
+                                            int b) {
+  if (!trans) {
+    tma_store_3d(map, s, col0, row0, b);
+    tma_store_3d(map, s + BOX_BYTES, col0, row0 + 64, b);
+  } else {
+    tma_store_3d(map, s, row0, col0, b);
+    tma_store_3d(map, s + BOX_BYTES, row0 + 64, col0, b);
   }
 }
 
-// Inverse of coop_load; also writes D2 = D + gamma I when D2 is set (same row mapping as
-// D): off the diagonal D2 takes the stored value, on the global diagonal (gi == gj <
-// diag_limit) it takes dg[u], the fp32 diagonal plus gamma rounded once (appendix B.2.3:
-// adding a_t I to an already rounded Z loses a_t's precision).
-__device__ void coop_store(const bf16* S, bf16* G, long long ld, long long sb, bf16* G2, long long ld2,
-                           long long sb2, const float* dg, int diag_limit, int b, int trans, int m0, int n0, int M,
-                           int N, const int* row_map, long long rms, int et) {
-  const int ew = et >> 5, lane = et & 31;
-  bf16* Gb = G + (long long)b * sb;
-  bf16* G2b = G2 ? G2 + (long long)b * sb2 : nullptr;
-  const int v0 = lane * 4;
-  for (int u = ew; u < TM; u += 4) {
-    const uint2 pk = *reinterpret_cast<const uint2*>(S + u * SPITCH + v0);
-    const bf16* pv = reinterpret_cast<const bf16*>(&pk);
-    if (!trans) {
-      const int gi = m0 + u;
-      const int gj = n0 + v0;
-      if (gi >= M) continue;
-      const int pi = row_map ? row_map[(long long)b * rms + gi] : gi;
-      const long long ro = (long long)pi * ld;
-      if (gj + 3 < N) {
-        *reinterpret_cast<uint2*>(Gb + ro + gj) = pk;
-      } else {
-        for (int e = 0; e < 4; ++e)
-          if (gj + e < N) Gb[ro + gj + e] = pv[e];
-      }
-      if (G2b) {
-        const long long ro2 = (long long)pi * ld2;
-        uint2 q = pk;
-        bf16* qv = reinterpret_cast<bf16*>(&q);
-        for (int e = 0; e < 4; ++e)
-          if (gi == gj + e && gi < diag_limit) qv[e] = f_to_bf16(dg[u]);
-        if (gj + 3 < N) {
-          *reinterpret_cast<uint2*>(G2b + ro2 + gj) = q;
-        } else {
-          for (int e = 0; e < 4; ++e)
-            if (gj + e < N) G2b[ro2 + gj + e] = qv[e];
-        }
-      }
-    } else {
-      const int gj = n0 + u;
-      const int gi = m0 + v0;
-      if (gj >= N) continue;
-      const long long ro = (long long)gj * ld;
-      if (!row_map && gi + 3 < M) {
-        *reinterpret_cast<uint2*>(Gb + ro + gi) = pk;
-      } else {
-        for (int e = 0; e < 4; ++e)
-          if (gi + e < M) Gb[ro + (row_map ? row_map[(long long)b * rms + gi + e] : gi + e)] = pv[e];
-      }
-    }
-  }
-}
-
-__global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_constant__ Params P) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+    gemm_kernel(const __grid_constant__ Params P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = smem;
-  bf16* S0 = reinterpret_cast<bf16*>(smem + STAGES * STAGE_BYTES);
-  bf16* S1 = S0 + TM * SPITCH;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES + 2 * STAGING_BYTES);
+  uint8_t* SC = smem + OFF_SC;
+  uint8_t* SD = smem + OFF_SD;
+  uint8_t* SM = smem + OFF_SM;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
   uint64_t* full = bars;
   uint64_t* empty = bars + STAGES;
   uint64_t* tfull = bars + 2 * STAGES;
   uint64_t* tempty = tfull + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
-  float* diag = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES + 2 * STAGING_BYTES + BAR_BYTES);
+  uint64_t* cbar = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cbar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* epi_flag = abort_flag + 1;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int pair = blockIdx.x >> 1;
+  const int npairs = gridDim.x >> 1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -225,8 +173,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 128);
+      mbar_init(&tempty[a], 8);  // one arrival per epilogue warp of both CTAs
     }
+    mbar_init(cbar, 1);
     *abort_flag = 0;
     *epi_flag = 1;
     mbar_fence_init();
@@ -238,44 +187,47 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
     }
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc2(tmem_slot, TMEM_COLS);
+    tmem_relinquish2();
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();  // the peer's barriers are initialised before any remote arrival
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------- TMA producer ----------------
+      // ---------------- TMA producer (both CTAs) ----------------
       int s = 0;
       uint32_t ph = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < P.total_tiles; tile += gridDim.x) {
+      for (int tile = pair; ok && tile < P.total_tiles; tile += npairs) {
         const TileCoord c = decode_tile(P, tile);
         const Problem& pr = P.prob[c.p];
-        const int m0 = c.tm * TM, n0 = c.tn * TN;
+        const int m0 = c.I * 256 + (int)rank * TM;
+        const int n0 = c.J * 256 + (int)rank * BN;
         for (int kb = 0; kb < pr.kblocks; ++kb) {
           if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, P.status)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
+          if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * STAGE_BYTES);
+          const uint32_t fb = mapa_shared(smem_u32(&full[s]), 0);
           uint8_t* sa = stages + s * STAGE_BYTES;
           uint8_t* sb = sa + A_BYTES;
           const int k0 = kb * TK;
           if (!pr.a_mn) {
-            tma_load_3d(sa, &pr.tmA, &full[s], k0, m0, c.b);
+            tma_load_3d_pair(sa, &pr.tmA, fb, k0, m0, c.b);
           } else {
-            tma_load_3d(sa, &pr.tmA, &full[s], m0, k0, c.b);
-            tma_load_3d(sa + 8192, &pr.tmA, &full[s], m0 + 64, k0, c.b);
+            tma_load_3d_pair(sa, &pr.tmA, fb, m0, k0, c.b);
+            tma_load_3d_pair(sa + BOX_BYTES, &pr.tmA, fb, m0 + 64, k0, c.b);
           }
           if (!pr.b_mn) {
-            tma_load_3d(sb, &pr.tmB, &full[s], k0, n0, c.b);
+            tma_load_3d_pair(sb, &pr.tmB, fb, k0, n0, c.b);
           } else {
-            tma_load_3d(sb, &pr.tmB, &full[s], n0, k0, c.b);
-            tma_load_3d(sb + 8192, &pr.tmB, &full[s], n0 + 64, k0, c.b);
+            tma_load_3d_pair(sb, &pr.tmB, fb, n0, k0, c.b);
+            tma_load_3d_pair(sb + BOX_BYTES, &pr.tmB, fb, n0 + 64, k0, c.b);
           }
           if (++s == STAGES) {
             s = 0;
@@ -285,13 +237,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer ----------------
+    if (lane == 0 && rank == 0) {
+      // ---------------- MMA issuer (leader CTA) ----------------
       int s = 0;
       uint32_t ph = 0;
       bool ok = true;
       int local = 0;
-      for (int tile = blockIdx.x; ok && tile < P.total_tiles; tile += gridDim.x, ++local) {
+      for (int tile = pair; ok && tile < P.total_tiles; tile += npairs, ++local) {
         const TileCoord c = decode_tile(P, tile);
         const Problem& pr = P.prob[c.p];
         const int acc = local & 1;
@@ -299,7 +251,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, P.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * TN;
-        const uint32_t idesc = idesc_bf16_f32(TM, TN, pr.a_mn, pr.b_mn);
+        const uint32_t idesc = idesc_bf16_f32(2 * TM, TN, pr.a_mn, pr.b_mn);
         for (int kb = 0; kb < pr.kblocks; ++kb) {
           if (!mbar_wait(&full[s], ph, abort_flag, P.status)) {
             ok = false;
@@ -310,26 +262,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
           const uint32_t sb = sa + A_BYTES;
 #pragma unroll
           for (int kk = 0; kk < TK / 16; ++kk) {
-            const uint64_t ad = pr.a_mn ? sdesc_sw128(sa + kk * 2048, 8192, 1024) : sdesc_sw128(sa + kk * 32, 16, 1024);
-            const uint64_t bd = pr.b_mn ? sdesc_sw128(sb + kk * 2048, 8192, 1024) : sdesc_sw128(sb + kk * 32, 16, 1024);
-            umma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            const uint64_t ad =
+                pr.a_mn ? sdesc_sw128(sa + kk * 2048, BOX_BYTES, 1024) : sdesc_sw128(sa + kk * 32, 16, 1024);
+            const uint64_t bd =
+                pr.b_mn ? sdesc_sw128(sb + kk * 2048, BOX_BYTES, 1024) : sdesc_sw128(sb + kk * 32, 16, 1024);
+            umma2_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
-          umma_commit(&empty[s]);
+          umma2_commit_multicast(&empty[s], 0x3);
           if (++s == STAGES) {
             s = 0;
             ph ^= 1u;
           }
         }
-        if (ok) umma_commit(&tfull[acc]);
+        if (ok) umma2_commit_multicast(&tfull[acc], 0x3);
       }
     }
   } else {
-    // ---------------- epilogue (warps 2..5) ----------------
+    // ---------------- epilogue (warps 2..5 of both CTAs) ----------------
     const int et = threadIdx.x - 64;
     const int quarter = warp & 3;  // TMEM lanes this warp may read
     const int r = quarter * 32 + lane;
+    const uint32_t tempty_leader0 = mapa_shared(smem_u32(&tempty[0]), 0);
+    const uint32_t tempty_leader1 = mapa_shared(smem_u32(&tempty[1]), 0);
+    uint32_t cph = 0;  // parity of the C-chunk barrier
+    uint32_t gc = 0;   // chunks stored so far (staging double buffer)
     int local = 0;
-    for (int tile = blockIdx.x; tile < P.total_tiles; tile += gridDim.x, ++local) {
+    for (int tile = pair; tile < P.total_tiles; tile += npairs, ++local) {
       const TileCoord c = decode_tile(P, tile);
       const Problem& pr = P.prob[c.p];
       const int acc = local & 1;
@@ -340,95 +298,137 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         alpha *= powi(sc, pr.alpha_pow);
         beta *= powi(sc, pr.beta_pow);
       }
-      const bool has_c = pr.C != nullptr && beta != 0.f;
-      const bool mirror = pr.sym && c.tm != c.tn;
-      const int m0 = c.tm * TM, n0 = c.tn * TN;
-      if (has_c) coop_load(S0, pr.C, pr.ldc, pr.sc, c.b, pr.c_trans, m0, n0, pr.M, pr.N, pr.row_map, pr.rm_stride, et);
+      const bool has_c = pr.has_c != 0;
+      const bool mirror = pr.sym && c.I != c.J;
+      const bool want_diag = pr.has_d2 && c.I == c.J;
+      const int m0 = c.I * 256 + (int)rank * TM;  // first row of this CTA's half
+      const int n0 = c.J * 256;
+      if (has_c && et == 0) {
+        mbar_arrive_expect_tx(cbar, CHUNK_BYTES);
+        chunk_load(SC, &pr.tmC, cbar, pr.c_trans, m0, n0, c.b);
+      }
       if (et == 0) *epi_flag = mbar_wait(&tfull[acc], aph, abort_flag, P.status) ? 1 : 0;
       named_bar_sync(1, 128);
       if (!*epi_flag) break;
       tc_fence_after();
-      const bool inplace = !has_c || (pr.c_trans == pr.d_trans);
-      bf16* SD = inplace ? S0 : S1;
-      const bool want_diag = pr.D2 != nullptr && c.tm == c.tn;
+      const int diag_col = (int)rank * TM + r;  // tile column of this row's diagonal element
       float dv = 0.f;
       bool bad = false;
-#pragma unroll 1
-      for (int ch = 0; ch < TN / 32; ++ch) {
-        uint32_t v[32];
-        __syncwarp();  // tcgen05.ld is warp-aligned
-        tmem_ld_32x32b_x32(tmem_base + acc * TN + ch * 32 + ((uint32_t)(quarter * 32) << 16), v);
-        tmem_ld_wait();
-        float o[32];
+      bool ok = true;
+      for (int ch = 0; ch < NCHUNK; ++ch, ++gc) {
+        uint8_t* sd = SD + (gc & 1) * CHUNK_BYTES;
+        uint8_t* sm = SM + (gc & 1) * CHUNK_BYTES;
+        if (et == 0) bulk_wait_read<1>();  // the stores that last read this buffer are done
+        named_bar_sync(1, 128);
         if (has_c) {
-          if (!pr.c_trans) {
-            const uint4* src = reinterpret_cast<const uint4*>(S0 + r * SPITCH + ch * 32);
+          if (!mbar_wait(cbar, cph, abort_flag, P.status)) ok = false;
+          cph ^= 1u;
+        }
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+          uint32_t v[32];
+          __syncwarp();
+          tmem_ld_32x32b_x32(tmem_base + acc * TN + ch * CHUNK + h * 32 + ((uint32_t)(quarter * 32) << 16), v);
+          tmem_ld_wait();
+          float o[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] = alpha * __uint_as_float(v[j]);
+          if (has_c) {
+            if (!pr.c_trans) {
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const uint4 w = *reinterpret_cast<const uint4*>(SC + off_direct(r, h * 32 + q * 8));
+                const bf16* wv = reinterpret_cast<const bf16*>(&w);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[q * 8 + e] = fmaf(beta, bf16_to_f(wv[e]), o[q * 8 + e]);
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                o[j] = fmaf(beta, bf16_to_f(*reinterpret_cast<const bf16*>(SC + off_trans(r, h * 32 + j))), o[j]);
+            }
+          }
+          if (pr.check_finite) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) bad |= !isfinite(o[j]);
+          }
+          if (want_diag && (diag_col >> 5) == ch * 2 + h) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j == (diag_col & 31)) dv = o[j];
+          }
+          if (!pr.d_trans) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              const uint4 w = src[q];
-              const bf16* wv = reinterpret_cast<const bf16*>(&w);
+              uint4 w;
+              bf16* wv = reinterpret_cast<bf16*>(&w);
 #pragma unroll
-              for (int e = 0; e < 8; ++e) o[q * 8 + e] = beta * bf16_to_f(wv[e]);
+              for (int e = 0; e < 8; ++e) wv[e] = f_to_bf16(o[q * 8 + e]);
+              *reinterpret_cast<uint4*>(sd + off_direct(r, h * 32 + q * 8)) = w;
             }
           } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) o[j] = beta * bf16_to_f(S0[(ch * 32 + j) * SPITCH + r]);
+            for (int j = 0; j < 32; ++j) *reinterpret_cast<bf16*>(sd + off_trans(r, h * 32 + j)) = f_to_bf16(o[j]);
           }
+          if (mirror) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) o[j] = fmaf(alpha, __uint_as_float(v[j]), o[j]);
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) o[j] = alpha * __uint_as_float(v[j]);
-        }
-        if (pr.check_finite) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) bad |= !isfinite(o[j]);
-        }
-        if (want_diag && (r >> 5) == ch) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j == (r & 31)) dv = o[j];
-        }
-        if (!pr.d_trans) {
-          uint4* dst = reinterpret_cast<uint4*>(SD + r * SPITCH + ch * 32);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint4 w;
-            bf16* wv = reinterpret_cast<bf16*>(&w);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) wv[e] = f_to_bf16(o[q * 8 + e]);
-            dst[q] = w;
+            for (int j = 0; j < 32; ++j) *reinterpret_cast<bf16*>(sm + off_trans(r, h * 32 + j)) = f_to_bf16(o[j]);
           }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) SD[(ch * 32 + j) * SPITCH + r] = f_to_bf16(o[j]);
         }
-        if (mirror) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) S1[(ch * 32 + j) * SPITCH + r] = f_to_bf16(o[j]);
+        if (ch == NCHUNK - 1) {
+          // the accumulator has been read: release it to the leader's MMA issuer
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(acc ? tempty_leader1 : tempty_leader0);
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        const int col0 = n0 + ch * CHUNK;
+        const bool chunk_has_diag = want_diag && (ch == 2 * (int)rank || ch == 2 * (int)rank + 1);
+        if (et == 0) {
+          if (has_c && ch + 1 < NCHUNK) {
+            mbar_arrive_expect_tx(cbar, CHUNK_BYTES);
+            chunk_load(SC, &pr.tmC, cbar, pr.c_trans, m0, col0 + CHUNK, c.b);
+          }
+          chunk_store(sd, &pr.tmD, pr.d_trans, m0, col0, c.b);
+          if (mirror) chunk_store(sm, &pr.tmD, 1, m0, col0, c.b);
+          if (pr.has_d2 && !chunk_has_diag) {
+            chunk_store(sd, &pr.tmD2, 0, m0, col0, c.b);
+            if (mirror) chunk_store(sm, &pr.tmD2, 1, m0, col0, c.b);
+          }
+          bulk_commit();
+        }
+        if (chunk_has_diag) {
+          // D2 = D + gamma I: patch the diagonal with the fp32 value plus gamma, rounded once
+          // (appendix B.2.3: adding a_t I to an already rounded Z loses a_t's precision)
+          if (et == 0) bulk_wait_read<0>();
+          named_bar_sync(1, 128);
+          if ((diag_col >> 6) == ch && m0 + r < pr.diag_limit)
+            *reinterpret_cast<bf16*>(sd + off_direct(r, diag_col & 63)) = f_to_bf16(dv + pr.gamma);
+          fence_proxy_async_smem();
+          named_bar_sync(1, 128);
+          if (et == 0) {
+            chunk_store(sd, &pr.tmD2, 0, m0, col0, c.b);
+            bulk_commit();
+          }
         }
       }
-      if (want_diag) diag[r] = dv + pr.gamma;
-      tc_fence_before();
-      mbar_arrive(&tempty[acc]);
       if (bad) set_status(P.status, GNS_DEVST_NONFINITE);
+      if (!ok) *epi_flag = 0;
       named_bar_sync(1, 128);
-      coop_store(SD, pr.D, pr.ldd, pr.sd, pr.D2, pr.ld2, pr.s2, diag, pr.diag_limit, c.b, pr.d_trans, m0, n0,
-                 pr.M, pr.N, pr.row_map, pr.rm_stride, et);
-      if (mirror)
-        coop_store(S1, pr.D, pr.ldd, pr.sd, pr.D2, pr.ld2, pr.s2, diag, pr.diag_limit, c.b, 0, n0, m0, pr.N,
-                   pr.M, nullptr, 0, et);
-      named_bar_sync(1, 128);
+      if (!*epi_flag) break;
     }
+    if (et == 0) bulk_wait_all();
   }
 
-  // lanes 1-31 of the producer and MMA warps wait here for lane 0 (aligned barrier below)
+  // lanes 1-31 of the producer and MMA warps wait here for lane 0 (aligned barriers below)
   __syncwarp();
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();  // no remote arrival or peer MMA can still target this CTA
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    tmem_dealloc2(tmem_base, TMEM_COLS);
   }
 }
 
@@ -452,8 +452,9 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn(std::string* err) {
   return fn;
 }
 
-// 3-D bf16 tensor map over a batch of row-major matrices: dims {cols, rows, batch}.
-static bool encode_map(CUtensorMap* map, const MatRef& m, int64_t batch, bool kmajor, std::string* err) {
+// 3-D bf16 tensor map over a batch of row-major matrices: dims {cols, rows, batch}, box
+// {64, box_rows, 1}, 128-byte swizzle, zero fill out of bounds.
+static bool encode_map(CUtensorMap* map, const MatRef& m, int64_t batch, int box_rows, std::string* err) {
   auto fn = get_encode_fn(err);
   if (!fn) return false;
   const int64_t ld_b = m.ld * 2;
@@ -462,7 +463,7 @@ static bool encode_map(CUtensorMap* map, const MatRef& m, int64_t batch, bool km
   if (st_b == 0) st_b = 16;
   cuuint64_t dims[3] = {(cuuint64_t)m.cols, (cuuint64_t)m.rows, (cuuint64_t)batch};
   cuuint64_t strides[2] = {(cuuint64_t)ld_b, (cuuint64_t)st_b};
-  cuuint32_t box[3] = {64u, kmajor ? 128u : 64u, 1u};
+  cuuint32_t box[3] = {64u, (cuuint32_t)box_rows, 1u};
   cuuint32_t estr[3] = {1u, 1u, 1u};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, m.ptr, dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -487,38 +488,63 @@ int device_sm_count() {
   return cached[dev];
 }
 
+// Number of CTA pairs of the GEMM kernel that can be resident at once (and the one-time
+// shared-memory opt-in).
+static int resident_pairs(std::string* err) {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (cached[dev]) return cached[dev];
+  cudaError_t e = cudaFuncSetAttribute(tc::gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_BYTES);
+  if (e != cudaSuccess) {
+    *err = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e);
+    return 0;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * (device_sm_count() / 2), 1, 1);
+  cfg.blockDim = dim3(tc::NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = tc::SMEM_BYTES;
+  int clusters = 0;
+  e = cudaOccupancyMaxActiveClusters(&clusters, tc::gemm_kernel, &cfg);
+  if (e != cudaSuccess || clusters < 1) {
+    (void)cudaGetLastError();
+    clusters = device_sm_count() / 2;
+  }
+  cached[dev] = clusters;
+  return clusters;
+}
+
 int gemm_launch_bf16(const GemmOp* ops, int nops, int32_t* dev_status, void* stream, std::string* err) {
   using namespace tc;
   if (nops < 1 || nops > MAX_PROB) {
     *err = "internal: bad number of grouped products";
     return GNS_ERR_INVALID;
   }
-  static bool attr_set[64] = {false};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) {
-      *err = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e);
-      return GNS_ERR_CUDA;
-    }
-    attr_set[dev] = true;
-  }
+  const int pairs_max = resident_pairs(err);
+  if (pairs_max < 1) return GNS_ERR_CUDA;
   Params P;
   memset(&P, 0, sizeof(P));
   int tiles = 0;
   for (int i = 0; i < nops; ++i) {
     const GemmOp& o = ops[i];
+    if (o.row_map) {
+      *err = "internal: row-mapped outputs are not handled by the tensor-core GEMM";
+      return GNS_ERR_INVALID;
+    }
     Problem& pr = P.prob[i];
-    if (!encode_map(&pr.tmA, o.A, o.batch, !o.a_mn, err)) return GNS_ERR_CUDA;
-    if (!encode_map(&pr.tmB, o.B, o.batch, !o.b_mn, err)) return GNS_ERR_CUDA;
+    if (!encode_map(&pr.tmA, o.A, o.batch, o.a_mn ? 64 : 128, err)) return GNS_ERR_CUDA;
+    if (!encode_map(&pr.tmB, o.B, o.batch, o.b_mn ? 64 : 128, err)) return GNS_ERR_CUDA;
+    pr.has_c = o.C.ptr != nullptr && o.beta != 0.f;
+    if (pr.has_c && !encode_map(&pr.tmC, o.C, o.batch, 64, err)) return GNS_ERR_CUDA;
+    if (!encode_map(&pr.tmD, o.D, o.batch, 64, err)) return GNS_ERR_CUDA;
+    pr.has_d2 = o.D2.ptr != nullptr;
+    if (pr.has_d2 && !encode_map(&pr.tmD2, o.D2, o.batch, 64, err)) return GNS_ERR_CUDA;
     pr.a_mn = o.a_mn;
     pr.b_mn = o.b_mn;
-    pr.M = (int)o.M;
-    pr.N = (int)o.N;
     pr.kblocks = (int)((o.K + TK - 1) / TK);
-    pr.tiles_m = (int)((o.M + TM - 1) / TM);
-    pr.tiles_n = (int)((o.N + TN - 1) / TN);
+    pr.tiles_m = (int)((o.M + 255) / 256);
+    pr.tiles_n = (int)((o.N + 255) / 256);
     pr.sym = o.sym;
     pr.tiles_per_mat = o.sym ? pr.tiles_m * (pr.tiles_m + 1) / 2 : pr.tiles_m * pr.tiles_n;
     pr.tile_begin = tiles;
@@ -529,29 +555,22 @@ int gemm_launch_bf16(const GemmOp* ops, int nops, int32_t* dev_status, void* str
     pr.alpha_pow = o.alpha_pow;
     pr.beta_pow = o.beta_pow;
     pr.scale = o.scale;
-    pr.C = static_cast<const bf16*>(o.C.ptr);
-    pr.ldc = o.C.ld;
-    pr.sc = o.C.stride;
     pr.c_trans = o.c_trans;
-    pr.D = static_cast<bf16*>(o.D.ptr);
-    pr.ldd = o.D.ld;
-    pr.sd = o.D.stride;
     pr.d_trans = o.d_trans;
-    pr.D2 = static_cast<bf16*>(o.D2.ptr);
-    pr.ld2 = o.D2.ld;
-    pr.s2 = o.D2.stride;
     pr.diag_limit = (int)o.diag_limit;
-    pr.row_map = o.row_map;
-    pr.rm_stride = o.row_map_stride;
     pr.check_finite = o.check_finite;
   }
   P.nprob = nops;
   P.total_tiles = tiles;
   P.status = dev_status;
   if (tiles == 0) return GNS_OK;
-  const int grid = std::min(tiles, device_sm_count());
-  gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, static_cast<cudaStream_t>(stream)>>>(P);
-  cudaError_t e = cudaGetLastError();
+  const int pairs = std::min(tiles, pairs_max);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_kernel, P);
   if (e != cudaSuccess) {
     *err = std::string("tcgen05 GEMM launch: ") + cudaGetErrorString(e);
     return GNS_ERR_CUDA;

@@ -544,6 +544,7 @@ static int plan_op(gns_op op, const gns_batch* x, int ngroups, gns_dtype dt, con
         a.take(sizeof(int) * s.n * s.B);
         a.take(sizeof(int) * k * s.B);
         a.take(sizeof(uint16_t) * (size_t)(s.B * round_up(k, PAD) * round_up(s.m, 8)));
+        a.take(sizeof(uint16_t) * (size_t)(s.B * k * round_up(s.m, 8)));
         GramBufs gb;
         plan_gram(a, s.B, k, s.m, dt, ns, &gb, true);
       }
@@ -772,6 +773,12 @@ int gns_muon_step(const gns_batch* W, const gns_batch* G, const gns_batch* M, in
       xs.ld = round_up(s.m, 8);
       xs.stride = round_up(k, PAD) * xs.ld;
       xs.ptr = a.take(sizeof(uint16_t) * (size_t)(s.B * xs.stride));
+      MatRef os;  // O = polar(M[S]) before it is scattered into W
+      os.rows = k;
+      os.cols = s.m;
+      os.ld = round_up(s.m, 8);
+      os.stride = k * os.ld;
+      os.ptr = a.take(sizeof(uint16_t) * (size_t)(s.B * os.stride));
       GramBufs gb;
       plan_gram(a, s.B, k, s.m, GNS_BF16, ns, &gb, true);
       // line 2: M <- M + G, with the exact l1 keys of the oriented rows
@@ -784,19 +791,16 @@ int gns_muon_step(const gns_batch* W, const gns_batch* G, const gns_batch* M, in
       // line 8 on the rows that are not updated below
       if (decay != 1.f && (rc = launch_scale_unselected(wm, s.B, s.trans, idx, k, decay, stream, &err)))
         return fail(rc, err);
-      // lines 4, 8, 9: O = polar(M[S]); W[S] <- (1 - lr wd) W[S] - lr scale O
+      // line 4: O = polar(M[S])
       Src src;
       src.mat = xs;
       src.trans = 0;
       Final fin;
-      fin.D = wm;
-      fin.d_trans = s.trans;
-      fin.alpha = -lr * mp->scale;
-      fin.beta = decay;
-      fin.has_c = true;
-      fin.row_map = idx;
-      fin.rms = k;
+      fin.D = os;
       if ((rc = run_gram(GNS_BF16, src, s.B, k, s.m, ns, gb, gb.inv, fin, dev_status, stream))) return rc;
+      // lines 8, 9: W[S] <- (1 - lr wd) W[S] - lr scale O, one rounding
+      if ((rc = launch_scatter_update(wm, os, s.B, s.trans, idx, k, -lr * mp->scale, decay, stream, &err)))
+        return fail(rc, err);
       // line 10: error feedback
       if ((rc = launch_decay_selected(mm, s.B, s.trans, idx, k, mu, stream, &err))) return fail(rc, err);
     }
