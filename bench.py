@@ -279,7 +279,7 @@ def run_ours(args, rank, world, dist):
                 "d2h_bytes_per_step": bytes_step},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_burst, "unit": "TFLOP/s",
                      "frac": achieved / peak_burst, "traffic": None,
-                     "kernel": "gns::tc::gemm_kernel (tcgen05 bf16 GEMM, all 17 launches of a step)",
+                     "kernel": f"gns::tc::gemm_kernel (tcgen05 bf16 GEMM; {per_step} launch(es) per step carry the 17 products)",
                      "peak_kind": f"dense bf16 burst, {peak_src}",
                      "frac_of_sustained": achieved / peak_sus,
                      "gemm_ms_per_step": gemm_ms, "gemm_launches_per_step": per_step},

@@ -251,5 +251,39 @@ GNS_DEV void umma2_commit_multicast(uint64_t* bar, uint16_t mask) {
       : "memory");
 }
 
+// ------------------------------------------------------------------------------------
+// cross-CTA completion counters (global memory)
+
+GNS_DEV int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+GNS_DEV void red_release_gpu_add(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+GNS_DEV void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+// Spin (bounded) until *ctr >= target; then order later async-proxy (TMA) reads after it.
+GNS_DEV bool wait_counter(const int* ctr, int target, volatile int* abort_flag, int* status) {
+  if (ld_acquire_gpu(ctr) < target) {
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 1;; ++i) {
+      if (ld_acquire_gpu(ctr) >= target) break;
+      __nanosleep(64);
+      if ((i & 15u) == 0u) {
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > GNS_WAIT_TIMEOUT_NS) {
+          *abort_flag = 1;
+          set_status(status, GNS_DEVST_TIMEOUT);
+          return false;
+        }
+      }
+    }
+  }
+  fence_proxy_async_global();
+  return true;
+}
+
 GNS_DEV float bf16_to_f(bf16 v) { return __bfloat162float(v); }
 GNS_DEV bf16 f_to_bf16(float v) { return __float2bfloat16_rn(v); }

@@ -51,24 +51,40 @@ struct GemmOp {
   int check_finite = 0;
 };
 
-// Enqueues all ops as one launch (ops must be mutually independent). Returns GNS_OK or an
-// error status with *err set.
-int gemm_launch_bf16(const GemmOp* ops, int nops, int32_t* dev_status, void* stream, std::string* err);
-int gemm_launch_f32(const GemmOp* ops, int nops, int32_t* dev_status, void* stream, std::string* err);
+// Enqueues ops as ONE launch. dep_masks[i] (nullable) names earlier ops of the same launch
+// whose tiles of the same matrix must be complete before a tile of op i starts (the
+// tensor-core kernel waits on per-(op, matrix) completion counters: `counters`, at least
+// sum(batch) ints of device memory, reset by the launch). Without masks the ops must be
+// mutually independent. Returns GNS_OK or an error status with *err set.
+int gemm_launch_bf16(const GemmOp* ops, int nops, const uint32_t* dep_masks, int* counters, int32_t* dev_status,
+                     void* stream, std::string* err);
+int gemm_launch_f32(const GemmOp* ops, int nops, const uint32_t* dep_masks, int* counters, int32_t* dev_status,
+                    void* stream, std::string* err);
 
 // Instrumentation (gns_profile_set): event records around GEMM launches, launch counts.
 void profile_gemm_begin(void* stream);
 void profile_gemm_end(void* stream);
 void profile_count_launch();
 
+// Independent ops as one launch.
 inline int gemm_launch(gns_dtype dt, const GemmOp* ops, int nops, int32_t* dev_status, void* stream,
                        std::string* err) {
   profile_gemm_begin(stream);
-  const int rc = dt == GNS_BF16 ? gemm_launch_bf16(ops, nops, dev_status, stream, err)
-                                : gemm_launch_f32(ops, nops, dev_status, stream, err);
+  const int rc = dt == GNS_BF16 ? gemm_launch_bf16(ops, nops, nullptr, nullptr, dev_status, stream, err)
+                                : gemm_launch_f32(ops, nops, nullptr, nullptr, dev_status, stream, err);
   profile_gemm_end(stream);
   return rc;
 }
+
+// Largest number of ops of one tensor-core launch.
+constexpr int kMaxProgramOps = 24;
+
+// A sequence of ops in program order (op j may read what op i < j wrote, or overwrite what
+// it read). bf16: as few launches as possible, dependencies between ops found from the
+// buffers they read (A, B, C) and write (D, D2) and enforced per matrix inside the launch;
+// fp32: one launch per op, ordered by the stream. `counters`: kMaxProgramOps * batch ints.
+int gemm_program(gns_dtype dt, const GemmOp* ops, int nops, int* counters, int32_t* dev_status, void* stream,
+                 std::string* err);
 
 // Number of SMs of the current device (cached per device).
 int device_sm_count();

@@ -172,7 +172,14 @@ __global__ void __launch_bounds__(256) gemm_kernel(const __grid_constant__ Param
 
 }  // namespace simt
 
-int gemm_launch_f32(const GemmOp* ops, int nops, int32_t* dev_status, void* stream, std::string* err) {
+int gemm_launch_f32(const GemmOp* ops, int nops, const uint32_t* dep_masks, int* counters, int32_t* dev_status,
+                    void* stream, std::string* err) {
+  (void)counters;
+  for (int i = 0; i < nops; ++i)
+    if (dep_masks && dep_masks[i]) {
+      *err = "internal: the fp32 GEMM launches dependent products one by one";
+      return GNS_ERR_INVALID;
+    }
   using namespace simt;
   if (nops < 1 || nops > MAX_PROB) {
     *err = "internal: bad number of grouped products";

@@ -13,11 +13,14 @@
 //             K-major operand is one 128 x 64 box, an MN-major one two 64 x 64 boxes);
 //             completion is signalled on the leader CTA's stage barrier.
 //   warp 1    TMEM allocation (both CTAs) and, in the leader CTA, the MMA issuer.
-//   warps 2-5 epilogue: tcgen05.ld of the accumulator (thread = row), alpha/beta with the
-//             C tile (TMA-loaded), result staged in 128-byte-swizzled shared memory and
-//             written with TMA stores in 64-column chunks; off-diagonal tiles of symmetric
-//             products are also stored transposed at the mirrored position, diagonal tiles
-//             once (Dion3 sec. 5 "Writing to the Transposed Tile", appendix C.1).
+//   warp 2    C-tile loader: TMA loads of the addend C, chunk by chunk, as soon as the
+//             epilogue frees each buffer (a whole main loop ahead of its use).
+//   warps 3-10 epilogue, two warps per TMEM lane quarter (thread = row, each warp 32 of a
+//             chunk's 64 columns): tcgen05.ld of the accumulator, alpha/beta with the C tile,
+//             result staged in 128-byte-swizzled shared memory and written with TMA stores
+//             in 64-column chunks; off-diagonal tiles of symmetric products are also stored
+//             transposed at the mirrored position, diagonal tiles once (Dion3 sec. 5
+//             "Writing to the Transposed Tile", appendix C.1).
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -34,22 +37,34 @@ constexpr int TM = 128;                          // accumulator rows per CTA (25
 constexpr int TN = 256;                          // tile columns
 constexpr int BN = 128;                          // B columns staged per CTA
 constexpr int TK = 64;                           // K slice per stage
-constexpr int STAGES = 4;
+#ifndef GNS_TC_STAGES
+#define GNS_TC_STAGES 4
+#endif
+#ifndef GNS_TC_OUTBUFS
+#define GNS_TC_OUTBUFS 1
+#endif
+constexpr int STAGES = GNS_TC_STAGES;
+constexpr int OUT_BUFS = GNS_TC_OUTBUFS;         // staging buffers for output (and mirror) chunks
 constexpr int A_BYTES = TM * TK * 2;             // 16 KiB
 constexpr int STAGE_BYTES = (TM + BN) * TK * 2;  // 32 KiB per CTA
 constexpr int CHUNK = 64;                        // epilogue columns per chunk
 constexpr int NCHUNK = TN / CHUNK;
 constexpr int BOX_BYTES = 64 * 64 * 2;           // one 64 x 64 bf16 box, 128-byte swizzle
 constexpr int CHUNK_BYTES = 2 * BOX_BYTES;       // 128 x 64 (or 64 x 128) elements
-constexpr int NUM_THREADS = 192;
-constexpr int MAX_PROB = 4;
+constexpr int C_WARP = 2;                        // loads the C tile ahead of the epilogue
+constexpr int FIRST_EPI_WARP = 3;
+constexpr int EPI_WARPS = 8;                     // two per TMEM lane quarter
+constexpr int EPI_THREADS = 32 * EPI_WARPS;
+constexpr int NUM_THREADS = 32 * (FIRST_EPI_WARP + EPI_WARPS);
+constexpr int MAX_PROB = 24;                     // stages of one launch
 constexpr int TMEM_COLS = 512;                   // two 256-column fp32 accumulators
-constexpr int OFF_SC = STAGES * STAGE_BYTES;     // C chunk
-constexpr int OFF_SD = OFF_SC + CHUNK_BYTES;     // 2 output chunks
-constexpr int OFF_SM = OFF_SD + 2 * CHUNK_BYTES; // 2 mirrored chunks
-constexpr int OFF_BAR = OFF_SM + 2 * CHUNK_BYTES;
+constexpr int OFF_SC = STAGES * STAGE_BYTES;     // C tile (NCHUNK chunks)
+constexpr int OFF_SD = OFF_SC + NCHUNK * CHUNK_BYTES;
+constexpr int OFF_SM = OFF_SD + OUT_BUFS * CHUNK_BYTES;
+constexpr int OFF_BAR = OFF_SM + OUT_BUFS * CHUNK_BYTES;
 constexpr int BAR_BYTES = 512;
 constexpr int SMEM_BYTES = 1024 + OFF_BAR + BAR_BYTES;
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 struct Problem {
   CUtensorMap tmA;
@@ -67,6 +82,8 @@ struct Problem {
   int has_c, c_trans, d_trans, has_d2;
   int diag_limit;
   int check_finite;
+  uint32_t dep_mask;  // earlier problems whose tiles of the same matrix must be complete
+  int ctr_off;        // this problem's completion counters: counters[ctr_off + b]
 };
 
 struct Params {
@@ -74,7 +91,20 @@ struct Params {
   int nprob;
   int total_tiles;
   int* status;
+  int* counters;  // per (problem, matrix): CTA-halves of tiles completed (zero at launch)
 };
+
+// Bounded wait until every problem this tile depends on has finished matrix b.
+__device__ __forceinline__ bool wait_deps(const Params& P, const Problem& pr, int b, volatile int* abort_flag) {
+  uint32_t m = pr.dep_mask;
+  while (m) {
+    const int d = __ffs(m) - 1;
+    m &= m - 1;
+    const Problem& pd = P.prob[d];
+    if (!wait_counter(P.counters + pd.ctr_off + b, 2 * pd.tiles_per_mat, abort_flag, P.status)) return false;
+  }
+  return true;
+}
 
 struct TileCoord {
   int p, b, I, J;
@@ -155,8 +185,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   uint64_t* empty = bars + STAGES;
   uint64_t* tfull = bars + 2 * STAGES;
   uint64_t* tempty = tfull + 2;
-  uint64_t* cbar = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cbar + 1);
+  uint64_t* cfull = tempty + 2;
+  uint64_t* cempty = cfull + NCHUNK;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cempty + NCHUNK);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* epi_flag = abort_flag + 1;
 
@@ -173,9 +204,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 8);  // one arrival per epilogue warp of both CTAs
+      mbar_init(&tempty[a], 2 * EPI_WARPS);  // one arrival per epilogue warp of both CTAs
     }
-    mbar_init(cbar, 1);
+    for (int ch = 0; ch < NCHUNK; ++ch) {
+      mbar_init(&cfull[ch], 1);
+      mbar_init(&cempty[ch], EPI_WARPS);
+    }
     *abort_flag = 0;
     *epi_flag = 1;
     mbar_fence_init();
@@ -207,6 +241,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         const Problem& pr = P.prob[c.p];
         const int m0 = c.I * 256 + (int)rank * TM;
         const int n0 = c.J * 256 + (int)rank * BN;
+        if (pr.dep_mask && !wait_deps(P, pr, c.b, abort_flag)) break;
         for (int kb = 0; kb < pr.kblocks; ++kb) {
           if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, P.status)) {
             ok = false;
@@ -277,15 +312,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         if (ok) umma2_commit_multicast(&tfull[acc], 0x3);
       }
     }
+  } else if (warp == C_WARP) {
+    if (lane == 0) {
+      // ---------------- C-tile loader (both CTAs) ----------------
+      // Loads the C chunks of the next tile as soon as the epilogue releases each buffer,
+      // a whole main loop ahead of their use.
+      uint32_t nc = 0;
+      for (int tile = pair; tile < P.total_tiles; tile += npairs) {
+        const TileCoord c = decode_tile(P, tile);
+        const Problem& pr = P.prob[c.p];
+        if (!pr.has_c) continue;
+        const int m0 = c.I * 256 + (int)rank * TM;
+        const int n0 = c.J * 256;
+        if (pr.dep_mask && !wait_deps(P, pr, c.b, abort_flag)) break;
+        bool ok = true;
+        for (int ch = 0; ch < NCHUNK; ++ch) {
+          if (!mbar_wait(&cempty[ch], (nc & 1u) ^ 1u, abort_flag, P.status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&cfull[ch], CHUNK_BYTES);
+          chunk_load(SC + ch * CHUNK_BYTES, &pr.tmC, &cfull[ch], pr.c_trans, m0, n0 + ch * CHUNK, c.b);
+        }
+        if (!ok) break;
+        ++nc;
+      }
+    }
   } else {
-    // ---------------- epilogue (warps 2..5 of both CTAs) ----------------
-    const int et = threadIdx.x - 64;
+    // ---------------- epilogue (warps 3..10 of both CTAs) ----------------
+    const int et = threadIdx.x - 32 * FIRST_EPI_WARP;
+    const int ew = warp - FIRST_EPI_WARP;
     const int quarter = warp & 3;  // TMEM lanes this warp may read
+    const int half = ew >> 2;      // which 32 of a chunk's 64 columns
     const int r = quarter * 32 + lane;
     const uint32_t tempty_leader0 = mapa_shared(smem_u32(&tempty[0]), 0);
     const uint32_t tempty_leader1 = mapa_shared(smem_u32(&tempty[1]), 0);
-    uint32_t cph = 0;  // parity of the C-chunk barrier
-    uint32_t gc = 0;   // chunks stored so far (staging double buffer)
+    uint32_t nc = 0;  // C tiles consumed (parity of the C-chunk barriers)
+    uint32_t gc = 0;  // chunks stored so far (output staging buffers)
     int local = 0;
     for (int tile = pair; tile < P.total_tiles; tile += npairs, ++local) {
       const TileCoord c = decode_tile(P, tile);
@@ -303,93 +366,85 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       const bool want_diag = pr.has_d2 && c.I == c.J;
       const int m0 = c.I * 256 + (int)rank * TM;  // first row of this CTA's half
       const int n0 = c.J * 256;
-      if (has_c && et == 0) {
-        mbar_arrive_expect_tx(cbar, CHUNK_BYTES);
-        chunk_load(SC, &pr.tmC, cbar, pr.c_trans, m0, n0, c.b);
-      }
       if (et == 0) *epi_flag = mbar_wait(&tfull[acc], aph, abort_flag, P.status) ? 1 : 0;
-      named_bar_sync(1, 128);
+      named_bar_sync(1, EPI_THREADS);
       if (!*epi_flag) break;
       tc_fence_after();
       const int diag_col = (int)rank * TM + r;  // tile column of this row's diagonal element
+      const bool diag_mine = want_diag && ((diag_col >> 5) & 1) == half;
       float dv = 0.f;
       bool bad = false;
-      bool ok = true;
       for (int ch = 0; ch < NCHUNK; ++ch, ++gc) {
-        uint8_t* sd = SD + (gc & 1) * CHUNK_BYTES;
-        uint8_t* sm = SM + (gc & 1) * CHUNK_BYTES;
-        if (et == 0) bulk_wait_read<1>();  // the stores that last read this buffer are done
-        named_bar_sync(1, 128);
-        if (has_c) {
-          if (!mbar_wait(cbar, cph, abort_flag, P.status)) ok = false;
-          cph ^= 1u;
+        uint8_t* sd = SD + (gc % OUT_BUFS) * CHUNK_BYTES;
+        uint8_t* sm = SM + (gc % OUT_BUFS) * CHUNK_BYTES;
+        // the stores that last read these buffers are done
+        if (et == 0) {
+          if (OUT_BUFS == 2) bulk_wait_read<1>(); else bulk_wait_read<0>();
         }
-#pragma unroll 1
-        for (int h = 0; h < 2; ++h) {
-          uint32_t v[32];
-          __syncwarp();
-          tmem_ld_32x32b_x32(tmem_base + acc * TN + ch * CHUNK + h * 32 + ((uint32_t)(quarter * 32) << 16), v);
-          tmem_ld_wait();
-          float o[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) o[j] = alpha * __uint_as_float(v[j]);
-          if (has_c) {
-            if (!pr.c_trans) {
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const uint4 w = *reinterpret_cast<const uint4*>(SC + off_direct(r, h * 32 + q * 8));
-                const bf16* wv = reinterpret_cast<const bf16*>(&w);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) o[q * 8 + e] = fmaf(beta, bf16_to_f(wv[e]), o[q * 8 + e]);
-              }
-            } else {
-#pragma unroll
-              for (int j = 0; j < 32; ++j)
-                o[j] = fmaf(beta, bf16_to_f(*reinterpret_cast<const bf16*>(SC + off_trans(r, h * 32 + j))), o[j]);
-            }
-          }
-          if (pr.check_finite) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) bad |= !isfinite(o[j]);
-          }
-          if (want_diag && (diag_col >> 5) == ch * 2 + h) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (j == (diag_col & 31)) dv = o[j];
-          }
-          if (!pr.d_trans) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint4 w;
-              bf16* wv = reinterpret_cast<bf16*>(&w);
-#pragma unroll
-              for (int e = 0; e < 8; ++e) wv[e] = f_to_bf16(o[q * 8 + e]);
-              *reinterpret_cast<uint4*>(sd + off_direct(r, h * 32 + q * 8)) = w;
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) *reinterpret_cast<bf16*>(sd + off_trans(r, h * 32 + j)) = f_to_bf16(o[j]);
-          }
-          if (mirror) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) *reinterpret_cast<bf16*>(sm + off_trans(r, h * 32 + j)) = f_to_bf16(o[j]);
-          }
-        }
+        named_bar_sync(1, EPI_THREADS);
+        uint32_t v[32];
+        __syncwarp();
+        tmem_ld_32x32b_x32(tmem_base + acc * TN + ch * CHUNK + half * 32 + ((uint32_t)(quarter * 32) << 16), v);
+        tmem_ld_wait();
         if (ch == NCHUNK - 1) {
           // the accumulator has been read: release it to the leader's MMA issuer
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(acc ? tempty_leader1 : tempty_leader0);
         }
+        float o[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) o[j] = alpha * __uint_as_float(v[j]);
+        if (has_c) {
+          const uint8_t* sc = SC + ch * CHUNK_BYTES;
+          if (!mbar_wait(&cfull[ch], nc & 1u, abort_flag, P.status)) *epi_flag = 0;
+          if (!pr.c_trans) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const uint4 w = *reinterpret_cast<const uint4*>(sc + off_direct(r, half * 32 + q * 8));
+              const bf16* wv = reinterpret_cast<const bf16*>(&w);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) o[q * 8 + e] = fmaf(beta, bf16_to_f(wv[e]), o[q * 8 + e]);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              o[j] = fmaf(beta, bf16_to_f(*reinterpret_cast<const bf16*>(sc + off_trans(r, half * 32 + j))), o[j]);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&cempty[ch]);
+        }
+        if (pr.check_finite) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) bad |= !isfinite(o[j]);
+        }
+        if (diag_mine && (diag_col >> 6) == ch) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j == (diag_col & 31)) dv = o[j];
+        }
+        if (!pr.d_trans) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 w;
+            bf16* wv = reinterpret_cast<bf16*>(&w);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) wv[e] = f_to_bf16(o[q * 8 + e]);
+            *reinterpret_cast<uint4*>(sd + off_direct(r, half * 32 + q * 8)) = w;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) *reinterpret_cast<bf16*>(sd + off_trans(r, half * 32 + j)) = f_to_bf16(o[j]);
+        }
+        if (mirror) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) *reinterpret_cast<bf16*>(sm + off_trans(r, half * 32 + j)) = f_to_bf16(o[j]);
+        }
         fence_proxy_async_smem();
-        named_bar_sync(1, 128);
+        named_bar_sync(1, EPI_THREADS);
         const int col0 = n0 + ch * CHUNK;
         const bool chunk_has_diag = want_diag && (ch == 2 * (int)rank || ch == 2 * (int)rank + 1);
         if (et == 0) {
-          if (has_c && ch + 1 < NCHUNK) {
-            mbar_arrive_expect_tx(cbar, CHUNK_BYTES);
-            chunk_load(SC, &pr.tmC, cbar, pr.c_trans, m0, col0 + CHUNK, c.b);
-          }
           chunk_store(sd, &pr.tmD, pr.d_trans, m0, col0, c.b);
           if (mirror) chunk_store(sm, &pr.tmD, 1, m0, col0, c.b);
           if (pr.has_d2 && !chunk_has_diag) {
@@ -402,20 +457,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           // D2 = D + gamma I: patch the diagonal with the fp32 value plus gamma, rounded once
           // (appendix B.2.3: adding a_t I to an already rounded Z loses a_t's precision)
           if (et == 0) bulk_wait_read<0>();
-          named_bar_sync(1, 128);
-          if ((diag_col >> 6) == ch && m0 + r < pr.diag_limit)
+          named_bar_sync(1, EPI_THREADS);
+          if (diag_mine && (diag_col >> 6) == ch && m0 + r < pr.diag_limit)
             *reinterpret_cast<bf16*>(sd + off_direct(r, diag_col & 63)) = f_to_bf16(dv + pr.gamma);
           fence_proxy_async_smem();
-          named_bar_sync(1, 128);
+          named_bar_sync(1, EPI_THREADS);
           if (et == 0) {
             chunk_store(sd, &pr.tmD2, 0, m0, col0, c.b);
             bulk_commit();
           }
         }
       }
+      if (has_c) ++nc;
       if (bad) set_status(P.status, GNS_DEVST_NONFINITE);
-      if (!ok) *epi_flag = 0;
-      named_bar_sync(1, 128);
+      if (et == 0 && P.counters) {
+        // this CTA's half of the tile is in global memory: publish it to dependent tiles
+        bulk_wait_all();
+        fence_proxy_async_global();
+        red_release_gpu_add(P.counters + pr.ctr_off + c.b, 1);
+      }
+      named_bar_sync(1, EPI_THREADS);
       if (!*epi_flag) break;
     }
     if (et == 0) bulk_wait_all();
@@ -515,10 +576,11 @@ static int resident_pairs(std::string* err) {
   return clusters;
 }
 
-int gemm_launch_bf16(const GemmOp* ops, int nops, int32_t* dev_status, void* stream, std::string* err) {
+int gemm_launch_bf16(const GemmOp* ops, int nops, const uint32_t* dep_masks, int* counters, int32_t* dev_status,
+                     void* stream, std::string* err) {
   using namespace tc;
   if (nops < 1 || nops > MAX_PROB) {
-    *err = "internal: bad number of grouped products";
+    *err = "internal: bad number of products in one launch";
     return GNS_ERR_INVALID;
   }
   const int pairs_max = resident_pairs(err);
@@ -559,10 +621,28 @@ int gemm_launch_bf16(const GemmOp* ops, int nops, int32_t* dev_status, void* str
     pr.d_trans = o.d_trans;
     pr.diag_limit = (int)o.diag_limit;
     pr.check_finite = o.check_finite;
+    pr.dep_mask = dep_masks ? dep_masks[i] : 0u;
+    if (pr.dep_mask && !counters) {
+      *err = "internal: dependent products need completion counters";
+      return GNS_ERR_INVALID;
+    }
+  }
+  int off = 0;
+  for (int i = 0; i < nops; ++i) {
+    P.prob[i].ctr_off = off;
+    off += (int)ops[i].batch;
   }
   P.nprob = nops;
   P.total_tiles = tiles;
   P.status = dev_status;
+  P.counters = counters;
+  if (counters && tiles > 0) {
+    cudaError_t me = cudaMemsetAsync(counters, 0, sizeof(int) * off, static_cast<cudaStream_t>(stream));
+    if (me != cudaSuccess) {
+      *err = std::string("counter reset: ") + cudaGetErrorString(me);
+      return GNS_ERR_CUDA;
+    }
+  }
   if (tiles == 0) return GNS_OK;
   const int pairs = std::min(tiles, pairs_max);
   cudaLaunchConfig_t cfg = {};

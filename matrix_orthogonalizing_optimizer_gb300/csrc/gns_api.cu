@@ -55,6 +55,54 @@ void profile_gemm_end(void* stream) {
 
 void profile_count_launch() { ++g_prof.all; }
 
+// ---------------------------------------------------------------------------------------
+// programs of dependent GEMMs
+
+static bool op_conflict(const GemmOp& first, const GemmOp& later) {
+  const void* w1[2] = {first.D.ptr, first.D2.ptr};
+  const void* r1[3] = {first.A.ptr, first.B.ptr, first.C.ptr};
+  const void* w2[2] = {later.D.ptr, later.D2.ptr};
+  const void* r2[3] = {later.A.ptr, later.B.ptr, later.C.ptr};
+  for (const void* w : w1) {
+    if (!w) continue;
+    for (const void* r : r2)
+      if (r == w) return true;  // read after write
+    for (const void* x : w2)
+      if (x == w) return true;  // write after write
+  }
+  for (const void* r : r1) {
+    if (!r) continue;
+    for (const void* x : w2)
+      if (x == r) return true;  // write after read
+  }
+  return false;
+}
+
+int gemm_program(gns_dtype dt, const GemmOp* ops, int nops, int* counters, int32_t* dev_status, void* stream,
+                 std::string* err) {
+  if (dt != GNS_BF16) {
+    for (int i = 0; i < nops; ++i) {
+      int rc = gemm_launch(dt, ops + i, 1, dev_status, stream, err);
+      if (rc) return rc;
+    }
+    return GNS_OK;
+  }
+  for (int base = 0; base < nops; base += kMaxProgramOps) {
+    const int n = std::min(kMaxProgramOps, nops - base);
+    uint32_t masks[kMaxProgramOps];
+    for (int j = 0; j < n; ++j) {
+      masks[j] = 0;
+      for (int i = 0; i < j; ++i)
+        if (op_conflict(ops[base + i], ops[base + j])) masks[j] |= 1u << i;
+    }
+    profile_gemm_begin(stream);
+    int rc = gemm_launch_bf16(ops + base, n, masks, counters, dev_status, stream, err);
+    profile_gemm_end(stream);
+    if (rc) return rc;
+  }
+  return GNS_OK;
+}
+
 constexpr int64_t PAD = 128;  // padding of the n x n workspace matrices (tile size)
 
 // ---------------------------------------------------------------------------------------
@@ -170,6 +218,7 @@ struct Final {
 struct GramBufs {
   float* partials = nullptr;
   float* inv = nullptr;
+  int* counters = nullptr;
   MatRef R, Z, RZ, Q[2], X[2];
   int64_t np = 0;
 };
@@ -177,6 +226,7 @@ struct GramBufs {
 struct StdBufs {
   float* partials = nullptr;
   float* inv = nullptr;
+  int* counters = nullptr;
   MatRef A, Bm, X[2];
   int64_t np = 0;
 };
@@ -199,6 +249,7 @@ static void plan_gram(Arena& a, int64_t B, int64_t n, int64_t m, gns_dtype dt, c
     g->partials = static_cast<float*>(a.take(sizeof(float) * NPART * B));
     g->inv = static_cast<float*>(a.take(sizeof(float) * B));
   }
+  g->counters = static_cast<int*>(a.take(sizeof(int) * kMaxProgramOps * B));
   g->R = ws_mat(a, B, g->np, g->np, g->np, g->np, es);
   g->Z = ws_mat(a, B, g->np, g->np, g->np, g->np, es);
   g->RZ = ws_mat(a, B, g->np, g->np, g->np, g->np, es);
@@ -218,6 +269,7 @@ static void plan_std(Arena& a, int64_t B, int64_t n, int64_t m, gns_dtype dt, St
     s->partials = static_cast<float*>(a.take(sizeof(float) * NPART * B));
     s->inv = static_cast<float*>(a.take(sizeof(float) * B));
   }
+  s->counters = static_cast<int*>(a.take(sizeof(int) * kMaxProgramOps * B));
   s->A = ws_mat(a, B, s->np, s->np, s->np, s->np, es);
   s->Bm = ws_mat(a, B, s->np, s->np, s->np, s->np, es);
   s->X[0] = ws_mat(a, B, s->np, n, m, ldx, es);
@@ -252,9 +304,10 @@ static int run_gram(gns_dtype dt, const Src& src, int64_t B, int64_t n, int64_t 
                     const GramBufs& g, const float* inv, const Final& fin, int32_t* st, void* stream) {
   std::string err;
   const int64_t np = g.np;
+  std::vector<GemmOp> prog;  // the whole sequence, in program order
   auto launch = [&](const GemmOp* ops, int nops) -> int {
-    int rc = gemm_launch(dt, ops, nops, st, stream, &err);
-    return rc ? fail(rc, err) : GNS_OK;
+    for (int i = 0; i < nops; ++i) prog.push_back(ops[i]);
+    return GNS_OK;
   };
   int rc;
   Src X = src;
@@ -358,7 +411,8 @@ static int run_gram(gns_dtype dt, const Src& src, int64_t B, int64_t n, int64_t 
     o.check_finite = fin.check_finite;
     if ((rc = launch(&o, 1))) return rc;
   }
-  return GNS_OK;
+  rc = gemm_program(dt, prog.data(), (int)prog.size(), g.counters, st, stream, &err);
+  return rc ? fail(rc, err) : GNS_OK;
 }
 
 // Dion3 Algorithm 1 with symmetric products (sec. 2.3). Writes X_T to fin.D (direct mode,
@@ -367,9 +421,10 @@ static int run_std(gns_dtype dt, const Src& src, int64_t B, int64_t n, int64_t m
                    const StdBufs& s, const float* inv, const Final* fin, MatRef* result, int32_t* st, void* stream) {
   std::string err;
   const int64_t np = s.np;
+  std::vector<GemmOp> prog;  // the whole sequence, in program order
   auto launch = [&](const GemmOp* ops, int nops) -> int {
-    int rc = gemm_launch(dt, ops, nops, st, stream, &err);
-    return rc ? fail(rc, err) : GNS_OK;
+    for (int i = 0; i < nops; ++i) prog.push_back(ops[i]);
+    return GNS_OK;
   };
   int rc;
   Src X = src;
@@ -422,7 +477,8 @@ static int run_std(gns_dtype dt, const Src& src, int64_t B, int64_t n, int64_t m
     X.user = false;
     if (last && result) *result = ox.D;
   }
-  return GNS_OK;
+  rc = gemm_program(dt, prog.data(), (int)prog.size(), s.counters, st, stream, &err);
+  return rc ? fail(rc, err) : GNS_OK;
 }
 
 // ---------------------------------------------------------------------------------------
