@@ -195,6 +195,25 @@ GNS_API int gns_muon_step(const gns_batch* W, const gns_batch* G, const gns_batc
 GNS_API int gns_frac_row_select(const gns_batch* m, int k, int32_t* idx, const gns_batch* gathered, void* ws,
                         size_t ws_bytes, void* stream);
 
+/* Size of the fixed scratch array behind gns_gram_ns_batched_noalloc (64 MiB). */
+#define GNS_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+
+/* Same computation and arguments as gns_gram_ns_batched, minus the workspace, for callers
+ * that cannot allocate device memory where they orthogonalize (a framework memory pool that
+ * forbids allocations it does not own, a real-time loop that must not allocate after
+ * start-up, a plug-in handed device pointers but no allocator). The scratch comes from a
+ * fixed device array of GNS_NOALLOC_SCRATCH_BYTES compiled into the library, which every
+ * GPU that loads the library's code reserves until the process exits; this call allocates
+ * nothing. The pages have no counterpart of this entry point.
+ * Returns GNS_ERR_WORKSPACE, with the reason in gns_last_error(), when the batches need more
+ * scratch than that (gns_workspace_size(GNS_OP_GRAM_NS, ...) tells how much).
+ * The first call on a device looks up the array's device address with that device current;
+ * make that first call before any stream capture. All calls share the array: each call
+ * resets the counters that must start at zero and writes every other scratch value before
+ * reading it, and calls whose executions overlap on the GPU race on it — serialise them. */
+GNS_API int gns_gram_ns_batched_noalloc(const gns_batch* x, const gns_batch* out, int ngroups, gns_dtype dtype,
+                                        const gns_ns_params* ns, int32_t* dev_status, void* stream);
+
 /* Optional instrumentation, off by default, per calling host thread.
  * gns_profile_set(events, capacity): events points to 2*capacity cudaEvent_t handles the
  * caller created; from now on every tensor-core / fp32 GEMM launch the library enqueues is

@@ -21,12 +21,13 @@ GNS_OP_NS_STANDARD = 1
 GNS_OP_MUON_STEP = 2
 GNS_OP_FRAC_SELECT = 3
 GNS_MAX_T = 16
+GNS_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 # Every symbol include/gns.h declares.
 EXPORTS = [
     "gns_version", "gns_status_string", "gns_last_error", "gns_ns_params_default", "gns_workspace_size",
     "gns_gram_ns_batched", "gns_ns_standard_batched", "gns_sym_gemm_xxt", "gns_sym_gemm",
-    "gns_sym_poly_update", "gns_muon_step", "gns_frac_row_select", "gns_profile_set", "gns_profile_query",
+    "gns_sym_poly_update", "gns_muon_step", "gns_frac_row_select", "gns_profile_set", "gns_profile_query", "gns_gram_ns_batched_noalloc",
 ]
 
 
@@ -87,6 +88,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.gns_muon_step.argtypes = [B, B, B, i32, P(GnsMuonParams), P(GnsNsParams), vp, sz, vp, vp]
     lib.gns_frac_row_select.restype = i32
     lib.gns_frac_row_select.argtypes = [B, i32, vp, B, vp, sz, vp]
+    lib.gns_gram_ns_batched_noalloc.restype = i32
+    lib.gns_gram_ns_batched_noalloc.argtypes = [B, B, i32, i32, P(GnsNsParams), vp, vp]
     lib.gns_profile_set.restype = i32
     lib.gns_profile_set.argtypes = [P(vp), i32]
     lib.gns_profile_query.restype = i32

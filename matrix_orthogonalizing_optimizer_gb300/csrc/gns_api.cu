@@ -25,6 +25,8 @@ static int fail(int code, const std::string& msg) {
 
 static int64_t round_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
 
+int set_error(int code, const std::string& msg) { return fail(code, msg); }
+
 // ---------------------------------------------------------------------------------------
 // instrumentation (gns_profile_set / gns_profile_query)
 
