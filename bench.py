@@ -44,6 +44,19 @@ def alg_flops_per_matrix(n=ROWS, m=COLS):
     return (14 + 6 * alpha) * n ** 3
 
 
+# DRAM bytes (read + write) of one launch of the GEMM kernel from an ncu capture
+# (profiles/gemm_kernel_fused_muon_step_24x1024x4096.md), keyed by the kernel source it was
+# taken on: reported only while that source is unchanged.
+GEMM_TRAFFIC = {"4a89962bbbbe19b4": 3.329170e9}
+
+
+def gemm_traffic():
+    import hashlib
+    p = os.path.join(ROOT, "matrix_orthogonalizing_optimizer_gb300", "csrc", "gemm_tc.cu")
+    h = hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+    return GEMM_TRAFFIC.get(h)
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -263,10 +276,13 @@ def run_ours(args, rank, world, dist):
         return 0
     cpu = None
     if not args.no_cpu_baseline:
-        n_cpu = 2
-        t = time_oracle(n_cpu)
+        # whole 24-matrix steps of the oracle until at least 10 s of CPU work
+        n_cpu, t = 0, 0.0
+        while t < 10.0 and n_cpu < 20 * COUNT:
+            t += time_oracle(COUNT, seed=1 + n_cpu)
+            n_cpu += COUNT
         cpu = {"value": n_cpu / t, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-               "sample": f"{n_cpu} of the 24 matrices, full Muon step in the fp64 numpy oracle "
+               "sample": f"{n_cpu // COUNT} full 24-matrix Muon steps in the fp64 numpy oracle "
                          f"({t:.1f} s)"}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -278,7 +294,7 @@ def run_ours(args, rank, world, dist):
         "e2e": {"value": world * COUNT / (e2e_ms / 1000.0), "unit": UNIT, "h2d_bytes_per_step": bytes_step,
                 "d2h_bytes_per_step": bytes_step},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_burst, "unit": "TFLOP/s",
-                     "frac": achieved / peak_burst, "traffic": None,
+                     "frac": achieved / peak_burst, "traffic": gemm_traffic() if per_step == 1 else None,
                      "kernel": f"gns::tc::gemm_kernel (tcgen05 bf16 GEMM; {per_step} launch(es) per step carry the 17 products)",
                      "peak_kind": f"dense bf16 burst, {peak_src}",
                      "frac_of_sustained": achieved / peak_sus,
