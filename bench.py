@@ -271,6 +271,29 @@ def run_ours(args, rank, world, dist):
     e2e_ms = max_over_ranks(f0.elapsed_time(f1) / e2e_steps)
     bytes_step = COUNT * ROWS * COLS * 2
 
+    # ---- Gram NS against standard NS on the same kernels (orthogonalization only) ----
+    X = M.clone()
+    out = torch.empty_like(X)
+    ws_g = gns.alloc_workspace(gns.workspace_size(_lib.GNS_OP_GRAM_NS, X, ns), dev)
+    ws_s = gns.alloc_workspace(gns.workspace_size(_lib.GNS_OP_NS_STANDARD, X, ns), dev)
+
+    def time_ns(fn, ws_):
+        for _ in range(3):
+            fn(X, outs=[out], ns=ns, workspace=ws_, stream=stream)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = max(10, args.steps // 4)
+        a.record(stream)
+        for _ in range(reps):
+            fn(X, outs=[out], ns=ns, workspace=ws_, stream=stream)
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    gram_ms = time_ns(gns.gram_ns_batched, ws_g)
+    std_ms = time_ns(gns.ns_standard_batched, ws_s)
+    del ws_g, ws_s, X, out
+
     st = int(status.item())
     if rank != 0:
         return 0
@@ -299,6 +322,9 @@ def run_ours(args, rank, world, dist):
                      "peak_kind": f"dense bf16 burst, {peak_src}",
                      "frac_of_sustained": achieved / peak_sus,
                      "gemm_ms_per_step": gemm_ms, "gemm_launches_per_step": per_step},
+        "gram_vs_standard": {"gram_ns_ms": gram_ms, "standard_ns_ms": std_ms, "speedup": std_ms / gram_ms,
+                             "note": "orthogonalization of the 24 matrices alone, same tcgen05 kernels, T=5; "
+                                     "standard NS with symmetric products (Dion3 Algorithm 1, sec. 2.3)"},
         "gpu_launches": n_all.value,
         "device_status": st,
         "clocks": clk,
