@@ -66,6 +66,24 @@ def load_peaks():
 
 
 # ---------------------------------------------------------------------------------------
+# replicas: every rank runs the whole workload on its own GPU; no data-path collective
+
+def max_over_ranks_of(dist, x, device="cpu"):
+    """Largest value of x over the ranks (x itself without a process group)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world, units_per_rank, ms_per_step_max):
+    """Units all ranks processed per second, timed by the slowest rank."""
+    return world * units_per_rank / (ms_per_step_max / 1000.0)
+
+
+# ---------------------------------------------------------------------------------------
 # clocks during the timed region
 
 class ClockSampler:
@@ -206,11 +224,7 @@ def run_ours(args, rank, world, dist):
             dist.barrier()
 
     def max_over_ranks(x):
-        if dist is None:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return max_over_ranks_of(dist, x, dev)
 
     # ---- timed region: inputs resident in HBM ----
     clocks = ClockSampler(local)
@@ -230,7 +244,7 @@ def run_ours(args, rank, world, dist):
     n_gemm, n_all = ctypes.c_int(0), ctypes.c_int(0)
     lib.gns_profile_query(ctypes.byref(n_gemm), ctypes.byref(n_all))
     ms = max_over_ranks(e0.elapsed_time(e1) / args.steps)
-    value = world * COUNT / (ms / 1000.0)
+    value = whole_job_rate(world, COUNT, ms)
     tflops = world * COUNT * alg_flops_per_matrix() / (ms / 1000.0) / 1e12
 
     # ---- instrumented repeat: CUDA events around every GEMM launch (same stream) ----
@@ -314,7 +328,7 @@ def run_ours(args, rank, world, dist):
         "config": {"workload": WORKLOAD, "matrices": COUNT, "rows": ROWS, "cols": COLS,
                    "l2": "inputs larger than L2 (W, G, M: 604 MB per rank)", "parallelism": f"replicas x{world}"},
         "tflops": tflops, "tflops_frac_of_peak": tflops / peak_burst,
-        "e2e": {"value": world * COUNT / (e2e_ms / 1000.0), "unit": UNIT, "h2d_bytes_per_step": bytes_step,
+        "e2e": {"value": whole_job_rate(world, COUNT, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": bytes_step,
                 "d2h_bytes_per_step": bytes_step},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_burst, "unit": "TFLOP/s",
                      "frac": achieved / peak_burst, "traffic": gemm_traffic() if per_step == 1 else None,
