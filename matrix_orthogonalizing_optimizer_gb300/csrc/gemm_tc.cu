@@ -106,6 +106,28 @@ __device__ __forceinline__ bool wait_deps(const Params& P, const Problem& pr, in
   return true;
 }
 
+// Bounded wait until the scout lane has found this tile's dependencies complete (its
+// published index reaches `tile`); then order later TMA reads after that observation.
+__device__ __forceinline__ bool wait_ready(volatile int* ready, int tile, volatile int* abort_flag, int* status) {
+  if (*ready < tile) {
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 1;; ++i) {
+      if (*ready >= tile) break;
+      if ((i & 63u) == 0u) {
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > GNS_WAIT_TIMEOUT_NS) {
+          *abort_flag = 1;
+          set_status(status, GNS_DEVST_TIMEOUT);
+          return false;
+        }
+      }
+    }
+  }
+  __threadfence_block();
+  fence_proxy_async_global();
+  return true;
+}
+
 struct TileCoord {
   int p, b, I, J;
 };
@@ -190,6 +212,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cempty + NCHUNK);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* epi_flag = abort_flag + 1;
+  volatile int* ready_tile = abort_flag + 2;  // highest tile of this pair whose inputs are complete
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -212,6 +235,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     }
     *abort_flag = 0;
     *epi_flag = 1;
+    *ready_tile = -1;
     mbar_fence_init();
   }
   if (warp == 0 && lane == 0) {
@@ -241,7 +265,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         const Problem& pr = P.prob[c.p];
         const int m0 = c.I * 256 + (int)rank * TM;
         const int n0 = c.J * 256 + (int)rank * BN;
-        if (pr.dep_mask && !wait_deps(P, pr, c.b, abort_flag)) break;
+        if (pr.dep_mask && !wait_ready(ready_tile, tile, abort_flag, P.status)) break;
         for (int kb = 0; kb < pr.kblocks; ++kb) {
           if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, P.status)) {
             ok = false;
@@ -313,6 +337,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       }
     }
   } else if (warp == C_WARP) {
+    if (lane == 1) {
+      // ---------------- dependency scout (both CTAs) ----------------
+      // Walks this pair's tiles ahead of the producer and the C loader, waits (bounded) on
+      // the completion counters of the problems each tile depends on, and publishes the
+      // highest tile whose inputs are complete, so the L2 round trips of those checks stay
+      // off the producer's path.
+      for (int tile = pair; tile < P.total_tiles; tile += npairs) {
+        const TileCoord c = decode_tile(P, tile);
+        const Problem& pr = P.prob[c.p];
+        if (pr.dep_mask && !wait_deps(P, pr, c.b, abort_flag)) break;
+        __threadfence_block();
+        *ready_tile = tile;
+      }
+    }
     if (lane == 0) {
       // ---------------- C-tile loader (both CTAs) ----------------
       // Loads the C chunks of the next tile as soon as the epilogue releases each buffer,
@@ -324,7 +362,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         if (!pr.has_c) continue;
         const int m0 = c.I * 256 + (int)rank * TM;
         const int n0 = c.J * 256;
-        if (pr.dep_mask && !wait_deps(P, pr, c.b, abort_flag)) break;
+        if (pr.dep_mask && !wait_ready(ready_tile, tile, abort_flag, P.status)) break;
         bool ok = true;
         for (int ch = 0; ch < NCHUNK; ++ch) {
           if (!mbar_wait(&cempty[ch], (nc & 1u) ^ 1u, abort_flag, P.status)) {
