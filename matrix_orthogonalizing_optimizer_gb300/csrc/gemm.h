@@ -49,6 +49,11 @@ struct GemmOp {
   const int32_t* row_map = nullptr;
   int64_t row_map_stride = 0;
   int check_finite = 0;
+  // bf16 kernel only: upper_out = this symmetric product stores its upper-triangle tiles
+  // only (no mirrored copies); a_upper / b_upper = that operand is such an upper-stored
+  // symmetric matrix, read transposed wherever a K slice falls below its diagonal.
+  int upper_out = 0;
+  int a_upper = 0, b_upper = 0;
 };
 
 // Enqueues ops as ONE launch. dep_masks[i] (nullable) names earlier ops of the same launch

@@ -69,6 +69,8 @@ static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 struct Problem {
   CUtensorMap tmA;
   CUtensorMap tmB;
+  CUtensorMap tmA2;  // the other major-ness of A / B (upper-stored symmetric operands)
+  CUtensorMap tmB2;
   CUtensorMap tmC;
   CUtensorMap tmD;
   CUtensorMap tmD2;
@@ -82,6 +84,7 @@ struct Problem {
   int has_c, c_trans, d_trans, has_d2;
   int diag_limit;
   int check_finite;
+  int a_upper, b_upper, mirror_out;
   uint32_t dep_mask;  // earlier problems whose tiles of the same matrix must be complete
   int ctr_off;        // this problem's completion counters: counters[ctr_off + b]
 };
@@ -131,6 +134,21 @@ __device__ __forceinline__ bool wait_ready(volatile int* ready, int tile, volati
 struct TileCoord {
   int p, b, I, J;
 };
+
+// Major-ness of the A (B) slice of 64-wide K block kb for tile row I (column J). An operand
+// that is the upper triangle of a symmetric matrix (256-blocks at or above the diagonal) is
+// read from the mirrored block, with the other major-ness, wherever the block it would read
+// lies below the diagonal.
+__device__ __forceinline__ int a_major(const Problem& pr, int I, int kb) {
+  const int kbl = kb >> 2;
+  const bool lower = pr.a_mn ? (kbl > I) : (I > kbl);
+  return pr.a_mn ^ ((pr.a_upper && lower) ? 1 : 0);
+}
+__device__ __forceinline__ int b_major(const Problem& pr, int J, int kb) {
+  const int kbl = kb >> 2;
+  const bool lower = pr.b_mn ? (kbl > J) : (J > kbl);
+  return pr.b_mn ^ ((pr.b_upper && lower) ? 1 : 0);
+}
 
 __device__ __forceinline__ TileCoord decode_tile(const Params& P, int tile) {
   TileCoord tc;
@@ -276,17 +294,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           uint8_t* sa = stages + s * STAGE_BYTES;
           uint8_t* sb = sa + A_BYTES;
           const int k0 = kb * TK;
-          if (!pr.a_mn) {
-            tma_load_3d_pair(sa, &pr.tmA, fb, k0, m0, c.b);
+          const int amn = a_major(pr, c.I, kb), bmn = b_major(pr, c.J, kb);
+          const CUtensorMap* ma = amn == pr.a_mn ? &pr.tmA : &pr.tmA2;
+          const CUtensorMap* mb = bmn == pr.b_mn ? &pr.tmB : &pr.tmB2;
+          if (!amn) {
+            tma_load_3d_pair(sa, ma, fb, k0, m0, c.b);
           } else {
-            tma_load_3d_pair(sa, &pr.tmA, fb, m0, k0, c.b);
-            tma_load_3d_pair(sa + BOX_BYTES, &pr.tmA, fb, m0 + 64, k0, c.b);
+            tma_load_3d_pair(sa, ma, fb, m0, k0, c.b);
+            tma_load_3d_pair(sa + BOX_BYTES, ma, fb, m0 + 64, k0, c.b);
           }
-          if (!pr.b_mn) {
-            tma_load_3d_pair(sb, &pr.tmB, fb, k0, n0, c.b);
+          if (!bmn) {
+            tma_load_3d_pair(sb, mb, fb, k0, n0, c.b);
           } else {
-            tma_load_3d_pair(sb, &pr.tmB, fb, n0, k0, c.b);
-            tma_load_3d_pair(sb + BOX_BYTES, &pr.tmB, fb, n0 + 64, k0, c.b);
+            tma_load_3d_pair(sb, mb, fb, n0, k0, c.b);
+            tma_load_3d_pair(sb + BOX_BYTES, mb, fb, n0 + 64, k0, c.b);
           }
           if (++s == STAGES) {
             s = 0;
@@ -310,8 +331,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, P.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * TN;
-        const uint32_t idesc = idesc_bf16_f32(2 * TM, TN, pr.a_mn, pr.b_mn);
         for (int kb = 0; kb < pr.kblocks; ++kb) {
+          const int amn = a_major(pr, c.I, kb), bmn = b_major(pr, c.J, kb);
+          const uint32_t idesc = idesc_bf16_f32(2 * TM, TN, amn, bmn);
           if (!mbar_wait(&full[s], ph, abort_flag, P.status)) {
             ok = false;
             break;
@@ -322,9 +344,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
           for (int kk = 0; kk < TK / 16; ++kk) {
             const uint64_t ad =
-                pr.a_mn ? sdesc_sw128(sa + kk * 2048, BOX_BYTES, 1024) : sdesc_sw128(sa + kk * 32, 16, 1024);
+                amn ? sdesc_sw128(sa + kk * 2048, BOX_BYTES, 1024) : sdesc_sw128(sa + kk * 32, 16, 1024);
             const uint64_t bd =
-                pr.b_mn ? sdesc_sw128(sb + kk * 2048, BOX_BYTES, 1024) : sdesc_sw128(sb + kk * 32, 16, 1024);
+                bmn ? sdesc_sw128(sb + kk * 2048, BOX_BYTES, 1024) : sdesc_sw128(sb + kk * 32, 16, 1024);
             umma2_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
           umma2_commit_multicast(&empty[s], 0x3);
@@ -400,7 +422,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         beta *= powi(sc, pr.beta_pow);
       }
       const bool has_c = pr.has_c != 0;
-      const bool mirror = pr.sym && c.I != c.J;
+      const bool mirror = pr.sym && c.I != c.J && pr.mirror_out;
       const bool want_diag = pr.has_d2 && c.I == c.J;
       const int m0 = c.I * 256 + (int)rank * TM;  // first row of this CTA's half
       const int n0 = c.J * 256;
@@ -635,6 +657,11 @@ int gemm_launch_bf16(const GemmOp* ops, int nops, const uint32_t* dep_masks, int
     Problem& pr = P.prob[i];
     if (!encode_map(&pr.tmA, o.A, o.batch, o.a_mn ? 64 : 128, err)) return GNS_ERR_CUDA;
     if (!encode_map(&pr.tmB, o.B, o.batch, o.b_mn ? 64 : 128, err)) return GNS_ERR_CUDA;
+    pr.a_upper = o.a_upper;
+    pr.b_upper = o.b_upper;
+    pr.mirror_out = o.upper_out ? 0 : 1;
+    if (o.a_upper && !encode_map(&pr.tmA2, o.A, o.batch, o.a_mn ? 128 : 64, err)) return GNS_ERR_CUDA;
+    if (o.b_upper && !encode_map(&pr.tmB2, o.B, o.batch, o.b_mn ? 128 : 64, err)) return GNS_ERR_CUDA;
     pr.has_c = o.C.ptr != nullptr && o.beta != 0.f;
     if (pr.has_c && !encode_map(&pr.tmC, o.C, o.batch, 64, err)) return GNS_ERR_CUDA;
     if (!encode_map(&pr.tmD, o.D, o.batch, 64, err)) return GNS_ERR_CUDA;

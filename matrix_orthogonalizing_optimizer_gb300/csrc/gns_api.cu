@@ -89,6 +89,21 @@ int gemm_program(gns_dtype dt, const GemmOp* ops, int nops, int* counters, int32
     }
     return GNS_OK;
   }
+  // upper-stored symmetric buffers: what a product with upper_out wrote
+  std::vector<GemmOp> prog(ops, ops + nops);
+  std::vector<const void*> upper;
+  for (int j = 0; j < nops; ++j) {
+    GemmOp& o = prog[j];
+    for (const void* u : upper) {
+      if (o.A.ptr == u) o.a_upper = 1;
+      if (o.B.ptr == u) o.b_upper = 1;
+    }
+    if (o.upper_out && o.sym) {
+      upper.push_back(o.D.ptr);
+      if (o.D2.ptr) upper.push_back(o.D2.ptr);
+    }
+  }
+  ops = prog.data();
   for (int base = 0; base < nops; base += kMaxProgramOps) {
     const int n = std::min(kMaxProgramOps, nops - base);
     uint32_t masks[kMaxProgramOps];
@@ -413,6 +428,7 @@ static int run_gram(gns_dtype dt, const Src& src, int64_t B, int64_t n, int64_t 
     o.check_finite = fin.check_finite;
     if ((rc = launch(&o, 1))) return rc;
   }
+  for (GemmOp& o : prog) o.upper_out = o.sym;  // internal symmetric buffers: upper tiles only
   rc = gemm_program(dt, prog.data(), (int)prog.size(), g.counters, st, stream, &err);
   return rc ? fail(rc, err) : GNS_OK;
 }
@@ -479,6 +495,7 @@ static int run_std(gns_dtype dt, const Src& src, int64_t B, int64_t n, int64_t m
     X.user = false;
     if (last && result) *result = ox.D;
   }
+  for (GemmOp& o : prog) o.upper_out = o.sym;  // internal symmetric buffers: upper tiles only
   rc = gemm_program(dt, prog.data(), (int)prog.size(), s.counters, st, stream, &err);
   return rc ? fail(rc, err) : GNS_OK;
 }
