@@ -43,8 +43,12 @@ constexpr int TK = 64;                           // K slice per stage
 #ifndef GNS_TC_OUTBUFS
 #define GNS_TC_OUTBUFS 1
 #endif
+#ifndef GNS_TC_CBUFS
+#define GNS_TC_CBUFS 4
+#endif
 constexpr int STAGES = GNS_TC_STAGES;
 constexpr int OUT_BUFS = GNS_TC_OUTBUFS;         // staging buffers for output (and mirror) chunks
+constexpr int C_BUFS = GNS_TC_CBUFS;             // ring of C-chunk buffers
 constexpr int A_BYTES = TM * TK * 2;             // 16 KiB
 constexpr int STAGE_BYTES = (TM + BN) * TK * 2;  // 32 KiB per CTA
 constexpr int CHUNK = 64;                        // epilogue columns per chunk
@@ -58,8 +62,8 @@ constexpr int EPI_THREADS = 32 * EPI_WARPS;
 constexpr int NUM_THREADS = 32 * (FIRST_EPI_WARP + EPI_WARPS);
 constexpr int MAX_PROB = 24;                     // stages of one launch
 constexpr int TMEM_COLS = 512;                   // two 256-column fp32 accumulators
-constexpr int OFF_SC = STAGES * STAGE_BYTES;     // C tile (NCHUNK chunks)
-constexpr int OFF_SD = OFF_SC + NCHUNK * CHUNK_BYTES;
+constexpr int OFF_SC = STAGES * STAGE_BYTES;     // C chunks (ring of C_BUFS)
+constexpr int OFF_SD = OFF_SC + C_BUFS * CHUNK_BYTES;
 constexpr int OFF_SM = OFF_SD + OUT_BUFS * CHUNK_BYTES;
 constexpr int OFF_BAR = OFF_SM + OUT_BUFS * CHUNK_BYTES;
 constexpr int BAR_BYTES = 512;
@@ -226,8 +230,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   uint64_t* tfull = bars + 2 * STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* cfull = tempty + 2;
-  uint64_t* cempty = cfull + NCHUNK;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cempty + NCHUNK);
+  uint64_t* cempty = cfull + C_BUFS;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cempty + C_BUFS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* epi_flag = abort_flag + 1;
   volatile int* ready_tile = abort_flag + 2;  // highest tile of this pair whose inputs are complete
@@ -247,9 +251,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       mbar_init(&tfull[a], 1);
       mbar_init(&tempty[a], 2 * EPI_WARPS);  // one arrival per epilogue warp of both CTAs
     }
-    for (int ch = 0; ch < NCHUNK; ++ch) {
-      mbar_init(&cfull[ch], 1);
-      mbar_init(&cempty[ch], EPI_WARPS);
+    for (int q = 0; q < C_BUFS; ++q) {
+      mbar_init(&cfull[q], 1);
+      mbar_init(&cempty[q], EPI_WARPS);
     }
     *abort_flag = 0;
     *epi_flag = 1;
@@ -377,7 +381,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       // ---------------- C-tile loader (both CTAs) ----------------
       // Loads the C chunks of the next tile as soon as the epilogue releases each buffer,
       // a whole main loop ahead of their use.
-      uint32_t nc = 0;
+      uint32_t qc = 0;  // C chunks loaded so far (ring slot and phase)
       for (int tile = pair; tile < P.total_tiles; tile += npairs) {
         const TileCoord c = decode_tile(P, tile);
         const Problem& pr = P.prob[c.p];
@@ -386,16 +390,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         const int n0 = c.J * 256;
         if (pr.dep_mask && !wait_ready(ready_tile, tile, abort_flag, P.status)) break;
         bool ok = true;
-        for (int ch = 0; ch < NCHUNK; ++ch) {
-          if (!mbar_wait(&cempty[ch], (nc & 1u) ^ 1u, abort_flag, P.status)) {
+        for (int ch = 0; ch < NCHUNK; ++ch, ++qc) {
+          const uint32_t q = qc % C_BUFS;
+          if (!mbar_wait(&cempty[q], ((qc / C_BUFS) & 1u) ^ 1u, abort_flag, P.status)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&cfull[ch], CHUNK_BYTES);
-          chunk_load(SC + ch * CHUNK_BYTES, &pr.tmC, &cfull[ch], pr.c_trans, m0, n0 + ch * CHUNK, c.b);
+          mbar_arrive_expect_tx(&cfull[q], CHUNK_BYTES);
+          chunk_load(SC + q * CHUNK_BYTES, &pr.tmC, &cfull[q], pr.c_trans, m0, n0 + ch * CHUNK, c.b);
         }
         if (!ok) break;
-        ++nc;
       }
     }
   } else {
@@ -407,7 +411,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     const int r = quarter * 32 + lane;
     const uint32_t tempty_leader0 = mapa_shared(smem_u32(&tempty[0]), 0);
     const uint32_t tempty_leader1 = mapa_shared(smem_u32(&tempty[1]), 0);
-    uint32_t nc = 0;  // C tiles consumed (parity of the C-chunk barriers)
+    uint32_t qc = 0;  // C chunks consumed so far (ring slot and phase)
     uint32_t gc = 0;  // chunks stored so far (output staging buffers)
     int local = 0;
     for (int tile = pair; tile < P.total_tiles; tile += npairs, ++local) {
@@ -456,8 +460,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
         for (int j = 0; j < 32; ++j) o[j] = alpha * __uint_as_float(v[j]);
         if (has_c) {
-          const uint8_t* sc = SC + ch * CHUNK_BYTES;
-          if (!mbar_wait(&cfull[ch], nc & 1u, abort_flag, P.status)) *epi_flag = 0;
+          const uint32_t q = qc % C_BUFS;
+          const uint8_t* sc = SC + q * CHUNK_BYTES;
+          if (!mbar_wait(&cfull[q], (qc / C_BUFS) & 1u, abort_flag, P.status)) *epi_flag = 0;
           if (!pr.c_trans) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -472,7 +477,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
               o[j] = fmaf(beta, bf16_to_f(*reinterpret_cast<const bf16*>(sc + off_trans(r, half * 32 + j))), o[j]);
           }
           __syncwarp();
-          if (lane == 0) mbar_arrive(&cempty[ch]);
+          if (lane == 0) mbar_arrive(&cempty[q]);
+          ++qc;
         }
         if (pr.check_finite) {
 #pragma unroll
@@ -528,7 +534,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           }
         }
       }
-      if (has_c) ++nc;
       if (bad) set_status(P.status, GNS_DEVST_NONFINITE);
       if (et == 0 && P.counters) {
         // this CTA's half of the tile is in global memory: publish it to dependent tiles
