@@ -18,13 +18,22 @@
  *   - Dion3 update rule (Dion3 sec. 6, Algorithm 4, Muon flavour): M <- M + G; S = the
  *     k = ceil(f n) rows of largest l1 norm; W <- (1 - eta wd) W; W[S] -= eta polar(M[S]);
  *     M[S] <- mu M[S].
+ *   - NorMuon (Dion3 sec. 2.1 eq. (2), Algorithm 4 lines 5-7): a per-row second moment
+ *     v_i <- beta2 v_i + (1 - beta2) mean_j O_ij^2 of the orthogonalized update, rows divided
+ *     by sqrt(v_i) + eps, the result rescaled to the Frobenius norm of O; fp32 arithmetic.
+ *   - RowNorm and Periodic Row-wise Muon (Scaling Muon for Diffusion Transformers, sec. 3.1
+ *     eq. (5), sec. 3.2 eq. (7)): R_eps(X)_i = X_i / max(||X_i||_2, eps) on the oriented
+ *     momentum, scaled by gamma, used on the steps t with t mod K != 0; Newton-Schulz on the
+ *     others.
+ *   - Safety factor (Dion3 appendix B.2.2): every polynomial replaced by p_t(x / s), i.e.
+ *     (a, b, c) -> (a / s, b / s^3, c / s^5).
  *
  * Conventions shared by every entry point:
  *   Matrices. A gns_batch describes `count` row-major matrices of one shape at a constant
  *     element stride (a "megabatch": Dion3 sec. 7 groups all same-shape matrices into one
  *     batch). All pointers are DEVICE addresses owned by the caller; the library never
  *     allocates or frees device memory. ptr must be 16-byte aligned; ld and stride must be
- *     multiples of 8 elements (16 bytes) for bf16 and of 4 elements for fp32; ld >= cols,
+ *     multiples of 8 elements (16 bytes) for bf16 / fp16 and of 4 elements for fp32; ld >= cols,
  *     stride >= rows * ld (stride is ignored when count == 1).
  *   Orientation. A matrix with rows > cols is orthogonalized through its transpose and the
  *     result is mapped back (Dion3 Algorithm 1 assumes n <= m); no transposed copy is made.
@@ -71,7 +80,9 @@ typedef enum {
 
 typedef enum {
   GNS_BF16 = 0, /* bf16 storage, tensor-core products with fp32 accumulation (hot path) */
-  GNS_F32 = 1   /* fp32 storage and fp32 arithmetic (validation path) */
+  GNS_F32 = 1,  /* fp32 storage and fp32 arithmetic (validation path) */
+  GNS_F16 = 2   /* fp16 storage, tensor-core products with fp32 accumulation (Dion3 Algorithm 3
+                   line 3 casts to float16; appendix B.2.2 prefers it to bfloat16) */
 } gns_dtype;
 
 /* `count` row-major matrices: element (b, i, j) at ptr + b*stride + i*ld + j (elements). */
@@ -85,8 +96,12 @@ typedef struct {
 } gns_batch;
 
 /* Newton-Schulz schedule: T iterations with coefficients (a_t, b_t, c_t), t = 1..T
- * (index t-1). Bit i of restart_mask (1 <= i < T) restarts after iteration i (Dion3
- * Algorithm 3 restarts after iteration 2: mask 1u << 2). eps as in Algorithm 1 line 2. */
+ * (index t-1), e.g. a caller's Polar Express table. Bit i of restart_mask (1 <= i < T)
+ * restarts after iteration i (Dion3 Algorithm 3 restarts after iteration 2: mask 1u << 2).
+ * eps as in Algorithm 1 line 2. safety = s > 0 applies the safety factor of Dion3 appendix
+ * B.2.2 to every iteration: p_t(x) becomes p_t(x / s), so (a, b, c) is used as
+ * (a / s, b / s^3, c / s^5); s = 1 leaves the table as given (the pages' conservative choice
+ * for Polar Express coefficients is s = 1.05). */
 typedef struct {
   int32_t T;
   float a[GNS_MAX_T];
@@ -94,17 +109,44 @@ typedef struct {
   float c[GNS_MAX_T];
   uint32_t restart_mask;
   float eps;
+  float safety;
 } gns_ns_params;
 
-/* Muon step hyper-parameters. frac = 1: dense Muon (eq. (1)); 0 < frac < 1: Dion3
- * fractional update (Algorithm 4) with k = ceil(frac * n) selected rows. The weight update
- * is W <- (1 - lr*weight_decay) W - lr*scale*O, fp32 arithmetic and one bf16 rounding. */
+/* Update flavours of gns_muon_step. */
+typedef enum {
+  GNS_FLAVOR_MUON = 0,     /* O = polar(M) (Dion3 eq. (1); Algorithm 4 Muon flavour) */
+  GNS_FLAVOR_NORMUON = 1,  /* O = NorMuon-normalised polar(M) (Dion3 eq. (2); Algorithm 4 l. 5-7) */
+  GNS_FLAVOR_ROWNORM = 2,  /* O = gamma R_eps(M) (Scaling Muon for DiTs eq. (5)); dense only */
+  GNS_FLAVOR_PERIODIC = 3  /* Periodic Row-wise Muon (ibid. eq. (7)): MUON when step % period
+                              == 0, else ROWNORM; dense only */
+} gns_flavor;
+
+/* Muon step hyper-parameters. frac = 1: dense step; 0 < frac < 1: Dion3 fractional update
+ * (Algorithm 4) with k = ceil(frac * n) selected rows. The weight update is
+ * W <- (1 - lr*weight_decay) W - lr*scale*O, fp32 arithmetic and one bf16 rounding.
+ * Fields after `frac` may be left zero: flavour MUON, Newton-Schulz in bf16.
+ *   flavor        gns_flavor.
+ *   ns_dtype      GNS_BF16 or GNS_F16: storage type of the Newton-Schulz products (W, G, M
+ *                 stay bf16; with GNS_F16 the normalised momentum is rounded to fp16 once,
+ *                 Dion3 Algorithm 3 line 3).
+ *   beta2         NorMuon second-moment decay, in [0, 1).
+ *   norm_eps      NorMuon: added to sqrt(v_i) (> 0). RowNorm: lower bound of a row norm
+ *                 (> 0).
+ *   rownorm_gamma RowNorm multiplier gamma (> 0; the page uses 0.15).
+ *   period, step  Periodic Row-wise Muon: K >= 1 (the page uses 3) and the step index t. */
 typedef struct {
   float lr;
   float momentum;
   float weight_decay;
   float scale;
   float frac;
+  int32_t flavor;
+  int32_t ns_dtype;
+  float beta2;
+  float norm_eps;
+  float rownorm_gamma;
+  int32_t period;
+  int32_t step;
 } gns_muon_params;
 
 typedef enum {
@@ -126,7 +168,7 @@ GNS_API int gns_last_error(char* buf, size_t len);
 
 /* Fills *p with the default schedule: T = 5, fixed quintic (a, b, c) = (3.4445, -4.7750,
  * 2.0315) every iteration (Scaling Muon for Diffusion Transformers, appendix D.3), restart
- * after iteration 2 (Dion3 Algorithm 3), eps = 1e-7 (Dion3 Algorithm 1 line 2). */
+ * after iteration 2 (Dion3 Algorithm 3), eps = 1e-7 (Dion3 Algorithm 1 line 2), safety 1. */
 GNS_API void gns_ns_params_default(gns_ns_params* p);
 
 /* Bytes of workspace `op` needs for these batches (the same arguments as the call).
@@ -176,16 +218,22 @@ GNS_API int gns_sym_poly_update(const gns_batch* R, const gns_batch* Q, const gn
                         const gns_batch* q_scratch, float a, float b, float c, int q_is_identity, int skip_r,
                         gns_dtype dtype, int32_t* dev_status, void* stream);
 
-/* One Muon step on ngroups bf16 batches (W, G, M of equal shapes per group):
+/* One optimizer step on ngroups bf16 batches (W, G, M of equal shapes per group):
  *   frac == 1: M <- mu M + G (fp32 arithmetic, bf16 store); O = Gram NS of M (oriented);
- *              W <- (1 - lr wd) W - lr scale O in the final product's epilogue.
+ *              W <- (1 - lr wd) W - lr scale O (in the final product's epilogue for the
+ *              Muon flavour).
  *   frac <  1: Dion3 Algorithm 4: M <- M + G; S = top-k rows (columns when rows > cols) by
  *              exact l1 norm, ties to the lower index; O = Gram NS of M[S]; W <- (1 - lr wd) W;
  *              W[S] -= lr scale O; M[S] <- mu M[S].
- * dtype must be GNS_BF16. W, G, M may not alias. */
-GNS_API int gns_muon_step(const gns_batch* W, const gns_batch* G, const gns_batch* M, int ngroups,
-                  const gns_muon_params* muon, const gns_ns_params* ns, void* ws, size_t ws_bytes,
-                  int32_t* dev_status, void* stream);
+ * Flavours (muon->flavor): NORMUON replaces O by the NorMuon update (eq. (2)) with the
+ * second moments of the oriented rows in V; ROWNORM (and PERIODIC off its refresh steps)
+ * replaces the Newton-Schulz of the dense step by O = gamma R_eps(M) of the oriented M.
+ * V: NULL unless the flavour is NORMUON; then per group an fp32 batch of count x 1 x n,
+ * n = min(rows, cols) (ld >= n, a multiple of 4), updated in place (row i of the oriented M;
+ * for frac < 1 only the selected rows). W, G, M, V may not alias. */
+GNS_API int gns_muon_step(const gns_batch* W, const gns_batch* G, const gns_batch* M, const gns_batch* V,
+                  int ngroups, const gns_muon_params* muon, const gns_ns_params* ns, void* ws,
+                  size_t ws_bytes, int32_t* dev_status, void* stream);
 
 /* Selection step of Dion3 Algorithm 4 (line 3) for one bf16 batch m: per matrix, the
  * k rows (columns when rows > cols) of largest exact l1 norm, ties to the lower index,

@@ -7,6 +7,7 @@ Importing the package does not load the library: the first API call does, and fa
 loudly when it has not been built.
 """
 from .api import (  # noqa: F401
+    MuonParams,
     NsParams,
     QUINTIC_FIXED,
     alloc_workspace,
@@ -24,6 +25,6 @@ from .api import (  # noqa: F401
 )
 
 __all__ = [
-    "NsParams", "QUINTIC_FIXED", "alloc_workspace", "batch_of", "empty_padded", "frac_k", "frac_row_select", "gram_ns_batched",
+    "MuonParams", "NsParams", "QUINTIC_FIXED", "alloc_workspace", "batch_of", "empty_padded", "frac_k", "frac_row_select", "gram_ns_batched",
     "muon_step", "ns_standard_batched", "sym_gemm", "sym_gemm_xxt", "sym_poly_update", "workspace_size",
 ]

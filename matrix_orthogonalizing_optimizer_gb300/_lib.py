@@ -16,6 +16,11 @@ GNS_DEVST_NONFINITE = 1
 GNS_DEVST_TIMEOUT = 2
 GNS_BF16 = 0
 GNS_F32 = 1
+GNS_F16 = 2
+GNS_FLAVOR_MUON = 0
+GNS_FLAVOR_NORMUON = 1
+GNS_FLAVOR_ROWNORM = 2
+GNS_FLAVOR_PERIODIC = 3
 GNS_OP_GRAM_NS = 0
 GNS_OP_NS_STANDARD = 1
 GNS_OP_MUON_STEP = 2
@@ -38,12 +43,15 @@ class GnsBatch(ctypes.Structure):
 
 class GnsNsParams(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int32), ("a", ctypes.c_float * GNS_MAX_T), ("b", ctypes.c_float * GNS_MAX_T),
-                ("c", ctypes.c_float * GNS_MAX_T), ("restart_mask", ctypes.c_uint32), ("eps", ctypes.c_float)]
+                ("c", ctypes.c_float * GNS_MAX_T), ("restart_mask", ctypes.c_uint32), ("eps", ctypes.c_float),
+                ("safety", ctypes.c_float)]
 
 
 class GnsMuonParams(ctypes.Structure):
     _fields_ = [("lr", ctypes.c_float), ("momentum", ctypes.c_float), ("weight_decay", ctypes.c_float),
-                ("scale", ctypes.c_float), ("frac", ctypes.c_float)]
+                ("scale", ctypes.c_float), ("frac", ctypes.c_float), ("flavor", ctypes.c_int32),
+                ("ns_dtype", ctypes.c_int32), ("beta2", ctypes.c_float), ("norm_eps", ctypes.c_float),
+                ("rownorm_gamma", ctypes.c_float), ("period", ctypes.c_int32), ("step", ctypes.c_int32)]
 
 
 _lib = None
@@ -85,7 +93,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.gns_sym_poly_update.restype = i32
     lib.gns_sym_poly_update.argtypes = [B, B, B, B, B, f32, f32, f32, i32, i32, i32, vp, vp]
     lib.gns_muon_step.restype = i32
-    lib.gns_muon_step.argtypes = [B, B, B, i32, P(GnsMuonParams), P(GnsNsParams), vp, sz, vp, vp]
+    lib.gns_muon_step.argtypes = [B, B, B, B, i32, P(GnsMuonParams), P(GnsNsParams), vp, sz, vp, vp]
     lib.gns_frac_row_select.restype = i32
     lib.gns_frac_row_select.argtypes = [B, i32, vp, B, vp, sz, vp]
     lib.gns_gram_ns_batched_noalloc.restype = i32

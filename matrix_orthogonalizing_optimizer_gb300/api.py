@@ -1,10 +1,10 @@
 """Python API over libgns with the C ABI's names. PyTorch supplies device memory and the
 stream; every step of the computation runs in the library's CUDA kernels.
 
-Tensors are CUDA tensors of dtype bfloat16 (hot path) or float32 (validation path), 2-D
-(one matrix) or 3-D (a batch of same-shape matrices, the megabatch of Dion3 sec. 7), with a
-contiguous last dimension, 16-byte aligned rows (ld a multiple of 16 bytes) and 16-byte
-aligned storage.
+Tensors are CUDA tensors of dtype bfloat16 (hot path), float16 (Dion3 Algorithm 3's
+float16 products) or float32 (validation path), 2-D (one matrix) or 3-D (a batch of
+same-shape matrices, the megabatch of Dion3 sec. 7), with a contiguous last dimension,
+16-byte aligned rows (ld a multiple of 16 bytes) and 16-byte aligned storage.
 """
 from __future__ import annotations
 
@@ -25,10 +25,13 @@ QUINTIC_FIXED = ((3.4445, -4.7750, 2.0315),) * 5
 @dataclass
 class NsParams:
     """Newton-Schulz schedule (T = len(coeffs)); restarts = iterations after which Gram NS
-    restarts (Dion3 Algorithm 3: after iteration 2)."""
+    restarts (Dion3 Algorithm 3: after iteration 2); safety = s runs every polynomial as
+    p_t(x / s) (Dion3 appendix B.2.2; 1.05 is the pages' conservative choice for a Polar
+    Express table, 1 leaves the coefficients as given)."""
     coeffs: Sequence = QUINTIC_FIXED
     restarts: Sequence[int] = (2,)
     eps: float = 1e-7
+    safety: float = 1.0
 
     def c_struct(self) -> GnsNsParams:
         p = GnsNsParams()
@@ -42,15 +45,52 @@ class NsParams:
             mask |= 1 << int(r)
         p.restart_mask = mask
         p.eps = float(self.eps)
+        p.safety = float(self.safety)
         return p
 
 
 def _dtype_code(t: torch.Tensor) -> int:
     if t.dtype == torch.bfloat16:
         return _lib.GNS_BF16
+    if t.dtype == torch.float16:
+        return _lib.GNS_F16
     if t.dtype == torch.float32:
         return _lib.GNS_F32
-    raise TypeError(f"unsupported dtype {t.dtype}: bfloat16 or float32")
+    raise TypeError(f"unsupported dtype {t.dtype}: bfloat16, float16 or float32")
+
+
+_FLAVORS = {"muon": _lib.GNS_FLAVOR_MUON, "normuon": _lib.GNS_FLAVOR_NORMUON, "rownorm": _lib.GNS_FLAVOR_ROWNORM,
+            "periodic": _lib.GNS_FLAVOR_PERIODIC}
+
+
+@dataclass
+class MuonParams:
+    """Hyper-parameters of one optimizer step (gns_muon_params). flavor: "muon" (Dion3 eq.
+    (1)), "normuon" (eq. (2)), "rownorm" (Scaling Muon for DiTs eq. (5)) or "periodic"
+    (ibid. eq. (7): Newton-Schulz when step % period == 0, RowNorm otherwise). ns_dtype:
+    torch.bfloat16 or torch.float16, the storage type of the Newton-Schulz products."""
+    lr: float
+    momentum: float = 0.95
+    weight_decay: float = 0.0
+    scale: float = 1.0
+    frac: float = 1.0
+    flavor: str = "muon"
+    ns_dtype: torch.dtype = torch.bfloat16
+    beta2: float = 0.95
+    norm_eps: float = 1e-8
+    rownorm_gamma: float = 0.15
+    period: int = 3
+    step: int = 0
+
+    def c_struct(self) -> GnsMuonParams:
+        if self.flavor not in _FLAVORS:
+            raise ValueError(f"flavor must be one of {sorted(_FLAVORS)}")
+        if self.ns_dtype not in (torch.bfloat16, torch.float16):
+            raise ValueError("ns_dtype must be torch.bfloat16 or torch.float16")
+        return GnsMuonParams(float(self.lr), float(self.momentum), float(self.weight_decay), float(self.scale),
+                             float(self.frac), _FLAVORS[self.flavor],
+                             _lib.GNS_F16 if self.ns_dtype == torch.float16 else _lib.GNS_BF16, float(self.beta2),
+                             float(self.norm_eps), float(self.rownorm_gamma), int(self.period), int(self.step))
 
 
 def batch_of(t: torch.Tensor) -> GnsBatch:
@@ -98,12 +138,13 @@ def _as_list(x) -> List[torch.Tensor]:
     return [x] if isinstance(x, torch.Tensor) else list(x)
 
 
-def workspace_size(op: int, xs, ns: Optional[NsParams] = None, frac: float = 1.0, dtype=None) -> int:
+def workspace_size(op: int, xs, ns: Optional[NsParams] = None, frac: float = 1.0, dtype=None,
+                   muon: Optional[MuonParams] = None) -> int:
     xs = _as_list(xs)
     arr, _ = _batches(xs)
     dt = _dtype_code(xs[0]) if dtype is None else dtype
     nsp = (ns or NsParams()).c_struct()
-    mp = GnsMuonParams(0.0, 0.0, 0.0, 1.0, float(frac))
+    mp = muon.c_struct() if muon is not None else GnsMuonParams(0.0, 0.0, 0.0, 1.0, float(frac))
     n = load().gns_workspace_size(op, arr, len(xs), dt, ctypes.byref(nsp), ctypes.byref(mp))
     if n == 0:
         raise _lib.GnsError(f"workspace_size: {_lib.last_error()}")
@@ -179,20 +220,31 @@ def sym_poly_update(R, Q, Z, RZ, q_scratch, a: float, b: float, c: float, q_is_i
     check(rc, "gns_sym_poly_update")
 
 
-def muon_step(W, G, M, lr: float, momentum: float = 0.95, weight_decay: float = 0.0, scale: float = 1.0,
-              frac: float = 1.0, ns: Optional[NsParams] = None, workspace=None, status=None, stream=None):
-    """One Muon step (frac = 1) or Dion3 fractional update (frac < 1), in place on W and M."""
+def muon_step(W, G, M, lr: Optional[float] = None, momentum: float = 0.95, weight_decay: float = 0.0, scale: float = 1.0,
+              frac: float = 1.0, ns: Optional[NsParams] = None, workspace=None, status=None, stream=None,
+              V=None, params: Optional[MuonParams] = None):
+    """One optimizer step in place on W and M (and V): Muon (frac = 1), the Dion3 fractional
+    update (frac < 1), or the flavour named in `params` (which then supplies every
+    hyper-parameter). V: NorMuon second moments, fp32 tensors (count, 1, min(rows, cols)) or
+    (1, min(rows, cols)) per group."""
     Ws, Gs, Ms = _as_list(W), _as_list(G), _as_list(M)
     ns = ns or NsParams()
-    need = workspace_size(_lib.GNS_OP_MUON_STEP, Ms, ns, frac=frac)
+    if params is None:
+        if lr is None:
+            raise ValueError("muon_step needs lr (or params)")
+        params = MuonParams(lr=lr, momentum=momentum, weight_decay=weight_decay, scale=scale, frac=frac)
+    need = workspace_size(_lib.GNS_OP_MUON_STEP, Ms, ns, muon=params)
     ws = workspace if workspace is not None else alloc_workspace(need, Ms[0].device)
     wa, _ = _batches(Ws)
     ga, _ = _batches(Gs)
     ma, _ = _batches(Ms)
+    va = None
+    if V is not None:
+        va, _ = _batches(_as_list(V))
     nsp = ns.c_struct()
-    mp = GnsMuonParams(float(lr), float(momentum), float(weight_decay), float(scale), float(frac))
-    rc = load().gns_muon_step(wa, ga, ma, len(Ms), ctypes.byref(mp), ctypes.byref(nsp), ws.data_ptr(), ws.numel(),
-                              _status_ptr(status), _stream_ptr(stream, Ms[0].device))
+    mp = params.c_struct()
+    rc = load().gns_muon_step(wa, ga, ma, va, len(Ms), ctypes.byref(mp), ctypes.byref(nsp), ws.data_ptr(),
+                              ws.numel(), _status_ptr(status), _stream_ptr(stream, Ms[0].device))
     check(rc, "gns_muon_step")
 
 

@@ -8,6 +8,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -114,8 +115,9 @@ GNS_DEV void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 GNS_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 GNS_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulator, one CTA.
-GNS_DEV void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+// D[tmem] (+)= A[smem] * B[smem]^T, 16-bit inputs (both bf16 or both fp16), fp32 accumulator,
+// one CTA.
+GNS_DEV void umma_f16kind(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
@@ -157,12 +159,12 @@ GNS_DEV uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_by
   return d;
 }
 
-// Instruction descriptor, kind::f16: D fp32, A and B bf16, shape M x N, K-major (0) or
-// MN-major (1) operands.
-__host__ __device__ inline uint32_t idesc_bf16_f32(int M, int N, int a_mn, int b_mn) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn) << 15) |
-         (static_cast<uint32_t>(b_mn) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
-         (static_cast<uint32_t>(M >> 4) << 24);
+// Instruction descriptor, kind::f16: D fp32, A and B both bf16 (ab_f16 = 0) or both fp16
+// (ab_f16 = 1), shape M x N, K-major (0) or MN-major (1) operands.
+__host__ __device__ inline uint32_t idesc_f16kind_f32(int M, int N, int a_mn, int b_mn, int ab_f16) {
+  const uint32_t ab = ab_f16 ? 0u : ((1u << 7) | (1u << 10));
+  return (1u << 4) | ab | (static_cast<uint32_t>(a_mn) << 15) | (static_cast<uint32_t>(b_mn) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 // Named barrier over `nthreads` threads; the calling warp is reconverged first because
@@ -232,7 +234,7 @@ GNS_DEV void tmem_dealloc2(uint32_t taddr, uint32_t ncols) {
 
 // D[tmem of both CTAs] (+)= A * B^T issued by the pair's leader: A rows split across the
 // two CTAs (128 each), B columns split across the two CTAs, same smem offsets in both.
-GNS_DEV void umma2_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+GNS_DEV void umma2_f16kind(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
@@ -287,3 +289,12 @@ GNS_DEV bool wait_counter(const int* ctr, int target, volatile int* abort_flag, 
 
 GNS_DEV float bf16_to_f(bf16 v) { return __bfloat162float(v); }
 GNS_DEV bf16 f_to_bf16(float v) { return __float2bfloat16_rn(v); }
+
+// 16-bit storage that is fp16 (is_f16) or bf16, by bit pattern; conversions round to nearest
+// even.
+GNS_DEV float h16_to_f(uint16_t bits, int is_f16) {
+  return is_f16 ? __half2float(__ushort_as_half(bits)) : __bfloat162float(__ushort_as_bfloat16(bits));
+}
+GNS_DEV uint16_t f_to_h16(float v, int is_f16) {
+  return is_f16 ? __half_as_ushort(__float2half_rn(v)) : __bfloat16_as_ushort(__float2bfloat16_rn(v));
+}

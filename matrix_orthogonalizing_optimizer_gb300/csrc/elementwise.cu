@@ -47,6 +47,25 @@ template <>
 __device__ __forceinline__ float to_f<bf16>(bf16 v) {
   return __bfloat162float(v);
 }
+template <>
+__device__ __forceinline__ float to_f<__half>(__half v) {
+  return __half2float(v);
+}
+
+template <typename T>
+__device__ __forceinline__ T from_f(float v);
+template <>
+__device__ __forceinline__ float from_f<float>(float v) {
+  return v;
+}
+template <>
+__device__ __forceinline__ bf16 from_f<bf16>(float v) {
+  return __float2bfloat16_rn(v);
+}
+template <>
+__device__ __forceinline__ __half from_f<__half>(float v) {
+  return __float2half_rn(v);
+}
 
 // ---------------------------------------------------------------------------------------
 // sum of squares per matrix (read only), partials[b * npart + part]
@@ -486,12 +505,13 @@ __global__ void scale_unselected_kernel(bf16* W, long long ldw, long long sw, in
   }
 }
 
-// Selected rows of W (or columns, trans = 1) take beta * W + alpha * O:
+// Selected rows of W (or columns, trans = 1) take beta * W + alpha * r_i * O:
 // W[idx[i]][j] (trans: W[j][idx[i]]) for O[i][j], i < k, j < len; fp32 arithmetic, one
-// rounding (the weight update of Dion3 sec. 6 on the selected rows only).
+// rounding (the weight update of Dion3 sec. 6 on the selected rows only). idx == NULL
+// selects every row (i itself); rs == NULL means r_i = 1 (NorMuon passes its row scales).
 __global__ void scatter_update_kernel(bf16* W, long long ldw, long long sw, const bf16* O, long long ldo,
-                                      long long so, const int* idx, int k, int len, int trans, float alpha,
-                                      float beta) {
+                                      long long so, const int* idx, const float* rs, int k, int len, int trans,
+                                      float alpha, float beta) {
   const int b = blockIdx.z;
   const long long total = (long long)k * len;
   for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (long long)gridDim.x * blockDim.x) {
@@ -503,25 +523,152 @@ __global__ void scatter_update_kernel(bf16* W, long long ldw, long long sw, cons
       j = (int)(e / k);
       i = (int)(e % k);
     }
-    const int sel = idx[(long long)b * k + i];
+    const int sel = idx ? idx[(long long)b * k + i] : i;
     bf16* p = W + (long long)b * sw + (trans ? (long long)j * ldw + sel : (long long)sel * ldw + j);
-    const float o = bf16_to_f(O[(long long)b * so + (long long)i * ldo + j]);
+    float o = bf16_to_f(O[(long long)b * so + (long long)i * ldo + j]);
+    if (rs) o *= rs[(long long)b * k + i];
     *p = f_to_bf16(fmaf(alpha, o, beta * bf16_to_f(*p)));
   }
 }
 
+// ---------------------------------------------------------------------------------------
+// NorMuon and RowNorm statistics
+
+// s[b*k + i] = sum_j X[b][i][j]^2 over the k rows of X (bf16), one warp per row, lanes in a
+// fixed order.
+__global__ void row_sumsq_kernel(const bf16* X, long long ldx, long long sx, int k, int cols, int count, float* s) {
+  const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= (long long)k * count) return;
+  const int b = (int)(row / k), i = (int)(row % k);
+  const bf16* r = X + (long long)b * sx + (long long)i * ldx;
+  float acc = 0.f;
+  for (int c = lane; c < cols; c += 32) {
+    const float v = bf16_to_f(r[c]);
+    acc = fmaf(v, v, acc);
+  }
+  acc = warp_sum(acc);
+  if (lane == 0) s[row] = acc;
+}
+
+// Column sums of squares of M (rows x cols, bf16) in NPART row slices:
+// part[(b * NPART + p) * cols + c]; a thread owns one column of one slice.
+__global__ void col_sumsq_part_kernel(const bf16* M, long long ldm, long long sm, int rows, int cols, int npart,
+                                      float* part) {
+  const int b = blockIdx.z, p = blockIdx.y;
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= cols) return;
+  const int rp = (rows + npart - 1) / npart;
+  const int r0 = p * rp, r1 = min(rows, r0 + rp);
+  const bf16* Mb = M + (long long)b * sm;
+  float acc = 0.f;
+  for (int r = r0; r < r1; ++r) {
+    const float v = bf16_to_f(Mb[(long long)r * ldm + c]);
+    acc = fmaf(v, v, acc);
+  }
+  part[((long long)b * npart + p) * cols + c] = acc;
+}
+
+// s[b*cols + c] = sum of the NPART slice sums, in slice order.
+__global__ void col_sumsq_finish_kernel(const float* part, int cols, int npart, int count, float* s) {
+  const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= (long long)cols * count) return;
+  const int b = (int)(e / cols), c = (int)(e % cols);
+  float acc = 0.f;
+  for (int p = 0; p < npart; ++p) acc += part[((long long)b * npart + p) * cols + c];
+  s[e] = acc;
+}
+
+// NorMuon (Dion3 eq. (2); Algorithm 4 lines 5-7), one block per matrix. For the k rows of O
+// with sums of squares s_i (of `len` columns each), row i being row sel(i) of the oriented
+// matrix (sel = idx or the identity):
+//   v <- beta2 v + (1 - beta2) s_i / len;  d_i = sqrt(v) + eps;
+//   r_i = (||O||_F / ||O / d||_F) / d_i, the factor that turns O_ij into the rescaled
+//   NorMuon update r_i O_ij.
+// The norms are reduced in fp64 in a fixed order; the per-row quantities are fp32.
+__global__ void __launch_bounds__(256) normuon_rows_kernel(const float* s, float* V, long long ldv, long long sv,
+                                                           const int* idx, int k, int len, float beta2, float eps,
+                                                           float* r) {
+  __shared__ double red[2][256];
+  const int b = blockIdx.x;
+  double o2 = 0.0, h2 = 0.0;
+  for (int i = threadIdx.x; i < k; i += blockDim.x) {
+    const int sel = idx ? idx[(long long)b * k + i] : i;
+    float* vp = V + (long long)b * sv + sel;
+    const float si = s[(long long)b * k + i];
+    const float v = fmaf(beta2, *vp, (1.f - beta2) * (si / (float)len));
+    *vp = v;
+    const float d = sqrtf(v) + eps;
+    r[(long long)b * k + i] = d;
+    o2 += (double)si;
+    h2 += (double)si / ((double)d * (double)d);
+  }
+  red[0][threadIdx.x] = o2;
+  red[1][threadIdx.x] = h2;
+  __syncthreads();
+  for (int w = blockDim.x / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) {
+      red[0][threadIdx.x] += red[0][threadIdx.x + w];
+      red[1][threadIdx.x] += red[1][threadIdx.x + w];
+    }
+    __syncthreads();
+  }
+  const double f = red[1][0] > 0.0 ? sqrt(red[0][0] / red[1][0]) : 0.0;
+  for (int i = threadIdx.x; i < k; i += blockDim.x) {
+    const long long e = (long long)b * k + i;
+    r[e] = (float)(f / (double)r[e]);
+  }
+}
+
+// RowNorm scales (Scaling Muon for DiTs eq. (5), multiplier gamma): r = gamma / max(sqrt(s), eps).
+__global__ void rownorm_scale_kernel(const float* s, long long n, float gamma, float eps, float* r) {
+  const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= n) return;
+  r[e] = gamma / fmaxf(sqrtf(s[e]), eps);
+}
+
+// W <- beta W + alpha r_q Y, elementwise over rows x cols, q = the row (trans = 0) or the
+// column (trans = 1) of the element: a per-oriented-row scaled update with W and Y in the same
+// physical layout. fp32 arithmetic, one rounding.
+__global__ void rowscale_update_kernel(bf16* W, long long ldw, long long sw, const bf16* Y, long long ldy,
+                                       long long sy, const float* r, int rows, int cols, int trans, float alpha,
+                                       float beta) {
+  const int b = blockIdx.z;
+  const long long total = (long long)rows * cols;
+  const long long nr = trans ? cols : rows;
+  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (long long)gridDim.x * blockDim.x) {
+    const int i = (int)(e / cols), j = (int)(e % cols);
+    bf16* p = W + (long long)b * sw + (long long)i * ldw + j;
+    const float y = bf16_to_f(Y[(long long)b * sy + (long long)i * ldy + j]) * r[(long long)b * nr + (trans ? j : i)];
+    *p = f_to_bf16(fmaf(alpha, y, beta * bf16_to_f(*p)));
+  }
+}
+
+// X16 = fp16(inv[b] * M), elementwise in the same layout (Dion3 Algorithm 3 lines 2-3 for a
+// bf16 momentum: normalise, then round once to float16).
+__global__ void cast_scaled_kernel(__half* X, long long ldx, long long sx, const bf16* M, long long ldm, long long sm,
+                                   const float* inv, int rows, int cols) {
+  const int b = blockIdx.z;
+  const long long total = (long long)rows * cols;
+  const float s = inv[b];
+  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (long long)gridDim.x * blockDim.x) {
+    const int i = (int)(e / cols), j = (int)(e % cols);
+    X[(long long)b * sx + (long long)i * ldx + j] =
+        __float2half_rn(s * bf16_to_f(M[(long long)b * sm + (long long)i * ldm + j]));
+  }
+}
+
 // W <- beta * W + alpha * Y (same shape), fp32 arithmetic, one rounding.
-template <typename T>
-__global__ void axpby_kernel(T* W, long long ldw, long long sw, const T* Y, long long ldy, long long sy, int rows,
+template <typename TW, typename TY>
+__global__ void axpby_kernel(TW* W, long long ldw, long long sw, const TY* Y, long long ldy, long long sy, int rows,
                              int cols, float alpha, float beta) {
   const int b = blockIdx.z;
   const long long total = (long long)rows * cols;
   for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (long long)gridDim.x * blockDim.x) {
     const int r = (int)(e / cols), c = (int)(e % cols);
-    T* p = W + (long long)b * sw + (long long)r * ldw + c;
+    TW* p = W + (long long)b * sw + (long long)r * ldw + c;
     const float y = to_f(Y[(long long)b * sy + (long long)r * ldy + c]);
-    const float o = fmaf(alpha, y, beta * to_f(*p));
-    if constexpr (sizeof(T) == 2) *p = f_to_bf16(o); else *p = o;
+    *p = from_f<TW>(fmaf(alpha, y, beta * to_f(*p)));
   }
 }
 
@@ -564,6 +711,9 @@ int launch_sumsq(gns_dtype dt, const MatRef& X, int64_t count, float* partials, 
   if (dt == GNS_BF16)
     sumsq_kernel<bf16><<<grid, 256, 0, S(stream)>>>(static_cast<const bf16*>(X.ptr), X.ld, X.stride, (int)X.rows,
                                                    (int)X.cols, NPART, partials);
+  else if (dt == GNS_F16)
+    sumsq_kernel<__half><<<grid, 256, 0, S(stream)>>>(static_cast<const __half*>(X.ptr), X.ld, X.stride, (int)X.rows,
+                                                     (int)X.cols, NPART, partials);
   else
     sumsq_kernel<float><<<grid, 256, 0, S(stream)>>>(static_cast<const float*>(X.ptr), X.ld, X.stride, (int)X.rows,
                                                     (int)X.cols, NPART, partials);
@@ -678,35 +828,99 @@ int launch_scale_unselected(const MatRef& W, int64_t count, int trans, const int
 }
 
 int launch_scatter_update(const MatRef& W, const MatRef& O, int64_t count, int trans, const int* idx, int64_t k,
-                          float alpha, float beta, void* stream, std::string* err) {
+                          float alpha, float beta, void* stream, std::string* err, const float* rs) {
   const int64_t len = O.cols;
   dim3 grid(grid_1d(k * len, 256), 1, (unsigned)count);
   scatter_update_kernel<<<grid, 256, 0, S(stream)>>>(static_cast<bf16*>(W.ptr), W.ld, W.stride,
-                                                     static_cast<const bf16*>(O.ptr), O.ld, O.stride, idx, (int)k,
+                                                     static_cast<const bf16*>(O.ptr), O.ld, O.stride, idx, rs, (int)k,
                                                      (int)len, trans, alpha, beta);
   return check_launch("scatter_update", err);
 }
 
-int launch_axpby(gns_dtype dt, const MatRef& W, const MatRef& Y, int64_t count, float alpha, float beta, void* stream,
-                 std::string* err) {
+int launch_row_sumsq(const MatRef& X, int64_t k, int64_t cols, int64_t count, float* s, void* stream,
+                     std::string* err) {
+  const long long rows = (long long)k * count;
+  row_sumsq_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, S(stream)>>>(static_cast<const bf16*>(X.ptr), X.ld, X.stride,
+                                                                      (int)k, (int)cols, (int)count, s);
+  return check_launch("row_sumsq", err);
+}
+
+int launch_col_sumsq(const MatRef& M, int64_t count, float* part, float* s, void* stream, std::string* err) {
+  dim3 grid((unsigned)((M.cols + 255) / 256), NPART, (unsigned)count);
+  col_sumsq_part_kernel<<<grid, 256, 0, S(stream)>>>(static_cast<const bf16*>(M.ptr), M.ld, M.stride, (int)M.rows,
+                                                     (int)M.cols, NPART, part);
+  int rc = check_launch("col_sumsq", err);
+  if (rc) return rc;
+  const long long n = (long long)M.cols * count;
+  col_sumsq_finish_kernel<<<(unsigned)((n + 255) / 256), 256, 0, S(stream)>>>(part, (int)M.cols, NPART, (int)count,
+                                                                             s);
+  return check_launch("col_sumsq_finish", err);
+}
+
+int launch_normuon_rows(const float* s, const MatRef& V, const int* idx, int64_t k, int64_t len, int64_t count,
+                        float beta2, float eps, float* r, void* stream, std::string* err) {
+  normuon_rows_kernel<<<(unsigned)count, 256, 0, S(stream)>>>(s, static_cast<float*>(V.ptr), V.ld, V.stride, idx,
+                                                              (int)k, (int)len, beta2, eps, r);
+  return check_launch("normuon_rows", err);
+}
+
+int launch_rownorm_scale(const float* s, int64_t n, float gamma, float eps, float* r, void* stream,
+                         std::string* err) {
+  rownorm_scale_kernel<<<(unsigned)((n + 255) / 256), 256, 0, S(stream)>>>(s, (long long)n, gamma, eps, r);
+  return check_launch("rownorm_scale", err);
+}
+
+int launch_rowscale_update(const MatRef& W, const MatRef& Y, const float* r, int64_t count, int trans, float alpha,
+                           float beta, void* stream, std::string* err) {
   dim3 grid(grid_1d(W.rows * W.cols, 256), 1, (unsigned)count);
-  if (dt == GNS_BF16)
-    axpby_kernel<bf16><<<grid, 256, 0, S(stream)>>>(static_cast<bf16*>(W.ptr), W.ld, W.stride,
-                                                   static_cast<const bf16*>(Y.ptr), Y.ld, Y.stride, (int)W.rows,
-                                                   (int)W.cols, alpha, beta);
-  else
-    axpby_kernel<float><<<grid, 256, 0, S(stream)>>>(static_cast<float*>(W.ptr), W.ld, W.stride,
-                                                    static_cast<const float*>(Y.ptr), Y.ld, Y.stride, (int)W.rows,
-                                                    (int)W.cols, alpha, beta);
+  rowscale_update_kernel<<<grid, 256, 0, S(stream)>>>(static_cast<bf16*>(W.ptr), W.ld, W.stride,
+                                                      static_cast<const bf16*>(Y.ptr), Y.ld, Y.stride, r, (int)W.rows,
+                                                      (int)W.cols, trans, alpha, beta);
+  return check_launch("rowscale_update", err);
+}
+
+int launch_cast_scaled(const MatRef& X16, const MatRef& M, const float* inv, int64_t count, void* stream,
+                       std::string* err) {
+  dim3 grid(grid_1d(M.rows * M.cols, 256), 1, (unsigned)count);
+  cast_scaled_kernel<<<grid, 256, 0, S(stream)>>>(static_cast<__half*>(X16.ptr), X16.ld, X16.stride,
+                                                  static_cast<const bf16*>(M.ptr), M.ld, M.stride, inv, (int)M.rows,
+                                                  (int)M.cols);
+  return check_launch("cast_scaled", err);
+}
+
+int launch_axpby(gns_dtype dt, const MatRef& W, const MatRef& Y, int64_t count, float alpha, float beta, void* stream,
+                 std::string* err, gns_dtype y_dt) {
+  dim3 grid(grid_1d(W.rows * W.cols, 256), 1, (unsigned)count);
+  if ((int)y_dt < 0) y_dt = dt;
+  if (dt == GNS_BF16 && y_dt == GNS_BF16)
+    axpby_kernel<bf16, bf16><<<grid, 256, 0, S(stream)>>>(static_cast<bf16*>(W.ptr), W.ld, W.stride,
+                                                         static_cast<const bf16*>(Y.ptr), Y.ld, Y.stride, (int)W.rows,
+                                                         (int)W.cols, alpha, beta);
+  else if (dt == GNS_BF16 && y_dt == GNS_F16)
+    axpby_kernel<bf16, __half><<<grid, 256, 0, S(stream)>>>(static_cast<bf16*>(W.ptr), W.ld, W.stride,
+                                                           static_cast<const __half*>(Y.ptr), Y.ld, Y.stride,
+                                                           (int)W.rows, (int)W.cols, alpha, beta);
+  else if (dt == GNS_F16 && y_dt == GNS_F16)
+    axpby_kernel<__half, __half><<<grid, 256, 0, S(stream)>>>(static_cast<__half*>(W.ptr), W.ld, W.stride,
+                                                             static_cast<const __half*>(Y.ptr), Y.ld, Y.stride,
+                                                             (int)W.rows, (int)W.cols, alpha, beta);
+  else if (dt == GNS_F32 && y_dt == GNS_F32)
+    axpby_kernel<float, float><<<grid, 256, 0, S(stream)>>>(static_cast<float*>(W.ptr), W.ld, W.stride,
+                                                           static_cast<const float*>(Y.ptr), Y.ld, Y.stride,
+                                                           (int)W.rows, (int)W.cols, alpha, beta);
+  else {
+    *err = "internal: unsupported axpby types";
+    return GNS_ERR_INVALID;
+  }
   return check_launch("axpby", err);
 }
 
 int launch_copy(gns_dtype dt, const MatRef& D, const MatRef& Sr, int64_t count, void* stream, std::string* err) {
   dim3 grid(grid_1d(D.rows * D.cols, 256), 1, (unsigned)count);
-  if (dt == GNS_BF16)
-    copy_kernel<bf16><<<grid, 256, 0, S(stream)>>>(static_cast<bf16*>(D.ptr), D.ld, D.stride,
-                                                  static_cast<const bf16*>(Sr.ptr), Sr.ld, Sr.stride, (int)D.rows,
-                                                  (int)D.cols);
+  if (dt == GNS_BF16 || dt == GNS_F16)  // 16-bit copies move bit patterns
+    copy_kernel<uint16_t><<<grid, 256, 0, S(stream)>>>(static_cast<uint16_t*>(D.ptr), D.ld, D.stride,
+                                                      static_cast<const uint16_t*>(Sr.ptr), Sr.ld, Sr.stride,
+                                                      (int)D.rows, (int)D.cols);
   else
     copy_kernel<float><<<grid, 256, 0, S(stream)>>>(static_cast<float*>(D.ptr), D.ld, D.stride,
                                                    static_cast<const float*>(Sr.ptr), Sr.ld, Sr.stride, (int)D.rows,

@@ -29,10 +29,30 @@ int launch_decay_selected(const MatRef& M, int64_t count, int trans, const int* 
                           void* stream, std::string* err);
 int launch_scale_unselected(const MatRef& W, int64_t count, int trans, const int* idx, int64_t k, float factor,
                             void* stream, std::string* err);
+// rs (nullable): per-row scale of O (NorMuon); idx NULL: every row, in order.
 int launch_scatter_update(const MatRef& W, const MatRef& O, int64_t count, int trans, const int* idx, int64_t k,
-                          float alpha, float beta, void* stream, std::string* err);
+                          float alpha, float beta, void* stream, std::string* err, const float* rs = nullptr);
+// y_dt: type of Y when it differs from W's (bf16 W with fp16 Y); -1 = dt.
 int launch_axpby(gns_dtype dt, const MatRef& W, const MatRef& Y, int64_t count, float alpha, float beta, void* stream,
-                 std::string* err);
+                 std::string* err, gns_dtype y_dt = (gns_dtype)-1);
+// s[b*k + i] = sum of squares of row i (of `cols` entries) of the bf16 batch X.
+int launch_row_sumsq(const MatRef& X, int64_t k, int64_t cols, int64_t count, float* s, void* stream,
+                     std::string* err);
+// s[b*cols + c] = sum of squares of column c of the bf16 batch M; part: NPART * cols * count
+// floats of scratch.
+int launch_col_sumsq(const MatRef& M, int64_t count, float* part, float* s, void* stream, std::string* err);
+// NorMuon second moments (V fp32, updated at rows idx or 0..k-1) and row scales r.
+int launch_normuon_rows(const float* s, const MatRef& V, const int* idx, int64_t k, int64_t len, int64_t count,
+                        float beta2, float eps, float* r, void* stream, std::string* err);
+// RowNorm scales r = gamma / max(sqrt(s), eps) over n entries.
+int launch_rownorm_scale(const float* s, int64_t n, float gamma, float eps, float* r, void* stream,
+                         std::string* err);
+// W <- beta W + alpha r_q Y with q the row (trans 0) or column (trans 1) of each element.
+int launch_rowscale_update(const MatRef& W, const MatRef& Y, const float* r, int64_t count, int trans, float alpha,
+                           float beta, void* stream, std::string* err);
+// X16 = fp16(inv[b] * M) in M's layout.
+int launch_cast_scaled(const MatRef& X16, const MatRef& M, const float* inv, int64_t count, void* stream,
+                       std::string* err);
 int launch_copy(gns_dtype dt, const MatRef& D, const MatRef& S, int64_t count, void* stream, std::string* err);
 
 }  // namespace gns

@@ -12,7 +12,12 @@
 // sym: M == N and only tiles with tile_row <= tile_col are computed; each off-diagonal tile
 // is also written to its mirrored position (j, i); diagonal tiles are written once.
 // D2 (optional, same layout as D): D + gamma * I on the diagonal entries i == j < diag_limit.
+// Element types: A and B share ab_dt; C and D (with D2) have c_dt and d_dt; -1 means the
+// dtype of the call that launches the op (gemm_launch / gemm_program). The tensor-core
+// kernel takes bf16 and fp16 in any combination of (ab, c, d); the fp32 path all fp32.
 #pragma once
+
+#include <vector>
 
 #include <stdint.h>
 
@@ -54,15 +59,27 @@ struct GemmOp {
   // symmetric matrix, read transposed wherever a K slice falls below its diagonal.
   int upper_out = 0;
   int a_upper = 0, b_upper = 0;
+  int ab_dt = -1, c_dt = -1, d_dt = -1;
 };
+
+// Copies of ops with every unset (-1) element type replaced by dt.
+inline std::vector<GemmOp> with_types(gns_dtype dt, const GemmOp* ops, int nops) {
+  std::vector<GemmOp> v(ops, ops + nops);
+  for (GemmOp& o : v) {
+    if (o.ab_dt < 0) o.ab_dt = dt;
+    if (o.c_dt < 0) o.c_dt = dt;
+    if (o.d_dt < 0) o.d_dt = dt;
+  }
+  return v;
+}
 
 // Enqueues ops as ONE launch. dep_masks[i] (nullable) names earlier ops of the same launch
 // whose tiles of the same matrix must be complete before a tile of op i starts (the
 // tensor-core kernel waits on per-(op, matrix) completion counters: `counters`, at least
 // sum(batch) ints of device memory, reset by the launch). Without masks the ops must be
 // mutually independent. Returns GNS_OK or an error status with *err set.
-int gemm_launch_bf16(const GemmOp* ops, int nops, const uint32_t* dep_masks, int* counters, int32_t* dev_status,
-                     void* stream, std::string* err);
+int gemm_launch_tc(const GemmOp* ops, int nops, const uint32_t* dep_masks, int* counters, int32_t* dev_status,
+                   void* stream, std::string* err);
 int gemm_launch_f32(const GemmOp* ops, int nops, const uint32_t* dep_masks, int* counters, int32_t* dev_status,
                     void* stream, std::string* err);
 
@@ -74,9 +91,10 @@ void profile_count_launch();
 // Independent ops as one launch.
 inline int gemm_launch(gns_dtype dt, const GemmOp* ops, int nops, int32_t* dev_status, void* stream,
                        std::string* err) {
+  const std::vector<GemmOp> typed = with_types(dt, ops, nops);
   profile_gemm_begin(stream);
-  const int rc = dt == GNS_BF16 ? gemm_launch_bf16(ops, nops, nullptr, nullptr, dev_status, stream, err)
-                                : gemm_launch_f32(ops, nops, nullptr, nullptr, dev_status, stream, err);
+  const int rc = dt != GNS_F32 ? gemm_launch_tc(typed.data(), nops, nullptr, nullptr, dev_status, stream, err)
+                               : gemm_launch_f32(typed.data(), nops, nullptr, nullptr, dev_status, stream, err);
   profile_gemm_end(stream);
   return rc;
 }
@@ -85,9 +103,9 @@ inline int gemm_launch(gns_dtype dt, const GemmOp* ops, int nops, int32_t* dev_s
 constexpr int kMaxProgramOps = 24;
 
 // A sequence of ops in program order (op j may read what op i < j wrote, or overwrite what
-// it read). bf16: as few launches as possible, dependencies between ops found from the
-// buffers they read (A, B, C) and write (D, D2) and enforced per matrix inside the launch;
-// fp32: one launch per op, ordered by the stream. `counters`: kMaxProgramOps * batch ints.
+// it read). bf16 / fp16: as few launches as possible, dependencies between ops found from
+// the buffers they read (A, B, C) and write (D, D2) and enforced per matrix inside the
+// launch; fp32: one launch per op, ordered by the stream. `counters`: kMaxProgramOps * batch ints.
 int gemm_program(gns_dtype dt, const GemmOp* ops, int nops, int* counters, int32_t* dev_status, void* stream,
                  std::string* err);
 

@@ -1,4 +1,6 @@
-// Batched bf16 GEMM on the 5th-generation tensor cores (tcgen05 + TMEM + TMA), sm_103a.
+// Batched 16-bit (bf16 or fp16) GEMM on the 5th-generation tensor cores (tcgen05 + TMEM +
+// TMA), sm_103a. A and B share one type (kind::f16 takes both bf16 or both fp16); the addend C
+// and the outputs D, D2 may each be bf16 or fp16.
 //
 // A cluster of two CTAs (a CTA pair on neighbouring SMs) computes one 256 x 256 output
 // tile with 2-CTA MMAs (tcgen05.mma.cta_group::2, M = 256, N = 256, K = 16): each CTA
@@ -53,7 +55,7 @@ constexpr int A_BYTES = TM * TK * 2;             // 16 KiB
 constexpr int STAGE_BYTES = (TM + BN) * TK * 2;  // 32 KiB per CTA
 constexpr int CHUNK = 64;                        // epilogue columns per chunk
 constexpr int NCHUNK = TN / CHUNK;
-constexpr int BOX_BYTES = 64 * 64 * 2;           // one 64 x 64 bf16 box, 128-byte swizzle
+constexpr int BOX_BYTES = 64 * 64 * 2;           // one 64 x 64 16-bit box, 128-byte swizzle
 constexpr int CHUNK_BYTES = 2 * BOX_BYTES;       // 128 x 64 (or 64 x 128) elements
 constexpr int C_WARP = 2;                        // loads the C tile ahead of the epilogue
 constexpr int FIRST_EPI_WARP = 3;
@@ -89,6 +91,7 @@ struct Problem {
   int diag_limit;
   int check_finite;
   int a_upper, b_upper, mirror_out;
+  int ab_f16, c_f16, d_f16;  // 16-bit element types: fp16 (1) or bf16 (0)
   uint32_t dep_mask;  // earlier problems whose tiles of the same matrix must be complete
   int ctr_off;        // this problem's completion counters: counters[ctr_off + b]
 };
@@ -337,7 +340,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         const uint32_t d_tmem = tmem_base + acc * TN;
         for (int kb = 0; kb < pr.kblocks; ++kb) {
           const int amn = a_major(pr, c.I, kb), bmn = b_major(pr, c.J, kb);
-          const uint32_t idesc = idesc_bf16_f32(2 * TM, TN, amn, bmn);
+          const uint32_t idesc = idesc_f16kind_f32(2 * TM, TN, amn, bmn, pr.ab_f16);
           if (!mbar_wait(&full[s], ph, abort_flag, P.status)) {
             ok = false;
             break;
@@ -351,7 +354,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                 amn ? sdesc_sw128(sa + kk * 2048, BOX_BYTES, 1024) : sdesc_sw128(sa + kk * 32, 16, 1024);
             const uint64_t bd =
                 bmn ? sdesc_sw128(sb + kk * 2048, BOX_BYTES, 1024) : sdesc_sw128(sb + kk * 32, 16, 1024);
-            umma2_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            umma2_f16kind(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
           umma2_commit_multicast(&empty[s], 0x3);
           if (++s == STAGES) {
@@ -467,14 +470,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               const uint4 w = *reinterpret_cast<const uint4*>(sc + off_direct(r, half * 32 + q * 8));
-              const bf16* wv = reinterpret_cast<const bf16*>(&w);
+              const uint16_t* wv = reinterpret_cast<const uint16_t*>(&w);
 #pragma unroll
-              for (int e = 0; e < 8; ++e) o[q * 8 + e] = fmaf(beta, bf16_to_f(wv[e]), o[q * 8 + e]);
+              for (int e = 0; e < 8; ++e) o[q * 8 + e] = fmaf(beta, h16_to_f(wv[e], pr.c_f16), o[q * 8 + e]);
             }
           } else {
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-              o[j] = fmaf(beta, bf16_to_f(*reinterpret_cast<const bf16*>(sc + off_trans(r, half * 32 + j))), o[j]);
+              o[j] = fmaf(beta, h16_to_f(*reinterpret_cast<const uint16_t*>(sc + off_trans(r, half * 32 + j)), pr.c_f16),
+                          o[j]);
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&cempty[q]);
@@ -493,18 +497,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             uint4 w;
-            bf16* wv = reinterpret_cast<bf16*>(&w);
+            uint16_t* wv = reinterpret_cast<uint16_t*>(&w);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) wv[e] = f_to_bf16(o[q * 8 + e]);
+            for (int e = 0; e < 8; ++e) wv[e] = f_to_h16(o[q * 8 + e], pr.d_f16);
             *reinterpret_cast<uint4*>(sd + off_direct(r, half * 32 + q * 8)) = w;
           }
         } else {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) *reinterpret_cast<bf16*>(sd + off_trans(r, half * 32 + j)) = f_to_bf16(o[j]);
+          for (int j = 0; j < 32; ++j)
+            *reinterpret_cast<uint16_t*>(sd + off_trans(r, half * 32 + j)) = f_to_h16(o[j], pr.d_f16);
         }
         if (mirror) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) *reinterpret_cast<bf16*>(sm + off_trans(r, half * 32 + j)) = f_to_bf16(o[j]);
+          for (int j = 0; j < 32; ++j)
+            *reinterpret_cast<uint16_t*>(sm + off_trans(r, half * 32 + j)) = f_to_h16(o[j], pr.d_f16);
         }
         fence_proxy_async_smem();
         named_bar_sync(1, EPI_THREADS);
@@ -525,7 +531,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           if (et == 0) bulk_wait_read<0>();
           named_bar_sync(1, EPI_THREADS);
           if (diag_mine && (diag_col >> 6) == ch && m0 + r < pr.diag_limit)
-            *reinterpret_cast<bf16*>(sd + off_direct(r, diag_col & 63)) = f_to_bf16(dv + pr.gamma);
+            *reinterpret_cast<uint16_t*>(sd + off_direct(r, diag_col & 63)) = f_to_h16(dv + pr.gamma, pr.d_f16);
           fence_proxy_async_smem();
           named_bar_sync(1, EPI_THREADS);
           if (et == 0) {
@@ -578,9 +584,10 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn(std::string* err) {
   return fn;
 }
 
-// 3-D bf16 tensor map over a batch of row-major matrices: dims {cols, rows, batch}, box
-// {64, box_rows, 1}, 128-byte swizzle, zero fill out of bounds.
-static bool encode_map(CUtensorMap* map, const MatRef& m, int64_t batch, int box_rows, std::string* err) {
+// 3-D tensor map of 16-bit elements (fp16 when f16, else bf16) over a batch of row-major
+// matrices: dims {cols, rows, batch}, box {64, box_rows, 1}, 128-byte swizzle, zero fill out
+// of bounds.
+static bool encode_map(CUtensorMap* map, const MatRef& m, int64_t batch, int box_rows, int f16, std::string* err) {
   auto fn = get_encode_fn(err);
   if (!fn) return false;
   const int64_t ld_b = m.ld * 2;
@@ -591,7 +598,8 @@ static bool encode_map(CUtensorMap* map, const MatRef& m, int64_t batch, int box
   cuuint64_t strides[2] = {(cuuint64_t)ld_b, (cuuint64_t)st_b};
   cuuint32_t box[3] = {64u, (cuuint32_t)box_rows, 1u};
   cuuint32_t estr[3] = {1u, 1u, 1u};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, m.ptr, dims, strides, box, estr,
+  CUresult r = fn(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, m.ptr, dims,
+                  strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
@@ -641,8 +649,8 @@ static int resident_pairs(std::string* err) {
   return clusters;
 }
 
-int gemm_launch_bf16(const GemmOp* ops, int nops, const uint32_t* dep_masks, int* counters, int32_t* dev_status,
-                     void* stream, std::string* err) {
+int gemm_launch_tc(const GemmOp* ops, int nops, const uint32_t* dep_masks, int* counters, int32_t* dev_status,
+                   void* stream, std::string* err) {
   using namespace tc;
   if (nops < 1 || nops > MAX_PROB) {
     *err = "internal: bad number of products in one launch";
@@ -660,18 +668,27 @@ int gemm_launch_bf16(const GemmOp* ops, int nops, const uint32_t* dep_masks, int
       return GNS_ERR_INVALID;
     }
     Problem& pr = P.prob[i];
-    if (!encode_map(&pr.tmA, o.A, o.batch, o.a_mn ? 64 : 128, err)) return GNS_ERR_CUDA;
-    if (!encode_map(&pr.tmB, o.B, o.batch, o.b_mn ? 64 : 128, err)) return GNS_ERR_CUDA;
+    const int dts[3] = {o.ab_dt, o.c_dt, o.d_dt};
+    for (int t : dts)
+      if (t != GNS_BF16 && t != GNS_F16) {
+        *err = "internal: the tensor-core GEMM takes bf16 or fp16 matrices";
+        return GNS_ERR_INVALID;
+      }
+    pr.ab_f16 = o.ab_dt == GNS_F16;
+    pr.c_f16 = o.c_dt == GNS_F16;
+    pr.d_f16 = o.d_dt == GNS_F16;
+    if (!encode_map(&pr.tmA, o.A, o.batch, o.a_mn ? 64 : 128, pr.ab_f16, err)) return GNS_ERR_CUDA;
+    if (!encode_map(&pr.tmB, o.B, o.batch, o.b_mn ? 64 : 128, pr.ab_f16, err)) return GNS_ERR_CUDA;
     pr.a_upper = o.a_upper;
     pr.b_upper = o.b_upper;
     pr.mirror_out = o.upper_out ? 0 : 1;
-    if (o.a_upper && !encode_map(&pr.tmA2, o.A, o.batch, o.a_mn ? 128 : 64, err)) return GNS_ERR_CUDA;
-    if (o.b_upper && !encode_map(&pr.tmB2, o.B, o.batch, o.b_mn ? 128 : 64, err)) return GNS_ERR_CUDA;
+    if (o.a_upper && !encode_map(&pr.tmA2, o.A, o.batch, o.a_mn ? 128 : 64, pr.ab_f16, err)) return GNS_ERR_CUDA;
+    if (o.b_upper && !encode_map(&pr.tmB2, o.B, o.batch, o.b_mn ? 128 : 64, pr.ab_f16, err)) return GNS_ERR_CUDA;
     pr.has_c = o.C.ptr != nullptr && o.beta != 0.f;
-    if (pr.has_c && !encode_map(&pr.tmC, o.C, o.batch, 64, err)) return GNS_ERR_CUDA;
-    if (!encode_map(&pr.tmD, o.D, o.batch, 64, err)) return GNS_ERR_CUDA;
+    if (pr.has_c && !encode_map(&pr.tmC, o.C, o.batch, 64, pr.c_f16, err)) return GNS_ERR_CUDA;
+    if (!encode_map(&pr.tmD, o.D, o.batch, 64, pr.d_f16, err)) return GNS_ERR_CUDA;
     pr.has_d2 = o.D2.ptr != nullptr;
-    if (pr.has_d2 && !encode_map(&pr.tmD2, o.D2, o.batch, 64, err)) return GNS_ERR_CUDA;
+    if (pr.has_d2 && !encode_map(&pr.tmD2, o.D2, o.batch, 64, pr.d_f16, err)) return GNS_ERR_CUDA;
     pr.a_mn = o.a_mn;
     pr.b_mn = o.b_mn;
     pr.kblocks = (int)((o.K + TK - 1) / TK);

@@ -82,7 +82,7 @@ static bool op_conflict(const GemmOp& first, const GemmOp& later) {
 
 int gemm_program(gns_dtype dt, const GemmOp* ops, int nops, int* counters, int32_t* dev_status, void* stream,
                  std::string* err) {
-  if (dt != GNS_BF16) {
+  if (dt == GNS_F32) {
     for (int i = 0; i < nops; ++i) {
       int rc = gemm_launch(dt, ops + i, 1, dev_status, stream, err);
       if (rc) return rc;
@@ -90,7 +90,7 @@ int gemm_program(gns_dtype dt, const GemmOp* ops, int nops, int* counters, int32
     return GNS_OK;
   }
   // upper-stored symmetric buffers: what a product with upper_out wrote
-  std::vector<GemmOp> prog(ops, ops + nops);
+  std::vector<GemmOp> prog = with_types(dt, ops, nops);
   std::vector<const void*> upper;
   for (int j = 0; j < nops; ++j) {
     GemmOp& o = prog[j];
@@ -113,7 +113,7 @@ int gemm_program(gns_dtype dt, const GemmOp* ops, int nops, int* counters, int32
         if (op_conflict(ops[base + i], ops[base + j])) masks[j] |= 1u << i;
     }
     profile_gemm_begin(stream);
-    int rc = gemm_launch_bf16(ops + base, n, masks, counters, dev_status, stream, err);
+    int rc = gemm_launch_tc(ops + base, n, masks, counters, dev_status, stream, err);
     profile_gemm_end(stream);
     if (rc) return rc;
   }
@@ -162,11 +162,11 @@ static MatRef to_ref(const gns_batch& b) {
 // ---------------------------------------------------------------------------------------
 // validation
 
-static size_t elem_size(gns_dtype dt) { return dt == GNS_BF16 ? 2 : 4; }
+static size_t elem_size(gns_dtype dt) { return dt == GNS_F32 ? 4 : 2; }
 
 static int check_batch(const gns_batch* b, gns_dtype dt, const char* name) {
   if (!b) return fail(GNS_ERR_INVALID, std::string(name) + ": null batch descriptor");
-  const int64_t al = dt == GNS_BF16 ? 8 : 4;
+  const int64_t al = dt == GNS_F32 ? 4 : 8;
   if (!b->ptr) return fail(GNS_ERR_INVALID, std::string(name) + ": null data pointer");
   if (b->count < 1 || b->rows < 1 || b->cols < 1)
     return fail(GNS_ERR_INVALID, std::string(name) + ": count, rows and cols must be >= 1");
@@ -193,7 +193,24 @@ static int check_ns(const gns_ns_params* ns) {
   for (int t = 0; t < ns->T; ++t)
     if (!std::isfinite(ns->a[t]) || !std::isfinite(ns->b[t]) || !std::isfinite(ns->c[t]))
       return fail(GNS_ERR_INVALID, "coefficients must be finite");
+  if (!(ns->safety > 0.f) || !std::isfinite(ns->safety))
+    return fail(GNS_ERR_INVALID, "safety must be finite and > 0 (1 = no safety factor)");
   return GNS_OK;
+}
+
+// The schedule actually run: the safety factor of Dion3 appendix B.2.2, p_t(x / s), folded
+// into the coefficients (a / s, b / s^3, c / s^5), computed in double and rounded once.
+static gns_ns_params effective_ns(const gns_ns_params& ns) {
+  gns_ns_params e = ns;
+  const double s = ns.safety;
+  if (s != 1.0)
+    for (int t = 0; t < ns.T; ++t) {
+      e.a[t] = (float)((double)ns.a[t] / s);
+      e.b[t] = (float)((double)ns.b[t] / (s * s * s));
+      e.c[t] = (float)((double)ns.c[t] / (s * s * s * s * s));
+    }
+  e.safety = 1.f;
+  return e;
 }
 
 static bool same_shape(const gns_batch& a, const gns_batch& b) {
@@ -221,8 +238,10 @@ static void as_right(const Src& s, MatRef* m, int* mn) {
 }
 
 // Final write: D = alpha' (Q X) + beta C with C = D (when has_c), optional row map.
+// out_dt: element type of D (and C) when it differs from the products' (-1 = the same).
 struct Final {
   MatRef D;
+  int out_dt = -1;
   int d_trans = 0;
   float alpha = 1.f;
   float beta = 0.f;
@@ -333,7 +352,7 @@ static int run_gram(gns_dtype dt, const Src& src, int64_t B, int64_t n, int64_t 
     MatRef xa;
     int mn;
     as_rows(X, &xa, &mn);
-    GemmOp o = sym_op(xa, mn, xa, mn, m, np, B, 1.f, 2, inv, nullptr, 0.f, g.R);
+    GemmOp o = sym_op(xa, mn, xa, mn, m, np, B, 1.f, X.user ? 2 : 0, inv, nullptr, 0.f, g.R);
     if ((rc = launch(&o, 1))) return rc;
   }
   bool q_id = true;
@@ -418,6 +437,7 @@ static int run_gram(gns_dtype dt, const Src& src, int64_t B, int64_t n, int64_t 
     o.scale = inv;
     o.D = fin.D;
     o.d_trans = fin.d_trans;
+    o.c_dt = o.d_dt = fin.out_dt;
     if (fin.has_c) {
       o.C = fin.D;
       o.c_trans = fin.d_trans;
@@ -482,6 +502,7 @@ static int run_std(gns_dtype dt, const Src& src, int64_t B, int64_t n, int64_t m
       ox.N = m;
       ox.D = fin->D;
       ox.d_trans = fin->d_trans;
+      ox.d_dt = fin->out_dt;
       ox.check_finite = fin->check_finite;
     } else {
       ox.M = n;
@@ -522,6 +543,80 @@ static GroupShape shape_of(const gns_batch& x) {
 static int64_t frac_k(float frac, int64_t n) {
   int64_t k = (int64_t)std::ceil((double)frac * (double)n - 1e-9);
   return std::max<int64_t>(1, std::min<int64_t>(k, n));
+}
+
+// The flavour one step runs: Periodic Row-wise Muon (Scaling Muon for DiTs eq. (7)) takes
+// Newton-Schulz on the refresh steps t mod K == 0 and RowNorm on the others.
+static int step_flavor(const gns_muon_params& mp) {
+  if (mp.flavor == GNS_FLAVOR_PERIODIC) {
+    const int64_t t = mp.step, K = mp.period;
+    return ((t % K) + K) % K == 0 ? GNS_FLAVOR_MUON : GNS_FLAVOR_ROWNORM;
+  }
+  return mp.flavor;
+}
+
+// Workspace of one group of a Muon step; the same code sizes (Arena without base) and
+// places the buffers.
+struct MuonBufs {
+  bool frac = false, use_std = false;
+  int flavor = GNS_FLAVOR_MUON;
+  gns_dtype nsdt = GNS_BF16;
+  int64_t k = 0;
+  StdBufs sb;
+  GramBufs gb;
+  MatRef x16;                          // normalised fp16 copy of M (or of M[S])
+  unsigned long long* keys = nullptr;  // frac: selection
+  int* nf = nullptr;
+  int* idx = nullptr;
+  MatRef xs, os;                       // frac: M[S] and O before the scatter
+  MatRef o;                            // dense NorMuon: O (oriented, bf16)
+  float* s = nullptr;                  // NorMuon / RowNorm: row sums of squares
+  float* r = nullptr;                  // and row scales
+  float* part = nullptr;               // RowNorm of a tall matrix: column partial sums
+};
+
+static void plan_muon(Arena& a, const GroupShape& sh, const gns_muon_params& mp, const gns_ns_params* ns,
+                      MuonBufs* mb) {
+  mb->flavor = step_flavor(mp);
+  mb->nsdt = mp.ns_dtype == GNS_F16 ? GNS_F16 : GNS_BF16;
+  mb->frac = mp.frac < 1.f;
+  const int64_t B = sh.B, n = sh.n, m = sh.m;
+  const int64_t ldm = round_up(m, 8);
+  if (mb->flavor == GNS_FLAVOR_ROWNORM) {
+    mb->s = static_cast<float*>(a.take(sizeof(float) * B * n));
+    mb->r = static_cast<float*>(a.take(sizeof(float) * B * n));
+    if (sh.trans) mb->part = static_cast<float*>(a.take(sizeof(float) * B * NPART * n));
+    return;
+  }
+  const bool normuon = mb->flavor == GNS_FLAVOR_NORMUON;
+  if (!mb->frac) {
+    mb->use_std = n == m;
+    if (mb->use_std)
+      plan_std(a, B, n, m, mb->nsdt, &mb->sb, true);
+    else
+      plan_gram(a, B, n, m, mb->nsdt, ns, &mb->gb, true);
+    if (mb->nsdt == GNS_F16)
+      mb->x16 = ws_mat(a, B, sh.rows, sh.rows, sh.cols, round_up(sh.cols, 8), 2);
+    if (normuon) {
+      mb->o = ws_mat(a, B, n, n, m, ldm, 2);
+      mb->s = static_cast<float*>(a.take(sizeof(float) * B * n));
+      mb->r = static_cast<float*>(a.take(sizeof(float) * B * n));
+    }
+    return;
+  }
+  const int64_t k = frac_k(mp.frac, n);
+  mb->k = k;
+  mb->keys = static_cast<unsigned long long*>(a.take(sizeof(unsigned long long) * KEY_DIGITS * n * B));
+  mb->nf = static_cast<int*>(a.take(sizeof(int) * n * B));
+  mb->idx = static_cast<int*>(a.take(sizeof(int) * k * B));
+  mb->xs = ws_mat(a, B, round_up(k, PAD), k, m, ldm, 2);
+  mb->os = ws_mat(a, B, k, k, m, ldm, 2);
+  if (mb->nsdt == GNS_F16) mb->x16 = ws_mat(a, B, round_up(k, PAD), k, m, ldm, 2);
+  plan_gram(a, B, k, m, mb->nsdt, ns, &mb->gb, true);
+  if (normuon) {
+    mb->s = static_cast<float*>(a.take(sizeof(float) * B * k));
+    mb->r = static_cast<float*>(a.take(sizeof(float) * B * k));
+  }
 }
 
 }  // namespace gns
@@ -578,12 +673,37 @@ void gns_ns_params_default(gns_ns_params* p) {
   }
   p->restart_mask = 1u << 2;
   p->eps = 1e-7f;
+  p->safety = 1.f;
+}
+
+static int check_muon(const gns_muon_params& mp) {
+  if (!(mp.frac > 0.f) || mp.frac > 1.f) return fail(GNS_ERR_INVALID, "frac must be in (0, 1]");
+  if (!std::isfinite(mp.lr) || !std::isfinite(mp.momentum) || !std::isfinite(mp.weight_decay) ||
+      !std::isfinite(mp.scale))
+    return fail(GNS_ERR_INVALID, "muon params must be finite");
+  if (mp.flavor < GNS_FLAVOR_MUON || mp.flavor > GNS_FLAVOR_PERIODIC) return fail(GNS_ERR_INVALID, "unknown flavor");
+  if (mp.ns_dtype != GNS_BF16 && mp.ns_dtype != GNS_F16)
+    return fail(GNS_ERR_INVALID, "ns_dtype must be GNS_BF16 or GNS_F16");
+  if (mp.flavor == GNS_FLAVOR_NORMUON) {
+    if (!(mp.beta2 >= 0.f && mp.beta2 < 1.f)) return fail(GNS_ERR_INVALID, "NorMuon beta2 must be in [0, 1)");
+    if (!(mp.norm_eps > 0.f) || !std::isfinite(mp.norm_eps))
+      return fail(GNS_ERR_INVALID, "NorMuon norm_eps must be finite and > 0");
+  }
+  if (mp.flavor == GNS_FLAVOR_ROWNORM || mp.flavor == GNS_FLAVOR_PERIODIC) {
+    if (mp.frac < 1.f) return fail(GNS_ERR_UNSUPPORTED, "RowNorm flavours are dense steps (frac = 1)");
+    if (!(mp.norm_eps > 0.f) || !std::isfinite(mp.norm_eps))
+      return fail(GNS_ERR_INVALID, "RowNorm norm_eps must be finite and > 0");
+    if (!(mp.rownorm_gamma > 0.f) || !std::isfinite(mp.rownorm_gamma))
+      return fail(GNS_ERR_INVALID, "rownorm_gamma must be finite and > 0");
+  }
+  if (mp.flavor == GNS_FLAVOR_PERIODIC && mp.period < 1) return fail(GNS_ERR_INVALID, "period must be >= 1");
+  return GNS_OK;
 }
 
 static int plan_op(gns_op op, const gns_batch* x, int ngroups, gns_dtype dt, const gns_ns_params* ns,
                    const gns_muon_params* mp, Arena& a) {
   if (!x || ngroups < 1) return fail(GNS_ERR_INVALID, "need at least one batch");
-  if (dt != GNS_BF16 && dt != GNS_F32) return fail(GNS_ERR_INVALID, "unknown dtype");
+  if (dt != GNS_BF16 && dt != GNS_F32 && dt != GNS_F16) return fail(GNS_ERR_INVALID, "unknown dtype");
   if (op != GNS_OP_FRAC_SELECT) {
     int rc = check_ns(ns);
     if (rc) return rc;
@@ -605,24 +725,10 @@ static int plan_op(gns_op op, const gns_batch* x, int ngroups, gns_dtype dt, con
       plan_std(a, s.B, s.n, s.m, dt, &sb, true);
     } else if (op == GNS_OP_MUON_STEP) {
       if (!mp) return fail(GNS_ERR_INVALID, "null muon params");
-      if (mp->frac >= 1.f) {
-        if (s.n == s.m) {
-          StdBufs sb;
-          plan_std(a, s.B, s.n, s.m, dt, &sb, true);
-        } else {
-          GramBufs gb;
-          plan_gram(a, s.B, s.n, s.m, dt, ns, &gb, true);
-        }
-      } else {
-        const int64_t k = frac_k(mp->frac, s.n);
-        a.take(sizeof(unsigned long long) * KEY_DIGITS * s.n * s.B);
-        a.take(sizeof(int) * s.n * s.B);
-        a.take(sizeof(int) * k * s.B);
-        a.take(sizeof(uint16_t) * (size_t)(s.B * round_up(k, PAD) * round_up(s.m, 8)));
-        a.take(sizeof(uint16_t) * (size_t)(s.B * k * round_up(s.m, 8)));
-        GramBufs gb;
-        plan_gram(a, s.B, k, s.m, dt, ns, &gb, true);
-      }
+      if (dt != GNS_BF16) return fail(GNS_ERR_UNSUPPORTED, "Muon steps take bf16 W, G, M");
+      if ((rc = check_muon(*mp))) return rc;
+      MuonBufs mb;
+      plan_muon(a, s, *mp, ns, &mb);
     } else if (op == GNS_OP_FRAC_SELECT) {
       a.take(sizeof(unsigned long long) * KEY_DIGITS * s.n * s.B);
       a.take(sizeof(int) * s.n * s.B);
@@ -665,6 +771,8 @@ static int ns_common(bool gram, const gns_batch* x, const gns_batch* out, int ng
   Arena a;
   a.base = static_cast<uint8_t*>(ws);
   std::string err;
+  const gns_ns_params nse = effective_ns(*ns);
+  ns = &nse;
   for (int gi = 0; gi < ngroups; ++gi) {
     GroupShape s = shape_of(x[gi]);
     Src src;
@@ -778,15 +886,15 @@ int gns_sym_poly_update(const gns_batch* R, const gns_batch* Q, const gns_batch*
   return GNS_OK;
 }
 
-int gns_muon_step(const gns_batch* W, const gns_batch* G, const gns_batch* M, int ngroups,
+int gns_muon_step(const gns_batch* W, const gns_batch* G, const gns_batch* M, const gns_batch* V, int ngroups,
                   const gns_muon_params* mp, const gns_ns_params* ns, void* ws, size_t ws_bytes,
                   int32_t* dev_status, void* stream) {
   if (!W || !G || !M || !mp) return fail(GNS_ERR_INVALID, "null argument");
-  if (!(mp->frac > 0.f) || mp->frac > 1.f) return fail(GNS_ERR_INVALID, "frac must be in (0, 1]");
-  if (!std::isfinite(mp->lr) || !std::isfinite(mp->momentum) || !std::isfinite(mp->weight_decay) ||
-      !std::isfinite(mp->scale))
-    return fail(GNS_ERR_INVALID, "muon params must be finite");
+  if (ngroups < 1) return fail(GNS_ERR_INVALID, "need at least one batch");
   int rc;
+  if ((rc = check_muon(*mp))) return rc;
+  const bool normuon = step_flavor(*mp) == GNS_FLAVOR_NORMUON;
+  if (normuon && !V) return fail(GNS_ERR_INVALID, "NorMuon needs the second-moment batches V");
   for (int gi = 0; gi < ngroups; ++gi) {
     if ((rc = check_batch(&W[gi], GNS_BF16, "W")) || (rc = check_batch(&G[gi], GNS_BF16, "G")) ||
         (rc = check_batch(&M[gi], GNS_BF16, "M")))
@@ -795,90 +903,136 @@ int gns_muon_step(const gns_batch* W, const gns_batch* G, const gns_batch* M, in
       return fail(GNS_ERR_INVALID, "W, G, M must have equal shapes");
     if (W[gi].ptr == G[gi].ptr || W[gi].ptr == M[gi].ptr || G[gi].ptr == M[gi].ptr)
       return fail(GNS_ERR_INVALID, "W, G, M may not alias");
+    if (normuon) {
+      if ((rc = check_batch(&V[gi], GNS_F32, "V"))) return rc;
+      if (V[gi].count != M[gi].count || V[gi].rows != 1 || V[gi].cols != std::min(M[gi].rows, M[gi].cols))
+        return fail(GNS_ERR_INVALID, "V must be count x 1 x min(rows, cols) (fp32)");
+      if (V[gi].ptr == W[gi].ptr || V[gi].ptr == G[gi].ptr || V[gi].ptr == M[gi].ptr)
+        return fail(GNS_ERR_INVALID, "V may not alias W, G or M");
+    }
   }
   size_t need = gns_workspace_size(GNS_OP_MUON_STEP, M, ngroups, GNS_BF16, ns, mp);
   if (!need) return GNS_ERR_INVALID;
   if ((rc = check_ws(ws, ws_bytes, need))) return rc;
+  const gns_ns_params nse = effective_ns(*ns);
+  ns = &nse;
   Arena a;
   a.base = static_cast<uint8_t*>(ws);
   std::string err;
   const float lr = mp->lr, mu = mp->momentum;
   const float decay = 1.f - mp->lr * mp->weight_decay;
+  const float step_scale = -lr * mp->scale;
   for (int gi = 0; gi < ngroups; ++gi) {
     GroupShape s = shape_of(M[gi]);
     MatRef mm = to_ref(M[gi]), gm = to_ref(G[gi]), wm = to_ref(W[gi]);
-    if (mp->frac >= 1.f) {
-      // Muon, eq. (1): M <- mu M + G; W <- (1 - lr wd) W - lr scale polar(M)
+    MatRef vm;
+    if (normuon) vm = to_ref(V[gi]);
+    MuonBufs mb;
+    plan_muon(a, s, *mp, ns, &mb);
+    if (mb.flavor == GNS_FLAVOR_ROWNORM) {
+      // Scaling Muon for DiTs eq. (5), (7) off a refresh step: M <- mu M + G;
+      // W <- (1 - lr wd) W - lr scale gamma R_eps(M) on the oriented rows of M
+      if ((rc = launch_momentum(mm, gm, s.B, mu, 0, nullptr, stream, &err))) return fail(rc, err);
+      if (!s.trans)
+        rc = launch_row_sumsq(mm, s.rows, s.cols, s.B, mb.s, stream, &err);
+      else
+        rc = launch_col_sumsq(mm, s.B, mb.part, mb.s, stream, &err);
+      if (rc) return fail(rc, err);
+      if ((rc = launch_rownorm_scale(mb.s, s.B * s.n, mp->rownorm_gamma, mp->norm_eps, mb.r, stream, &err)))
+        return fail(rc, err);
+      if ((rc = launch_rowscale_update(wm, mm, mb.r, s.B, s.trans, step_scale, decay, stream, &err)))
+        return fail(rc, err);
+      continue;
+    }
+    if (!mb.frac) {
+      // Muon, eq. (1) (NorMuon, eq. (2)): M <- mu M + G; O = polar(M); W <- (1 - lr wd) W - lr scale O
+      float* partials = mb.use_std ? mb.sb.partials : mb.gb.partials;
+      float* inv = mb.use_std ? mb.sb.inv : mb.gb.inv;
+      if ((rc = launch_momentum(mm, gm, s.B, mu, 0, partials, stream, &err))) return fail(rc, err);
+      if ((rc = launch_finalize_norm(partials, s.B, ns->eps, inv, stream, &err))) return fail(rc, err);
       Src src;
       src.mat = mm;
       src.trans = s.trans;
-      if (s.n == s.m) {
-        StdBufs sb;
-        plan_std(a, s.B, s.n, s.m, GNS_BF16, &sb, true);
-        if ((rc = launch_momentum(mm, gm, s.B, mu, 0, sb.partials, stream, &err))) return fail(rc, err);
-        if ((rc = launch_finalize_norm(sb.partials, s.B, ns->eps, sb.inv, stream, &err))) return fail(rc, err);
-        MatRef xt;
-        if ((rc = run_std(GNS_BF16, src, s.B, s.n, s.m, ns, sb, sb.inv, nullptr, &xt, dev_status, stream)))
-          return rc;
-        MatRef xv = xt;
-        xv.rows = s.n;
-        if ((rc = launch_axpby(GNS_BF16, wm, xv, s.B, -lr * mp->scale, decay, stream, &err))) return fail(rc, err);
-      } else {
-        GramBufs gb;
-        plan_gram(a, s.B, s.n, s.m, GNS_BF16, ns, &gb, true);
-        if ((rc = launch_momentum(mm, gm, s.B, mu, 0, gb.partials, stream, &err))) return fail(rc, err);
-        if ((rc = launch_finalize_norm(gb.partials, s.B, ns->eps, gb.inv, stream, &err))) return fail(rc, err);
-        Final fin;
-        fin.D = wm;
+      if (mb.nsdt == GNS_F16) {
+        // Dion3 Algorithm 3 lines 2-3: the normalised momentum, rounded once to float16
+        if ((rc = launch_cast_scaled(mb.x16, mm, inv, s.B, stream, &err))) return fail(rc, err);
+        src.mat = mb.x16;
+        src.user = false;
+      }
+      Final fin;
+      fin.out_dt = GNS_BF16;
+      if (normuon) {
+        fin.D = mb.o;  // O, oriented
+      } else if (!mb.use_std) {
+        fin.D = wm;  // the weight update in the last product's epilogue
         fin.d_trans = s.trans;
-        fin.alpha = -lr * mp->scale;
+        fin.alpha = step_scale;
         fin.beta = decay;
         fin.has_c = true;
-        if ((rc = run_gram(GNS_BF16, src, s.B, s.n, s.m, ns, gb, gb.inv, fin, dev_status, stream))) return rc;
       }
-    } else {
-      // Dion3 Algorithm 4 (Muon flavour)
-      const int64_t k = frac_k(mp->frac, s.n);
-      auto* keys = static_cast<unsigned long long*>(a.take(sizeof(unsigned long long) * KEY_DIGITS * s.n * s.B));
-      auto* nf = static_cast<int*>(a.take(sizeof(int) * s.n * s.B));
-      auto* idx = static_cast<int*>(a.take(sizeof(int) * k * s.B));
-      MatRef xs;
-      xs.rows = k;
-      xs.cols = s.m;
-      xs.ld = round_up(s.m, 8);
-      xs.stride = round_up(k, PAD) * xs.ld;
-      xs.ptr = a.take(sizeof(uint16_t) * (size_t)(s.B * xs.stride));
-      MatRef os;  // O = polar(M[S]) before it is scattered into W
-      os.rows = k;
-      os.cols = s.m;
-      os.ld = round_up(s.m, 8);
-      os.stride = k * os.ld;
-      os.ptr = a.take(sizeof(uint16_t) * (size_t)(s.B * os.stride));
-      GramBufs gb;
-      plan_gram(a, s.B, k, s.m, GNS_BF16, ns, &gb, true);
-      // line 2: M <- M + G, with the exact l1 keys of the oriented rows
-      if ((rc = launch_frac_add_keys(mm, gm, s.B, s.trans, keys, nf, stream, &err))) return fail(rc, err);
-      // line 3: selection
-      if ((rc = launch_select_topk(keys, nf, s.n, k, s.B, idx, stream, &err))) return fail(rc, err);
-      // gather M[S, :] and its Frobenius norm
-      if ((rc = launch_gather(mm, s.B, s.trans, idx, k, xs, gb.partials, stream, &err))) return fail(rc, err);
-      if ((rc = launch_finalize_norm(gb.partials, s.B, ns->eps, gb.inv, stream, &err))) return fail(rc, err);
-      // line 8 on the rows that are not updated below
-      if (decay != 1.f && (rc = launch_scale_unselected(wm, s.B, s.trans, idx, k, decay, stream, &err)))
-        return fail(rc, err);
-      // line 4: O = polar(M[S])
-      Src src;
-      src.mat = xs;
-      src.trans = 0;
-      Final fin;
-      fin.D = os;
-      if ((rc = run_gram(GNS_BF16, src, s.B, k, s.m, ns, gb, gb.inv, fin, dev_status, stream))) return rc;
-      // lines 8, 9: W[S] <- (1 - lr wd) W[S] - lr scale O, one rounding
-      if ((rc = launch_scatter_update(wm, os, s.B, s.trans, idx, k, -lr * mp->scale, decay, stream, &err)))
-        return fail(rc, err);
-      // line 10: error feedback
-      if ((rc = launch_decay_selected(mm, s.B, s.trans, idx, k, mu, stream, &err))) return fail(rc, err);
+      if (mb.use_std) {
+        MatRef xt;
+        if ((rc = run_std(mb.nsdt, src, s.B, s.n, s.m, ns, mb.sb, inv, normuon ? &fin : nullptr, &xt, dev_status,
+                          stream)))
+          return rc;
+        if (!normuon) {
+          MatRef xv = xt;
+          xv.rows = s.n;
+          if ((rc = launch_axpby(GNS_BF16, wm, xv, s.B, step_scale, decay, stream, &err, mb.nsdt)))
+            return fail(rc, err);
+        }
+      } else {
+        if ((rc = run_gram(mb.nsdt, src, s.B, s.n, s.m, ns, mb.gb, inv, fin, dev_status, stream))) return rc;
+      }
+      if (normuon) {
+        // eq. (2): second moments of the rows of O, row scaling, Frobenius rescale, update
+        if ((rc = launch_row_sumsq(mb.o, s.n, s.m, s.B, mb.s, stream, &err))) return fail(rc, err);
+        if ((rc = launch_normuon_rows(mb.s, vm, nullptr, s.n, s.m, s.B, mp->beta2, mp->norm_eps, mb.r, stream,
+                                      &err)))
+          return fail(rc, err);
+        if ((rc = launch_scatter_update(wm, mb.o, s.B, s.trans, nullptr, s.n, step_scale, decay, stream, &err,
+                                        mb.r)))
+          return fail(rc, err);
+      }
+      continue;
     }
+    // Dion3 Algorithm 4
+    const int64_t k = mb.k;
+    // line 2: M <- M + G, with the exact l1 keys of the oriented rows
+    if ((rc = launch_frac_add_keys(mm, gm, s.B, s.trans, mb.keys, mb.nf, stream, &err))) return fail(rc, err);
+    // line 3: selection
+    if ((rc = launch_select_topk(mb.keys, mb.nf, s.n, k, s.B, mb.idx, stream, &err))) return fail(rc, err);
+    // gather M[S, :] and its Frobenius norm
+    if ((rc = launch_gather(mm, s.B, s.trans, mb.idx, k, mb.xs, mb.gb.partials, stream, &err))) return fail(rc, err);
+    if ((rc = launch_finalize_norm(mb.gb.partials, s.B, ns->eps, mb.gb.inv, stream, &err))) return fail(rc, err);
+    // line 8 on the rows that are not updated below
+    if (decay != 1.f && (rc = launch_scale_unselected(wm, s.B, s.trans, mb.idx, k, decay, stream, &err)))
+      return fail(rc, err);
+    // line 4: O = polar(M[S])
+    Src src;
+    src.mat = mb.xs;
+    src.trans = 0;
+    if (mb.nsdt == GNS_F16) {
+      if ((rc = launch_cast_scaled(mb.x16, mb.xs, mb.gb.inv, s.B, stream, &err))) return fail(rc, err);
+      src.mat = mb.x16;
+      src.user = false;
+    }
+    Final fin;
+    fin.D = mb.os;
+    fin.out_dt = GNS_BF16;
+    if ((rc = run_gram(mb.nsdt, src, s.B, k, s.m, ns, mb.gb, mb.gb.inv, fin, dev_status, stream))) return rc;
+    // lines 5-7 (NorMuon flavour): second moments of the selected rows, scaling, rescale
+    if (normuon) {
+      if ((rc = launch_row_sumsq(mb.os, k, s.m, s.B, mb.s, stream, &err))) return fail(rc, err);
+      if ((rc = launch_normuon_rows(mb.s, vm, mb.idx, k, s.m, s.B, mp->beta2, mp->norm_eps, mb.r, stream, &err)))
+        return fail(rc, err);
+    }
+    // lines 8, 9: W[S] <- (1 - lr wd) W[S] - lr scale O, one rounding
+    if ((rc = launch_scatter_update(wm, mb.os, s.B, s.trans, mb.idx, k, step_scale, decay, stream, &err,
+                                    normuon ? mb.r : nullptr)))
+      return fail(rc, err);
+    // line 10: error feedback
+    if ((rc = launch_decay_selected(mm, s.B, s.trans, mb.idx, k, mu, stream, &err))) return fail(rc, err);
   }
   return GNS_OK;
 }

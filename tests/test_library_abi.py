@@ -120,8 +120,8 @@ def test_calls_reject_bad_arguments_before_launch(lib):
                                  None, None)
     assert rc == _lib.GNS_ERR_INVALID and b"alias" in _lib.last_error().encode()
     mp = _lib.GnsMuonParams(0.02, 0.95, 0.0, 1.0, 1.5)
-    rc = lib.gns_muon_step(b, o, _batch(1, 64, 128, ptr=1 << 22), 1, ctypes.byref(mp), ctypes.byref(_ns()), None, 0,
-                           None, None)
+    rc = lib.gns_muon_step(b, o, _batch(1, 64, 128, ptr=1 << 22), None, 1, ctypes.byref(mp), ctypes.byref(_ns()),
+                           None, 0, None, None)
     assert rc == _lib.GNS_ERR_INVALID and b"frac" in _lib.last_error().encode()
     rc = lib.gns_frac_row_select(b, 65, ctypes.c_void_p(1 << 23), None, ctypes.c_void_p(1 << 24), 1 << 30, None)
     assert rc == _lib.GNS_ERR_INVALID

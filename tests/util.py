@@ -69,3 +69,15 @@ def bf16_ulp(x):
     x = np.abs(np.asarray(x, dtype=np.float64))
     e = np.floor(np.log2(np.maximum(x, 2.0 ** -126)))
     return 2.0 ** (e - 7)
+
+
+def f16_input(seed, shape, scale=1.0, stream=0):
+    """(float16 array, float64 decoded) of a seeded input rounded once to fp16 (numpy's
+    float16 conversion rounds to nearest even)."""
+    x16 = (inputs.gaussian(seed, shape, scale, stream=stream)).astype(np.float16)
+    return x16, x16.astype(np.float64)
+
+
+def f16_to_torch(x16, device="cuda"):
+    import torch
+    return padded_copy(torch.from_numpy(np.ascontiguousarray(x16)).to(device))
