@@ -308,6 +308,54 @@ def run_ours(args, rank, world, dist):
     std_ms = time_ns(gns.ns_standard_batched, ws_s)
     del ws_g, ws_s, X, out
 
+    # ---- the other update flavours on the same workload (whole steps, inputs in HBM) ----
+    V = torch.zeros((COUNT, 1, ROWS), dtype=torch.float32, device=dev)
+
+    def time_flavor(params, with_v=False):
+        need = gns.workspace_size(_lib.GNS_OP_MUON_STEP, M, ns, muon=params)
+        ws_f = gns.alloc_workspace(need, dev)
+
+        def go():
+            gns.muon_step(W, G, M, ns=ns, workspace=ws_f, status=status, stream=stream, params=params,
+                          V=V if with_v else None)
+        for _ in range(3):
+            go()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = max(10, args.steps // 4)
+        a.record(stream)
+        for _ in range(reps):
+            go()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    base = dict(lr=LR, momentum=MU)
+    f16_ms = time_flavor(gns.MuonParams(**base, ns_dtype=torch.float16))
+    normuon_ms = time_flavor(gns.MuonParams(**base, flavor="normuon", beta2=0.95, norm_eps=1e-8), with_v=True)
+    rownorm_ms = time_flavor(gns.MuonParams(**base, flavor="rownorm", rownorm_gamma=0.15, norm_eps=1e-8))
+    frac_ms = time_flavor(gns.MuonParams(**base, frac=0.25))
+    _, _, hbm_peak, _ = load_peaks()
+    # RowNorm step: algorithmic traffic = read G, M, W and write M, W once (bf16)
+    rn_bytes = COUNT * ROWS * COLS * 2 * 5
+    flavors = {
+        "note": "whole optimizer steps on the same 24 x 1024 x 4096 bf16 workload, inputs in HBM",
+        "fp16_products": {"ms_per_step": f16_ms, "matrices_per_s": COUNT / (f16_ms / 1000.0),
+                          "what": "Muon step with the Newton-Schulz products in fp16 (Dion3 Algorithm 3 line 3)"},
+        "normuon": {"ms_per_step": normuon_ms, "matrices_per_s": COUNT / (normuon_ms / 1000.0),
+                    "what": "NorMuon (Dion3 eq. (2)): Gram NS to O, row second moments, row scaling, update"},
+        "rownorm": {"ms_per_step": rownorm_ms, "matrices_per_s": COUNT / (rownorm_ms / 1000.0),
+                    "what": "RowNorm off-refresh step (Scaling Muon for DiTs eq. (5), (7))",
+                    "roofline": {"bound": "hbm", "achieved": rn_bytes / (rownorm_ms / 1000.0) / 1e9,
+                                 "peak": hbm_peak, "unit": "GB/s",
+                                 "frac": rn_bytes / (rownorm_ms / 1000.0) / 1e9 / hbm_peak,
+                                 "algorithmic_bytes": rn_bytes}},
+        "periodic_K3_mean_ms_per_step": ms / 3.0 + 2.0 * rownorm_ms / 3.0,
+        "frac_quarter": {"ms_per_step": frac_ms, "matrices_per_s": COUNT / (frac_ms / 1000.0),
+                         "what": "Dion3 fractional update, f = 1/4 (Algorithm 4, Muon flavour)"},
+    }
+    del V
+
     st = int(status.item())
     if rank != 0:
         return 0
@@ -339,6 +387,7 @@ def run_ours(args, rank, world, dist):
         "gram_vs_standard": {"gram_ns_ms": gram_ms, "standard_ns_ms": std_ms, "speedup": std_ms / gram_ms,
                              "note": "orthogonalization of the 24 matrices alone, same tcgen05 kernels, T=5; "
                                      "standard NS with symmetric products (Dion3 Algorithm 1, sec. 2.3)"},
+        "flavors": flavors,
         "gpu_launches": n_all.value,
         "device_status": st,
         "clocks": clk,

@@ -70,17 +70,31 @@ __device__ __forceinline__ __half from_f<__half>(float v) {
 // ---------------------------------------------------------------------------------------
 // sum of squares per matrix (read only), partials[b * npart + part]
 
+// Rows start on 16-byte boundaries (ld and the base are 16-byte aligned), so each thread
+// reads 16-byte vectors of VEC elements; a scalar tail covers cols % VEC.
 template <typename T>
 __global__ void sumsq_kernel(const T* X, long long ld, long long stride, int rows, int cols, int npart,
                              float* partials) {
+  constexpr int VEC = 16 / sizeof(T);
   const int b = blockIdx.y, part = blockIdx.x;
   const int rp = (rows + npart - 1) / npart;
   const int r0 = part * rp, r1 = min(rows, r0 + rp);
   const T* Xb = X + (long long)b * stride;
+  const int cvec = cols - cols % VEC;
   float acc = 0.f;
   for (int r = r0; r < r1; ++r) {
     const T* row = Xb + (long long)r * ld;
-    for (int c = threadIdx.x; c < cols; c += blockDim.x) {
+#pragma unroll 4
+    for (int c = threadIdx.x * VEC; c < cvec; c += blockDim.x * VEC) {
+      const uint4 u = *reinterpret_cast<const uint4*>(row + c);
+      const T* e = reinterpret_cast<const T*>(&u);
+#pragma unroll
+      for (int q = 0; q < VEC; ++q) {
+        const float v = to_f(e[q]);
+        acc = fmaf(v, v, acc);
+      }
+    }
+    for (int c = cvec + threadIdx.x; c < cols; c += blockDim.x) {
       const float v = to_f(row[c]);
       acc = fmaf(v, v, acc);
     }
@@ -88,6 +102,10 @@ __global__ void sumsq_kernel(const T* X, long long ld, long long stride, int row
   const float s = block_sum_256(acc);
   if (threadIdx.x == 0) partials[(long long)b * npart + part] = s;
 }
+
+// Rows of a batch processed by one block each chunk of ROWS_PER_BLOCK rows, threads over
+// 16-byte vectors of the row.
+constexpr int ROWS_PER_BLOCK = 4;
 
 // ---------------------------------------------------------------------------------------
 // momentum: M <- mu * M + G (mode 0; fp32 product, fp32 sum, one bf16 rounding) or
@@ -348,7 +366,7 @@ __global__ void __launch_bounds__(1024) select_topk_kernel(unsigned long long* k
                                                            int* idx) {
   extern __shared__ uint8_t st[];  // n states: 0 candidate, 1 selected, 2 rejected
   __shared__ unsigned hist[256];
-  __shared__ int sh_T, sh_kleft, sh_cnt;
+  __shared__ int sh_T, sh_kleft, sh_cnt, sh_top;
   const int b = blockIdx.x;
   unsigned long long* K = keys + (long long)b * n * KEY_DIGITS;
   const int* F = nf + (long long)b * n;
@@ -368,9 +386,25 @@ __global__ void __launch_bounds__(1024) select_topk_kernel(unsigned long long* k
     }
     st[i] = 0;
   }
+  if (threadIdx.x == 0) sh_top = 0;
+  __syncthreads();
+  // the most significant non-zero key byte: the bytes above it are zero in every key, so
+  // the radix passes start there
+  {
+    int top = 0;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+      const unsigned long long* kr = K + (long long)i * KEY_DIGITS;
+      for (int d = KEY_DIGITS - 1; d >= 0; --d)
+        if (kr[d]) {
+          top = max(top, d * 4 + (31 - __clz((unsigned)kr[d])) / 8);
+          break;
+        }
+    }
+    atomicMax(&sh_top, top);
+  }
   int kleft = k;
   __syncthreads();
-  for (int p = KEY_DIGITS * 4 - 1; p >= 0; --p) {
+  for (int p = sh_top; p >= 0; --p) {
     for (int h = threadIdx.x; h < 256; h += blockDim.x) hist[h] = 0;
     __syncthreads();
     const int dg = p >> 2, sh = (p & 3) * 8;
@@ -440,7 +474,18 @@ __global__ void gather_rows_kernel(const bf16* M, long long ldm, long long sm, c
     const int r = idx[(long long)b * k + i];
     const bf16* src = M + (long long)b * sm + (long long)r * ldm;
     bf16* dst = X + (long long)b * sx + (long long)i * ldx;
-    for (int c = threadIdx.x; c < cols; c += blockDim.x) {
+    const int cvec = cols & ~7;
+    for (int c = threadIdx.x * 8; c < cvec; c += blockDim.x * 8) {
+      const uint4 u = *reinterpret_cast<const uint4*>(src + c);
+      *reinterpret_cast<uint4*>(dst + c) = u;
+      const bf16* e = reinterpret_cast<const bf16*>(&u);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float f = bf16_to_f(e[q]);
+        acc = fmaf(f, f, acc);
+      }
+    }
+    for (int c = cvec + threadIdx.x; c < cols; c += blockDim.x) {
       const bf16 v = src[c];
       dst[c] = v;
       const float f = bf16_to_f(v);
@@ -471,71 +516,136 @@ __global__ void gather_cols_kernel(const bf16* M, long long ldm, long long sm, c
   }
 }
 
-// M[b][idx[i]][:] <- bf16(mu * M) (trans = 0) or M[b][:][idx[i]] (trans = 1).
-__global__ void decay_selected_kernel(bf16* M, long long ldm, long long sm, const int* idx, int k, int len,
-                                      int trans, float mu) {
+// M[b][idx[i]][:] <- bf16(mu * M): one block per selected row, 16-byte vectors.
+__global__ void decay_selected_rows_kernel(bf16* M, long long ldm, long long sm, const int* idx, int k, int len,
+                                           float mu) {
+  const int b = blockIdx.y, i = blockIdx.x;
+  bf16* row = M + (long long)b * sm + (long long)idx[(long long)b * k + i] * ldm;
+  const int cvec = len & ~7;
+  for (int c = threadIdx.x * 8; c < cvec; c += blockDim.x * 8) {
+    uint4 u = *reinterpret_cast<const uint4*>(row + c);
+    bf16* e = reinterpret_cast<bf16*>(&u);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) e[q] = f_to_bf16(__fmul_rn(mu, bf16_to_f(e[q])));
+    *reinterpret_cast<uint4*>(row + c) = u;
+  }
+  for (int c = cvec + threadIdx.x; c < len; c += blockDim.x) row[c] = f_to_bf16(__fmul_rn(mu, bf16_to_f(row[c])));
+}
+
+// M[b][:][idx[i]] <- bf16(mu * M) (selected columns): 32 selected columns x 32 rows per
+// block, consecutive threads on consecutive selected columns.
+__global__ void decay_selected_cols_kernel(bf16* M, long long ldm, long long sm, const int* idx, int k, int rows,
+                                           float mu) {
   const int b = blockIdx.z;
-  const int i = blockIdx.y;
+  const int i = blockIdx.x * 32 + (threadIdx.x & 31);
+  if (i >= k) return;
   const int sel = idx[(long long)b * k + i];
-  bf16* Mb = M + (long long)b * sm;
-  for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < len; j += gridDim.x * blockDim.x) {
-    bf16* p = trans ? Mb + (long long)j * ldm + sel : Mb + (long long)sel * ldm + j;
-    *p = f_to_bf16(__fmul_rn(mu, bf16_to_f(*p)));
+  bf16* Mb = M + (long long)b * sm + sel;
+  const int j0 = blockIdx.y * 32;
+  for (int jj = threadIdx.x >> 5; jj < 32; jj += blockDim.x >> 5) {
+    const int j = j0 + jj;
+    if (j < rows) {
+      bf16* p = Mb + (long long)j * ldm;
+      *p = f_to_bf16(__fmul_rn(mu, bf16_to_f(*p)));
+    }
   }
 }
 
-// Rows (trans = 0) or columns (trans = 1) of W that are NOT in idx get W <- bf16(factor W).
-__global__ void scale_unselected_kernel(bf16* W, long long ldw, long long sw, int rows, int cols, const int* idx,
-                                        int k, int trans, float factor) {
-  const int b = blockIdx.z;
-  const int* sel = idx + (long long)b * k;
-  bf16* Wb = W + (long long)b * sw;
-  const long long total = (long long)rows * cols;
-  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (long long)gridDim.x * blockDim.x) {
-    const int r = (int)(e / cols), c = (int)(e % cols);
-    const int key = trans ? c : r;
-    int lo = 0, hi = k;
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (sel[mid] < key) lo = mid + 1; else hi = mid;
+// flags[b*n + idx[b*k + i]] = 1 (flags zeroed before).
+__global__ void mark_selected_kernel(const int* idx, int k, int n, int count, int* flags) {
+  const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= (long long)k * count) return;
+  const int b = (int)(e / k);
+  flags[(long long)b * n + idx[e]] = 1;
+}
+
+// Rows (trans = 0) or columns (trans = 1) of W whose flag is 0 get W <- bf16(factor W); a
+// block per ROWS_PER_BLOCK rows, 16-byte vectors.
+__global__ void scale_unselected_kernel(bf16* W, long long ldw, long long sw, int rows, int cols, const int* flags,
+                                        int trans, float factor) {
+  const int b = blockIdx.y;
+  const int nf = trans ? cols : rows;
+  const int* F = flags + (long long)b * nf;
+  const int cvec = cols & ~7;
+  for (int r = blockIdx.x * ROWS_PER_BLOCK; r < min(rows, (int)(blockIdx.x + 1) * ROWS_PER_BLOCK); ++r) {
+    if (!trans && F[r]) continue;
+    bf16* row = W + (long long)b * sw + (long long)r * ldw;
+    for (int c = threadIdx.x * 8; c < cvec; c += blockDim.x * 8) {
+      uint4 u = *reinterpret_cast<const uint4*>(row + c);
+      bf16* e = reinterpret_cast<bf16*>(&u);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (!trans || !F[c + q]) e[q] = f_to_bf16(__fmul_rn(factor, bf16_to_f(e[q])));
+      *reinterpret_cast<uint4*>(row + c) = u;
     }
-    if (lo < k && sel[lo] == key) continue;
-    bf16* p = Wb + (long long)r * ldw + c;
-    *p = f_to_bf16(__fmul_rn(factor, bf16_to_f(*p)));
+    for (int c = cvec + threadIdx.x; c < cols; c += blockDim.x)
+      if (!trans || !F[c]) row[c] = f_to_bf16(__fmul_rn(factor, bf16_to_f(row[c])));
   }
 }
 
-// Selected rows of W (or columns, trans = 1) take beta * W + alpha * r_i * O:
-// W[idx[i]][j] (trans: W[j][idx[i]]) for O[i][j], i < k, j < len; fp32 arithmetic, one
-// rounding (the weight update of Dion3 sec. 6 on the selected rows only). idx == NULL
-// selects every row (i itself); rs == NULL means r_i = 1 (NorMuon passes its row scales).
-__global__ void scatter_update_kernel(bf16* W, long long ldw, long long sw, const bf16* O, long long ldo,
-                                      long long so, const int* idx, const float* rs, int k, int len, int trans,
-                                      float alpha, float beta) {
+// Selected rows of W take beta * W + alpha * r_i * O: W[idx[i]][j] for O[i][j], i < k,
+// j < len; fp32 arithmetic, one rounding (the weight update of Dion3 sec. 6 on the selected
+// rows only). idx == NULL selects every row (i itself); rs == NULL means r_i = 1 (NorMuon
+// passes its row scales). One block per row of O, 16-byte vectors.
+__global__ void scatter_update_rows_kernel(bf16* W, long long ldw, long long sw, const bf16* O, long long ldo,
+                                           long long so, const int* idx, const float* rs, int k, int len, float alpha,
+                                           float beta) {
+  const int b = blockIdx.y, i = blockIdx.x;
+  const long long e = (long long)b * k + i;
+  const int sel = idx ? idx[e] : i;
+  const float a = rs ? alpha * rs[e] : alpha;
+  bf16* wr = W + (long long)b * sw + (long long)sel * ldw;
+  const bf16* orow = O + (long long)b * so + (long long)i * ldo;
+  const int cvec = len & ~7;
+  for (int c = threadIdx.x * 8; c < cvec; c += blockDim.x * 8) {
+    uint4 wu = *reinterpret_cast<const uint4*>(wr + c);
+    const uint4 ou = *reinterpret_cast<const uint4*>(orow + c);
+    bf16* we = reinterpret_cast<bf16*>(&wu);
+    const bf16* oe = reinterpret_cast<const bf16*>(&ou);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) we[q] = f_to_bf16(fmaf(a, bf16_to_f(oe[q]), beta * bf16_to_f(we[q])));
+    *reinterpret_cast<uint4*>(wr + c) = wu;
+  }
+  for (int c = cvec + threadIdx.x; c < len; c += blockDim.x)
+    wr[c] = f_to_bf16(fmaf(a, bf16_to_f(orow[c]), beta * bf16_to_f(wr[c])));
+}
+
+// The same for the columns of a tall W: W[j][idx[i]] for O[i][j]. A 32 x 32 tile of O goes
+// through shared memory so that both the O reads and the W accesses are along rows.
+__global__ void scatter_update_cols_kernel(bf16* W, long long ldw, long long sw, const bf16* O, long long ldo,
+                                           long long so, const int* idx, const float* rs, int k, int len, float alpha,
+                                           float beta) {
+  __shared__ float tile[32][33];
   const int b = blockIdx.z;
-  const long long total = (long long)k * len;
-  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (long long)gridDim.x * blockDim.x) {
-    int i, j;
-    if (!trans) {
-      i = (int)(e / len);
-      j = (int)(e % len);
-    } else {
-      j = (int)(e / k);
-      i = (int)(e % k);
+  const int i0 = blockIdx.x * 32, j0 = blockIdx.y * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
+  for (int ii = ty; ii < 32; ii += 8) {
+    const int i = i0 + ii, j = j0 + tx;
+    float v = 0.f;
+    if (i < k && j < len) {
+      v = bf16_to_f(O[(long long)b * so + (long long)i * ldo + j]);
+      if (rs) v *= rs[(long long)b * k + i];
     }
-    const int sel = idx ? idx[(long long)b * k + i] : i;
-    bf16* p = W + (long long)b * sw + (trans ? (long long)j * ldw + sel : (long long)sel * ldw + j);
-    float o = bf16_to_f(O[(long long)b * so + (long long)i * ldo + j]);
-    if (rs) o *= rs[(long long)b * k + i];
-    *p = f_to_bf16(fmaf(alpha, o, beta * bf16_to_f(*p)));
+    tile[ii][tx] = v;
+  }
+  __syncthreads();
+  const int i = i0 + tx;
+  if (i >= k) return;
+  const int sel = idx ? idx[(long long)b * k + i] : i;
+  for (int jj = ty; jj < 32; jj += 8) {
+    const int j = j0 + jj;
+    if (j < len) {
+      bf16* p = W + (long long)b * sw + (long long)j * ldw + sel;
+      *p = f_to_bf16(fmaf(alpha, tile[tx][jj], beta * bf16_to_f(*p)));
+    }
   }
 }
 
 // ---------------------------------------------------------------------------------------
 // NorMuon and RowNorm statistics
 
-// s[b*k + i] = sum_j X[b][i][j]^2 over the k rows of X (bf16), one warp per row, lanes in a
-// fixed order.
+// s[b*k + i] = sum_j X[b][i][j]^2 over the k rows of X (bf16), one warp per row, lanes on
+// 16-byte vectors in a fixed order.
 __global__ void row_sumsq_kernel(const bf16* X, long long ldx, long long sx, int k, int cols, int count, float* s) {
   const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -543,7 +653,18 @@ __global__ void row_sumsq_kernel(const bf16* X, long long ldx, long long sx, int
   const int b = (int)(row / k), i = (int)(row % k);
   const bf16* r = X + (long long)b * sx + (long long)i * ldx;
   float acc = 0.f;
-  for (int c = lane; c < cols; c += 32) {
+  const int cvec = cols & ~7;
+#pragma unroll 4
+  for (int c = lane * 8; c < cvec; c += 32 * 8) {
+    const uint4 u = *reinterpret_cast<const uint4*>(r + c);
+    const bf16* e = reinterpret_cast<const bf16*>(&u);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float v = bf16_to_f(e[q]);
+      acc = fmaf(v, v, acc);
+    }
+  }
+  for (int c = cvec + lane; c < cols; c += 32) {
     const float v = bf16_to_f(r[c]);
     acc = fmaf(v, v, acc);
   }
@@ -627,34 +748,58 @@ __global__ void rownorm_scale_kernel(const float* s, long long n, float gamma, f
   r[e] = gamma / fmaxf(sqrtf(s[e]), eps);
 }
 
-// W <- beta W + alpha r_q Y, elementwise over rows x cols, q = the row (trans = 0) or the
-// column (trans = 1) of the element: a per-oriented-row scaled update with W and Y in the same
-// physical layout. fp32 arithmetic, one rounding.
+// W <- beta W + alpha r_q Y with q the row (trans = 0) or the column (trans = 1) of each
+// element: a per-oriented-row scaled update, W and Y in the same physical layout. fp32
+// arithmetic, one rounding; a block per ROWS_PER_BLOCK rows, 16-byte vectors.
 __global__ void rowscale_update_kernel(bf16* W, long long ldw, long long sw, const bf16* Y, long long ldy,
                                        long long sy, const float* r, int rows, int cols, int trans, float alpha,
                                        float beta) {
-  const int b = blockIdx.z;
-  const long long total = (long long)rows * cols;
-  const long long nr = trans ? cols : rows;
-  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (long long)gridDim.x * blockDim.x) {
-    const int i = (int)(e / cols), j = (int)(e % cols);
-    bf16* p = W + (long long)b * sw + (long long)i * ldw + j;
-    const float y = bf16_to_f(Y[(long long)b * sy + (long long)i * ldy + j]) * r[(long long)b * nr + (trans ? j : i)];
-    *p = f_to_bf16(fmaf(alpha, y, beta * bf16_to_f(*p)));
+  const int b = blockIdx.y;
+  const float* R = r + (long long)b * (trans ? cols : rows);
+  const int cvec = cols & ~7;
+  for (int i = blockIdx.x * ROWS_PER_BLOCK; i < min(rows, (int)(blockIdx.x + 1) * ROWS_PER_BLOCK); ++i) {
+    bf16* wr = W + (long long)b * sw + (long long)i * ldw;
+    const bf16* yr = Y + (long long)b * sy + (long long)i * ldy;
+    const float ar = trans ? alpha : alpha * R[i];
+    for (int c = threadIdx.x * 8; c < cvec; c += blockDim.x * 8) {
+      uint4 wu = *reinterpret_cast<const uint4*>(wr + c);
+      const uint4 yu = *reinterpret_cast<const uint4*>(yr + c);
+      bf16* we = reinterpret_cast<bf16*>(&wu);
+      const bf16* ye = reinterpret_cast<const bf16*>(&yu);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float a = trans ? alpha * R[c + q] : ar;
+        we[q] = f_to_bf16(fmaf(a, bf16_to_f(ye[q]), beta * bf16_to_f(we[q])));
+      }
+      *reinterpret_cast<uint4*>(wr + c) = wu;
+    }
+    for (int c = cvec + threadIdx.x; c < cols; c += blockDim.x) {
+      const float a = trans ? alpha * R[c] : ar;
+      wr[c] = f_to_bf16(fmaf(a, bf16_to_f(yr[c]), beta * bf16_to_f(wr[c])));
+    }
   }
 }
 
-// X16 = fp16(inv[b] * M), elementwise in the same layout (Dion3 Algorithm 3 lines 2-3 for a
-// bf16 momentum: normalise, then round once to float16).
+// X16 = fp16(inv[b] * M) in the same layout (Dion3 Algorithm 3 lines 2-3 for a bf16
+// momentum: normalise, then round once to float16); 16-byte vectors.
 __global__ void cast_scaled_kernel(__half* X, long long ldx, long long sx, const bf16* M, long long ldm, long long sm,
                                    const float* inv, int rows, int cols) {
-  const int b = blockIdx.z;
-  const long long total = (long long)rows * cols;
+  const int b = blockIdx.y;
   const float s = inv[b];
-  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (long long)gridDim.x * blockDim.x) {
-    const int i = (int)(e / cols), j = (int)(e % cols);
-    X[(long long)b * sx + (long long)i * ldx + j] =
-        __float2half_rn(s * bf16_to_f(M[(long long)b * sm + (long long)i * ldm + j]));
+  const int cvec = cols & ~7;
+  for (int i = blockIdx.x * ROWS_PER_BLOCK; i < min(rows, (int)(blockIdx.x + 1) * ROWS_PER_BLOCK); ++i) {
+    const bf16* mr = M + (long long)b * sm + (long long)i * ldm;
+    __half* xr = X + (long long)b * sx + (long long)i * ldx;
+    for (int c = threadIdx.x * 8; c < cvec; c += blockDim.x * 8) {
+      const uint4 mu = *reinterpret_cast<const uint4*>(mr + c);
+      const bf16* me = reinterpret_cast<const bf16*>(&mu);
+      uint4 xu;
+      __half* xe = reinterpret_cast<__half*>(&xu);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) xe[q] = __float2half_rn(s * bf16_to_f(me[q]));
+      *reinterpret_cast<uint4*>(xr + c) = xu;
+    }
+    for (int c = cvec + threadIdx.x; c < cols; c += blockDim.x) xr[c] = __float2half_rn(s * bf16_to_f(mr[c]));
   }
 }
 
@@ -812,28 +957,46 @@ int launch_gather(const MatRef& M, int64_t count, int trans, const int* idx, int
 
 int launch_decay_selected(const MatRef& M, int64_t count, int trans, const int* idx, int64_t k, float mu,
                           void* stream, std::string* err) {
-  const int64_t len = trans ? M.rows : M.cols;
-  dim3 grid((unsigned)std::min<int64_t>((len + 255) / 256, 64), (unsigned)k, (unsigned)count);
-  decay_selected_kernel<<<grid, 256, 0, S(stream)>>>(static_cast<bf16*>(M.ptr), M.ld, M.stride, idx, (int)k, (int)len,
-                                                     trans, mu);
+  if (!trans) {
+    dim3 grid((unsigned)k, (unsigned)count);
+    decay_selected_rows_kernel<<<grid, 256, 0, S(stream)>>>(static_cast<bf16*>(M.ptr), M.ld, M.stride, idx, (int)k,
+                                                            (int)M.cols, mu);
+  } else {
+    dim3 grid((unsigned)((k + 31) / 32), (unsigned)((M.rows + 31) / 32), (unsigned)count);
+    decay_selected_cols_kernel<<<grid, 256, 0, S(stream)>>>(static_cast<bf16*>(M.ptr), M.ld, M.stride, idx, (int)k,
+                                                            (int)M.rows, mu);
+  }
   return check_launch("decay_selected", err);
 }
 
 int launch_scale_unselected(const MatRef& W, int64_t count, int trans, const int* idx, int64_t k, float factor,
-                            void* stream, std::string* err) {
-  dim3 grid(grid_1d(W.rows * W.cols, 256), 1, (unsigned)count);
+                            int* flags, void* stream, std::string* err) {
+  const int64_t n = trans ? W.cols : W.rows;
+  cudaMemsetAsync(flags, 0, sizeof(int) * n * count, S(stream));
+  mark_selected_kernel<<<(unsigned)((k * count + 255) / 256), 256, 0, S(stream)>>>(idx, (int)k, (int)n, (int)count,
+                                                                                  flags);
+  int rc = check_launch("mark_selected", err);
+  if (rc) return rc;
+  dim3 grid((unsigned)((W.rows + ROWS_PER_BLOCK - 1) / ROWS_PER_BLOCK), (unsigned)count);
   scale_unselected_kernel<<<grid, 256, 0, S(stream)>>>(static_cast<bf16*>(W.ptr), W.ld, W.stride, (int)W.rows,
-                                                       (int)W.cols, idx, (int)k, trans, factor);
+                                                       (int)W.cols, flags, trans, factor);
   return check_launch("scale_unselected", err);
 }
 
 int launch_scatter_update(const MatRef& W, const MatRef& O, int64_t count, int trans, const int* idx, int64_t k,
                           float alpha, float beta, void* stream, std::string* err, const float* rs) {
   const int64_t len = O.cols;
-  dim3 grid(grid_1d(k * len, 256), 1, (unsigned)count);
-  scatter_update_kernel<<<grid, 256, 0, S(stream)>>>(static_cast<bf16*>(W.ptr), W.ld, W.stride,
-                                                     static_cast<const bf16*>(O.ptr), O.ld, O.stride, idx, rs, (int)k,
-                                                     (int)len, trans, alpha, beta);
+  if (!trans) {
+    dim3 grid((unsigned)k, (unsigned)count);
+    scatter_update_rows_kernel<<<grid, 256, 0, S(stream)>>>(static_cast<bf16*>(W.ptr), W.ld, W.stride,
+                                                            static_cast<const bf16*>(O.ptr), O.ld, O.stride, idx, rs,
+                                                            (int)k, (int)len, alpha, beta);
+  } else {
+    dim3 grid((unsigned)((k + 31) / 32), (unsigned)((len + 31) / 32), (unsigned)count);
+    scatter_update_cols_kernel<<<grid, 256, 0, S(stream)>>>(static_cast<bf16*>(W.ptr), W.ld, W.stride,
+                                                            static_cast<const bf16*>(O.ptr), O.ld, O.stride, idx, rs,
+                                                            (int)k, (int)len, alpha, beta);
+  }
   return check_launch("scatter_update", err);
 }
 
@@ -872,7 +1035,7 @@ int launch_rownorm_scale(const float* s, int64_t n, float gamma, float eps, floa
 
 int launch_rowscale_update(const MatRef& W, const MatRef& Y, const float* r, int64_t count, int trans, float alpha,
                            float beta, void* stream, std::string* err) {
-  dim3 grid(grid_1d(W.rows * W.cols, 256), 1, (unsigned)count);
+  dim3 grid((unsigned)((W.rows + ROWS_PER_BLOCK - 1) / ROWS_PER_BLOCK), (unsigned)count);
   rowscale_update_kernel<<<grid, 256, 0, S(stream)>>>(static_cast<bf16*>(W.ptr), W.ld, W.stride,
                                                       static_cast<const bf16*>(Y.ptr), Y.ld, Y.stride, r, (int)W.rows,
                                                       (int)W.cols, trans, alpha, beta);
@@ -881,7 +1044,7 @@ int launch_rowscale_update(const MatRef& W, const MatRef& Y, const float* r, int
 
 int launch_cast_scaled(const MatRef& X16, const MatRef& M, const float* inv, int64_t count, void* stream,
                        std::string* err) {
-  dim3 grid(grid_1d(M.rows * M.cols, 256), 1, (unsigned)count);
+  dim3 grid((unsigned)((M.rows + ROWS_PER_BLOCK - 1) / ROWS_PER_BLOCK), (unsigned)count);
   cast_scaled_kernel<<<grid, 256, 0, S(stream)>>>(static_cast<__half*>(X16.ptr), X16.ld, X16.stride,
                                                   static_cast<const bf16*>(M.ptr), M.ld, M.stride, inv, (int)M.rows,
                                                   (int)M.cols);

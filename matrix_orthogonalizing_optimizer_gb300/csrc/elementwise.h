@@ -27,8 +27,9 @@ int launch_gather(const MatRef& M, int64_t count, int trans, const int* idx, int
                   float* partials, void* stream, std::string* err);
 int launch_decay_selected(const MatRef& M, int64_t count, int trans, const int* idx, int64_t k, float mu,
                           void* stream, std::string* err);
+// flags: count * n ints of scratch (n = rows, or cols when trans).
 int launch_scale_unselected(const MatRef& W, int64_t count, int trans, const int* idx, int64_t k, float factor,
-                            void* stream, std::string* err);
+                            int* flags, void* stream, std::string* err);
 // rs (nullable): per-row scale of O (NorMuon); idx NULL: every row, in order.
 int launch_scatter_update(const MatRef& W, const MatRef& O, int64_t count, int trans, const int* idx, int64_t k,
                           float alpha, float beta, void* stream, std::string* err, const float* rs = nullptr);

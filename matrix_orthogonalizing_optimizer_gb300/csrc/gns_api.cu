@@ -1006,7 +1006,7 @@ int gns_muon_step(const gns_batch* W, const gns_batch* G, const gns_batch* M, co
     if ((rc = launch_gather(mm, s.B, s.trans, mb.idx, k, mb.xs, mb.gb.partials, stream, &err))) return fail(rc, err);
     if ((rc = launch_finalize_norm(mb.gb.partials, s.B, ns->eps, mb.gb.inv, stream, &err))) return fail(rc, err);
     // line 8 on the rows that are not updated below
-    if (decay != 1.f && (rc = launch_scale_unselected(wm, s.B, s.trans, mb.idx, k, decay, stream, &err)))
+    if (decay != 1.f && (rc = launch_scale_unselected(wm, s.B, s.trans, mb.idx, k, decay, mb.nf, stream, &err)))
       return fail(rc, err);
     // line 4: O = polar(M[S])
     Src src;
