@@ -741,6 +741,60 @@ __global__ void __launch_bounds__(256) normuon_rows_kernel(const float* s, float
   }
 }
 
+// One RowNorm step on the rows of a wide matrix in a single pass (Scaling Muon for DiTs
+// eq. (5), (7) off a refresh step): per row, M <- bf16(mu M + G) (fp32 product, fp32 sum),
+// s = sum of the stored M^2, r = gamma / max(sqrt(s), eps), W <- bf16(beta W + alpha r M).
+// One block of 256 threads per row; the row's new M stays in registers (VPT 16-byte
+// vectors per thread, cols = 2048 VPT at most, a multiple of 8): reads G, M, W and writes
+// M, W once, the algorithmic minimum of 10 bytes per element.
+template <int VPT>
+__global__ void __launch_bounds__(256) rownorm_fused_rows_kernel(bf16* M, long long ldm, long long sm, const bf16* G,
+                                                                 long long ldg, long long sg, bf16* W, long long ldw,
+                                                                 long long sw, int cols, float mu, float gamma,
+                                                                 float eps, float alpha, float beta) {
+  const int b = blockIdx.y, i = blockIdx.x;
+  bf16* mr = M + (long long)b * sm + (long long)i * ldm;
+  const bf16* gr = G + (long long)b * sg + (long long)i * ldg;
+  bf16* wr = W + (long long)b * sw + (long long)i * ldw;
+  uint4 mv[VPT];
+  float acc = 0.f;
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) {
+    const int c = (v * 256 + threadIdx.x) * 8;
+    if (c < cols) {
+      uint4 m4 = *reinterpret_cast<const uint4*>(mr + c);
+      const uint4 g4 = *reinterpret_cast<const uint4*>(gr + c);
+      bf16* me = reinterpret_cast<bf16*>(&m4);
+      const bf16* ge = reinterpret_cast<const bf16*>(&g4);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        me[q] = f_to_bf16(__fadd_rn(__fmul_rn(mu, bf16_to_f(me[q])), bf16_to_f(ge[q])));
+        const float f = bf16_to_f(me[q]);
+        acc = fmaf(f, f, acc);
+      }
+      *reinterpret_cast<uint4*>(mr + c) = m4;
+      mv[v] = m4;
+    }
+  }
+  __shared__ float r_sh;
+  const float tot = block_sum_256(acc);
+  if (threadIdx.x == 0) r_sh = gamma / fmaxf(sqrtf(tot), eps);
+  __syncthreads();
+  const float a = alpha * r_sh;
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) {
+    const int c = (v * 256 + threadIdx.x) * 8;
+    if (c < cols) {
+      uint4 w4 = *reinterpret_cast<const uint4*>(wr + c);
+      bf16* we = reinterpret_cast<bf16*>(&w4);
+      const bf16* me = reinterpret_cast<const bf16*>(&mv[v]);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) we[q] = f_to_bf16(fmaf(a, bf16_to_f(me[q]), beta * bf16_to_f(we[q])));
+      *reinterpret_cast<uint4*>(wr + c) = w4;
+    }
+  }
+}
+
 // RowNorm scales (Scaling Muon for DiTs eq. (5), multiplier gamma): r = gamma / max(sqrt(s), eps).
 __global__ void rownorm_scale_kernel(const float* s, long long n, float gamma, float eps, float* r) {
   const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -1025,6 +1079,27 @@ int launch_normuon_rows(const float* s, const MatRef& V, const int* idx, int64_t
   normuon_rows_kernel<<<(unsigned)count, 256, 0, S(stream)>>>(s, static_cast<float*>(V.ptr), V.ld, V.stride, idx,
                                                               (int)k, (int)len, beta2, eps, r);
   return check_launch("normuon_rows", err);
+}
+
+bool rownorm_fused_supported(int64_t cols) { return cols % 8 == 0 && cols <= 2048 * 8; }
+
+int launch_rownorm_fused_rows(const MatRef& M, const MatRef& G, const MatRef& W, int64_t count, float mu, float gamma,
+                              float eps, float alpha, float beta, void* stream, std::string* err) {
+  dim3 grid((unsigned)M.rows, (unsigned)count);
+  const int vpt = (int)((M.cols + 2047) / 2048);
+#define GNS_RN_ARGS                                                                                             \
+  static_cast<bf16*>(M.ptr), M.ld, M.stride, static_cast<const bf16*>(G.ptr), G.ld, G.stride,                 \
+      static_cast<bf16*>(W.ptr), W.ld, W.stride, (int)M.cols, mu, gamma, eps, alpha, beta
+  if (vpt <= 1)
+    rownorm_fused_rows_kernel<1><<<grid, 256, 0, S(stream)>>>(GNS_RN_ARGS);
+  else if (vpt <= 2)
+    rownorm_fused_rows_kernel<2><<<grid, 256, 0, S(stream)>>>(GNS_RN_ARGS);
+  else if (vpt <= 4)
+    rownorm_fused_rows_kernel<4><<<grid, 256, 0, S(stream)>>>(GNS_RN_ARGS);
+  else
+    rownorm_fused_rows_kernel<8><<<grid, 256, 0, S(stream)>>>(GNS_RN_ARGS);
+#undef GNS_RN_ARGS
+  return check_launch("rownorm_fused_rows", err);
 }
 
 int launch_rownorm_scale(const float* s, int64_t n, float gamma, float eps, float* r, void* stream,

@@ -45,6 +45,11 @@ int launch_col_sumsq(const MatRef& M, int64_t count, float* part, float* s, void
 // NorMuon second moments (V fp32, updated at rows idx or 0..k-1) and row scales r.
 int launch_normuon_rows(const float* s, const MatRef& V, const int* idx, int64_t k, int64_t len, int64_t count,
                         float beta2, float eps, float* r, void* stream, std::string* err);
+// Single-pass RowNorm step on the rows of a wide matrix (cols a multiple of 8, at most
+// 16384): momentum, row norm and the scaled weight update in one kernel.
+bool rownorm_fused_supported(int64_t cols);
+int launch_rownorm_fused_rows(const MatRef& M, const MatRef& G, const MatRef& W, int64_t count, float mu, float gamma,
+                              float eps, float alpha, float beta, void* stream, std::string* err);
 // RowNorm scales r = gamma / max(sqrt(s), eps) over n entries.
 int launch_rownorm_scale(const float* s, int64_t n, float gamma, float eps, float* r, void* stream,
                          std::string* err);

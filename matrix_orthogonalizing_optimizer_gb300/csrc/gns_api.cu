@@ -932,6 +932,12 @@ int gns_muon_step(const gns_batch* W, const gns_batch* G, const gns_batch* M, co
     if (mb.flavor == GNS_FLAVOR_ROWNORM) {
       // Scaling Muon for DiTs eq. (5), (7) off a refresh step: M <- mu M + G;
       // W <- (1 - lr wd) W - lr scale gamma R_eps(M) on the oriented rows of M
+      if (!s.trans && rownorm_fused_supported(s.cols)) {
+        if ((rc = launch_rownorm_fused_rows(mm, gm, wm, s.B, mu, mp->rownorm_gamma, mp->norm_eps, step_scale, decay,
+                                            stream, &err)))
+          return fail(rc, err);
+        continue;
+      }
       if ((rc = launch_momentum(mm, gm, s.B, mu, 0, nullptr, stream, &err))) return fail(rc, err);
       if (!s.trans)
         rc = launch_row_sumsq(mm, s.rows, s.cols, s.B, mb.s, stream, &err);
