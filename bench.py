@@ -365,6 +365,41 @@ def run_ours(args, rank, world, dist):
         torch.cuda.synchronize()
         return a.elapsed_time(b) / reps
 
+    # ---- the MoE-expert alpha = 4 batch: Gram NS alone on 256 x 2048 x 8192 ----
+    def moe_experts():
+        count, n, m = 256, 2048, 8192
+        X = (torch.randn((count, n, m), generator=gen, device=dev, dtype=torch.float32) / m ** 0.5).to(torch.bfloat16)
+        Xo = torch.empty_like(X)
+        ws_m = gns.alloc_workspace(gns.workspace_size(_lib.GNS_OP_GRAM_NS, X, ns), dev)
+        gns.gram_ns_batched(X, outs=[Xo], ns=ns, workspace=ws_m, stream=stream)
+        torch.cuda.synchronize()
+        reps = 3
+        evm = [torch.cuda.Event(enable_timing=True) for _ in range(2 * reps)]
+        for e in evm:
+            e.record(stream)
+        hm = (ctypes.c_void_p * (2 * reps))(*[ctypes.c_void_p(e.cuda_event) for e in evm])
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        lib.gns_profile_set(hm, reps)
+        a.record(stream)
+        for _ in range(reps):
+            gns.gram_ns_batched(X, outs=[Xo], ns=ns, workspace=ws_m, stream=stream)
+        b.record(stream)
+        torch.cuda.synchronize()
+        lib.gns_profile_set(None, 0)
+        call_ms = a.elapsed_time(b) / reps
+        g_ms = sum(evm[2 * i].elapsed_time(evm[2 * i + 1]) for i in range(reps)) / reps
+        fl = count * alg_flops_per_matrix(n, m)
+        del X, Xo, ws_m
+        torch.cuda.empty_cache()
+        return {"what": "Gram NS alone (T=5, restart@2) on 256 expert matrices 2048 x 8192 bf16 (alpha = 4), "
+                        "N(0,1)/sqrt(m) entries", "ms_per_call": call_ms, "matrices_per_s": count / (call_ms / 1000.0),
+                "gemm_ms": g_ms, "gemm_tflops": fl / (g_ms / 1000.0) / 1e12,
+                "gemm_frac_of_burst_peak": fl / (g_ms / 1000.0) / 1e12 / load_peaks()[0],
+                "gemm_frac_of_sustained_peak": fl / (g_ms / 1000.0) / 1e12 / load_peaks()[1]}
+
+    moe = moe_experts()
+
     base = dict(lr=LR, momentum=MU)
     f16_ms = time_flavor(gns.MuonParams(**base, ns_dtype=torch.float16))
     normuon_ms = time_flavor(gns.MuonParams(**base, flavor="normuon", beta2=0.95, norm_eps=1e-8), with_v=True)
@@ -425,6 +460,7 @@ def run_ours(args, rank, world, dist):
                              "note": "orthogonalization of the 24 matrices alone, same tcgen05 kernels, T=5; "
                                      "standard NS with symmetric products (Dion3 Algorithm 1, sec. 2.3)"},
         "flavors": flavors,
+        "moe_experts_alpha4": moe,
         "gpu_launches": n_all.value,
         "device_status": st,
         "clocks": clk,
