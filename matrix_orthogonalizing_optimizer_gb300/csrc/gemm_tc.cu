@@ -146,20 +146,38 @@ struct TileCoord {
 // that is the upper triangle of a symmetric matrix (256-blocks at or above the diagonal) is
 // read from the mirrored block, with the other major-ness, wherever the block it would read
 // lies below the diagonal.
-__device__ __forceinline__ int a_major(const Problem& pr, int I, int kb) {
+// The per-product fields a K loop reads, copied into registers once per tile: the loops'
+// inline assembly clobbers memory, which would otherwise reload them from the parameter
+// block at every K slice.
+struct KLoop {
+  int kblocks, a_mn, b_mn, a_upper, b_upper, ab_f16;
+};
+__device__ __forceinline__ KLoop kloop_of(const Problem& pr) {
+  KLoop k;
+  k.kblocks = pr.kblocks;
+  k.a_mn = pr.a_mn;
+  k.b_mn = pr.b_mn;
+  k.a_upper = pr.a_upper;
+  k.b_upper = pr.b_upper;
+  k.ab_f16 = pr.ab_f16;
+  return k;
+}
+__device__ __forceinline__ int a_major(const KLoop& pr, int I, int kb) {
   const int kbl = kb >> 2;
   const bool lower = pr.a_mn ? (kbl > I) : (I > kbl);
   return pr.a_mn ^ ((pr.a_upper && lower) ? 1 : 0);
 }
-__device__ __forceinline__ int b_major(const Problem& pr, int J, int kb) {
+__device__ __forceinline__ int b_major(const KLoop& pr, int J, int kb) {
   const int kbl = kb >> 2;
   const bool lower = pr.b_mn ? (kbl > J) : (J > kbl);
   return pr.b_mn ^ ((pr.b_upper && lower) ? 1 : 0);
 }
 
-__device__ __forceinline__ TileCoord decode_tile(const Params& P, int tile) {
+// p0: a problem index at or below the tile's (every role walks its tiles in increasing
+// order, so the previous tile's problem is a valid start).
+__device__ __forceinline__ TileCoord decode_tile(const Params& P, int tile, int p0 = 0) {
   TileCoord tc;
-  int p = 0;
+  int p = p0;
   while (p + 1 < P.nprob && tile >= P.prob[p + 1].tile_begin) ++p;
   const Problem& pr = P.prob[p];
   int t = tile - pr.tile_begin;
@@ -282,28 +300,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer (both CTAs) ----------------
+      int* const status = P.status;
+      const uint32_t full0 = mapa_shared(smem_u32(&full[0]), 0);  // stage barriers in the leader
       int s = 0;
       uint32_t ph = 0;
       bool ok = true;
+      int last_p = 0;
       for (int tile = pair; ok && tile < P.total_tiles; tile += npairs) {
-        const TileCoord c = decode_tile(P, tile);
+        const TileCoord c = decode_tile(P, tile, last_p);
+      last_p = c.p;
         const Problem& pr = P.prob[c.p];
         const int m0 = c.I * 256 + (int)rank * TM;
         const int n0 = c.J * 256 + (int)rank * BN;
-        if (pr.dep_mask && !wait_ready(ready_tile, tile, abort_flag, P.status)) break;
-        for (int kb = 0; kb < pr.kblocks; ++kb) {
-          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, P.status)) {
+        const KLoop kl = kloop_of(pr);
+        const CUtensorMap* const tmA = &pr.tmA;
+        const CUtensorMap* const tmA2 = &pr.tmA2;
+        const CUtensorMap* const tmB = &pr.tmB;
+        const CUtensorMap* const tmB2 = &pr.tmB2;
+        if (pr.dep_mask && !wait_ready(ready_tile, tile, abort_flag, status)) break;
+        for (int kb = 0; kb < kl.kblocks; ++kb) {
+          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, status)) {
             ok = false;
             break;
           }
           if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * STAGE_BYTES);
-          const uint32_t fb = mapa_shared(smem_u32(&full[s]), 0);
+          const uint32_t fb = full0 + 8u * (uint32_t)s;
           uint8_t* sa = stages + s * STAGE_BYTES;
           uint8_t* sb = sa + A_BYTES;
           const int k0 = kb * TK;
-          const int amn = a_major(pr, c.I, kb), bmn = b_major(pr, c.J, kb);
-          const CUtensorMap* ma = amn == pr.a_mn ? &pr.tmA : &pr.tmA2;
-          const CUtensorMap* mb = bmn == pr.b_mn ? &pr.tmB : &pr.tmB2;
+          const int amn = a_major(kl, c.I, kb), bmn = b_major(kl, c.J, kb);
+          const CUtensorMap* ma = amn == kl.a_mn ? tmA : tmA2;
+          const CUtensorMap* mb = bmn == kl.b_mn ? tmB : tmB2;
           if (!amn) {
             tma_load_3d_pair(sa, ma, fb, k0, m0, c.b);
           } else {
@@ -326,36 +353,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
       // ---------------- MMA issuer (leader CTA) ----------------
+      int* const status = P.status;
+      const uint32_t stages_u = smem_u32(stages);
       int s = 0;
       uint32_t ph = 0;
       bool ok = true;
       int local = 0;
+      int last_p = 0;
       for (int tile = pair; ok && tile < P.total_tiles; tile += npairs, ++local) {
-        const TileCoord c = decode_tile(P, tile);
+        const TileCoord c = decode_tile(P, tile, last_p);
+      last_p = c.p;
         const Problem& pr = P.prob[c.p];
         const int acc = local & 1;
         const uint32_t aph = (local >> 1) & 1;
-        if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, P.status)) break;
+        if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * TN;
-        for (int kb = 0; kb < pr.kblocks; ++kb) {
-          const int amn = a_major(pr, c.I, kb), bmn = b_major(pr, c.J, kb);
-          const uint32_t idesc = idesc_f16kind_f32(2 * TM, TN, amn, bmn, pr.ab_f16);
-          if (!mbar_wait(&full[s], ph, abort_flag, P.status)) {
+        const KLoop kl = kloop_of(pr);
+        for (int kb = 0; kb < kl.kblocks; ++kb) {
+          const int amn = a_major(kl, c.I, kb), bmn = b_major(kl, c.J, kb);
+          const uint32_t idesc = idesc_f16kind_f32(2 * TM, TN, amn, bmn, kl.ab_f16);
+          if (!mbar_wait(&full[s], ph, abort_flag, status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sa = smem_u32(stages + s * STAGE_BYTES);
+          const uint32_t sa = stages_u + (uint32_t)s * STAGE_BYTES;
           const uint32_t sb = sa + A_BYTES;
+          // descriptors of the slice's first K=16 step; the next steps advance the start
+          // address field (16-byte units): 32 bytes along K for a K-major operand, 16 rows of
+          // 128 bytes for an MN-major one (stage addresses stay far below the field's 256 KiB)
+          const uint64_t ad0 = amn ? sdesc_sw128(sa, BOX_BYTES, 1024) : sdesc_sw128(sa, 16, 1024);
+          const uint64_t bd0 = bmn ? sdesc_sw128(sb, BOX_BYTES, 1024) : sdesc_sw128(sb, 16, 1024);
+          const uint64_t astep = amn ? 2048 / 16 : 32 / 16;
+          const uint64_t bstep = bmn ? 2048 / 16 : 32 / 16;
 #pragma unroll
-          for (int kk = 0; kk < TK / 16; ++kk) {
-            const uint64_t ad =
-                amn ? sdesc_sw128(sa + kk * 2048, BOX_BYTES, 1024) : sdesc_sw128(sa + kk * 32, 16, 1024);
-            const uint64_t bd =
-                bmn ? sdesc_sw128(sb + kk * 2048, BOX_BYTES, 1024) : sdesc_sw128(sb + kk * 32, 16, 1024);
-            umma2_f16kind(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
-          }
+          for (int kk = 0; kk < TK / 16; ++kk)
+            umma2_f16kind(d_tmem, ad0 + astep * kk, bd0 + bstep * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
           umma2_commit_multicast(&empty[s], 0x3);
           if (++s == STAGES) {
             s = 0;
@@ -372,8 +406,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       // the completion counters of the problems each tile depends on, and publishes the
       // highest tile whose inputs are complete, so the L2 round trips of those checks stay
       // off the producer's path.
+      int last_p = 0;
       for (int tile = pair; tile < P.total_tiles; tile += npairs) {
-        const TileCoord c = decode_tile(P, tile);
+        const TileCoord c = decode_tile(P, tile, last_p);
+      last_p = c.p;
         const Problem& pr = P.prob[c.p];
         if (pr.dep_mask && !wait_deps(P, pr, c.b, abort_flag)) break;
         __threadfence_block();
@@ -385,14 +421,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       // Loads the C chunks of the next tile as soon as the epilogue releases each buffer,
       // a whole main loop ahead of their use.
       uint32_t qc = 0;  // C chunks loaded so far (ring slot and phase)
+      int last_p = 0;
       for (int tile = pair; tile < P.total_tiles; tile += npairs) {
-        const TileCoord c = decode_tile(P, tile);
+        const TileCoord c = decode_tile(P, tile, last_p);
+      last_p = c.p;
         const Problem& pr = P.prob[c.p];
         if (!pr.has_c) continue;
         const int m0 = c.I * 256 + (int)rank * TM;
         const int n0 = c.J * 256;
         if (pr.dep_mask && !wait_ready(ready_tile, tile, abort_flag, P.status)) break;
         bool ok = true;
+        const CUtensorMap* const tmC = &pr.tmC;
+        const int c_trans = pr.c_trans;
         for (int ch = 0; ch < NCHUNK; ++ch, ++qc) {
           const uint32_t q = qc % C_BUFS;
           if (!mbar_wait(&cempty[q], ((qc / C_BUFS) & 1u) ^ 1u, abort_flag, P.status)) {
@@ -400,7 +440,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             break;
           }
           mbar_arrive_expect_tx(&cfull[q], CHUNK_BYTES);
-          chunk_load(SC + q * CHUNK_BYTES, &pr.tmC, &cfull[q], pr.c_trans, m0, n0 + ch * CHUNK, c.b);
+          chunk_load(SC + q * CHUNK_BYTES, tmC, &cfull[q], c_trans, m0, n0 + ch * CHUNK, c.b);
         }
         if (!ok) break;
       }
@@ -417,8 +457,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     uint32_t qc = 0;  // C chunks consumed so far (ring slot and phase)
     uint32_t gc = 0;  // chunks stored so far (output staging buffers)
     int local = 0;
+    int last_p = 0;
     for (int tile = pair; tile < P.total_tiles; tile += npairs, ++local) {
-      const TileCoord c = decode_tile(P, tile);
+      const TileCoord c = decode_tile(P, tile, last_p);
+      last_p = c.p;
       const Problem& pr = P.prob[c.p];
       const int acc = local & 1;
       const uint32_t aph = (local >> 1) & 1;
@@ -431,6 +473,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       const bool has_c = pr.has_c != 0;
       const bool mirror = pr.sym && c.I != c.J && pr.mirror_out;
       const bool want_diag = pr.has_d2 && c.I == c.J;
+      // per-product fields used inside the chunk loop, in registers (see KLoop)
+      const int c_trans = pr.c_trans, c_f16 = pr.c_f16, d_trans = pr.d_trans, d_f16 = pr.d_f16;
+      const int check_finite = pr.check_finite, has_d2 = pr.has_d2, diag_limit = pr.diag_limit;
+      const float gamma = pr.gamma;
       const int m0 = c.I * 256 + (int)rank * TM;  // first row of this CTA's half
       const int n0 = c.J * 256;
       if (et == 0) *epi_flag = mbar_wait(&tfull[acc], aph, abort_flag, P.status) ? 1 : 0;
@@ -466,25 +512,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           const uint32_t q = qc % C_BUFS;
           const uint8_t* sc = SC + q * CHUNK_BYTES;
           if (!mbar_wait(&cfull[q], (qc / C_BUFS) & 1u, abort_flag, P.status)) *epi_flag = 0;
-          if (!pr.c_trans) {
+          if (!c_trans) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               const uint4 w = *reinterpret_cast<const uint4*>(sc + off_direct(r, half * 32 + q * 8));
               const uint16_t* wv = reinterpret_cast<const uint16_t*>(&w);
 #pragma unroll
-              for (int e = 0; e < 8; ++e) o[q * 8 + e] = fmaf(beta, h16_to_f(wv[e], pr.c_f16), o[q * 8 + e]);
+              for (int e = 0; e < 8; ++e) o[q * 8 + e] = fmaf(beta, h16_to_f(wv[e], c_f16), o[q * 8 + e]);
             }
           } else {
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-              o[j] = fmaf(beta, h16_to_f(*reinterpret_cast<const uint16_t*>(sc + off_trans(r, half * 32 + j)), pr.c_f16),
+              o[j] = fmaf(beta, h16_to_f(*reinterpret_cast<const uint16_t*>(sc + off_trans(r, half * 32 + j)), c_f16),
                           o[j]);
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&cempty[q]);
           ++qc;
         }
-        if (pr.check_finite) {
+        if (check_finite) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) bad |= !isfinite(o[j]);
         }
@@ -493,33 +539,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           for (int j = 0; j < 32; ++j)
             if (j == (diag_col & 31)) dv = o[j];
         }
-        if (!pr.d_trans) {
+        if (!d_trans) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             uint4 w;
             uint16_t* wv = reinterpret_cast<uint16_t*>(&w);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) wv[e] = f_to_h16(o[q * 8 + e], pr.d_f16);
+            for (int e = 0; e < 8; ++e) wv[e] = f_to_h16(o[q * 8 + e], d_f16);
             *reinterpret_cast<uint4*>(sd + off_direct(r, half * 32 + q * 8)) = w;
           }
         } else {
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            *reinterpret_cast<uint16_t*>(sd + off_trans(r, half * 32 + j)) = f_to_h16(o[j], pr.d_f16);
+            *reinterpret_cast<uint16_t*>(sd + off_trans(r, half * 32 + j)) = f_to_h16(o[j], d_f16);
         }
         if (mirror) {
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            *reinterpret_cast<uint16_t*>(sm + off_trans(r, half * 32 + j)) = f_to_h16(o[j], pr.d_f16);
+            *reinterpret_cast<uint16_t*>(sm + off_trans(r, half * 32 + j)) = f_to_h16(o[j], d_f16);
         }
         fence_proxy_async_smem();
         named_bar_sync(1, EPI_THREADS);
         const int col0 = n0 + ch * CHUNK;
         const bool chunk_has_diag = want_diag && (ch == 2 * (int)rank || ch == 2 * (int)rank + 1);
         if (et == 0) {
-          chunk_store(sd, &pr.tmD, pr.d_trans, m0, col0, c.b);
+          chunk_store(sd, &pr.tmD, d_trans, m0, col0, c.b);
           if (mirror) chunk_store(sm, &pr.tmD, 1, m0, col0, c.b);
-          if (pr.has_d2 && !chunk_has_diag) {
+          if (has_d2 && !chunk_has_diag) {
             chunk_store(sd, &pr.tmD2, 0, m0, col0, c.b);
             if (mirror) chunk_store(sm, &pr.tmD2, 1, m0, col0, c.b);
           }
@@ -530,8 +576,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           // (appendix B.2.3: adding a_t I to an already rounded Z loses a_t's precision)
           if (et == 0) bulk_wait_read<0>();
           named_bar_sync(1, EPI_THREADS);
-          if (diag_mine && (diag_col >> 6) == ch && m0 + r < pr.diag_limit)
-            *reinterpret_cast<uint16_t*>(sd + off_direct(r, diag_col & 63)) = f_to_h16(dv + pr.gamma, pr.d_f16);
+          if (diag_mine && (diag_col >> 6) == ch && m0 + r < diag_limit)
+            *reinterpret_cast<uint16_t*>(sd + off_direct(r, diag_col & 63)) = f_to_h16(dv + gamma, d_f16);
           fence_proxy_async_smem();
           named_bar_sync(1, EPI_THREADS);
           if (et == 0) {
