@@ -92,6 +92,7 @@ struct Problem {
   int check_finite;
   int a_upper, b_upper, mirror_out;
   int ab_f16, c_f16, d_f16;  // 16-bit element types: fp16 (1) or bf16 (0)
+  int c_mode, d_mode;        // chunk modes of the C loads and of the direct D / D2 stores
   uint32_t dep_mask;  // earlier problems whose tiles of the same matrix must be complete
   int ctr_off;        // this problem's completion counters: counters[ctr_off + b]
 };
@@ -214,11 +215,16 @@ __device__ __forceinline__ uint32_t off_trans(int r, int c) {
   return (uint32_t)((r >> 6) * BOX_BYTES + c * 128 + (((x >> 3) ^ (c & 7)) << 4) + ((x & 7) << 1));
 }
 
-// The two 64 x 64 boxes of one chunk: rows [row0, row0+128) x cols [col0, col0+64) of the
-// matrix (trans = 0), or rows [col0, col0+64) x cols [row0, row0+128) (trans = 1).
-__device__ __forceinline__ void chunk_load(uint8_t* s, const CUtensorMap* map, uint64_t* bar, int trans, int row0,
+// One chunk = rows [row0, row0+128) x cols [col0, col0+64) of the matrix (mode 0: two
+// 64 x 64 boxes; mode 2: one 128-row box, same shared-memory layout, for maps encoded with
+// 128-row boxes), or rows [col0, col0+64) x cols [row0, row0+128) (mode 1, transposed: two
+// 64 x 64 boxes). Every TMA box costs the SM's TMA unit a roughly fixed time, so chunks
+// take one box wherever the map allows.
+__device__ __forceinline__ void chunk_load(uint8_t* s, const CUtensorMap* map, uint64_t* bar, int mode, int row0,
                                            int col0, int b) {
-  if (!trans) {
+  if (mode == 2) {
+    tma_load_3d(s, map, bar, col0, row0, b);
+  } else if (mode == 0) {
     tma_load_3d(s, map, bar, col0, row0, b);
     tma_load_3d(s + BOX_BYTES, map, bar, col0, row0 + 64, b);
   } else {
@@ -226,9 +232,11 @@ __device__ __forceinline__ void chunk_load(uint8_t* s, const CUtensorMap* map, u
     tma_load_3d(s + BOX_BYTES, map, bar, row0 + 64, col0, b);
   }
 }
-__device__ __forceinline__ void chunk_store(const uint8_t* s, const CUtensorMap* map, int trans, int row0, int col0,
+__device__ __forceinline__ void chunk_store(const uint8_t* s, const CUtensorMap* map, int mode, int row0, int col0,
                                             int b) {
-  if (!trans) {
+  if (mode == 2) {
+    tma_store_3d(map, s, col0, row0, b);
+  } else if (mode == 0) {
     tma_store_3d(map, s, col0, row0, b);
     tma_store_3d(map, s + BOX_BYTES, col0, row0 + 64, b);
   } else {
@@ -432,7 +440,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         if (pr.dep_mask && !wait_ready(ready_tile, tile, abort_flag, P.status)) break;
         bool ok = true;
         const CUtensorMap* const tmC = &pr.tmC;
-        const int c_trans = pr.c_trans;
+        const int c_mode = pr.c_mode;
         for (int ch = 0; ch < NCHUNK; ++ch, ++qc) {
           const uint32_t q = qc % C_BUFS;
           if (!mbar_wait(&cempty[q], ((qc / C_BUFS) & 1u) ^ 1u, abort_flag, P.status)) {
@@ -440,7 +448,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             break;
           }
           mbar_arrive_expect_tx(&cfull[q], CHUNK_BYTES);
-          chunk_load(SC + q * CHUNK_BYTES, tmC, &cfull[q], c_trans, m0, n0 + ch * CHUNK, c.b);
+          chunk_load(SC + q * CHUNK_BYTES, tmC, &cfull[q], c_mode, m0, n0 + ch * CHUNK, c.b);
         }
         if (!ok) break;
       }
@@ -475,6 +483,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       const bool want_diag = pr.has_d2 && c.I == c.J;
       // per-product fields used inside the chunk loop, in registers (see KLoop)
       const int c_trans = pr.c_trans, c_f16 = pr.c_f16, d_trans = pr.d_trans, d_f16 = pr.d_f16;
+      const int d_mode = d_trans ? 1 : pr.d_mode;
       const int check_finite = pr.check_finite, has_d2 = pr.has_d2, diag_limit = pr.diag_limit;
       const float gamma = pr.gamma;
       const int m0 = c.I * 256 + (int)rank * TM;  // first row of this CTA's half
@@ -563,10 +572,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         const int col0 = n0 + ch * CHUNK;
         const bool chunk_has_diag = want_diag && (ch == 2 * (int)rank || ch == 2 * (int)rank + 1);
         if (et == 0) {
-          chunk_store(sd, &pr.tmD, d_trans, m0, col0, c.b);
+          chunk_store(sd, &pr.tmD, d_mode, m0, col0, c.b);
           if (mirror) chunk_store(sm, &pr.tmD, 1, m0, col0, c.b);
           if (has_d2 && !chunk_has_diag) {
-            chunk_store(sd, &pr.tmD2, 0, m0, col0, c.b);
+            chunk_store(sd, &pr.tmD2, d_mode, m0, col0, c.b);
             if (mirror) chunk_store(sm, &pr.tmD2, 1, m0, col0, c.b);
           }
           bulk_commit();
@@ -581,7 +590,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           fence_proxy_async_smem();
           named_bar_sync(1, EPI_THREADS);
           if (et == 0) {
-            chunk_store(sd, &pr.tmD2, 0, m0, col0, c.b);
+            chunk_store(sd, &pr.tmD2, d_mode, m0, col0, c.b);
             bulk_commit();
           }
         }
@@ -731,10 +740,14 @@ int gemm_launch_tc(const GemmOp* ops, int nops, const uint32_t* dep_masks, int* 
     if (o.a_upper && !encode_map(&pr.tmA2, o.A, o.batch, o.a_mn ? 128 : 64, pr.ab_f16, err)) return GNS_ERR_CUDA;
     if (o.b_upper && !encode_map(&pr.tmB2, o.B, o.batch, o.b_mn ? 128 : 64, pr.ab_f16, err)) return GNS_ERR_CUDA;
     pr.has_c = o.C.ptr != nullptr && o.beta != 0.f;
-    if (pr.has_c && !encode_map(&pr.tmC, o.C, o.batch, 64, pr.c_f16, err)) return GNS_ERR_CUDA;
-    if (!encode_map(&pr.tmD, o.D, o.batch, 64, pr.d_f16, err)) return GNS_ERR_CUDA;
+    // one 128-row box per chunk where a map serves only direct chunks
+    pr.c_mode = o.c_trans ? 1 : 2;
+    const bool d_one_box = !o.d_trans && !(o.sym && !o.upper_out);
+    pr.d_mode = d_one_box ? 2 : 0;
+    if (pr.has_c && !encode_map(&pr.tmC, o.C, o.batch, o.c_trans ? 64 : 128, pr.c_f16, err)) return GNS_ERR_CUDA;
+    if (!encode_map(&pr.tmD, o.D, o.batch, d_one_box ? 128 : 64, pr.d_f16, err)) return GNS_ERR_CUDA;
     pr.has_d2 = o.D2.ptr != nullptr;
-    if (pr.has_d2 && !encode_map(&pr.tmD2, o.D2, o.batch, 64, pr.d_f16, err)) return GNS_ERR_CUDA;
+    if (pr.has_d2 && !encode_map(&pr.tmD2, o.D2, o.batch, d_one_box ? 128 : 64, pr.d_f16, err)) return GNS_ERR_CUDA;
     pr.a_mn = o.a_mn;
     pr.b_mn = o.b_mn;
     pr.kblocks = (int)((o.K + TK - 1) / TK);
