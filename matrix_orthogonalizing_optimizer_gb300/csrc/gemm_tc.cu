@@ -316,7 +316,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       int last_p = 0;
       for (int tile = pair; ok && tile < P.total_tiles; tile += npairs) {
         const TileCoord c = decode_tile(P, tile, last_p);
-      last_p = c.p;
+        last_p = c.p;
         const Problem& pr = P.prob[c.p];
         const int m0 = c.I * 256 + (int)rank * TM;
         const int n0 = c.J * 256 + (int)rank * BN;
@@ -370,7 +370,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       int last_p = 0;
       for (int tile = pair; ok && tile < P.total_tiles; tile += npairs, ++local) {
         const TileCoord c = decode_tile(P, tile, last_p);
-      last_p = c.p;
+        last_p = c.p;
         const Problem& pr = P.prob[c.p];
         const int acc = local & 1;
         const uint32_t aph = (local >> 1) & 1;
@@ -417,7 +417,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       int last_p = 0;
       for (int tile = pair; tile < P.total_tiles; tile += npairs) {
         const TileCoord c = decode_tile(P, tile, last_p);
-      last_p = c.p;
+        last_p = c.p;
         const Problem& pr = P.prob[c.p];
         if (pr.dep_mask && !wait_deps(P, pr, c.b, abort_flag)) break;
         __threadfence_block();
@@ -432,7 +432,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       int last_p = 0;
       for (int tile = pair; tile < P.total_tiles; tile += npairs) {
         const TileCoord c = decode_tile(P, tile, last_p);
-      last_p = c.p;
+        last_p = c.p;
         const Problem& pr = P.prob[c.p];
         if (!pr.has_c) continue;
         const int m0 = c.I * 256 + (int)rank * TM;
