@@ -400,6 +400,42 @@ def run_ours(args, rank, world, dist):
 
     moe = moe_experts()
 
+    # ---- the fractional-update configuration: 32 x 4096 x 16384, f = 1/4 (k = 1024) ----
+    def frac_config():
+        count, rows, cols = 32, 4096, 16384
+        sc = 1.0 / cols ** 0.5
+
+        def rnd():
+            return (torch.randn((count, rows, cols), generator=gen, device=dev, dtype=torch.float32) * sc).to(
+                torch.bfloat16)
+        Wf, Gf, Mf = rnd(), rnd(), rnd()
+        pf = gns.MuonParams(lr=LR, momentum=MU, frac=0.25)
+        ws_f = gns.alloc_workspace(gns.workspace_size(_lib.GNS_OP_MUON_STEP, Mf, ns, muon=pf), dev)
+
+        def go():
+            gns.muon_step(Wf, Gf, Mf, ns=ns, workspace=ws_f, status=status, stream=stream, params=pf)
+        for _ in range(2):
+            go()
+        torch.cuda.synchronize()
+        reps = 5
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            go()
+        b.record(stream)
+        torch.cuda.synchronize()
+        f_ms = a.elapsed_time(b) / reps
+        k = 1024
+        fl = count * alg_flops_per_matrix(k, cols)
+        del Wf, Gf, Mf, ws_f
+        torch.cuda.empty_cache()
+        return {"what": "Dion3 fractional update f = 1/4 on 32 bf16 momentum matrices 4096 x 16384: exact l1 "
+                        "top-1024 rows, Gram NS of the 1024 x 16384 subsets, scatter, error feedback",
+                "ms_per_step": f_ms, "matrices_per_s": count / (f_ms / 1000.0),
+                "orthogonalization_tflops_over_step": fl / (f_ms / 1000.0) / 1e12}
+
+    frac_cfg = frac_config()
+
     base = dict(lr=LR, momentum=MU)
     f16_ms = time_flavor(gns.MuonParams(**base, ns_dtype=torch.float16))
     normuon_ms = time_flavor(gns.MuonParams(**base, flavor="normuon", beta2=0.95, norm_eps=1e-8), with_v=True)
@@ -461,6 +497,7 @@ def run_ours(args, rank, world, dist):
                                      "standard NS with symmetric products (Dion3 Algorithm 1, sec. 2.3)"},
         "flavors": flavors,
         "moe_experts_alpha4": moe,
+        "frac_quarter_4096x16384": frac_cfg,
         "gpu_launches": n_all.value,
         "device_status": st,
         "clocks": clk,
