@@ -222,6 +222,58 @@ struct KeyAcc {
   }
 };
 
+// The same accumulator with its eight digit sums in shared memory (one slot of 8 per
+// thread): they change only when a value's exponent leaves the current digit, so keeping
+// them out of registers costs little and lets more warps stream the matrix.
+struct KeyAccS {
+  uint64_t* acc;
+  uint64_t cur;
+  uint32_t dcur;
+  bool nonfinite;
+  __device__ void init(uint64_t* slot) {
+    acc = slot;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0;
+    cur = 0;
+    dcur = 0;
+    nonfinite = false;
+  }
+  __device__ __forceinline__ void flush() {
+    acc[dcur] += cur;
+    cur = 0;
+  }
+  __device__ __forceinline__ void add(uint16_t bits) {
+    const uint32_t E = (bits >> 7) & 0xFFu;
+    if (E == 0xFFu) {
+      nonfinite = true;
+      return;
+    }
+    const uint32_t f = bits & 0x7Fu;
+    const uint32_t mant = E ? (f | 0x80u) : f;
+    if (!mant) return;
+    const uint32_t ee = E ? E - 1u : 0u;
+    const uint32_t d = ee >> 5;
+    const uint64_t v = static_cast<uint64_t>(mant) << (ee & 31u);
+    if (d != dcur) {
+      flush();
+      dcur = d;
+    }
+    cur += v;
+  }
+  __device__ void digits(uint32_t (&dg)[KEY_DIGITS]) {
+    flush();
+    uint64_t carry = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint64_t t = acc[i] + carry;
+      dg[i] = static_cast<uint32_t>(t);
+      carry = t >> 32;
+    }
+    dg[8] = static_cast<uint32_t>(carry);
+    dg[9] = static_cast<uint32_t>(carry >> 32);
+  }
+};
+
 // Rows of the (non-transposed) matrix: M <- M + G and the key of each row. One warp per
 // row; per-lane digits are summed across the warp (each sum < 2^37) and stored.
 __global__ void frac_add_keys_rows_kernel(bf16* M, long long ldm, long long sm, const bf16* G, long long ldg,
@@ -234,8 +286,9 @@ __global__ void frac_add_keys_rows_kernel(bf16* M, long long ldm, long long sm, 
   const int b = (int)(gw / rows), r = (int)(gw % rows);
   bf16* mr = M + (long long)b * sm + (long long)r * ldm;
   const bf16* gr = G + (long long)b * sg + (long long)r * ldg;
-  KeyAcc ka;
-  ka.init();
+  __shared__ uint64_t slots[256 * 8];
+  KeyAccS ka;
+  ka.init(slots + threadIdx.x * 8);
   const int cvec = cols & ~7;
   for (int c = lane * 8; c < cvec; c += 32 * 8) {
     uint4 mv = *reinterpret_cast<const uint4*>(mr + c);
