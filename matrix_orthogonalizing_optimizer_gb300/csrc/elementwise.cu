@@ -517,32 +517,41 @@ __global__ void __launch_bounds__(1024) select_topk_kernel(unsigned long long* k
 // gathers, decays, copies
 
 // X[b][i][:] = M[b][idx[b*k + i]][:] (rows), with sum-of-squares partials of X.
-__global__ void gather_rows_kernel(const bf16* M, long long ldm, long long sm, const int* idx, int k, int cols,
-                                   bf16* X, long long ldx, long long sx, int npart, float* partials) {
+// With decay, the selected rows of M are also replaced by bf16(mu * M) (Dion3 Algorithm 4's
+// error feedback, line 10) once copied: nothing reads M[S] after the gather, so the decay
+// rides on this pass.
+__global__ void gather_rows_kernel(bf16* M, long long ldm, long long sm, const int* idx, int k, int cols,
+                                   bf16* X, long long ldx, long long sx, int npart, float* partials, int decay,
+                                   float mu) {
   const int b = blockIdx.y, part = blockIdx.x;
   const int rp = (k + npart - 1) / npart;
   const int i0 = part * rp, i1 = min(k, i0 + rp);
   float acc = 0.f;
   for (int i = i0; i < i1; ++i) {
     const int r = idx[(long long)b * k + i];
-    const bf16* src = M + (long long)b * sm + (long long)r * ldm;
+    bf16* src = M + (long long)b * sm + (long long)r * ldm;
     bf16* dst = X + (long long)b * sx + (long long)i * ldx;
     const int cvec = cols & ~7;
     for (int c = threadIdx.x * 8; c < cvec; c += blockDim.x * 8) {
       const uint4 u = *reinterpret_cast<const uint4*>(src + c);
       *reinterpret_cast<uint4*>(dst + c) = u;
       const bf16* e = reinterpret_cast<const bf16*>(&u);
+      uint4 dv;
+      bf16* de = reinterpret_cast<bf16*>(&dv);
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         const float f = bf16_to_f(e[q]);
         acc = fmaf(f, f, acc);
+        de[q] = f_to_bf16(__fmul_rn(mu, f));
       }
+      if (decay) *reinterpret_cast<uint4*>(src + c) = dv;
     }
     for (int c = cvec + threadIdx.x; c < cols; c += blockDim.x) {
       const bf16 v = src[c];
       dst[c] = v;
       const float f = bf16_to_f(v);
       acc = fmaf(f, f, acc);
+      if (decay) src[c] = f_to_bf16(__fmul_rn(mu, f));
     }
   }
   const float s = block_sum_256(acc);
@@ -550,8 +559,8 @@ __global__ void gather_rows_kernel(const bf16* M, long long ldm, long long sm, c
 }
 
 // X[b][i][j] = M[b][j][idx[b*k + i]] (columns of M become rows of X); 32 x 32 tiles.
-__global__ void gather_cols_kernel(const bf16* M, long long ldm, long long sm, const int* idx, int k, int rows,
-                                   bf16* X, long long ldx, long long sx) {
+__global__ void gather_cols_kernel(bf16* M, long long ldm, long long sm, const int* idx, int k, int rows,
+                                   bf16* X, long long ldx, long long sx, int decay, float mu) {
   __shared__ bf16 tile[32][33];
   const int b = blockIdx.z;
   const int i0 = blockIdx.x * 32, j0 = blockIdx.y * 32;
@@ -559,48 +568,17 @@ __global__ void gather_cols_kernel(const bf16* M, long long ldm, long long sm, c
   for (int jj = ty; jj < 32; jj += 8) {
     const int j = j0 + jj, i = i0 + tx;
     bf16 v = f_to_bf16(0.f);
-    if (j < rows && i < k) v = M[(long long)b * sm + (long long)j * ldm + idx[(long long)b * k + i]];
+    if (j < rows && i < k) {
+      bf16* p = M + (long long)b * sm + (long long)j * ldm + idx[(long long)b * k + i];
+      v = *p;
+      if (decay) *p = f_to_bf16(__fmul_rn(mu, bf16_to_f(v)));
+    }
     tile[jj][tx] = v;
   }
   __syncthreads();
   for (int ii = ty; ii < 32; ii += 8) {
     const int i = i0 + ii, j = j0 + tx;
     if (i < k && j < rows) X[(long long)b * sx + (long long)i * ldx + j] = tile[tx][ii];
-  }
-}
-
-// M[b][idx[i]][:] <- bf16(mu * M): one block per selected row, 16-byte vectors.
-__global__ void decay_selected_rows_kernel(bf16* M, long long ldm, long long sm, const int* idx, int k, int len,
-                                           float mu) {
-  const int b = blockIdx.y, i = blockIdx.x;
-  bf16* row = M + (long long)b * sm + (long long)idx[(long long)b * k + i] * ldm;
-  const int cvec = len & ~7;
-  for (int c = threadIdx.x * 8; c < cvec; c += blockDim.x * 8) {
-    uint4 u = *reinterpret_cast<const uint4*>(row + c);
-    bf16* e = reinterpret_cast<bf16*>(&u);
-#pragma unroll
-    for (int q = 0; q < 8; ++q) e[q] = f_to_bf16(__fmul_rn(mu, bf16_to_f(e[q])));
-    *reinterpret_cast<uint4*>(row + c) = u;
-  }
-  for (int c = cvec + threadIdx.x; c < len; c += blockDim.x) row[c] = f_to_bf16(__fmul_rn(mu, bf16_to_f(row[c])));
-}
-
-// M[b][:][idx[i]] <- bf16(mu * M) (selected columns): 32 selected columns x 32 rows per
-// block, consecutive threads on consecutive selected columns.
-__global__ void decay_selected_cols_kernel(bf16* M, long long ldm, long long sm, const int* idx, int k, int rows,
-                                           float mu) {
-  const int b = blockIdx.z;
-  const int i = blockIdx.x * 32 + (threadIdx.x & 31);
-  if (i >= k) return;
-  const int sel = idx[(long long)b * k + i];
-  bf16* Mb = M + (long long)b * sm + sel;
-  const int j0 = blockIdx.y * 32;
-  for (int jj = threadIdx.x >> 5; jj < 32; jj += blockDim.x >> 5) {
-    const int j = j0 + jj;
-    if (j < rows) {
-      bf16* p = Mb + (long long)j * ldm;
-      *p = f_to_bf16(__fmul_rn(mu, bf16_to_f(*p)));
-    }
   }
 }
 
@@ -1041,16 +1019,17 @@ int launch_select_topk(unsigned long long* keys, const int* nf, int64_t n, int64
 }
 
 int launch_gather(const MatRef& M, int64_t count, int trans, const int* idx, int64_t k, const MatRef& X,
-                  float* partials, void* stream, std::string* err) {
+                  float* partials, void* stream, std::string* err, bool decay, float mu) {
   if (!trans) {
     dim3 grid(NPART, (unsigned)count);
-    gather_rows_kernel<<<grid, 256, 0, S(stream)>>>(static_cast<const bf16*>(M.ptr), M.ld, M.stride, idx, (int)k,
+    gather_rows_kernel<<<grid, 256, 0, S(stream)>>>(static_cast<bf16*>(M.ptr), M.ld, M.stride, idx, (int)k,
                                                     (int)M.cols, static_cast<bf16*>(X.ptr), X.ld, X.stride, NPART,
-                                                    partials);
+                                                    partials, decay ? 1 : 0, mu);
   } else {
     dim3 grid((unsigned)((k + 31) / 32), (unsigned)((M.rows + 31) / 32), (unsigned)count);
-    gather_cols_kernel<<<grid, 256, 0, S(stream)>>>(static_cast<const bf16*>(M.ptr), M.ld, M.stride, idx, (int)k,
-                                                    (int)M.rows, static_cast<bf16*>(X.ptr), X.ld, X.stride);
+    gather_cols_kernel<<<grid, 256, 0, S(stream)>>>(static_cast<bf16*>(M.ptr), M.ld, M.stride, idx, (int)k,
+                                                    (int)M.rows, static_cast<bf16*>(X.ptr), X.ld, X.stride,
+                                                    decay ? 1 : 0, mu);
     if (partials) {
       MatRef xs = X;
       xs.rows = k;
@@ -1060,20 +1039,6 @@ int launch_gather(const MatRef& M, int64_t count, int trans, const int* idx, int
     }
   }
   return check_launch("gather", err);
-}
-
-int launch_decay_selected(const MatRef& M, int64_t count, int trans, const int* idx, int64_t k, float mu,
-                          void* stream, std::string* err) {
-  if (!trans) {
-    dim3 grid((unsigned)k, (unsigned)count);
-    decay_selected_rows_kernel<<<grid, 256, 0, S(stream)>>>(static_cast<bf16*>(M.ptr), M.ld, M.stride, idx, (int)k,
-                                                            (int)M.cols, mu);
-  } else {
-    dim3 grid((unsigned)((k + 31) / 32), (unsigned)((M.rows + 31) / 32), (unsigned)count);
-    decay_selected_cols_kernel<<<grid, 256, 0, S(stream)>>>(static_cast<bf16*>(M.ptr), M.ld, M.stride, idx, (int)k,
-                                                            (int)M.rows, mu);
-  }
-  return check_launch("decay_selected", err);
 }
 
 int launch_scale_unselected(const MatRef& W, int64_t count, int trans, const int* idx, int64_t k, float factor,

@@ -23,10 +23,9 @@ int launch_keys_only(const MatRef& M, int64_t count, int trans, unsigned long lo
                      std::string* err);
 int launch_select_topk(unsigned long long* keys, const int* nf, int64_t n, int64_t k, int64_t count, int* idx,
                        void* stream, std::string* err);
+// decay: also M[S] <- bf16(mu * M[S]) in the same pass (Algorithm 4's error feedback).
 int launch_gather(const MatRef& M, int64_t count, int trans, const int* idx, int64_t k, const MatRef& X,
-                  float* partials, void* stream, std::string* err);
-int launch_decay_selected(const MatRef& M, int64_t count, int trans, const int* idx, int64_t k, float mu,
-                          void* stream, std::string* err);
+                  float* partials, void* stream, std::string* err, bool decay = false, float mu = 1.f);
 // flags: count * n ints of scratch (n = rows, or cols when trans).
 int launch_scale_unselected(const MatRef& W, int64_t count, int trans, const int* idx, int64_t k, float factor,
                             int* flags, void* stream, std::string* err);

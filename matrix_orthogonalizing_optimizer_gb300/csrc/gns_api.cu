@@ -1008,8 +1008,10 @@ int gns_muon_step(const gns_batch* W, const gns_batch* G, const gns_batch* M, co
     if ((rc = launch_frac_add_keys(mm, gm, s.B, s.trans, mb.keys, mb.nf, stream, &err))) return fail(rc, err);
     // line 3: selection
     if ((rc = launch_select_topk(mb.keys, mb.nf, s.n, k, s.B, mb.idx, stream, &err))) return fail(rc, err);
-    // gather M[S, :] and its Frobenius norm
-    if ((rc = launch_gather(mm, s.B, s.trans, mb.idx, k, mb.xs, mb.gb.partials, stream, &err))) return fail(rc, err);
+    // gather M[S, :] and its Frobenius norm; line 10 (error feedback, M[S] <- mu M[S]) rides
+    // on the same pass: M[S] is not read again
+    if ((rc = launch_gather(mm, s.B, s.trans, mb.idx, k, mb.xs, mb.gb.partials, stream, &err, true, mu)))
+      return fail(rc, err);
     if ((rc = launch_finalize_norm(mb.gb.partials, s.B, ns->eps, mb.gb.inv, stream, &err))) return fail(rc, err);
     // line 8 on the rows that are not updated below
     if (decay != 1.f && (rc = launch_scale_unselected(wm, s.B, s.trans, mb.idx, k, decay, mb.nf, stream, &err)))
@@ -1037,8 +1039,6 @@ int gns_muon_step(const gns_batch* W, const gns_batch* G, const gns_batch* M, co
     if ((rc = launch_scatter_update(wm, mb.os, s.B, s.trans, mb.idx, k, step_scale, decay, stream, &err,
                                     normuon ? mb.r : nullptr)))
       return fail(rc, err);
-    // line 10: error feedback
-    if ((rc = launch_decay_selected(mm, s.B, s.trans, mb.idx, k, mu, stream, &err))) return fail(rc, err);
   }
   return GNS_OK;
 }
