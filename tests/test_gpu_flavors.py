@@ -274,3 +274,66 @@ def test_periodic_takes_newton_schulz_on_refresh_steps_only():
         want = (muon_w, muon_m) if ofl.refresh(t, 3) else (rn_w, rn_m)
         assert np.array_equal(w, want[0]) and np.array_equal(m, want[1]), t
     assert not np.array_equal(muon_w, rn_w)
+
+
+# ---------------------------------------------------------------------------------------
+# the benchmark's workload (24 x 1024 x 4096 bf16, the configuration bench.py times for each
+# flavour), checked on sampled matrices of the batch
+
+FULL = (24, 1024, 4096)
+SAMPLES = (0, 11, 23)
+
+
+def _full_inputs(seed):
+    from matrix_orthogonalizing_optimizer_gb300 import inputs
+    count, rows, cols = FULL
+    s = 1.0 / np.sqrt(cols)
+    W = inputs.round_to_bf16_bits(inputs.gaussian(seed, FULL, s, stream=0))
+    G = inputs.round_to_bf16_bits(inputs.gaussian(seed, FULL, s, stream=1))
+    M = inputs.round_to_bf16_bits(inputs.gaussian(seed, FULL, s, stream=2))
+    return W, G, M
+
+
+def test_full_size_f16_products():
+    Wb, Gb, Mb = _full_inputs(200)
+    Wt, Gt, Mt = bits_to_torch(Wb), bits_to_torch(Gb), bits_to_torch(Mb)
+    st = _status()
+    gns.muon_step(Wt, Gt, Mt, params=gns.MuonParams(lr=0.02, momentum=0.95, ns_dtype=torch.float16), status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    Mg, Wg = torch_to_bits(Mt), torch_to_f64(Wt)
+    for b in SAMPLES:
+        W_or, M_or, O = omuon.muon_step(Wb[b], Gb[b], Mb[b], lr=0.02, mu=0.95)
+        assert np.array_equal(Mg[b], M_or)
+        e = _w_excess(Wg[b], W_or, 0.02 * O)
+        assert e < TOL_F16, (b, e)
+
+
+def test_full_size_normuon():
+    Wb, Gb, Mb = _full_inputs(201)
+    v0 = _v0(FULL[0], FULL[1], 202)
+    Wt, Gt, Mt = bits_to_torch(Wb), bits_to_torch(Gb), bits_to_torch(Mb)
+    Vt = torch.from_numpy(v0).cuda()
+    gns.muon_step(Wt, Gt, Mt, V=Vt, params=gns.MuonParams(lr=0.02, momentum=0.95, flavor="normuon", beta2=0.95,
+                                                          norm_eps=1e-8))
+    torch.cuda.synchronize()
+    Mg, Wg, Vg = torch_to_bits(Mt), torch_to_f64(Wt), Vt.double().cpu().numpy()
+    for b in SAMPLES:
+        W_or, M_or, v_or, D = ofl.normuon_step(Wb[b], Gb[b], Mb[b], v0[b, 0].astype(np.float64), lr=0.02, mu=0.95,
+                                               beta2=0.95, eps=1e-8)
+        assert np.array_equal(Mg[b], M_or)
+        assert _w_excess(Wg[b], W_or, 0.02 * D) < TOL_BF16
+        assert rel_fro(Vg[b, 0], v_or) < TOL_V
+
+
+def test_full_size_rownorm_every_matrix():
+    Wb, Gb, Mb = _full_inputs(203)
+    Wt, Gt, Mt = bits_to_torch(Wb), bits_to_torch(Gb), bits_to_torch(Mb)
+    gns.muon_step(Wt, Gt, Mt, params=gns.MuonParams(lr=0.02, momentum=0.95, flavor="rownorm", rownorm_gamma=0.15,
+                                                    norm_eps=1e-8))
+    torch.cuda.synchronize()
+    Mg, Wg = torch_to_bits(Mt), torch_to_f64(Wt)
+    for b in range(FULL[0]):
+        W_or, M_or, D = ofl.rownorm_step(Wb[b], Gb[b], Mb[b], lr=0.02, mu=0.95, gamma=0.15, eps=1e-8)
+        assert np.array_equal(Mg[b], M_or)
+        assert _w_excess(Wg[b], W_or, 0.02 * D) < TOL_ROWNORM, b
