@@ -370,7 +370,24 @@ def run_ours(args, rank, world, dist):
             go()
         b.record(stream)
         torch.cuda.synchronize()
-        return a.elapsed_time(b) / reps
+        step_ms = a.elapsed_time(b) / reps
+        # instrumented repeat: CUDA events around the GEMM launches of each step
+        cap = 8 * reps
+        evf = [torch.cuda.Event(enable_timing=True) for _ in range(2 * cap)]
+        for e in evf:
+            e.record(stream)
+        hf = (ctypes.c_void_p * (2 * cap))(*[ctypes.c_void_p(e.cuda_event) for e in evf])
+        torch.cuda.synchronize()
+        lib.gns_profile_set(hf, cap)
+        for _ in range(reps):
+            go()
+        torch.cuda.synchronize()
+        ng = ctypes.c_int(0)
+        lib.gns_profile_query(ctypes.byref(ng), None)
+        lib.gns_profile_set(None, 0)
+        n_rec = min(ng.value, cap)
+        g_ms = sum(evf[2 * i].elapsed_time(evf[2 * i + 1]) for i in range(n_rec)) / reps
+        return step_ms, g_ms
 
     # ---- the MoE-expert alpha = 4 batch: Gram NS alone on 256 x 2048 x 8192 ----
     def moe_experts():
@@ -482,19 +499,30 @@ def run_ours(args, rank, world, dist):
     dense = dense_layers()
 
     base = dict(lr=LR, momentum=MU)
-    f16_ms = time_flavor(gns.MuonParams(**base, ns_dtype=torch.float16))
-    normuon_ms = time_flavor(gns.MuonParams(**base, flavor="normuon", beta2=0.95, norm_eps=1e-8), with_v=True)
-    rownorm_ms = time_flavor(gns.MuonParams(**base, flavor="rownorm", rownorm_gamma=0.15, norm_eps=1e-8))
-    frac_ms = time_flavor(gns.MuonParams(**base, frac=0.25))
+    f16_ms, f16_gemm = time_flavor(gns.MuonParams(**base, ns_dtype=torch.float16))
+    normuon_ms, normuon_gemm = time_flavor(gns.MuonParams(**base, flavor="normuon", beta2=0.95, norm_eps=1e-8),
+                                           with_v=True)
+    rownorm_ms, _ = time_flavor(gns.MuonParams(**base, flavor="rownorm", rownorm_gamma=0.15, norm_eps=1e-8))
+    frac_ms, _ = time_flavor(gns.MuonParams(**base, frac=0.25))
+    step_flops = COUNT * alg_flops_per_matrix()
+
+    def gemm_roofline(g_ms, what):
+        ach = step_flops / (g_ms / 1000.0) / 1e12
+        return {"bound": "tensor", "achieved": ach, "peak": peak_burst, "unit": "TFLOP/s", "frac": ach / peak_burst,
+                "frac_of_sustained": ach / peak_sus, "gemm_ms_per_step": g_ms, "kernel": what,
+                "peak_kind": f"dense bf16 burst, {peak_src} (fp16 dense rate = bf16 dense rate)"}
     _, _, hbm_peak, _ = load_peaks()
     # RowNorm step: algorithmic traffic = read G, M, W and write M, W once (bf16)
     rn_bytes = COUNT * ROWS * COLS * 2 * 5
     flavors = {
         "note": "whole optimizer steps on the same 24 x 1024 x 4096 bf16 workload, inputs in HBM",
         "fp16_products": {"ms_per_step": f16_ms, "matrices_per_s": COUNT / (f16_ms / 1000.0),
-                          "what": "Muon step with the Newton-Schulz products in fp16 (Dion3 Algorithm 3 line 3)"},
+                          "what": "Muon step with the Newton-Schulz products in fp16 (Dion3 Algorithm 3 line 3)",
+                          "roofline": gemm_roofline(f16_gemm, "gns::tc::gemm_kernel, fp16 operands")},
         "normuon": {"ms_per_step": normuon_ms, "matrices_per_s": COUNT / (normuon_ms / 1000.0),
-                    "what": "NorMuon (Dion3 eq. (2)): Gram NS to O, row second moments, row scaling, update"},
+                    "what": "NorMuon (Dion3 eq. (2)): Gram NS to O, row second moments, row scaling, update",
+                    "roofline": gemm_roofline(normuon_gemm, "gns::tc::gemm_kernel, bf16, O written for the "
+                                                            "NorMuon statistics")},
         "rownorm": {"ms_per_step": rownorm_ms, "matrices_per_s": COUNT / (rownorm_ms / 1000.0),
                     "what": "RowNorm off-refresh step (Scaling Muon for DiTs eq. (5), (7))",
                     "roofline": {"bound": "hbm", "achieved": rn_bytes / (rownorm_ms / 1000.0) / 1e9,
