@@ -890,15 +890,28 @@ __global__ void cast_scaled_kernel(__half* X, long long ldx, long long sx, const
 
 // W <- beta * W + alpha * Y (same shape), fp32 arithmetic, one rounding.
 template <typename TW, typename TY>
+// (W and Y have elements of one size: 16-byte vectors of VEC elements along each row, a
+// block per ROWS_PER_BLOCK rows.)
 __global__ void axpby_kernel(TW* W, long long ldw, long long sw, const TY* Y, long long ldy, long long sy, int rows,
                              int cols, float alpha, float beta) {
-  const int b = blockIdx.z;
-  const long long total = (long long)rows * cols;
-  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (long long)gridDim.x * blockDim.x) {
-    const int r = (int)(e / cols), c = (int)(e % cols);
-    TW* p = W + (long long)b * sw + (long long)r * ldw + c;
-    const float y = to_f(Y[(long long)b * sy + (long long)r * ldy + c]);
-    *p = from_f<TW>(fmaf(alpha, y, beta * to_f(*p)));
+  static_assert(sizeof(TW) == sizeof(TY), "W and Y share an element size");
+  constexpr int VEC = 16 / sizeof(TW);
+  const int b = blockIdx.y;
+  const int cvec = cols - cols % VEC;
+  for (int r = blockIdx.x * ROWS_PER_BLOCK; r < min(rows, (int)(blockIdx.x + 1) * ROWS_PER_BLOCK); ++r) {
+    TW* wr = W + (long long)b * sw + (long long)r * ldw;
+    const TY* yr = Y + (long long)b * sy + (long long)r * ldy;
+    for (int c = threadIdx.x * VEC; c < cvec; c += blockDim.x * VEC) {
+      uint4 wu = *reinterpret_cast<const uint4*>(wr + c);
+      const uint4 yu = *reinterpret_cast<const uint4*>(yr + c);
+      TW* we = reinterpret_cast<TW*>(&wu);
+      const TY* ye = reinterpret_cast<const TY*>(&yu);
+#pragma unroll
+      for (int q = 0; q < VEC; ++q) we[q] = from_f<TW>(fmaf(alpha, to_f(ye[q]), beta * to_f(we[q])));
+      *reinterpret_cast<uint4*>(wr + c) = wu;
+    }
+    for (int c = cvec + threadIdx.x; c < cols; c += blockDim.x)
+      wr[c] = from_f<TW>(fmaf(alpha, to_f(yr[c]), beta * to_f(wr[c])));
   }
 }
 
@@ -1146,7 +1159,7 @@ int launch_cast_scaled(const MatRef& X16, const MatRef& M, const float* inv, int
 
 int launch_axpby(gns_dtype dt, const MatRef& W, const MatRef& Y, int64_t count, float alpha, float beta, void* stream,
                  std::string* err, gns_dtype y_dt) {
-  dim3 grid(grid_1d(W.rows * W.cols, 256), 1, (unsigned)count);
+  dim3 grid((unsigned)((W.rows + ROWS_PER_BLOCK - 1) / ROWS_PER_BLOCK), (unsigned)count);
   if ((int)y_dt < 0) y_dt = dt;
   if (dt == GNS_BF16 && y_dt == GNS_BF16)
     axpby_kernel<bf16, bf16><<<grid, 256, 0, S(stream)>>>(static_cast<bf16*>(W.ptr), W.ld, W.stride,
