@@ -13,7 +13,8 @@
 // Warp roles in each CTA:
 //   warp 0    TMA producer: 64-wide K slices into a 4-stage ring (128-byte swizzle; a
 //             K-major operand is one 128 x 64 box, an MN-major one two 64 x 64 boxes);
-//             completion is signalled on the leader CTA's stage barrier.
+//             completion is signalled on the leader CTA's stage barrier. Warp 0 fills the
+//             even stages, warp 11 (a second producer) the odd ones.
 //   warp 1    TMEM allocation (both CTAs) and, in the leader CTA, the MMA issuer.
 //   warp 2    C-tile loader: TMA loads of the addend C, chunk by chunk, as soon as the
 //             epilogue frees each buffer (a whole main loop ahead of its use).
@@ -61,7 +62,11 @@ constexpr int C_WARP = 2;                        // loads the C tile ahead of th
 constexpr int FIRST_EPI_WARP = 3;
 constexpr int EPI_WARPS = 8;                     // two per TMEM lane quarter
 constexpr int EPI_THREADS = 32 * EPI_WARPS;
-constexpr int NUM_THREADS = 32 * (FIRST_EPI_WARP + EPI_WARPS);
+// A second TMA producer in a warp of its own takes the odd ring stages: two issuing threads
+// keep more operand loads in flight than one (warps 0 and PROD2_WARP; a producer sharing a
+// warp with another role would run divergent with it).
+constexpr int PROD2_WARP = FIRST_EPI_WARP + EPI_WARPS;
+constexpr int NUM_THREADS = 32 * (FIRST_EPI_WARP + EPI_WARPS + 1);
 constexpr int MAX_PROB = 24;                     // stages of one launch
 constexpr int TMEM_COLS = 512;                   // two 256-column fp32 accumulators
 constexpr int OFF_SC = STAGES * STAGE_BYTES;     // C chunks (ring of C_BUFS)
@@ -71,6 +76,7 @@ constexpr int OFF_BAR = OFF_SM + OUT_BUFS * CHUNK_BYTES;
 constexpr int BAR_BYTES = 512;
 constexpr int SMEM_BYTES = 1024 + OFF_BAR + BAR_BYTES;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+static_assert(STAGES % 2 == 0, "the two producers take alternate stages");
 
 struct Problem {
   CUtensorMap tmA;
@@ -305,9 +311,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp == 0) {
+  if (warp == 0 || warp == PROD2_WARP) {
     if (lane == 0) {
-      // ---------------- TMA producer (both CTAs) ----------------
+      // ---------------- TMA producers (both CTAs): even stages / odd stages ----------------
+      const int pid = warp == 0 ? 0 : 1;
       int* const status = P.status;
       const uint32_t full0 = mapa_shared(smem_u32(&full[0]), 0);  // stage barriers in the leader
       int s = 0;
@@ -327,6 +334,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         const CUtensorMap* const tmB2 = &pr.tmB2;
         if (pr.dep_mask && !wait_ready(ready_tile, tile, abort_flag, status)) break;
         for (int kb = 0; kb < kl.kblocks; ++kb) {
+          if ((s & 1) != pid) {  // the other producer's stage
+            if (++s == STAGES) {
+              s = 0;
+              ph ^= 1u;
+            }
+            continue;
+          }
           if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, status)) {
             ok = false;
             break;
@@ -453,7 +467,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         if (!ok) break;
       }
     }
-  } else {
+  } else if (warp < PROD2_WARP) {
     // ---------------- epilogue (warps 3..10 of both CTAs) ----------------
     const int et = threadIdx.x - 32 * FIRST_EPI_WARP;
     const int ew = warp - FIRST_EPI_WARP;
