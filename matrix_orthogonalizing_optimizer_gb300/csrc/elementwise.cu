@@ -222,9 +222,14 @@ struct KeyAcc {
   }
 };
 
-// The same accumulator with its eight digit sums in shared memory (one slot of 8 per
-// thread): they change only when a value's exponent leaves the current digit, so keeping
-// them out of registers costs little and lets more warps stream the matrix.
+// The row kernel's accumulator: the same exact sum, counted in units of 2^-135 (every key
+// of a matrix is four times the sum above, which leaves their order unchanged), with the
+// eight digit sums in shared memory (one slot of 8 per thread; they change only when a
+// value's exponent leaves the current digit, so keeping them out of registers costs little
+// and lets more warps stream the matrix). With q = E - min(E, 1) + 2 a finite value adds
+// mant << (q & 31) to digit q >> 5 (at most 7); Inf / NaN (E = 255) land in digit 8, which
+// no finite value reaches, so they are caught on the rare path that changes digits, and
+// zeros keep the current digit (they add nothing).
 struct KeyAccS {
   uint64_t* acc;
   uint64_t cur;
@@ -242,23 +247,29 @@ struct KeyAccS {
     acc[dcur] += cur;
     cur = 0;
   }
-  __device__ __forceinline__ void add(uint16_t bits) {
-    const uint32_t E = (bits >> 7) & 0xFFu;
-    if (E == 0xFFu) {
-      nonfinite = true;
-      return;
-    }
-    const uint32_t f = bits & 0x7Fu;
-    const uint32_t mant = E ? (f | 0x80u) : f;
-    if (!mant) return;
-    const uint32_t ee = E ? E - 1u : 0u;
-    const uint32_t d = ee >> 5;
-    const uint64_t v = static_cast<uint64_t>(mant) << (ee & 31u);
+  // one value given by its exponent field E and fraction f
+  __device__ __forceinline__ void add(uint32_t E, uint32_t f) {
+    const uint32_t h = min(E, 1u);
+    const uint32_t mant = f + (h << 7);
+    const uint32_t q = E - h + 2u;
+    const uint32_t d = mant ? (q >> 5) : dcur;
     if (d != dcur) {
-      flush();
-      dcur = d;
+      if (d > 7u) {
+        nonfinite = true;  // the row's key is replaced; what this lane adds no longer matters
+      } else {
+        flush();
+        dcur = d;
+      }
     }
-    cur += v;
+    uint32_t lo, hi;  // mant << (q & 31) as a 64-bit value
+    asm("shf.l.wrap.b32 %0, %1, %2, %3;" : "=r"(lo) : "r"(0u), "r"(mant), "r"(q));
+    asm("shf.l.wrap.b32 %0, %1, %2, %3;" : "=r"(hi) : "r"(mant), "r"(0u), "r"(q));
+    cur += (static_cast<uint64_t>(hi) << 32) | lo;
+  }
+  // both bf16 values of a 32-bit word
+  __device__ __forceinline__ void add2(uint32_t w) {
+    add((w >> 7) & 0xFFu, w & 0x7Fu);
+    add((w >> 23) & 0xFFu, (w >> 16) & 0x7Fu);
   }
   __device__ void digits(uint32_t (&dg)[KEY_DIGITS]) {
     flush();
@@ -273,6 +284,14 @@ struct KeyAccS {
     dg[9] = static_cast<uint32_t>(carry >> 32);
   }
 };
+
+// M + G of two bf16 pairs, each sum rounded once to bf16 (a correctly rounded bf16 add is
+// the fp32 sum rounded to bf16: fp32 holds more than twice bf16's significand bits, so the
+// double rounding cannot differ)
+__device__ __forceinline__ uint32_t bf16x2_add(uint32_t a, uint32_t b) {
+  const __nv_bfloat162 r = __hadd2(*reinterpret_cast<const __nv_bfloat162*>(&a), *reinterpret_cast<const __nv_bfloat162*>(&b));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
 
 // Rows of the (non-transposed) matrix: M <- M + G and the key of each row. One warp per
 // row; per-lane digits are summed across the warp (each sum < 2^37) and stored.
@@ -293,19 +312,21 @@ __global__ void frac_add_keys_rows_kernel(bf16* M, long long ldm, long long sm, 
   for (int c = lane * 8; c < cvec; c += 32 * 8) {
     uint4 mv = *reinterpret_cast<const uint4*>(mr + c);
     const uint4 gv = *reinterpret_cast<const uint4*>(gr + c);
-    bf16* me = reinterpret_cast<bf16*>(&mv);
-    const bf16* ge = reinterpret_cast<const bf16*>(&gv);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      me[e] = f_to_bf16(__fadd_rn(bf16_to_f(me[e]), bf16_to_f(ge[e])));
-      ka.add(__bfloat16_as_ushort(me[e]));
-    }
+    mv.x = bf16x2_add(mv.x, gv.x);
+    mv.y = bf16x2_add(mv.y, gv.y);
+    mv.z = bf16x2_add(mv.z, gv.z);
+    mv.w = bf16x2_add(mv.w, gv.w);
     *reinterpret_cast<uint4*>(mr + c) = mv;
+    ka.add2(mv.x);
+    ka.add2(mv.y);
+    ka.add2(mv.z);
+    ka.add2(mv.w);
   }
   for (int c = cvec + lane; c < cols; c += 32) {
     const bf16 nv = f_to_bf16(__fadd_rn(bf16_to_f(mr[c]), bf16_to_f(gr[c])));
     mr[c] = nv;
-    ka.add(__bfloat16_as_ushort(nv));
+    const uint32_t u = __bfloat16_as_ushort(nv);
+    ka.add((u >> 7) & 0xFFu, u & 0x7Fu);
   }
   uint32_t dg[KEY_DIGITS];
   ka.digits(dg);

@@ -359,6 +359,38 @@ def test_frac_row_select_exact(rows, cols, k):
         assert np.array_equal(torch_to_bits(gath)[b], X[S])
 
 
+@pytest.mark.parametrize("cols", [1024, 1020])
+def test_frac_step_special_values(cols):
+    """The fused M <- M + G and row-key pass on values the exponent arithmetic treats apart:
+    subnormal sums, exact cancellations, signed zeros, all-zero rows, values in the top
+    digit of the key, and a row holding an Inf; M after the step (the sum, the selection and
+    the decay of the selected rows) must match bit for bit."""
+    count, rows, frac, mu = 3, 256, 0.25, 0.95
+    Wb, Gb, Mb = _frac_case(40, count, rows, cols, frac, ties=True)
+    sub = np.array([0x0001, 0x0003, 0x007F, 0x8002, 0x0040, 0x8001, 0x0010, 0x0000], dtype=np.uint16)
+    Mb[0, 3, :] = np.resize(sub, cols)                        # subnormal + subnormal
+    Gb[0, 3, :] = np.resize(sub[::-1], cols)
+    Mb[0, 4, :] = Gb[0, 4, :] ^ 0x8000                         # x + (-x) = +0: an all-zero row
+    Mb[0, 6, ::2] = 0x8000; Gb[0, 6, ::2] = 0x8000             # (-0) + (-0) = -0
+    Mb[0, 8, :] = np.resize(np.array([0x0080, 0x007F], dtype=np.uint16), cols)  # normal <-> subnormal
+    Gb[0, 8, :] = np.resize(np.array([0x8001, 0x0001], dtype=np.uint16), cols)
+    Mb[1, 7, :5] = 0x7E00; Gb[1, 7, :5] = 0                    # 2^125: the key's top digit
+    Mb[1, 9, -3:] = 0x7000                                     # 2^97 in the last (tail) columns
+    Mb[2, 3, 10] = 0x7F80                                      # +Inf: the row's key is maximal
+    Mb[2, 12, cols - 1] = 0xFF80                               # -Inf in a tail column
+    Wt, Gt, Mt = bits_to_torch(Wb), bits_to_torch(Gb), bits_to_torch(Mb)
+    gns.muon_step(Wt, Gt, Mt, lr=0.02, momentum=mu, frac=frac)
+    torch.cuda.synchronize()
+    Mg = torch_to_bits(Mt)
+    k = int(np.ceil(frac * rows))
+    for b in range(count):
+        Msum = omuon.momentum_update_bf16(Mb[b], Gb[b], 1.0)
+        S = omuon.top_k_rows(omuon.l1_keys_exact(Msum), k)
+        M_or = omuon.decay_rows_bf16(Msum, S, mu)
+        assert np.array_equal(Mg[b], M_or), b
+    assert 3 in S and 12 in S
+
+
 # ---------------------------------------------------------------------------------------
 # full-size workload: 24 x 1024 x 4096 Muon step (every matrix checked)
 
