@@ -251,6 +251,43 @@ __device__ __forceinline__ void chunk_store(const uint8_t* s, const CUtensorMap*
   }
 }
 
+// o += beta * C for 32 values held two per word (fp16 when f16, else bf16); the element type
+// is decided once per chunk, not per value.
+__device__ __forceinline__ void axpy_h16x2(float (&o)[32], const uint32_t (&cw)[16], float beta, int f16) {
+  if (f16) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&cw[i]));
+      o[2 * i] = fmaf(beta, f.x, o[2 * i]);
+      o[2 * i + 1] = fmaf(beta, f.y, o[2 * i + 1]);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {  // bf16 -> fp32 is exact: the bits move up 16 places
+      o[2 * i] = fmaf(beta, __uint_as_float(cw[i] << 16), o[2 * i]);
+      o[2 * i + 1] = fmaf(beta, __uint_as_float(cw[i] & 0xFFFF0000u), o[2 * i + 1]);
+    }
+  }
+}
+
+// 32 fp32 values rounded to nearest even, two per word (the first in the low half), with
+// the paired conversion instructions.
+__device__ __forceinline__ void pack_h16x2(const float (&o)[32], uint32_t (&pk)[16], int f16) {
+  if (f16) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const __half2 h = __floats2half2_rn(o[2 * i], o[2 * i + 1]);
+      pk[i] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const __nv_bfloat162 h = __floats2bfloat162_rn(o[2 * i], o[2 * i + 1]);
+      pk[i] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+  }
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ Params P) {
   extern __shared__ uint8_t smem_raw[];
@@ -535,51 +572,55 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           const uint32_t q = qc % C_BUFS;
           const uint8_t* sc = SC + q * CHUNK_BYTES;
           if (!mbar_wait(&cfull[q], (qc / C_BUFS) & 1u, abort_flag, P.status)) *epi_flag = 0;
+          uint32_t cw[16];  // the row's 32 C values, two per word
           if (!c_trans) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               const uint4 w = *reinterpret_cast<const uint4*>(sc + off_direct(r, half * 32 + q * 8));
-              const uint16_t* wv = reinterpret_cast<const uint16_t*>(&w);
-#pragma unroll
-              for (int e = 0; e < 8; ++e) o[q * 8 + e] = fmaf(beta, h16_to_f(wv[e], c_f16), o[q * 8 + e]);
+              cw[4 * q] = w.x;
+              cw[4 * q + 1] = w.y;
+              cw[4 * q + 2] = w.z;
+              cw[4 * q + 3] = w.w;
             }
           } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              o[j] = fmaf(beta, h16_to_f(*reinterpret_cast<const uint16_t*>(sc + off_trans(r, half * 32 + j)), c_f16),
-                          o[j]);
+            for (int i = 0; i < 16; ++i)
+              cw[i] = (uint32_t)*reinterpret_cast<const uint16_t*>(sc + off_trans(r, half * 32 + 2 * i)) |
+                      ((uint32_t)*reinterpret_cast<const uint16_t*>(sc + off_trans(r, half * 32 + 2 * i + 1)) << 16);
           }
+          axpy_h16x2(o, cw, beta, c_f16);
           __syncwarp();
           if (lane == 0) mbar_arrive(&cempty[q]);
           ++qc;
         }
         if (check_finite) {
+          // x * 0 is 0 for every finite x and NaN for Inf / NaN: one FMA per value
+          float z = 0.f;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) bad |= !isfinite(o[j]);
+          for (int j = 0; j < 32; ++j) z = fmaf(o[j], 0.f, z);
+          bad |= !(z == 0.f);
         }
         if (diag_mine && (diag_col >> 6) == ch) {
 #pragma unroll
           for (int j = 0; j < 32; ++j)
             if (j == (diag_col & 31)) dv = o[j];
         }
+        uint32_t pk[16];  // the row's 32 outputs rounded once, two per word
+        pack_h16x2(o, pk, d_f16);
         if (!d_trans) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint4 w;
-            uint16_t* wv = reinterpret_cast<uint16_t*>(&w);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) wv[e] = f_to_h16(o[q * 8 + e], d_f16);
-            *reinterpret_cast<uint4*>(sd + off_direct(r, half * 32 + q * 8)) = w;
-          }
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4*>(sd + off_direct(r, half * 32 + q * 8)) =
+                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
         } else {
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            *reinterpret_cast<uint16_t*>(sd + off_trans(r, half * 32 + j)) = f_to_h16(o[j], d_f16);
+            *reinterpret_cast<uint16_t*>(sd + off_trans(r, half * 32 + j)) = (uint16_t)(pk[j >> 1] >> (16 * (j & 1)));
         }
         if (mirror) {
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            *reinterpret_cast<uint16_t*>(sm + off_trans(r, half * 32 + j)) = f_to_h16(o[j], d_f16);
+            *reinterpret_cast<uint16_t*>(sm + off_trans(r, half * 32 + j)) = (uint16_t)(pk[j >> 1] >> (16 * (j & 1)));
         }
         fence_proxy_async_smem();
         named_bar_sync(1, EPI_THREADS);
