@@ -11,19 +11,20 @@
 // upper-triangle tiles of a symmetric one (Dion3 sec. 5, "Triangular Scheduler").
 //
 // Warp roles in each CTA:
-//   warp 0    TMA producer: 64-wide K slices into a 4-stage ring (128-byte swizzle; a
+//   warp 0    TMA producer: 64-wide K slices into a ring of stages (128-byte swizzle; a
 //             K-major operand is one 128 x 64 box, an MN-major one two 64 x 64 boxes);
-//             completion is signalled on the leader CTA's stage barrier. Warp 0 fills the
-//             even stages, warp 11 (a second producer) the odd ones.
+//             completion is signalled on the leader CTA's stage barrier. Warp 0 loads the
+//             even K slices of the pair's sequence, warp 11 (a second producer) the odd ones.
 //   warp 1    TMEM allocation (both CTAs) and, in the leader CTA, the MMA issuer.
-//   warp 2    C-tile loader: TMA loads of the addend C, chunk by chunk, as soon as the
-//             epilogue frees each buffer (a whole main loop ahead of its use).
+//   warp 2    C-tile loader: TMA loads of the addend C, chunk by chunk, into a small ring
+//             as soon as the epilogue frees each buffer.
 //   warps 3-10 epilogue, two warps per TMEM lane quarter (thread = row, each warp 32 of a
 //             chunk's 64 columns): tcgen05.ld of the accumulator, alpha/beta with the C tile,
 //             result staged in 128-byte-swizzled shared memory and written with TMA stores
 //             in 64-column chunks; off-diagonal tiles of symmetric products are also stored
-//             transposed at the mirrored position, diagonal tiles once (Dion3 sec. 5
-//             "Writing to the Transposed Tile", appendix C.1).
+//             transposed at the mirrored position (through the same staging buffer),
+//             diagonal tiles once (Dion3 sec. 5 "Writing to the Transposed Tile",
+//             appendix C.1).
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -40,18 +41,10 @@ constexpr int TM = 128;                          // accumulator rows per CTA (25
 constexpr int TN = 256;                          // tile columns
 constexpr int BN = 128;                          // B columns staged per CTA
 constexpr int TK = 64;                           // K slice per stage
-#ifndef GNS_TC_STAGES
-#define GNS_TC_STAGES 4
-#endif
 #ifndef GNS_TC_OUTBUFS
 #define GNS_TC_OUTBUFS 1
 #endif
-#ifndef GNS_TC_CBUFS
-#define GNS_TC_CBUFS 4
-#endif
-constexpr int STAGES = GNS_TC_STAGES;
 constexpr int OUT_BUFS = GNS_TC_OUTBUFS;         // staging buffers for output (and mirror) chunks
-constexpr int C_BUFS = GNS_TC_CBUFS;             // ring of C-chunk buffers
 constexpr int A_BYTES = TM * TK * 2;             // 16 KiB
 constexpr int STAGE_BYTES = (TM + BN) * TK * 2;  // 32 KiB per CTA
 constexpr int CHUNK = 64;                        // epilogue columns per chunk
@@ -62,21 +55,35 @@ constexpr int C_WARP = 2;                        // loads the C tile ahead of th
 constexpr int FIRST_EPI_WARP = 3;
 constexpr int EPI_WARPS = 8;                     // two per TMEM lane quarter
 constexpr int EPI_THREADS = 32 * EPI_WARPS;
-// A second TMA producer in a warp of its own takes the odd ring stages: two issuing threads
+// A second TMA producer in a warp of its own takes the odd K slices: two issuing threads
 // keep more operand loads in flight than one (warps 0 and PROD2_WARP; a producer sharing a
 // warp with another role would run divergent with it).
 constexpr int PROD2_WARP = FIRST_EPI_WARP + EPI_WARPS;
 constexpr int NUM_THREADS = 32 * (FIRST_EPI_WARP + EPI_WARPS + 1);
 constexpr int MAX_PROB = 24;                     // stages of one launch
 constexpr int TMEM_COLS = 512;                   // two 256-column fp32 accumulators
-constexpr int OFF_SC = STAGES * STAGE_BYTES;     // C chunks (ring of C_BUFS)
-constexpr int OFF_SD = OFF_SC + C_BUFS * CHUNK_BYTES;
-constexpr int OFF_SM = OFF_SD + OUT_BUFS * CHUNK_BYTES;
-constexpr int OFF_BAR = OFF_SM + OUT_BUFS * CHUNK_BYTES;
 constexpr int BAR_BYTES = 512;
-constexpr int SMEM_BYTES = 1024 + OFF_BAR + BAR_BYTES;
-static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-static_assert(STAGES % 2 == 0, "the two producers take alternate stages");
+
+// Shared-memory plan of a kernel with STAGES operand stages and a ring of C_BUFS C chunks.
+// Two plans are compiled: a deep operand ring (6 stages, 1 C chunk) pays on launches of
+// short tiles (few K slices per tile: the ring also covers the switch to the next tile);
+// a shallow one (4 stages, 4 C chunks) on launches of long tiles, where a deeper ring only
+// keeps more operand lines in flight and costs L2 reuse.
+template <int STAGES_, int C_BUFS_>
+struct Plan {
+  static constexpr int STAGES = STAGES_;
+  static constexpr int C_BUFS = C_BUFS_;
+  static constexpr int OFF_SC = STAGES * STAGE_BYTES;  // C chunks (ring of C_BUFS)
+  static constexpr int OFF_SD = OFF_SC + C_BUFS * CHUNK_BYTES;
+  static constexpr int OFF_BAR = OFF_SD + OUT_BUFS * CHUNK_BYTES;
+  static constexpr int SMEM_BYTES = 1024 + OFF_BAR + BAR_BYTES;
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  static_assert((2 * STAGES + 4 + 2 * C_BUFS) * 8 + 16 <= BAR_BYTES, "barrier area");
+};
+using DeepPlan = Plan<6, 1>;
+using ShallowPlan = Plan<4, 4>;
+// Launches whose tiles average at most this many K slices take the deep plan.
+constexpr int DEEP_MAX_SLICES_PER_TILE = 24;
 
 struct Problem {
   CUtensorMap tmA;
@@ -288,14 +295,19 @@ __device__ __forceinline__ void pack_h16x2(const float (&o)[32], uint32_t (&pk)[
   }
 }
 
+template <class L>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ Params P) {
+  constexpr int STAGES = L::STAGES;
+  constexpr int C_BUFS = L::C_BUFS;
+  constexpr int OFF_SC = L::OFF_SC;
+  constexpr int OFF_SD = L::OFF_SD;
+  constexpr int OFF_BAR = L::OFF_BAR;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = smem;
   uint8_t* SC = smem + OFF_SC;
   uint8_t* SD = smem + OFF_SD;
-  uint8_t* SM = smem + OFF_SM;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
   uint64_t* full = bars;
   uint64_t* empty = bars + STAGES;
@@ -350,10 +362,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 
   if (warp == 0 || warp == PROD2_WARP) {
     if (lane == 0) {
-      // ---------------- TMA producers (both CTAs): even stages / odd stages ----------------
+      // ---------------- TMA producers (both CTAs): even K slices / odd K slices ----------------
       const int pid = warp == 0 ? 0 : 1;
       int* const status = P.status;
       const uint32_t full0 = mapa_shared(smem_u32(&full[0]), 0);  // stage barriers in the leader
+      uint32_t g = 0;  // K slices of this pair so far: producer g & 1 takes slice g
       int s = 0;
       uint32_t ph = 0;
       bool ok = true;
@@ -371,7 +384,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         const CUtensorMap* const tmB2 = &pr.tmB2;
         if (pr.dep_mask && !wait_ready(ready_tile, tile, abort_flag, status)) break;
         for (int kb = 0; kb < kl.kblocks; ++kb) {
-          if ((s & 1) != pid) {  // the other producer's stage
+          if ((g++ & 1u) != (uint32_t)pid) {  // the other producer's slice
             if (++s == STAGES) {
               s = 0;
               ph ^= 1u;
@@ -549,7 +562,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       bool bad = false;
       for (int ch = 0; ch < NCHUNK; ++ch, ++gc) {
         uint8_t* sd = SD + (gc % OUT_BUFS) * CHUNK_BYTES;
-        uint8_t* sm = SM + (gc % OUT_BUFS) * CHUNK_BYTES;
         // the stores that last read these buffers are done
         if (et == 0) {
           if (OUT_BUFS == 2) bulk_wait_read<1>(); else bulk_wait_read<0>();
@@ -617,23 +629,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           for (int j = 0; j < 32; ++j)
             *reinterpret_cast<uint16_t*>(sd + off_trans(r, half * 32 + j)) = (uint16_t)(pk[j >> 1] >> (16 * (j & 1)));
         }
-        if (mirror) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            *reinterpret_cast<uint16_t*>(sm + off_trans(r, half * 32 + j)) = (uint16_t)(pk[j >> 1] >> (16 * (j & 1)));
-        }
         fence_proxy_async_smem();
         named_bar_sync(1, EPI_THREADS);
         const int col0 = n0 + ch * CHUNK;
         const bool chunk_has_diag = want_diag && (ch == 2 * (int)rank || ch == 2 * (int)rank + 1);
         if (et == 0) {
           chunk_store(sd, &pr.tmD, d_mode, m0, col0, c.b);
-          if (mirror) chunk_store(sm, &pr.tmD, 1, m0, col0, c.b);
-          if (has_d2 && !chunk_has_diag) {
-            chunk_store(sd, &pr.tmD2, d_mode, m0, col0, c.b);
-            if (mirror) chunk_store(sm, &pr.tmD2, 1, m0, col0, c.b);
-          }
+          if (has_d2 && !chunk_has_diag) chunk_store(sd, &pr.tmD2, d_mode, m0, col0, c.b);
           bulk_commit();
+        }
+        if (mirror) {
+          // the transposed copy goes through the same staging buffer once the stores above
+          // have read it (mirrored tiles are never diagonal ones)
+          if (et == 0) bulk_wait_read<0>();
+          named_bar_sync(1, EPI_THREADS);
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            *reinterpret_cast<uint16_t*>(sd + off_trans(r, half * 32 + j)) = (uint16_t)(pk[j >> 1] >> (16 * (j & 1)));
+          fence_proxy_async_smem();
+          named_bar_sync(1, EPI_THREADS);
+          if (et == 0) {
+            chunk_store(sd, &pr.tmD, 1, m0, col0, c.b);
+            if (has_d2) chunk_store(sd, &pr.tmD2, 1, m0, col0, c.b);
+            bulk_commit();
+          }
         }
         if (chunk_has_diag) {
           // D2 = D + gamma I: patch the diagonal with the fp32 value plus gamma, rounded once
@@ -734,13 +753,14 @@ int device_sm_count() {
 
 // Number of CTA pairs of the GEMM kernel that can be resident at once (and the one-time
 // shared-memory opt-in).
+template <class L>
 static int resident_pairs(std::string* err) {
   static int cached[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) dev = 0;
   if (cached[dev]) return cached[dev];
-  cudaError_t e = cudaFuncSetAttribute(tc::gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_BYTES);
+  cudaError_t e = cudaFuncSetAttribute(tc::gemm_kernel<L>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_BYTES);
   if (e != cudaSuccess) {
     *err = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e);
     return 0;
@@ -748,9 +768,9 @@ static int resident_pairs(std::string* err) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * (device_sm_count() / 2), 1, 1);
   cfg.blockDim = dim3(tc::NUM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = tc::SMEM_BYTES;
+  cfg.dynamicSmemBytes = L::SMEM_BYTES;
   int clusters = 0;
-  e = cudaOccupancyMaxActiveClusters(&clusters, tc::gemm_kernel, &cfg);
+  e = cudaOccupancyMaxActiveClusters(&clusters, tc::gemm_kernel<L>, &cfg);
   if (e != cudaSuccess || clusters < 1) {
     (void)cudaGetLastError();
     clusters = device_sm_count() / 2;
@@ -766,8 +786,10 @@ int gemm_launch_tc(const GemmOp* ops, int nops, const uint32_t* dep_masks, int* 
     *err = "internal: bad number of products in one launch";
     return GNS_ERR_INVALID;
   }
-  const int pairs_max = resident_pairs(err);
-  if (pairs_max < 1) return GNS_ERR_CUDA;
+  const int pairs_deep = resident_pairs<DeepPlan>(err);
+  if (pairs_deep < 1) return GNS_ERR_CUDA;
+  const int pairs_shallow = resident_pairs<ShallowPlan>(err);
+  if (pairs_shallow < 1) return GNS_ERR_CUDA;
   Params P;
   memset(&P, 0, sizeof(P));
   int tiles = 0;
@@ -845,13 +867,18 @@ int gemm_launch_tc(const GemmOp* ops, int nops, const uint32_t* dep_masks, int* 
     }
   }
   if (tiles == 0) return GNS_OK;
-  const int pairs = std::min(tiles, pairs_max);
+  long long slices = 0;  // K slices over all tiles of the launch
+  for (int i = 0; i < nops; ++i)
+    slices += (long long)P.prob[i].kblocks * P.prob[i].tiles_per_mat * ops[i].batch;
+  const bool deep = slices <= (long long)DEEP_MAX_SLICES_PER_TILE * tiles;
+  const int pairs = std::min(tiles, deep ? pairs_deep : pairs_shallow);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * pairs, 1, 1);
   cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.dynamicSmemBytes = deep ? DeepPlan::SMEM_BYTES : ShallowPlan::SMEM_BYTES;
   cfg.stream = static_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_kernel, P);
+  cudaError_t e = deep ? cudaLaunchKernelEx(&cfg, gemm_kernel<DeepPlan>, P)
+                       : cudaLaunchKernelEx(&cfg, gemm_kernel<ShallowPlan>, P);
   if (e != cudaSuccess) {
     *err = std::string("tcgen05 GEMM launch: ") + cudaGetErrorString(e);
     return GNS_ERR_CUDA;
