@@ -258,38 +258,37 @@ __device__ __forceinline__ void chunk_store(const uint8_t* s, const CUtensorMap*
   }
 }
 
+// The epilogue's arithmetic runs on value pairs (the paired fp32 instructions, each element
+// rounded as its scalar form would be): its warps share the SMs' issue slots with the
+// single-thread producer and MMA roles, so every instruction saved there is main-loop time.
+//
 // o += beta * C for 32 values held two per word (fp16 when f16, else bf16); the element type
 // is decided once per chunk, not per value.
-__device__ __forceinline__ void axpy_h16x2(float (&o)[32], const uint32_t (&cw)[16], float beta, int f16) {
+__device__ __forceinline__ void axpy_h16x2(float2 (&o)[16], const uint32_t (&cw)[16], float beta, int f16) {
+  const float2 b2 = make_float2(beta, beta);
   if (f16) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&cw[i]));
-      o[2 * i] = fmaf(beta, f.x, o[2 * i]);
-      o[2 * i + 1] = fmaf(beta, f.y, o[2 * i + 1]);
-    }
+    for (int i = 0; i < 16; ++i) o[i] = __ffma2_rn(b2, __half22float2(*reinterpret_cast<const __half2*>(&cw[i])), o[i]);
   } else {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {  // bf16 -> fp32 is exact: the bits move up 16 places
-      o[2 * i] = fmaf(beta, __uint_as_float(cw[i] << 16), o[2 * i]);
-      o[2 * i + 1] = fmaf(beta, __uint_as_float(cw[i] & 0xFFFF0000u), o[2 * i + 1]);
-    }
+    for (int i = 0; i < 16; ++i)  // bf16 -> fp32 is exact: the bits move up 16 places
+      o[i] = __ffma2_rn(b2, make_float2(__uint_as_float(cw[i] << 16), __uint_as_float(cw[i] & 0xFFFF0000u)), o[i]);
   }
 }
 
 // 32 fp32 values rounded to nearest even, two per word (the first in the low half), with
 // the paired conversion instructions.
-__device__ __forceinline__ void pack_h16x2(const float (&o)[32], uint32_t (&pk)[16], int f16) {
+__device__ __forceinline__ void pack_h16x2(const float2 (&o)[16], uint32_t (&pk)[16], int f16) {
   if (f16) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      const __half2 h = __floats2half2_rn(o[2 * i], o[2 * i + 1]);
+      const __half2 h = __float22half2_rn(o[i]);
       pk[i] = *reinterpret_cast<const uint32_t*>(&h);
     }
   } else {
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      const __nv_bfloat162 h = __floats2bfloat162_rn(o[2 * i], o[2 * i + 1]);
+      const __nv_bfloat162 h = __float22bfloat162_rn(o[i]);
       pk[i] = *reinterpret_cast<const uint32_t*>(&h);
     }
   }
@@ -577,9 +576,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(acc ? tempty_leader1 : tempty_leader0);
         }
-        float o[32];
+        float2 o[16];  // the row's 32 values, in pairs
 #pragma unroll
-        for (int j = 0; j < 32; ++j) o[j] = alpha * __uint_as_float(v[j]);
+        for (int i = 0; i < 16; ++i) o[i] = make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+        if (alpha != 1.f) {
+          const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) o[i] = __fmul2_rn(a2, o[i]);
+        }
         if (has_c) {
           const uint32_t q = qc % C_BUFS;
           const uint8_t* sc = SC + q * CHUNK_BYTES;
@@ -606,16 +610,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           ++qc;
         }
         if (check_finite) {
-          // x * 0 is 0 for every finite x and NaN for Inf / NaN: one FMA per value
-          float z = 0.f;
+          // x * 0 is 0 for every finite x and NaN for Inf / NaN: one paired FMA per two values
+          float2 z = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) z = fmaf(o[j], 0.f, z);
-          bad |= !(z == 0.f);
+          for (int i = 0; i < 16; ++i) z = __ffma2_rn(o[i], make_float2(0.f, 0.f), z);
+          bad |= !(z.x == 0.f && z.y == 0.f);
         }
         if (diag_mine && (diag_col >> 6) == ch) {
+          const int dj = diag_col & 31;
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j == (diag_col & 31)) dv = o[j];
+          for (int i = 0; i < 16; ++i) {
+            if (2 * i == dj) dv = o[i].x;
+            if (2 * i + 1 == dj) dv = o[i].y;
+          }
         }
         uint32_t pk[16];  // the row's 32 outputs rounded once, two per word
         pack_h16x2(o, pk, d_f16);
