@@ -485,18 +485,36 @@ __global__ void __launch_bounds__(1024) select_topk_kernel(unsigned long long* k
     for (int i = threadIdx.x; i < n; i += blockDim.x)
       if (st[i] == 0) atomicAdd(&hist[(K[(long long)i * KEY_DIGITS + dg] >> sh) & 0xFF], 1u);
     __syncthreads();
-    if (threadIdx.x == 0) {
-      int cum = 0, T = 0;
-      for (int bk = 255; bk >= 0; --bk) {
-        if (cum + (int)hist[bk] >= kleft) {
-          T = bk;
-          break;
-        }
-        cum += (int)hist[bk];
+    if (threadIdx.x < 32) {
+      // the bucket T holding the kleft-th largest candidate, found by warp 0: lane l sums
+      // buckets 255 - 8l down to 248 - 8l, a warp scan gives the counts above each lane's
+      // group, and the lane whose group crosses kleft walks its eight buckets
+      const int lane = threadIdx.x;
+      int grp = 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) grp += (int)hist[255 - 8 * lane - e];
+      int incl = grp;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
       }
-      sh_T = T;
-      sh_kleft = kleft - cum;
-      sh_cnt = (int)hist[T];
+      const int above = incl - grp;  // candidates in the buckets above this lane's group
+      const unsigned hit = __ballot_sync(0xffffffffu, above < kleft && incl >= kleft);
+      if (lane == __ffs(hit) - 1) {
+        int cum = above, T = 255 - 8 * lane;
+        for (int e = 0; e < 8; ++e) {
+          const int bk = 255 - 8 * lane - e;
+          if (cum + (int)hist[bk] >= kleft) {
+            T = bk;
+            break;
+          }
+          cum += (int)hist[bk];
+        }
+        sh_T = T;
+        sh_kleft = kleft - cum;
+        sh_cnt = (int)hist[T];
+      }
     }
     __syncthreads();
     const unsigned T = (unsigned)sh_T;
