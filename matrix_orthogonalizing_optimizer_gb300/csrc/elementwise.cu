@@ -309,9 +309,20 @@ __global__ void frac_add_keys_rows_kernel(bf16* M, long long ldm, long long sm, 
   KeyAccS ka;
   ka.init(slots + threadIdx.x * 8);
   const int cvec = cols & ~7;
-  for (int c = lane * 8; c < cvec; c += 32 * 8) {
-    uint4 mv = *reinterpret_cast<const uint4*>(mr + c);
-    const uint4 gv = *reinterpret_cast<const uint4*>(gr + c);
+  // software-pipelined: the next 16-byte vectors are in flight while this one is summed
+  int c = lane * 8;
+  uint4 mv = make_uint4(0, 0, 0, 0), gv = mv;
+  if (c < cvec) {
+    mv = *reinterpret_cast<const uint4*>(mr + c);
+    gv = *reinterpret_cast<const uint4*>(gr + c);
+  }
+  for (; c < cvec; c += 32 * 8) {
+    const int cn = c + 32 * 8;
+    uint4 mn = make_uint4(0, 0, 0, 0), gn = mn;
+    if (cn < cvec) {
+      mn = *reinterpret_cast<const uint4*>(mr + cn);
+      gn = *reinterpret_cast<const uint4*>(gr + cn);
+    }
     mv.x = bf16x2_add(mv.x, gv.x);
     mv.y = bf16x2_add(mv.y, gv.y);
     mv.z = bf16x2_add(mv.z, gv.z);
@@ -321,6 +332,8 @@ __global__ void frac_add_keys_rows_kernel(bf16* M, long long ldm, long long sm, 
     ka.add2(mv.y);
     ka.add2(mv.z);
     ka.add2(mv.w);
+    mv = mn;
+    gv = gn;
   }
   for (int c = cvec + lane; c < cols; c += 32) {
     const bf16 nv = f_to_bf16(__fadd_rn(bf16_to_f(mr[c]), bf16_to_f(gr[c])));
