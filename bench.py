@@ -44,6 +44,11 @@ def alg_flops_per_matrix(n=ROWS, m=COLS):
     return (14 + 6 * alpha) * n ** 3
 
 
+def std_flops_per_matrix(n, m, T=5):
+    """T (3 alpha + 1) n^3: standard Newton-Schulz with symmetric products (Dion3 sec. 2.3)."""
+    return T * (3 * m / n + 1) * n ** 3
+
+
 # DRAM bytes (read + write) of one launch of the GEMM kernel from an ncu capture
 # (profiles/gemm_kernel_fused_muon_step_24x1024x4096.md), keyed by the kernel source it was
 # taken on: reported only while that source is unchanged.
@@ -393,12 +398,12 @@ def run_ours(args, rank, world, dist):
         return step_ms, g_ms
 
     # ---- the MoE-expert alpha = 4 batch: Gram NS alone on 256 x 2048 x 8192 ----
-    def moe_experts():
-        count, n, m = 256, 2048, 8192
-        X = (torch.randn((count, n, m), generator=gen, device=dev, dtype=torch.float32) / m ** 0.5).to(torch.bfloat16)
+    def time_orth(X, fn, op, flops):
+        """One batched orthogonalization call (warm-up, then 3 timed calls): call time and the
+        GEMM launches' time from the library's event hooks."""
         Xo = torch.empty_like(X)
-        ws_m = gns.alloc_workspace(gns.workspace_size(_lib.GNS_OP_GRAM_NS, X, ns), dev)
-        gns.gram_ns_batched(X, outs=[Xo], ns=ns, workspace=ws_m, stream=stream)
+        ws_m = gns.alloc_workspace(gns.workspace_size(op, X, ns), dev)
+        fn(X, outs=[Xo], ns=ns, workspace=ws_m, stream=stream)
         torch.cuda.synchronize()
         reps = 3
         evm = [torch.cuda.Event(enable_timing=True) for _ in range(2 * reps)]
@@ -410,22 +415,44 @@ def run_ours(args, rank, world, dist):
         lib.gns_profile_set(hm, reps)
         a.record(stream)
         for _ in range(reps):
-            gns.gram_ns_batched(X, outs=[Xo], ns=ns, workspace=ws_m, stream=stream)
+            fn(X, outs=[Xo], ns=ns, workspace=ws_m, stream=stream)
         b.record(stream)
         torch.cuda.synchronize()
         lib.gns_profile_set(None, 0)
         call_ms = a.elapsed_time(b) / reps
         g_ms = sum(evm[2 * i].elapsed_time(evm[2 * i + 1]) for i in range(reps)) / reps
-        fl = count * alg_flops_per_matrix(n, m)
-        del X, Xo, ws_m
+        del Xo, ws_m
         torch.cuda.empty_cache()
-        return {"what": "Gram NS alone (T=5, restart@2) on 256 expert matrices 2048 x 8192 bf16 (alpha = 4), "
-                        "N(0,1)/sqrt(m) entries", "ms_per_call": call_ms, "matrices_per_s": count / (call_ms / 1000.0),
-                "gemm_ms": g_ms, "gemm_tflops": fl / (g_ms / 1000.0) / 1e12,
-                "gemm_frac_of_burst_peak": fl / (g_ms / 1000.0) / 1e12 / load_peaks()[0],
-                "gemm_frac_of_sustained_peak": fl / (g_ms / 1000.0) / 1e12 / load_peaks()[1]}
+        tf = flops / (g_ms / 1000.0) / 1e12
+        return {"ms_per_call": call_ms, "matrices_per_s": X.shape[0] / (call_ms / 1000.0), "gemm_ms": g_ms,
+                "gemm_tflops": tf, "gemm_frac_of_burst_peak": tf / load_peaks()[0],
+                "gemm_frac_of_sustained_peak": tf / load_peaks()[1]}
+
+    def moe_experts():
+        count, n, m = 256, 2048, 8192
+        X = (torch.randn((count, n, m), generator=gen, device=dev, dtype=torch.float32) / m ** 0.5).to(torch.bfloat16)
+        r = {"what": "Gram NS alone (T=5, restart@2) on 256 expert matrices 2048 x 8192 bf16 (alpha = 4), "
+                     "N(0,1)/sqrt(m) entries"}
+        r.update(time_orth(X, gns.gram_ns_batched, _lib.GNS_OP_GRAM_NS, count * alg_flops_per_matrix(n, m)))
+        std = time_orth(X, gns.ns_standard_batched, _lib.GNS_OP_NS_STANDARD, count * std_flops_per_matrix(n, m))
+        r["standard_ns_ms_per_call"] = std["ms_per_call"]
+        r["gram_vs_standard_speedup"] = std["ms_per_call"] / r["ms_per_call"]
+        del X
+        torch.cuda.empty_cache()
+        return r
+
+    def moe_squares():
+        count, n = 64, 7168
+        X = (torch.randn((count, n, n), generator=gen, device=dev, dtype=torch.float32) / n ** 0.5).to(torch.bfloat16)
+        r = {"what": "standard NS (T=5, symmetric products; alpha = 1, where Gram NS saves nothing) on 64 square "
+                     "matrices 7168 x 7168 bf16, N(0,1)/sqrt(n) entries"}
+        r.update(time_orth(X, gns.ns_standard_batched, _lib.GNS_OP_NS_STANDARD, count * std_flops_per_matrix(n, n)))
+        del X
+        torch.cuda.empty_cache()
+        return r
 
     moe = moe_experts()
+    moe_sq = moe_squares()
 
     # ---- the fractional-update configuration: 32 x 4096 x 16384, f = 1/4 (k = 1024) ----
     def frac_config():
@@ -574,6 +601,7 @@ def run_ours(args, rank, world, dist):
                                      "standard NS with symmetric products (Dion3 Algorithm 1, sec. 2.3)"},
         "flavors": flavors,
         "moe_experts_alpha4": moe,
+        "moe_squares_7168": moe_sq,
         "frac_quarter_4096x16384": frac_cfg,
         "dense_layers_32": dense,
         "gpu_launches": n_all.value,
