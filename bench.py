@@ -52,7 +52,7 @@ def std_flops_per_matrix(n, m, T=5):
 # DRAM bytes (read + write) of one launch of the GEMM kernel from an ncu capture
 # (profiles/gemm_kernel_fused_muon_step_24x1024x4096.md), keyed by the kernel source it was
 # taken on: reported only while that source is unchanged.
-GEMM_TRAFFIC = {"7016fdbd1b6c518a": 2.305295e9}
+GEMM_TRAFFIC = {"a08be551760510ae": 2.300315e9}
 
 
 def gemm_traffic():

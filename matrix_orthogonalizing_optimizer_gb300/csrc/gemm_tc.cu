@@ -838,7 +838,12 @@ int gemm_launch_tc(const GemmOp* ops, int nops, const uint32_t* dep_masks, int* 
     pr.tiles_m = (int)((o.M + 255) / 256);
     pr.tiles_n = (int)((o.N + 255) / 256);
     pr.sym = o.sym;
-    pr.tiles_per_mat = o.sym ? pr.tiles_m * (pr.tiles_m + 1) / 2 : pr.tiles_m * pr.tiles_n;
+    const long long tpm = o.sym ? (long long)pr.tiles_m * (pr.tiles_m + 1) / 2 : (long long)pr.tiles_m * pr.tiles_n;
+    if (tpm * o.batch + tiles > (long long)INT32_MAX) {
+      *err = "the products of one call have more than 2^31 output tiles";
+      return GNS_ERR_UNSUPPORTED;
+    }
+    pr.tiles_per_mat = (int)tpm;
     pr.tile_begin = tiles;
     tiles += pr.tiles_per_mat * (int)o.batch;
     pr.alpha = o.alpha;
