@@ -252,6 +252,33 @@ def run_ours(args, rank, world, dist):
     value = whole_job_rate(world, COUNT, ms)
     tflops = world * COUNT * alg_flops_per_matrix() / (ms / 1000.0) / 1e12
 
+    # ---- the same step captured once into a CUDA graph: 5 warm-up replays, then 25 replays
+    #      each bracketed by events (per-step median and interquartile range) ----
+    def graph_timing(reps=25):
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap):
+            gns.muon_step(W, G, M, lr=LR, momentum=MU, ns=ns, workspace=ws, status=status, stream=cap)
+        torch.cuda.synchronize()
+        for _ in range(5):
+            graph.replay()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for a, b in ev:
+            a.record()
+            graph.replay()
+            b.record()
+        torch.cuda.synchronize()
+        t = sorted(a.elapsed_time(b) for a, b in ev)
+        q = lambda f: t[min(reps - 1, int(round(f * (reps - 1))))]
+        med = q(0.5)
+        del graph
+        return {"replays": reps, "median_ms": med, "iqr_ms": [q(0.25), q(0.75)],
+                "matrices_per_s_at_median": COUNT / (med / 1000.0)}
+
+    graph = graph_timing()
+
     # ---- instrumented repeat: CUDA events around every GEMM launch (same stream) ----
     per_step = n_gemm.value // max(args.steps, 1)
     cap = per_step * args.steps
@@ -596,6 +623,7 @@ def run_ours(args, rank, world, dist):
                      "peak_kind": f"dense bf16 burst, {peak_src}",
                      "frac_of_sustained": achieved / peak_sus,
                      "gemm_ms_per_step": gemm_ms, "gemm_launches_per_step": per_step},
+        "graph_replay": graph,
         "gram_vs_standard": {"gram_ns_ms": gram_ms, "standard_ns_ms": std_ms, "speedup": std_ms / gram_ms,
                              "note": "orthogonalization of the 24 matrices alone, same tcgen05 kernels, T=5; "
                                      "standard NS with symmetric products (Dion3 Algorithm 1, sec. 2.3)"},
