@@ -140,8 +140,9 @@ def test_safety_factor_runs_the_adjusted_table(dtype):
 # ---------------------------------------------------------------------------------------
 # Muon step with fp16 Newton-Schulz
 
+# (1, 2048, 8192): tiles of 32 to 128 K slices, the GEMM's shallow shared-memory plan
 @pytest.mark.parametrize("count,rows,cols,frac", [(2, 256, 1024, 1.0), (2, 384, 384, 1.0), (2, 700, 200, 1.0),
-                                                  (2, 256, 1024, 0.25)])
+                                                  (2, 256, 1024, 0.25), (1, 2048, 8192, 1.0)])
 def test_muon_step_f16_products(count, rows, cols, frac):
     Wb, W = bf16_input(36, (count, rows, cols), 1.0 / np.sqrt(cols))
     Gb, _ = bf16_input(37, (count, rows, cols), 1.0 / np.sqrt(cols))
@@ -178,7 +179,8 @@ def _v0(count, n, seed):
 
 
 @pytest.mark.parametrize("count,rows,cols,ns_dtype", [(2, 128, 512, "bf16"), (1, 384, 128, "bf16"),
-                                                      (2, 256, 256, "bf16"), (2, 128, 512, "f16")])
+                                                      (2, 256, 256, "bf16"), (2, 128, 512, "f16"),
+                                                      (1, 2048, 8192, "bf16"), (1, 8192, 2048, "f16")])
 def test_normuon_dense(count, rows, cols, ns_dtype):
     Wb, W = bf16_input(40, (count, rows, cols), 1.0 / np.sqrt(cols))
     Gb, _ = bf16_input(41, (count, rows, cols), 1.0 / np.sqrt(cols))
