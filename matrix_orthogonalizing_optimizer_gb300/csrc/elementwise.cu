@@ -383,6 +383,93 @@ __global__ void frac_add_keys_cols_kernel(bf16* M, long long ldm, long long sm, 
   if (ka.nonfinite) atomicOr(nf + (long long)b * cols + c, 1);
 }
 
+// Columns of the matrix, 16-byte vectors: the same pass with each thread on 8 adjacent
+// columns (one vector of M and of G per row) over a chunk of rows, M + G by packed bf16x2
+// adds. Every column keeps, in registers, the running sum of its current digit window in
+// the row kernel's units (2^-135, digit window q >> 5 with q = E - min(E, 1) + 2; keys of
+// one matrix all come from this kernel, so only their order matters); a window change, and
+// the end of the chunk, add that sum into the column's key digit with a 64-bit atomic
+// (integer sums: order-independent), to be carried into canonical digits by the selection
+// kernel. Inf / NaN land in window 8 and flag the column. keys / nf must be zero on entry;
+// cols must be a multiple of 8 and the rows 16-byte aligned.
+struct ColKeys8 {
+  uint64_t cur[8];
+  uint32_t dcur[8];
+  uint32_t nonfinite;  // bit e: column e saw an Inf / NaN
+  __device__ __forceinline__ void init() {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      cur[e] = 0;
+      dcur[e] = 0;
+    }
+    nonfinite = 0;
+  }
+  __device__ __forceinline__ void add(int e, uint32_t u, unsigned long long* key) {
+    const uint32_t E = (u >> 7) & 0xFFu, f = u & 0x7Fu;
+    const uint32_t h = min(E, 1u);
+    const uint32_t mant = f + (h << 7);
+    const uint32_t q = E - h + 2u;
+    const uint32_t d = mant ? (q >> 5) : dcur[e];
+    if (d != dcur[e]) {
+      if (d > 7u) {
+        nonfinite |= 1u << e;  // the column's key is replaced; what is added no longer matters
+      } else {
+        if (cur[e]) atomicAdd(key + dcur[e], (unsigned long long)cur[e]);
+        cur[e] = 0;
+        dcur[e] = d;
+      }
+    }
+    uint32_t lo, hi;
+    asm("shf.l.wrap.b32 %0, %1, %2, %3;" : "=r"(lo) : "r"(0u), "r"(mant), "r"(q));
+    asm("shf.l.wrap.b32 %0, %1, %2, %3;" : "=r"(hi) : "r"(mant), "r"(0u), "r"(q));
+    cur[e] += (static_cast<uint64_t>(hi) << 32) | lo;
+  }
+};
+
+__global__ void __launch_bounds__(256) frac_add_keys_cols8_kernel(bf16* M, long long ldm, long long sm,
+                                                                  const bf16* G, long long ldg, long long sg,
+                                                                  int rows, int cols, int rows_per_chunk,
+                                                                  unsigned long long* keys, int* nf) {
+  const int b = blockIdx.z;
+  const int c0 = (blockIdx.x * blockDim.x + threadIdx.x) * 8;
+  if (c0 >= cols) return;
+  const int r0 = blockIdx.y * rows_per_chunk, r1 = min(rows, r0 + rows_per_chunk);
+  bf16* Mb = M + (long long)b * sm + c0;
+  const bf16* Gb = G + (long long)b * sg + c0;
+  unsigned long long* kb = keys + ((long long)b * cols + c0) * KEY_DIGITS;
+  ColKeys8 ka;
+  ka.init();
+  uint4 mv = make_uint4(0, 0, 0, 0), gv = mv;
+  if (r0 < r1) {
+    mv = *reinterpret_cast<const uint4*>(Mb + (long long)r0 * ldm);
+    gv = *reinterpret_cast<const uint4*>(Gb + (long long)r0 * ldg);
+  }
+  for (int r = r0; r < r1; ++r) {
+    // the next row's vectors are in flight while this one is summed
+    uint4 mn = make_uint4(0, 0, 0, 0), gn = mn;
+    if (r + 1 < r1) {
+      mn = *reinterpret_cast<const uint4*>(Mb + (long long)(r + 1) * ldm);
+      gn = *reinterpret_cast<const uint4*>(Gb + (long long)(r + 1) * ldg);
+    }
+    mv.x = bf16x2_add(mv.x, gv.x);
+    mv.y = bf16x2_add(mv.y, gv.y);
+    mv.z = bf16x2_add(mv.z, gv.z);
+    mv.w = bf16x2_add(mv.w, gv.w);
+    *reinterpret_cast<uint4*>(Mb + (long long)r * ldm) = mv;
+    const uint32_t w[4] = {mv.x, mv.y, mv.z, mv.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      ka.add(e, (w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu, kb + (long long)e * KEY_DIGITS);
+    mv = mn;
+    gv = gn;
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    if (ka.cur[e]) atomicAdd(kb + (long long)e * KEY_DIGITS + ka.dcur[e], (unsigned long long)ka.cur[e]);
+    if ((ka.nonfinite >> e) & 1u) atomicOr(nf + (long long)b * cols + c0 + e, 1);
+  }
+}
+
 // Keys of the rows (trans = 0) or columns (trans = 1) of M, without updating M.
 __global__ void keys_only_kernel(const bf16* M, long long ldm, long long sm, int rows, int cols, int trans,
                                  int rows_per_chunk, unsigned long long* keys, int* nf) {
@@ -1040,11 +1127,24 @@ int launch_frac_add_keys(const MatRef& M, const MatRef& G, int64_t count, int tr
   } else {
     cudaMemsetAsync(keys, 0, sizeof(unsigned long long) * KEY_DIGITS * M.cols * count, S(stream));
     cudaMemsetAsync(nf, 0, sizeof(int) * M.cols * count, S(stream));
-    const int rpc = 256;
-    dim3 grid((unsigned)((M.cols + 255) / 256), (unsigned)((M.rows + rpc - 1) / rpc), (unsigned)count);
-    frac_add_keys_cols_kernel<<<grid, 256, 0, S(stream)>>>(static_cast<bf16*>(M.ptr), M.ld, M.stride,
-                                                           static_cast<const bf16*>(G.ptr), G.ld, G.stride,
-                                                           (int)M.rows, (int)M.cols, rpc, keys, nf);
+    const bool vec = M.cols % 8 == 0 && M.ld % 8 == 0 && G.ld % 8 == 0 && (count == 1 || (M.stride % 8 == 0 && G.stride % 8 == 0));
+    if (vec) {
+      // chunks of rows sized for about four waves of 8 resident blocks per SM
+      const long long col_blocks = (M.cols / 8 + 255) / 256;
+      const long long want = 4LL * 8 * device_sm_count();
+      long long chunks = std::max(1LL, want / std::max(1LL, col_blocks * count));
+      const int rpc = (int)std::max(64LL, (M.rows + chunks - 1) / chunks);
+      dim3 grid((unsigned)col_blocks, (unsigned)((M.rows + rpc - 1) / rpc), (unsigned)count);
+      frac_add_keys_cols8_kernel<<<grid, 256, 0, S(stream)>>>(static_cast<bf16*>(M.ptr), M.ld, M.stride,
+                                                              static_cast<const bf16*>(G.ptr), G.ld, G.stride,
+                                                              (int)M.rows, (int)M.cols, rpc, keys, nf);
+    } else {
+      const int rpc = 256;
+      dim3 grid((unsigned)((M.cols + 255) / 256), (unsigned)((M.rows + rpc - 1) / rpc), (unsigned)count);
+      frac_add_keys_cols_kernel<<<grid, 256, 0, S(stream)>>>(static_cast<bf16*>(M.ptr), M.ld, M.stride,
+                                                             static_cast<const bf16*>(G.ptr), G.ld, G.stride,
+                                                             (int)M.rows, (int)M.cols, rpc, keys, nf);
+    }
   }
   return check_launch("frac_add_keys", err);
 }

@@ -391,6 +391,38 @@ def test_frac_step_special_values(cols):
     assert 3 in S and 12 in S
 
 
+@pytest.mark.parametrize("rows,cols", [(1024, 256), (1020, 256), (1024, 252)])
+def test_frac_step_special_values_tall(rows, cols):
+    """The column pass of a tall matrix (keys of its columns) on the same special values,
+    planted in columns: M after the step must match bit for bit (cols = 252: the scalar
+    column kernel; otherwise the 16-byte one)."""
+    count, frac, mu = 3, 0.25, 0.95
+    Wb, Gb, Mb = _frac_case(50, count, rows, cols, frac, ties=True)
+    sub = np.array([0x0001, 0x0003, 0x007F, 0x8002, 0x0040, 0x8001, 0x0010, 0x0000], dtype=np.uint16)
+    Mb[0, :, 3] = np.resize(sub, rows)
+    Gb[0, :, 3] = np.resize(sub[::-1], rows)
+    Mb[0, :, 4] = Gb[0, :, 4] ^ 0x8000
+    Mb[0, ::2, 6] = 0x8000; Gb[0, ::2, 6] = 0x8000
+    Mb[0, :, 8] = np.resize(np.array([0x0080, 0x007F], dtype=np.uint16), rows)
+    Gb[0, :, 8] = np.resize(np.array([0x8001, 0x0001], dtype=np.uint16), rows)
+    Mb[1, :5, 7] = 0x7E00; Gb[1, :5, 7] = 0
+    Mb[1, -3:, 9] = 0x7000
+    Mb[2, 10, 3] = 0x7F80
+    Mb[2, rows - 1, 12] = 0xFF80
+    Wt, Gt, Mt = bits_to_torch(Wb), bits_to_torch(Gb), bits_to_torch(Mb)
+    gns.muon_step(Wt, Gt, Mt, lr=0.02, momentum=mu, frac=frac)
+    torch.cuda.synchronize()
+    Mg = torch_to_bits(Mt)
+    k = int(np.ceil(frac * cols))
+    for b in range(count):
+        Msum = omuon.momentum_update_bf16(Mb[b], Gb[b], 1.0)
+        Xt = np.ascontiguousarray(Msum.T)
+        S = omuon.top_k_rows(omuon.l1_keys_exact(Xt), k)
+        M_or = np.ascontiguousarray(omuon.decay_rows_bf16(Xt, S, mu).T)
+        assert np.array_equal(Mg[b], M_or), b
+    assert 3 in S and 12 in S
+
+
 # ---------------------------------------------------------------------------------------
 # full-size workload: 24 x 1024 x 4096 Muon step (every matrix checked)
 
