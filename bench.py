@@ -482,8 +482,8 @@ def run_ours(args, rank, world, dist):
     moe_sq = moe_squares()
 
     # ---- the fractional-update configuration: 32 x 4096 x 16384, f = 1/4 (k = 1024) ----
-    def frac_config():
-        count, rows, cols = 32, 4096, 16384
+    def frac_config(rows=4096, cols=16384):
+        count = 32
         sc = 1.0 / cols ** 0.5
 
         def rnd():
@@ -506,16 +506,19 @@ def run_ours(args, rank, world, dist):
         b.record(stream)
         torch.cuda.synchronize()
         f_ms = a.elapsed_time(b) / reps
-        k = 1024
-        fl = count * alg_flops_per_matrix(k, cols)
+        n, m = min(rows, cols), max(rows, cols)
+        k = (n + 3) // 4
+        fl = count * alg_flops_per_matrix(k, m)
         del Wf, Gf, Mf, ws_f
         torch.cuda.empty_cache()
-        return {"what": "Dion3 fractional update f = 1/4 on 32 bf16 momentum matrices 4096 x 16384: exact l1 "
-                        "top-1024 rows, Gram NS of the 1024 x 16384 subsets, scatter, error feedback",
+        sel = "rows" if rows <= cols else "columns (the rows of the transpose)"
+        return {"what": f"Dion3 fractional update f = 1/4 on 32 bf16 momentum matrices {rows} x {cols}: exact l1 "
+                        f"top-{k} {sel}, Gram NS of the {k} x {m} subsets, scatter, error feedback",
                 "ms_per_step": f_ms, "matrices_per_s": count / (f_ms / 1000.0),
                 "orthogonalization_tflops_over_step": fl / (f_ms / 1000.0) / 1e12}
 
     frac_cfg = frac_config()
+    frac_tall = frac_config(16384, 4096)
 
     # ---- the mixed dense-transformer layer set: 32 layers of one 4096 x 4096 (alpha = 1,
     # standard NS) and two 4096 x 11008 plus one 11008 x 4096 (alpha = 2.69, Gram NS) ----
@@ -631,6 +634,7 @@ def run_ours(args, rank, world, dist):
         "moe_experts_alpha4": moe,
         "moe_squares_7168": moe_sq,
         "frac_quarter_4096x16384": frac_cfg,
+        "frac_quarter_16384x4096_tall": frac_tall,
         "dense_layers_32": dense,
         "gpu_launches": n_all.value,
         "device_status": st,
