@@ -657,7 +657,7 @@ __global__ void __launch_bounds__(1024) select_topk_kernel(unsigned long long* k
 
 // X[b][i][:] = M[b][idx[b*k + i]][:] (rows), with sum-of-squares partials of X.
 // With decay, the selected rows of M are also replaced by bf16(mu * M) (Dion3 Algorithm 4's
-// error feedback, line 10) once copied: nothing reads M[S] after the gather, so the decay
+// error feedback) once copied: nothing reads M[S] after the gather, so the decay
 // rides on this pass.
 __global__ void gather_rows_kernel(bf16* M, long long ldm, long long sm, const int* idx, int k, int cols,
                                    bf16* X, long long ldx, long long sx, int npart, float* partials, int decay,
@@ -697,27 +697,47 @@ __global__ void gather_rows_kernel(bf16* M, long long ldm, long long sm, const i
   if (threadIdx.x == 0) partials[(long long)b * npart + part] = s;
 }
 
-// X[b][i][j] = M[b][j][idx[b*k + i]] (columns of M become rows of X); 32 x 32 tiles.
-__global__ void gather_cols_kernel(bf16* M, long long ldm, long long sm, const int* idx, int k, int rows,
-                                   bf16* X, long long ldx, long long sx, int decay, float mu) {
-  __shared__ bf16 tile[32][33];
+// Rows per block of the column gather / scatter of a tall matrix (32 selected columns wide).
+constexpr int COL_TILE_ROWS = 64;
+
+// X[b][i][j] = M[b][j][idx[b*k + i]] (columns of M become rows of X), with the decay
+// M[b][j][idx[i]] = bf16(mu * M) when asked; 32 x TJ tiles staged in shared memory.
+template <int TJ>
+__global__ void __launch_bounds__(256) gather_cols_kernel(bf16* M, long long ldm, long long sm, const int* idx, int k,
+                                                          int rows, bf16* X, long long ldx, long long sx, int decay,
+                                                          float mu) {
+  // 32 selected columns x TJ rows per block: each thread issues its TJ / 8 loads before
+  // using any of them
+  __shared__ bf16 tile[TJ][33];
+  constexpr int R = TJ / 8;
   const int b = blockIdx.z;
-  const int i0 = blockIdx.x * 32, j0 = blockIdx.y * 32;
+  const int i0 = blockIdx.x * 32, j0 = blockIdx.y * TJ;
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
-  for (int jj = ty; jj < 32; jj += 8) {
-    const int j = j0 + jj, i = i0 + tx;
-    bf16 v = f_to_bf16(0.f);
-    if (j < rows && i < k) {
-      bf16* p = M + (long long)b * sm + (long long)j * ldm + idx[(long long)b * k + i];
-      v = *p;
-      if (decay) *p = f_to_bf16(__fmul_rn(mu, bf16_to_f(v)));
-    }
-    tile[jj][tx] = v;
+  const int i = i0 + tx;
+  const bool iv = i < k;
+  bf16* col = M + (long long)b * sm + (iv ? idx[(long long)b * k + i] : 0);
+  bf16 v[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int j = j0 + ty + 8 * r;
+    v[r] = f_to_bf16(0.f);
+    if (iv && j < rows) v[r] = col[(long long)j * ldm];
+  }
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int j = j0 + ty + 8 * r;
+    if (decay && iv && j < rows) col[(long long)j * ldm] = f_to_bf16(__fmul_rn(mu, bf16_to_f(v[r])));
+    tile[ty + 8 * r][tx] = v[r];
   }
   __syncthreads();
   for (int ii = ty; ii < 32; ii += 8) {
-    const int i = i0 + ii, j = j0 + tx;
-    if (i < k && j < rows) X[(long long)b * sx + (long long)i * ldx + j] = tile[tx][ii];
+    const int iw = i0 + ii;
+    if (iw >= k) break;
+#pragma unroll
+    for (int jj = tx; jj < TJ; jj += 32) {
+      const int j = j0 + jj;
+      if (j < rows) X[(long long)b * sx + (long long)iw * ldx + j] = tile[jj][ii];
+    }
   }
 }
 
@@ -780,34 +800,47 @@ __global__ void scatter_update_rows_kernel(bf16* W, long long ldw, long long sw,
     wr[c] = f_to_bf16(fmaf(a, bf16_to_f(orow[c]), beta * bf16_to_f(wr[c])));
 }
 
-// The same for the columns of a tall W: W[j][idx[i]] for O[i][j]. A 32 x 32 tile of O goes
+// The same for the columns of a tall W: W[j][idx[i]] for O[i][j]. A 32 x TJ tile of O goes
 // through shared memory so that both the O reads and the W accesses are along rows.
-__global__ void scatter_update_cols_kernel(bf16* W, long long ldw, long long sw, const bf16* O, long long ldo,
-                                           long long so, const int* idx, const float* rs, int k, int len, float alpha,
-                                           float beta) {
-  __shared__ float tile[32][33];
+template <int TJ>
+__global__ void __launch_bounds__(256) scatter_update_cols_kernel(bf16* W, long long ldw, long long sw, const bf16* O,
+                                                                  long long ldo, long long so, const int* idx,
+                                                                  const float* rs, int k, int len, float alpha,
+                                                                  float beta) {
+  // 32 selected columns x TJ rows per block; the TJ / 8 loads of W a thread makes are all
+  // issued before the first update
+  __shared__ float tile[32][TJ + 1];
+  constexpr int R = TJ / 8;
   const int b = blockIdx.z;
-  const int i0 = blockIdx.x * 32, j0 = blockIdx.y * 32;
+  const int i0 = blockIdx.x * 32, j0 = blockIdx.y * TJ;
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
   for (int ii = ty; ii < 32; ii += 8) {
-    const int i = i0 + ii, j = j0 + tx;
-    float v = 0.f;
-    if (i < k && j < len) {
-      v = bf16_to_f(O[(long long)b * so + (long long)i * ldo + j]);
-      if (rs) v *= rs[(long long)b * k + i];
+    const int i = i0 + ii;
+#pragma unroll
+    for (int jj = tx; jj < TJ; jj += 32) {
+      const int j = j0 + jj;
+      float v = 0.f;
+      if (i < k && j < len) {
+        v = bf16_to_f(O[(long long)b * so + (long long)i * ldo + j]);
+        if (rs) v *= rs[(long long)b * k + i];
+      }
+      tile[ii][jj] = v;
     }
-    tile[ii][tx] = v;
   }
   __syncthreads();
   const int i = i0 + tx;
   if (i >= k) return;
-  const int sel = idx ? idx[(long long)b * k + i] : i;
-  for (int jj = ty; jj < 32; jj += 8) {
-    const int j = j0 + jj;
-    if (j < len) {
-      bf16* p = W + (long long)b * sw + (long long)j * ldw + sel;
-      *p = f_to_bf16(fmaf(alpha, tile[tx][jj], beta * bf16_to_f(*p)));
-    }
+  bf16* col = W + (long long)b * sw + (idx ? idx[(long long)b * k + i] : i);
+  bf16 w[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int j = j0 + ty + 8 * r;
+    if (j < len) w[r] = col[(long long)j * ldw];
+  }
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int j = j0 + ty + 8 * r;
+    if (j < len) col[(long long)j * ldw] = f_to_bf16(fmaf(alpha, tile[tx][ty + 8 * r], beta * bf16_to_f(w[r])));
   }
 }
 
@@ -870,7 +903,7 @@ __global__ void col_sumsq_finish_kernel(const float* part, int cols, int npart, 
   s[e] = acc;
 }
 
-// NorMuon (Dion3 eq. (2); Algorithm 4 lines 5-7), one block per matrix. For the k rows of O
+// NorMuon (Dion3 eq. (2); the NorMuon steps of Algorithm 4), one block per matrix. For the k rows of O
 // with sums of squares s_i (of `len` columns each), row i being row sel(i) of the oriented
 // matrix (sel = idx or the identity):
 //   v <- beta2 v + (1 - beta2) s_i / len;  d_i = sqrt(v) + eps;
@@ -1004,7 +1037,7 @@ __global__ void rowscale_update_kernel(bf16* W, long long ldw, long long sw, con
   }
 }
 
-// X16 = fp16(inv[b] * M) in the same layout (Dion3 Algorithm 3 lines 2-3 for a bf16
+// X16 = fp16(inv[b] * M) in the same layout (Dion3 Algorithm 3's first steps for a bf16
 // momentum: normalise, then round once to float16); 16-byte vectors.
 __global__ void cast_scaled_kernel(__half* X, long long ldx, long long sx, const bf16* M, long long ldm, long long sm,
                                    const float* inv, int rows, int cols) {
@@ -1191,8 +1224,8 @@ int launch_gather(const MatRef& M, int64_t count, int trans, const int* idx, int
                                                     (int)M.cols, static_cast<bf16*>(X.ptr), X.ld, X.stride, NPART,
                                                     partials, decay ? 1 : 0, mu);
   } else {
-    dim3 grid((unsigned)((k + 31) / 32), (unsigned)((M.rows + 31) / 32), (unsigned)count);
-    gather_cols_kernel<<<grid, 256, 0, S(stream)>>>(static_cast<bf16*>(M.ptr), M.ld, M.stride, idx, (int)k,
+    dim3 grid((unsigned)((k + 31) / 32), (unsigned)((M.rows + COL_TILE_ROWS - 1) / COL_TILE_ROWS), (unsigned)count);
+    gather_cols_kernel<COL_TILE_ROWS><<<grid, 256, 0, S(stream)>>>(static_cast<bf16*>(M.ptr), M.ld, M.stride, idx, (int)k,
                                                     (int)M.rows, static_cast<bf16*>(X.ptr), X.ld, X.stride,
                                                     decay ? 1 : 0, mu);
     if (partials) {
@@ -1229,8 +1262,8 @@ int launch_scatter_update(const MatRef& W, const MatRef& O, int64_t count, int t
                                                             static_cast<const bf16*>(O.ptr), O.ld, O.stride, idx, rs,
                                                             (int)k, (int)len, alpha, beta);
   } else {
-    dim3 grid((unsigned)((k + 31) / 32), (unsigned)((len + 31) / 32), (unsigned)count);
-    scatter_update_cols_kernel<<<grid, 256, 0, S(stream)>>>(static_cast<bf16*>(W.ptr), W.ld, W.stride,
+    dim3 grid((unsigned)((k + 31) / 32), (unsigned)((len + COL_TILE_ROWS - 1) / COL_TILE_ROWS), (unsigned)count);
+    scatter_update_cols_kernel<COL_TILE_ROWS><<<grid, 256, 0, S(stream)>>>(static_cast<bf16*>(W.ptr), W.ld, W.stride,
                                                             static_cast<const bf16*>(O.ptr), O.ld, O.stride, idx, rs,
                                                             (int)k, (int)len, alpha, beta);
   }

@@ -115,7 +115,7 @@ def test_sym_gemm_xxt_f32(n, K):
 
 
 # ---------------------------------------------------------------------------------------
-# one iteration of Algorithm 3 (lines 12-15)
+# one iteration of the loop of Algorithm 3 (Z, Q, RZ and R updates)
 
 @pytest.mark.parametrize("q_is_identity,skip_r", [(True, False), (False, False), (False, True)])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
@@ -313,7 +313,8 @@ def _frac_case(seed, count, rows, cols, frac, ties=False):
 
 
 @pytest.mark.parametrize("count,rows,cols,frac", [(2, 256, 1024, 0.25), (2, 300, 900, 0.5), (2, 640, 192, 0.25),
-                                                  (1, 64, 512, 1.0 / 64)])
+                                                  (1, 64, 512, 1.0 / 64), (2, 1000, 320, 0.25),
+                                                  (1, 2600, 2560, 0.25)])
 def test_frac_step(count, rows, cols, frac):
     Wb, Gb, Mb = _frac_case(20, count, rows, cols, frac, ties=True)
     Wt, Gt, Mt = bits_to_torch(Wb), bits_to_torch(Gb), bits_to_torch(Mb)
