@@ -577,7 +577,7 @@ def run_ours(args, rank, world, dist):
     flavors = {
         "note": "whole optimizer steps on the same 24 x 1024 x 4096 bf16 workload, inputs in HBM",
         "fp16_products": {"ms_per_step": f16_ms, "matrices_per_s": COUNT / (f16_ms / 1000.0),
-                          "what": "Muon step with the Newton-Schulz products in fp16 (Dion3 Algorithm 3 line 3)",
+                          "what": "Muon step with the Newton-Schulz products in fp16 (the float16 cast of Dion3 Algorithm 3)",
                           "roofline": gemm_roofline(f16_gemm, "gns::tc::gemm_kernel, fp16 operands")},
         "normuon": {"ms_per_step": normuon_ms, "matrices_per_s": COUNT / (normuon_ms / 1000.0),
                     "what": "NorMuon (Dion3 eq. (2)): Gram NS to O, row second moments, row scaling, update",

@@ -18,7 +18,7 @@
  *   - Dion3 update rule (Dion3 sec. 6, Algorithm 4, Muon flavour): M <- M + G; S = the
  *     k = ceil(f n) rows of largest l1 norm; W <- (1 - eta wd) W; W[S] -= eta polar(M[S]);
  *     M[S] <- mu M[S].
- *   - NorMuon (Dion3 sec. 2.1 eq. (2), Algorithm 4 lines 5-7): a per-row second moment
+ *   - NorMuon (Dion3 sec. 2.1 eq. (2) and the NorMuon steps of Algorithm 4): a per-row second moment
  *     v_i <- beta2 v_i + (1 - beta2) mean_j O_ij^2 of the orthogonalized update, rows divided
  *     by sqrt(v_i) + eps, the result rescaled to the Frobenius norm of O; fp32 arithmetic.
  *   - RowNorm and Periodic Row-wise Muon (Scaling Muon for Diffusion Transformers, sec. 3.1
@@ -85,7 +85,7 @@ typedef enum {
   GNS_BF16 = 0, /* bf16 storage, tensor-core products with fp32 accumulation (hot path) */
   GNS_F32 = 1,  /* fp32 storage and fp32 arithmetic (validation path) */
   GNS_F16 = 2   /* fp16 storage, tensor-core products with fp32 accumulation (Dion3 Algorithm 3
-                   line 3 casts to float16; appendix B.2.2 prefers it to bfloat16) */
+                   casts to float16; appendix B.2.2 prefers it to bfloat16) */
 } gns_dtype;
 
 /* `count` row-major matrices: element (b, i, j) at ptr + b*stride + i*ld + j (elements). */
@@ -101,7 +101,7 @@ typedef struct {
 /* Newton-Schulz schedule: T iterations with coefficients (a_t, b_t, c_t), t = 1..T
  * (index t-1), e.g. a caller's Polar Express table. Bit i of restart_mask (1 <= i < T)
  * restarts after iteration i (Dion3 Algorithm 3 restarts after iteration 2: mask 1u << 2).
- * eps as in Algorithm 1 line 2. safety = s > 0 applies the safety factor of Dion3 appendix
+ * eps as in the normalisation step of Algorithm 1. safety = s > 0 applies the safety factor of Dion3 appendix
  * B.2.2 to every iteration: p_t(x) becomes p_t(x / s), so (a, b, c) is used as
  * (a / s, b / s^3, c / s^5); s = 1 leaves the table as given (the pages' conservative choice
  * for Polar Express coefficients is s = 1.05). */
@@ -118,7 +118,7 @@ typedef struct {
 /* Update flavours of gns_muon_step. */
 typedef enum {
   GNS_FLAVOR_MUON = 0,     /* O = polar(M) (Dion3 eq. (1); Algorithm 4 Muon flavour) */
-  GNS_FLAVOR_NORMUON = 1,  /* O = NorMuon-normalised polar(M) (Dion3 eq. (2); Algorithm 4 l. 5-7) */
+  GNS_FLAVOR_NORMUON = 1,  /* O = NorMuon-normalised polar(M) (Dion3 eq. (2); NorMuon steps of Algorithm 4) */
   GNS_FLAVOR_ROWNORM = 2,  /* O = gamma R_eps(M) (Scaling Muon for DiTs eq. (5)); dense only */
   GNS_FLAVOR_PERIODIC = 3  /* Periodic Row-wise Muon (ibid. eq. (7)): MUON when step % period
                               == 0, else ROWNORM; dense only */
@@ -131,7 +131,7 @@ typedef enum {
  *   flavor        gns_flavor.
  *   ns_dtype      GNS_BF16 or GNS_F16: storage type of the Newton-Schulz products (W, G, M
  *                 stay bf16; with GNS_F16 the normalised momentum is rounded to fp16 once,
- *                 Dion3 Algorithm 3 line 3).
+ *                 as in Dion3 Algorithm 3).
  *   beta2         NorMuon second-moment decay, in [0, 1).
  *   norm_eps      NorMuon: added to sqrt(v_i) (> 0). RowNorm: lower bound of a row norm
  *                 (> 0).
@@ -171,7 +171,7 @@ GNS_API int gns_last_error(char* buf, size_t len);
 
 /* Fills *p with the default schedule: T = 5, fixed quintic (a, b, c) = (3.4445, -4.7750,
  * 2.0315) every iteration (Scaling Muon for Diffusion Transformers, appendix D.3), restart
- * after iteration 2 (Dion3 Algorithm 3), eps = 1e-7 (Dion3 Algorithm 1 line 2), safety 1. */
+ * after iteration 2 (Dion3 Algorithm 3), eps = 1e-7 (the normalisation of Dion3 Algorithm 1), safety 1. */
 GNS_API void gns_ns_params_default(gns_ns_params* p);
 
 /* Bytes of workspace `op` needs for these batches (the same arguments as the call).
@@ -195,7 +195,7 @@ GNS_API int gns_ns_standard_batched(const gns_batch* x, const gns_batch* out, in
                             const gns_ns_params* ns, void* ws, size_t ws_bytes, int32_t* dev_status,
                             void* stream);
 
-/* Symmetric rank-K product (Dion3 sec. 5, the X X^T of Algorithm 3 line 4):
+/* Symmetric rank-K product (Dion3 sec. 5, the X X^T Gram product of Algorithm 3):
  * C <- alpha X X^T + beta C for every matrix of the batch; x is n x K, c is n x n; both
  * triangles of C are written (upper tiles computed, mirrored), diagonal tiles once.
  * beta != 0 reads C, which must then be symmetric. */
@@ -209,7 +209,7 @@ GNS_API int gns_sym_gemm_xxt(const gns_batch* x, const gns_batch* c, float alpha
 GNS_API int gns_sym_gemm(const gns_batch* a, const gns_batch* b, const gns_batch* c, const gns_batch* d, float alpha,
                  float beta, gns_dtype dtype, int32_t* dev_status, void* stream);
 
-/* One iteration of Dion3 Algorithm 3 (lines 12-15) on n x n batches, in place:
+/* One iteration of the loop of Dion3 Algorithm 3 (its Z, Q, RZ and R updates) on n x n batches, in place:
  *   Z  <- b R + c R^2
  *   Q  <- Q Z + a Q          (q_is_identity != 0: Q <- Z + a I without a product)
  *   RZ <- R Z + a R          (skipped when skip_r != 0)
@@ -238,7 +238,7 @@ GNS_API int gns_muon_step(const gns_batch* W, const gns_batch* G, const gns_batc
                   int ngroups, const gns_muon_params* muon, const gns_ns_params* ns, void* ws,
                   size_t ws_bytes, int32_t* dev_status, void* stream);
 
-/* Selection step of Dion3 Algorithm 4 (line 3) for one bf16 batch m: per matrix, the
+/* Selection step of Dion3 Algorithm 4 for one bf16 batch m: per matrix, the
  * k rows (columns when rows > cols) of largest exact l1 norm, ties to the lower index,
  * written ascending to idx[b*k .. b*k+k-1] (device int32). When gathered != NULL it also
  * receives the selected rows (count x k x cols, or k x rows for a tall matrix, i.e. the

@@ -347,7 +347,7 @@ static int run_gram(gns_dtype dt, const Src& src, int64_t B, int64_t n, int64_t 
   };
   int rc;
   Src X = src;
-  // R_0 = X X^T (scaled by inv^2), Algorithm 3 line 4
+  // R_0 = X X^T (scaled by inv^2), the first Gram product of Algorithm 3
   {
     MatRef xa;
     int mn;
@@ -362,7 +362,7 @@ static int run_gram(gns_dtype dt, const Src& src, int64_t B, int64_t n, int64_t 
   for (int t = 1; t <= T; ++t) {
     const float a = ns->a[t - 1], b = ns->b[t - 1], c = ns->c[t - 1];
     if (t > 1 && ((ns->restart_mask >> (t - 1)) & 1u)) {
-      // restart (lines 7-11): X <- Q X; R <- X X^T; Q <- I
+      // restart: X <- Q X; R <- X X^T; Q <- I
       MatRef xb;
       int bmn;
       as_right(X, &xb, &bmn);
@@ -389,10 +389,10 @@ static int run_gram(gns_dtype dt, const Src& src, int64_t B, int64_t n, int64_t 
       if ((rc = launch(&r, 1))) return rc;
       q_id = true;
     }
-    // line 12: Z = b R + c R^2 (a_t I is never added to Z, appendix B.2.3)
+    // Z = b R + c R^2 (a_t I is never added to Z, appendix B.2.3)
     GemmOp oz = sym_op(g.R, 0, g.R, 1, np, np, B, c, 0, nullptr, &g.R, b, g.Z);
     if (q_id) {
-      // line 13 with Q_{t-1} = I: Q_t = Z_t + a_t I, written by the same launch
+      // the Q update with Q_{t-1} = I: Q_t = Z_t + a_t I, written by the same launch
       oz.D2 = g.Q[qc];
       oz.gamma = a;
       oz.diag_limit = n;
@@ -402,23 +402,23 @@ static int run_gram(gns_dtype dt, const Src& src, int64_t B, int64_t n, int64_t 
     GemmOp ops[2];
     int nops = 0;
     if (!q_id) {
-      // line 13: Q_t = Q_{t-1} Z_t + a_t Q_{t-1}
+      // Q_t = Q_{t-1} Z_t + a_t Q_{t-1}
       ops[nops++] = sym_op(g.Q[qc], 0, g.Z, 1, np, np, B, 1.f, 0, nullptr, &g.Q[qc], a, g.Q[1 - qc]);
     }
     if (r_needed) {
-      // line 14: RZ_t = R_{t-1} Z_t + a_t R_{t-1}
+      // RZ_t = R_{t-1} Z_t + a_t R_{t-1}
       ops[nops++] = sym_op(g.R, 0, g.Z, 1, np, np, B, 1.f, 0, nullptr, &g.R, a, g.RZ);
     }
     if (nops && (rc = launch(ops, nops))) return rc;
     if (!q_id) qc = 1 - qc;
     if (r_needed) {
-      // line 15: R_t = Z_t RZ_t + a_t RZ_t
+      // R_t = Z_t RZ_t + a_t RZ_t
       GemmOp orr = sym_op(g.Z, 0, g.RZ, 1, np, np, B, 1.f, 0, nullptr, &g.RZ, a, g.R);
       if ((rc = launch(&orr, 1))) return rc;
     }
     q_id = false;
   }
-  // line 17: X <- Q_T X, written (or added) to the final destination
+  // X <- Q_T X, written (or added) to the final destination
   {
     MatRef xb;
     int bmn;
@@ -960,7 +960,7 @@ int gns_muon_step(const gns_batch* W, const gns_batch* G, const gns_batch* M, co
       src.mat = mm;
       src.trans = s.trans;
       if (mb.nsdt == GNS_F16) {
-        // Dion3 Algorithm 3 lines 2-3: the normalised momentum, rounded once to float16
+        // Dion3 Algorithm 3, normalise then cast: the normalised momentum, rounded once to float16
         if ((rc = launch_cast_scaled(mb.x16, mm, inv, s.B, stream, &err))) return fail(rc, err);
         src.mat = mb.x16;
         src.user = false;
@@ -1004,19 +1004,19 @@ int gns_muon_step(const gns_batch* W, const gns_batch* G, const gns_batch* M, co
     }
     // Dion3 Algorithm 4
     const int64_t k = mb.k;
-    // line 2: M <- M + G, with the exact l1 keys of the oriented rows
+    // M <- M + G, with the exact l1 keys of the oriented rows
     if ((rc = launch_frac_add_keys(mm, gm, s.B, s.trans, mb.keys, mb.nf, stream, &err))) return fail(rc, err);
-    // line 3: selection
+    // selection
     if ((rc = launch_select_topk(mb.keys, mb.nf, s.n, k, s.B, mb.idx, stream, &err))) return fail(rc, err);
-    // gather M[S, :] and its Frobenius norm; line 10 (error feedback, M[S] <- mu M[S]) rides
+    // gather M[S, :] and its Frobenius norm; the error feedback (M[S] <- mu M[S]) rides
     // on the same pass: M[S] is not read again
     if ((rc = launch_gather(mm, s.B, s.trans, mb.idx, k, mb.xs, mb.gb.partials, stream, &err, true, mu)))
       return fail(rc, err);
     if ((rc = launch_finalize_norm(mb.gb.partials, s.B, ns->eps, mb.gb.inv, stream, &err))) return fail(rc, err);
-    // line 8 on the rows that are not updated below
+    // weight decay on the rows that are not updated below
     if (decay != 1.f && (rc = launch_scale_unselected(wm, s.B, s.trans, mb.idx, k, decay, mb.nf, stream, &err)))
       return fail(rc, err);
-    // line 4: O = polar(M[S])
+    // O = polar(M[S])
     Src src;
     src.mat = mb.xs;
     src.trans = 0;
@@ -1029,13 +1029,13 @@ int gns_muon_step(const gns_batch* W, const gns_batch* G, const gns_batch* M, co
     fin.D = mb.os;
     fin.out_dt = GNS_BF16;
     if ((rc = run_gram(mb.nsdt, src, s.B, k, s.m, ns, mb.gb, mb.gb.inv, fin, dev_status, stream))) return rc;
-    // lines 5-7 (NorMuon flavour): second moments of the selected rows, scaling, rescale
+    // NorMuon flavour: second moments of the selected rows, scaling, rescale
     if (normuon) {
       if ((rc = launch_row_sumsq(mb.os, k, s.m, s.B, mb.s, stream, &err))) return fail(rc, err);
       if ((rc = launch_normuon_rows(mb.s, vm, mb.idx, k, s.m, s.B, mp->beta2, mp->norm_eps, mb.r, stream, &err)))
         return fail(rc, err);
     }
-    // lines 8, 9: W[S] <- (1 - lr wd) W[S] - lr scale O, one rounding
+    // W[S] <- (1 - lr wd) W[S] - lr scale O, one rounding
     if ((rc = launch_scatter_update(wm, mb.os, s.B, s.trans, mb.idx, k, step_scale, decay, stream, &err,
                                     normuon ? mb.r : nullptr)))
       return fail(rc, err);

@@ -7,8 +7,9 @@ Sources (restated, nothing copied):
   * Dion3 sec. 2.1 eq. (2) (NorMuon): M <- mu M + G; O = polar(M);
     v_i <- beta2 v_i + (1 - beta2) mean_j O_ij^2; O_ij <- O_ij / (sqrt(v_i) + eps);
     W <- W - eta (||O||_F / ||O_hat||_F) O_hat, with O the orthogonalized update before the
-    row scaling. Algorithm 4 lines 5-7 apply the same three steps to the selected rows of the
-    fractional update (only v_i, i in S, change), then lines 8-10 as in the Muon flavour.
+    row scaling. Algorithm 4 applies the same three steps to the selected rows of the
+    fractional update (only v_i, i in S, change), then decay, update and error feedback as in
+    the Muon flavour.
   * Scaling Muon for Diffusion Transformers, sec. 3.1 eq. (5) (RowNorm):
     R_eps(X)_i = X_i / max(||X_i||_2, eps) on the oriented momentum (rows = the smaller
     dimension); sec. 3.2 eq. (7) (Periodic Row-wise Muon): rho_t = [t mod K = 0]; the update
@@ -40,18 +41,18 @@ def safety_adjust(coeffs, s):
 
 
 def normuon(O, v, beta2, eps, rows=None):
-    """Eq. (2) / Algorithm 4 lines 5-7 on O (k x m, row i of O is row rows[i] of v).
+    """Eq. (2) / the NorMuon steps of Algorithm 4 on O (k x m, row i of O is row rows[i] of v).
 
     Returns (D, v_new) with D = (||O||_F / ||O_hat||_F) O_hat the update that replaces O.
     """
     O = np.asarray(O, dtype=np.float64)
     v_new = np.array(v, dtype=np.float64, copy=True)
     idx = np.arange(O.shape[0]) if rows is None else np.asarray(rows)
-    ms = np.mean(O * O, axis=1)                                  # line 5
+    ms = np.mean(O * O, axis=1)                                  # second moments
     v_new[idx] = beta2 * v_new[idx] + (1.0 - beta2) * ms
-    O_hat = O / (np.sqrt(v_new[idx]) + eps)[:, None]             # line 6
+    O_hat = O / (np.sqrt(v_new[idx]) + eps)[:, None]             # row scaling
     nh = np.linalg.norm(O_hat)
-    D = O_hat * (np.linalg.norm(O) / nh) if nh > 0 else np.zeros_like(O)   # line 7
+    D = O_hat * (np.linalg.norm(O) / nh) if nh > 0 else np.zeros_like(O)   # Frobenius rescale
     return D, v_new
 
 
@@ -84,23 +85,23 @@ def normuon_step(W_bits, G_bits, M_bits, v, lr, mu, beta2, eps, weight_decay=0.0
 
 def normuon_frac_step(W_bits, G_bits, M_bits, v, frac, lr, mu, beta2, eps, weight_decay=0.0, scale=1.0,
                       coeffs=QUINTIC_FIXED, restarts=(2,), ns_eps=EPS):
-    """Algorithm 4 with the NorMuon steps (lines 5-7) on the selected oriented rows.
+    """Algorithm 4 with the NorMuon steps on the selected oriented rows.
 
     Returns (W_new float64, M_new bf16 bits, v_new, S, D k x m).
     """
     M_bits = np.asarray(M_bits, dtype=np.uint16)
-    Msum = momentum_update_bf16(M_bits, G_bits, 1.0)                 # line 2
+    Msum = momentum_update_bf16(M_bits, G_bits, 1.0)                 # M <- M + G
     Xb, tr = orient(Msum)
     n = Xb.shape[0]
     k = max(1, min(n, int(np.ceil(frac * n - 1e-12))))
-    S = top_k_rows(l1_keys_exact(Xb), k)                             # line 3
-    O = gram_ns_stabilized(bf16_decode(Xb[S, :]), coeffs, restarts=restarts, eps=ns_eps)  # line 4
-    D, v_new = normuon(O, v, beta2, eps, rows=S)                     # lines 5-7
-    W = (1.0 - lr * weight_decay) * bf16_decode(W_bits)              # line 8
+    S = top_k_rows(l1_keys_exact(Xb), k)                             # selection
+    O = gram_ns_stabilized(bf16_decode(Xb[S, :]), coeffs, restarts=restarts, eps=ns_eps)  # O = polar(M[S])
+    D, v_new = normuon(O, v, beta2, eps, rows=S)                     # NorMuon steps
+    W = (1.0 - lr * weight_decay) * bf16_decode(W_bits)              # weight decay
     Wo, _ = orient(W)
     Wo = Wo.copy()
-    Wo[S, :] -= lr * scale * D                                       # line 9
-    Xn = decay_rows_bf16(np.ascontiguousarray(Xb), S, mu)            # line 10
+    Wo[S, :] -= lr * scale * D                                       # update of the selected rows
+    Xn = decay_rows_bf16(np.ascontiguousarray(Xb), S, mu)            # error feedback
     M_new = np.ascontiguousarray(Xn.T) if tr else Xn
     return (Wo.T if tr else Wo), M_new, v_new, S, D
 

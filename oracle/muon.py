@@ -65,7 +65,7 @@ def decay_rows_bf16(M_bits, rows, mu):
 
 
 # ---------------------------------------------------------------------------------------
-# Exact l1 keys and top-k (Algorithm 4 line 3)
+# Exact l1 keys and top-k (the selection step of Algorithm 4)
 
 NONFINITE_KEY = 1 << 400  # above every finite key (a finite bf16 row sum is < 2^290)
 
@@ -139,19 +139,19 @@ def frac_step(W_bits, G_bits, M_bits, frac, lr, mu, weight_decay=0.0, scale=1.0,
     Returns (W_new float64, M_new bf16 bits, S int64 ascending, O float64 k x m).
     """
     M_bits = np.asarray(M_bits, dtype=np.uint16)
-    Msum = momentum_update_bf16(M_bits, G_bits, 1.0)         # line 2: M <- M + G
+    Msum = momentum_update_bf16(M_bits, G_bits, 1.0)         # M <- M + G
     Xb, tr = orient(Msum)
     n = Xb.shape[0]
     k = int(math.ceil(frac * n - 1e-12))
     k = max(1, min(k, n))
-    S = top_k_rows(l1_keys_exact(Xb), k)                     # line 3
-    O = gram_ns_stabilized(bf16_decode(Xb[S, :]), coeffs, restarts=restarts, eps=eps)  # line 4
+    S = top_k_rows(l1_keys_exact(Xb), k)                     # selection
+    O = gram_ns_stabilized(bf16_decode(Xb[S, :]), coeffs, restarts=restarts, eps=eps)  # O = polar(M[S])
     W = bf16_decode(W_bits)
-    W = (1.0 - lr * weight_decay) * W                        # line 8 (all rows)
+    W = (1.0 - lr * weight_decay) * W                        # weight decay (all rows)
     Wo, _ = orient(W)
     Wo = Wo.copy()
-    Wo[S, :] -= lr * scale * O                               # line 9 (selected rows)
+    Wo[S, :] -= lr * scale * O                               # update (selected rows)
     W_new = Wo.T if tr else Wo
-    Xn = decay_rows_bf16(np.ascontiguousarray(Xb), S, mu)    # line 10: error feedback
+    Xn = decay_rows_bf16(np.ascontiguousarray(Xb), S, mu)    # error feedback
     M_new = np.ascontiguousarray(Xn.T) if tr else Xn
     return W_new, M_new, S, O

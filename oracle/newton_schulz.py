@@ -28,7 +28,7 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
-EPS = 1e-7  # Algorithm 1-3 line 2: X <- X / (||X||_F + eps), eps = 1e-7
+EPS = 1e-7  # Algorithms 1-3, normalisation step: X <- X / (||X||_F + eps), eps = 1e-7
 
 # Scaling Muon for Diffusion Transformers, appendix D.3: fixed quintic, five iterations.
 QUINTIC_FIXED = [(3.4445, -4.7750, 2.0315)] * 5
@@ -57,7 +57,7 @@ def _mm(A, B, counter, symmetric, name):
 
 
 def frobenius_normalize(X: np.ndarray, eps: float = EPS) -> np.ndarray:
-    """Algorithm 1-3 line 2: divide by the Frobenius norm plus eps (eps added, not a max)."""
+    """Algorithms 1-3, normalisation step: divide by the Frobenius norm plus eps (eps added, not a max)."""
     return X / (np.linalg.norm(X) + eps)
 
 
@@ -111,7 +111,7 @@ def scalar_recurrence(x, coeffs, restarts=()):
 
 
 def ns_standard(X, coeffs, eps=EPS, counter=None, symmetric_products=True, normalize=True):
-    """Algorithm 1 in float64 (the bfloat16 cast of line 3 is left out: the oracle is exact).
+    """Algorithm 1 in float64 (the bfloat16 cast after the normalisation is left out: the oracle is exact).
 
     Each iteration: A = X X^T; B = b A + c A^2; X = a X + B X. With symmetric_products the
     counter charges A and A^2 as symmetric (sec. 2.3: T(3 alpha + 1) n^3 in total); without,

@@ -53,7 +53,7 @@ def _w_excess(W_gpu, W_or, dW_or):
 
 
 # ---------------------------------------------------------------------------------------
-# fp16 products (Dion3 Algorithm 3 line 3, appendix B.2.2)
+# fp16 products (the float16 cast of Dion3 Algorithm 3, appendix B.2.2)
 
 @pytest.mark.parametrize("count,rows,cols", [(2, 128, 512), (3, 100, 300), (1, 300, 100), (2, 256, 256),
                                              (1, 257, 1000)])
@@ -171,7 +171,7 @@ def test_muon_step_f16_products(count, rows, cols, frac):
 
 
 # ---------------------------------------------------------------------------------------
-# NorMuon (Dion3 eq. (2), Algorithm 4 lines 5-7)
+# NorMuon (Dion3 eq. (2), the NorMuon steps of Algorithm 4)
 
 def _v0(count, n, seed):
     g = np.random.default_rng(seed)

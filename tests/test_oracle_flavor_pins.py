@@ -69,7 +69,7 @@ def test_safety_one_is_identity_and_gram_ns_runs_adjusted_table():
 
 
 # ---------------------------------------------------------------------------------------
-# NorMuon (Dion3 eq. (2), Algorithm 4 lines 5-7)
+# NorMuon (Dion3 eq. (2), the NorMuon steps of Algorithm 4)
 
 def test_normuon_keeps_the_frobenius_norm():
     O = inputs.gaussian(2, (12, 40))
