@@ -34,7 +34,9 @@
  *     batch). All pointers are DEVICE addresses owned by the caller; the library never
  *     allocates or frees device memory. ptr must be 16-byte aligned; ld and stride must be
  *     multiples of 8 elements (16 bytes) for bf16 / fp16 and of 4 elements for fp32; ld >= cols,
- *     stride >= rows * ld (stride is ignored when count == 1).
+ *     stride >= rows * ld (stride is ignored when count == 1). count and min(rows, cols) are
+ *     at most 65535 and max(rows, cols) at most 4194240 (65535 x 64), the kernels' grid
+ *     limits; larger values are argument errors.
  *   Orientation. A matrix with rows > cols is orthogonalized through its transpose and the
  *     result is mapped back (Dion3 Algorithm 1 assumes n <= m); no transposed copy is made.
  *   Streams. Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default stream)

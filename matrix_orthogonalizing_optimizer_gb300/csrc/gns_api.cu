@@ -170,8 +170,12 @@ static int check_batch(const gns_batch* b, gns_dtype dt, const char* name) {
   if (!b->ptr) return fail(GNS_ERR_INVALID, std::string(name) + ": null data pointer");
   if (b->count < 1 || b->rows < 1 || b->cols < 1)
     return fail(GNS_ERR_INVALID, std::string(name) + ": count, rows and cols must be >= 1");
-  if (b->rows > (1 << 30) || b->cols > (1 << 30) || b->count > (1 << 24))
-    return fail(GNS_ERR_INVALID, std::string(name) + ": dimension too large");
+  // launch-grid limits: the matrix index and the smaller dimension run along grid y or z
+  // (at most 65535 blocks), the larger dimension along y in tiles of at least 64
+  if (b->count > 65535 || std::min(b->rows, b->cols) > 65535 || std::max(b->rows, b->cols) > 65535LL * 64)
+    return fail(GNS_ERR_INVALID, std::string(name) +
+                                     ": dimension too large (count and the smaller dimension at most 65535, the "
+                                     "larger at most 4194240)");
   if (b->ld < b->cols) return fail(GNS_ERR_INVALID, std::string(name) + ": ld < cols");
   if (b->ld % al) return fail(GNS_ERR_UNSUPPORTED, std::string(name) + ": ld must be a multiple of 16 bytes");
   if (reinterpret_cast<uintptr_t>(b->ptr) % 16)

@@ -89,6 +89,9 @@ def test_workspace_sizes(lib):
     (dict(ptr=(1 << 20) + 8), b"aligned"),
     (dict(rows=0), b">= 1"),
     (dict(count=2, stride=100 * 64), b"stride"),
+    (dict(count=65536, stride=100 * 128), b"too large"),
+    (dict(rows=65536, cols=65536, ld=65536), b"too large"),
+    (dict(rows=8, cols=65535 * 64 + 8, ld=65535 * 64 + 8), b"too large"),
 ])
 def test_invalid_batches(lib, kw, msg):
     args = dict(count=1, rows=100, cols=128)
@@ -96,6 +99,13 @@ def test_invalid_batches(lib, kw, msg):
     b = _batch(**args)
     assert lib.gns_workspace_size(_lib.GNS_OP_GRAM_NS, b, 1, _lib.GNS_BF16, ctypes.byref(_ns()), None) == 0
     assert msg in _lib.last_error().encode()
+
+
+@pytest.mark.parametrize("kw", [dict(count=65535, stride=100 * 128), dict(rows=8, cols=65535 * 64, ld=65535 * 64)])
+def test_batches_at_the_grid_limits(lib, kw):
+    args = dict(count=1, rows=100, cols=128)
+    args.update(kw)
+    assert lib.gns_workspace_size(_lib.GNS_OP_GRAM_NS, _batch(**args), 1, _lib.GNS_BF16, ctypes.byref(_ns()), None) > 0
 
 
 @pytest.mark.parametrize("kw,msg", [
