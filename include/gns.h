@@ -74,7 +74,7 @@ extern "C" {
 typedef enum {
   GNS_OK = 0,
   GNS_ERR_INVALID = -1,     /* bad argument (shape, alignment, null pointer, T range ...) */
-  GNS_ERR_UNSUPPORTED = -2, /* valid request this build does not implement */
+  GNS_ERR_UNSUPPORTED = -2, /* valid request the library does not implement */
   GNS_ERR_WORKSPACE = -3,   /* ws too small or misaligned */
   GNS_ERR_CUDA = -4         /* a CUDA runtime call failed (launch, tensor-map encode ...) */
 } gns_status;
