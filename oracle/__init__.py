@@ -17,12 +17,14 @@ reordering beyond what the algorithm states:
   and the FLOP accounting of Dion3 sections 2.2, 2.3, 4.1 and 4.2.
 * ``muon``: the Muon step (Dion3 eq. (1)), the Dion3 fractional update (Dion3
   Algorithm 4 and section 6), exact l1 row keys and top-k selection.
-* ``stability``: the spectrum experiments of Dion3 appendix B (eigenvalue tracking,
-  restart-location sweep).
+* ``stability``: the spectrum experiments of Dion3 appendix B (eigenvalue tracking with
+  the diagonalisation error, restart-location sweep).
 
 Parity unpinned: none of the functions above; every one is pinned in
 ``tests/test_oracle_pins.py`` against closed forms, SVD, brute force or the pages'
-printed numbers. What stays unpinned is outside the oracle: training quality
+printed numbers (``stability.spectrum_trace`` against the polynomial composition in the
+singular basis, ``stability.restart_sweep`` against the matrix form of Algorithm 3 with the
+planted eigenvalue). What stays unpinned is outside the oracle: training quality
 (validation perplexity) and the Polar Express coefficient values, which no page prints.
 """
 from . import newton_schulz, muon, stability  # noqa: F401

@@ -7,8 +7,13 @@
   recurrence of Theorem 2. Every eigen-direction has a true x_0 in [0, 1]; whenever a Gram
   matrix is formed its eigenvalue is lowered by delta (4e-4 on the pages) to model the
   spurious negative eigenvalue rounding introduces. For each restart location the sweep
-  records max_t cond(Q_t) (largest |q_t| over smallest |q_t| across directions) and
-  min_t min r_t; the best location minimizes the former.
+  records max_t cond(Q_t) (largest |q_t| over smallest |q_t| across directions),
+  min_t min r_t and max_t max |q_t|.
+
+Pins (tests/test_oracle_pins.py): the traced diagonals equal the composition of the
+printed polynomials in the singular basis with a zero off-diagonal fraction in exact
+arithmetic; the sweep's figures equal those of the matrix Algorithm 3 run with the same
+planted eigenvalue.
 """
 from __future__ import annotations
 
@@ -68,8 +73,3 @@ def restart_sweep(coeffs, delta=4e-4, grid=None):
         res[loc] = (float(cond), float(rs.min()), float(aq.max()))
     return res
 
-
-def best_restart(coeffs, delta=4e-4):
-    sweep = restart_sweep(coeffs, delta)
-    locs = [k for k in sweep if k is not None]
-    return min(locs, key=lambda k: sweep[k][0]), sweep

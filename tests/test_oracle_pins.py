@@ -344,3 +344,58 @@ def test_frac_step_rows_and_error_feedback():
     Wt, Mt, St, Ot = muon.frac_step(W.T.copy(), G.T.copy(), M.T.copy(), 0.25, lr=0.02, mu=0.95)
     assert list(St) == list(S) and rel(Wt, Wn.T) < 1e-12 and np.array_equal(Mt, Mn.T)
     assert math.ceil(0.25 * 4096) == 1024
+
+
+def test_spectrum_trace_follows_the_polynomial_map_in_the_singular_basis():
+    """Appendix B.1.1 eigen-tracking: in exact arithmetic every R_t and Q_t of Gram NS is
+    diagonal in the basis U of X's left singular vectors, with R_t's eigenvalue along u_i
+    equal to phi_t(s_i)^2 and Q_t's equal to phi_t(s_i) / s_i (Theorem 2: q_t x_0 is the
+    composition of the first t polynomials; s_i the normalised singular values). Checked
+    against the composition of the printed polynomials, and the off-diagonal fraction of
+    U^T Q U (B.1.3's diagonalisation error) must be zero up to fp64 rounding; with R_0
+    rounded through bf16 (B.1.2) it must not be."""
+    X = inputs.exp_spectrum(3, 24, 96, decades=2.0)
+    C = ns.QUINTIC_FIXED
+    tr = []
+    ns.gram_ns_naive(X, C, trace=tr)
+    rows = st.spectrum_trace(X, tr)
+    assert [r[0] for r in rows] == list(range(len(C) + 1))
+    s = np.linalg.svd(X, compute_uv=False) / (np.linalg.norm(X) + ns.EPS)   # descending, as U's columns
+    for (t, dr, dq, off) in rows:
+        phi = ns.compose(s, C[:t])
+        if t < len(C):          # R_T is not formed (sec. 4.1): the trace repeats R_{T-1}
+            assert np.max(np.abs(dr - phi ** 2)) < 1e-11 * max(1.0, np.max(phi ** 2)), t
+        assert np.max(np.abs(dq - phi / s)) < 1e-10 * np.max(np.abs(phi / s)), t
+        assert off < 1e-12, (t, off)
+    # a rounded R_0 leaves the basis: the off-diagonal fraction becomes visible
+    trp = []
+    with np.errstate(all="ignore"):
+        ns.gram_ns_naive(X, C, trace=trp, gram_perturb=inputs.bf16_round)
+    offs = [r[3] for r in st.spectrum_trace(X, trp)]
+    assert offs[0] < 1e-12 and max(offs[1:]) > 1e-4   # Q_0 = I
+
+
+@pytest.mark.parametrize("loc", [None, 1, 2, 3, 4])
+def test_restart_sweep_matches_algorithm3_with_a_planted_eigenvalue(loc):
+    """Appendix B.2.1's sweep on the scalar recurrence against the matrix algorithm: with
+    X = U diag(x) V^T and -delta I planted into every Gram matrix Algorithm 3 forms (R_0
+    and the restart's R), the eigenvalues of every Q_t are the scalar q_t of each direction,
+    so the sweep's max_t cond(Q_t) and max_t max|q_t| must equal those of the matrix run."""
+    delta = -GOLD["spurious_eigenvalue"]["value"]
+    x = np.array([1.0, 0.8, 0.5, 0.2, 0.05, 0.01, 1e-3])
+    n, m = len(x), 20
+    g = np.random.default_rng(11)
+    U, _ = np.linalg.qr(g.standard_normal((n, n)))
+    V, _ = np.linalg.qr(g.standard_normal((m, n)))
+    X = (U * x) @ V.T
+    grid = x / (np.linalg.norm(x) + ns.EPS)   # singular values after the normalisation
+    cond_s, _, qmax_s = st.restart_sweep(ns.QUINTIC_FIXED, delta=delta, grid=grid)[loc]
+    tr = []
+    ns.gram_ns_stabilized(X, ns.QUINTIC_FIXED, restarts=() if loc is None else (loc,), trace=tr,
+                          gram_perturb=lambda R: R - delta * np.eye(R.shape[0]))
+    qs = [np.linalg.eigvalsh(0.5 * (Q + Q.T)) for (t, R, Q) in tr if isinstance(t, int) and t >= 1]
+    assert len(qs) == len(ns.QUINTIC_FIXED)
+    cond_m = max(np.abs(q).max() / np.abs(q).min() for q in qs)
+    qmax_m = max(np.abs(q).max() for q in qs)
+    assert cond_s == pytest.approx(cond_m, rel=1e-8)
+    assert qmax_s == pytest.approx(qmax_m, rel=1e-8)
