@@ -49,17 +49,23 @@ def std_flops_per_matrix(n, m, T=5):
     return T * (3 * m / n + 1) * n ** 3
 
 
-# DRAM bytes (read + write) of one launch of the GEMM kernel from an ncu capture
-# (profiles/gemm_kernel_fused_muon_step_24x1024x4096.md), keyed by the kernel source it was
-# taken on: reported only while that source is unchanged.
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the GEMM kernel
+# on this workload, from an ncu capture of `bench.py --metric-only`, keyed by the sha256
+# prefix of the kernel sources it was taken on: reported only while those sources are
+# unchanged (null otherwise), never measured inside this run.
 GEMM_TRAFFIC = {"a08be551760510ae": 2.300315e9}
 
 
-def gemm_traffic():
+def gemm_source_hash():
     import hashlib
-    p = os.path.join(ROOT, "matrix_orthogonalizing_optimizer_gb300", "csrc", "gemm_tc.cu")
-    h = hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
-    return GEMM_TRAFFIC.get(h)
+    h = hashlib.sha256()
+    for f in ("gemm_tc.cu", "common.cuh"):
+        h.update(open(os.path.join(ROOT, "matrix_orthogonalizing_optimizer_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def gemm_traffic():
+    return GEMM_TRAFFIC.get(gemm_source_hash())
 
 
 def load_peaks():
@@ -297,6 +303,16 @@ def run_ours(args, rank, world, dist):
     flops_per_launch = COUNT * alg_flops_per_matrix() / max(per_step, 1)
     achieved = flops_per_launch / (gemm_launch_ms / 1000.0) / 1e12
     peak_burst, peak_sus, _, peak_src = load_peaks()
+    if args.metric_only:
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "value": value, "unit": UNIT, "ms_per_step": ms, "steps": args.steps,
+                              "warmup": args.warmup, "graph_replay": graph,
+                              "gemm_ms_per_step": gemm_ms, "gemm_launches_per_step": per_step,
+                              "gemm_frac_of_burst": achieved / peak_burst, "step_frac_of_burst": tflops / peak_burst,
+                              "gpu_launches": n_all.value, "clocks": clk, "device_status": int(status.item()),
+                              "note": "--metric-only: the metric step alone (for profiling), not a bench line"}),
+                  flush=True)
+        return 0
 
     # ---- end to end: gradient in from pinned host memory, weights back, every step ----
     # The copies of step t overlap compute as a training loop would overlap them: the next
@@ -566,6 +582,30 @@ def run_ours(args, rank, world, dist):
     frac_ms, _ = time_flavor(gns.MuonParams(**base, frac=0.25))
     step_flops = COUNT * alg_flops_per_matrix()
 
+    # Periodic Row-wise Muon, K = 3: the three steps of one period (Newton-Schulz on t = 0,
+    # RowNorm on t = 1, 2), each timed, over several periods
+    def periodic_timing(periods=10):
+        pp = [gns.MuonParams(**base, flavor="periodic", period=3, step=t, rownorm_gamma=0.15, norm_eps=1e-8)
+              for t in range(3)]
+        ws_p = gns.alloc_workspace(max(gns.workspace_size(_lib.GNS_OP_MUON_STEP, M, ns, muon=p) for p in pp), dev)
+        for p in pp:
+            gns.muon_step(W, G, M, ns=ns, workspace=ws_p, status=status, stream=stream, params=p)
+        torch.cuda.synchronize()
+        evp = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(3)]
+               for _ in range(periods)]
+        for per in evp:
+            for t, (a, b) in enumerate(per):
+                a.record(stream)
+                gns.muon_step(W, G, M, ns=ns, workspace=ws_p, status=status, stream=stream, params=pp[t])
+                b.record(stream)
+        torch.cuda.synchronize()
+        per_t = [sum(per[t][0].elapsed_time(per[t][1]) for per in evp) / periods for t in range(3)]
+        return {"ms_per_step_t0_ns": per_t[0], "ms_per_step_t1_rownorm": per_t[1], "ms_per_step_t2_rownorm": per_t[2],
+                "mean_ms_per_step": sum(per_t) / 3.0, "periods_timed": periods,
+                "what": "Periodic Row-wise Muon (K = 3, gamma = 0.15): each step of a period timed with CUDA events"}
+
+    periodic = periodic_timing()
+
     def gemm_roofline(g_ms, what):
         ach = step_flops / (g_ms / 1000.0) / 1e12
         return {"bound": "tensor", "achieved": ach, "peak": peak_burst, "unit": "TFLOP/s", "frac": ach / peak_burst,
@@ -589,7 +629,7 @@ def run_ours(args, rank, world, dist):
                                  "peak": hbm_peak, "unit": "GB/s",
                                  "frac": rn_bytes / (rownorm_ms / 1000.0) / 1e9 / hbm_peak,
                                  "algorithmic_bytes": rn_bytes}},
-        "periodic_K3_mean_ms_per_step": ms / 3.0 + 2.0 * rownorm_ms / 3.0,
+        "periodic_K3": periodic,
         "frac_quarter": {"ms_per_step": frac_ms, "matrices_per_s": COUNT / (frac_ms / 1000.0),
                          "what": "Dion3 fractional update, f = 1/4 (Algorithm 4, Muon flavour)"},
     }
@@ -622,6 +662,9 @@ def run_ours(args, rank, world, dist):
                        "every step"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_burst, "unit": "TFLOP/s",
                      "frac": achieved / peak_burst, "traffic": gemm_traffic() if per_step == 1 else None,
+                     "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch, captured on "
+                                       f"this kernel source ({gemm_source_hash()}) by bench.py --metric-only; "
+                                       "null when no capture of this source is on record",
                      "kernel": f"gns::tc::gemm_kernel (tcgen05 bf16 GEMM; {per_step} launch(es) per step carry the 17 products)",
                      "peak_kind": f"dense bf16 burst, {peak_src}",
                      "frac_of_sustained": achieved / peak_sus,
@@ -652,6 +695,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--metric-only", action="store_true",
+                    help="time the metric step alone and print a short line (for profiling runs)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

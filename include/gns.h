@@ -248,6 +248,19 @@ GNS_API int gns_muon_step(const gns_batch* W, const gns_batch* G, const gns_batc
 GNS_API int gns_frac_row_select(const gns_batch* m, int k, int32_t* idx, const gns_batch* gathered, void* ws,
                         size_t ws_bytes, void* stream);
 
+/* Self-test of the failure detection every kernel of the library relies on (no GPU fault is
+ * involved). Launches one thread that waits, through the same bounded-wait code the GEMM
+ * kernel uses, first until the device int32 *counter reaches target (the cross-CTA completion
+ * counters of a persistent launch) and then on an mbarrier phase that nothing completes (the
+ * operand, accumulator and C rings), each wait giving up after limit_us microseconds
+ * (1 .. 2000000; the library's own waits give up after 2 s). A wait that runs out ORs
+ * GNS_DEVST_TIMEOUT into *dev_status (nullable) and the kernel returns normally, so the
+ * context stays usable. out (nullable, device, two uint64): out[0] = nanoseconds spent in
+ * both waits, out[1] = bit 0 set if the counter wait succeeded, bit 1 if the mbarrier wait
+ * did (it cannot). The caller owns every buffer; argument errors return GNS_ERR_INVALID. */
+GNS_API int gns_selftest_bounded_wait(const int32_t* counter, int32_t target, uint32_t limit_us,
+                                      int32_t* dev_status, uint64_t* out, void* stream);
+
 /* Size of the fixed scratch array behind gns_gram_ns_batched_noalloc (64 MiB). */
 #define GNS_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 
@@ -260,8 +273,11 @@ GNS_API int gns_frac_row_select(const gns_batch* m, int k, int32_t* idx, const g
  * nothing. The pages have no counterpart of this entry point.
  * Returns GNS_ERR_WORKSPACE, with the reason in gns_last_error(), when the batches need more
  * scratch than that (gns_workspace_size(GNS_OP_GRAM_NS, ...) tells how much).
- * The first call on a device looks up the array's device address with that device current;
- * make that first call before any stream capture. All calls share the array: each call
+ * Every call outside stream capture looks up the array's device address with the call's
+ * device current (so the address stays valid after a cudaDeviceReset); a call under capture
+ * uses the address the last uncaptured call on that device found, so make the first call on
+ * a device before any stream capture (a first call under capture returns GNS_ERR_INVALID).
+ * All calls share the array: each call
  * resets the counters that must start at zero and writes every other scratch value before
  * reading it, and calls whose executions overlap on the GPU race on it — serialise them. */
 GNS_API int gns_gram_ns_batched_noalloc(const gns_batch* x, const gns_batch* out, int ngroups, gns_dtype dtype,

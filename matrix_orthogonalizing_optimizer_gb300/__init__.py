@@ -12,6 +12,7 @@ from .api import (  # noqa: F401
     QUINTIC_FIXED,
     alloc_workspace,
     batch_of,
+    check_status,
     empty_padded,
     frac_k,
     frac_row_select,
@@ -23,8 +24,10 @@ from .api import (  # noqa: F401
     sym_poly_update,
     workspace_size,
 )
+from ._lib import GnsDeviceError, GnsError  # noqa: F401
 
 __all__ = [
-    "MuonParams", "NsParams", "QUINTIC_FIXED", "alloc_workspace", "batch_of", "empty_padded", "frac_k", "frac_row_select", "gram_ns_batched",
+    "MuonParams", "NsParams", "QUINTIC_FIXED", "alloc_workspace", "batch_of", "check_status", "empty_padded", "frac_k", "frac_row_select", "gram_ns_batched",
     "muon_step", "ns_standard_batched", "sym_gemm", "sym_gemm_xxt", "sym_poly_update", "workspace_size",
+    "GnsDeviceError", "GnsError",
 ]

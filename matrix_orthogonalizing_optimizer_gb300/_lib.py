@@ -33,6 +33,7 @@ EXPORTS = [
     "gns_version", "gns_status_string", "gns_last_error", "gns_ns_params_default", "gns_workspace_size",
     "gns_gram_ns_batched", "gns_ns_standard_batched", "gns_sym_gemm_xxt", "gns_sym_gemm",
     "gns_sym_poly_update", "gns_muon_step", "gns_frac_row_select", "gns_profile_set", "gns_profile_query", "gns_gram_ns_batched_noalloc",
+    "gns_selftest_bounded_wait",
 ]
 
 
@@ -59,6 +60,17 @@ _lib = None
 
 class GnsError(RuntimeError):
     pass
+
+
+class GnsDeviceError(GnsError):
+    """A condition the GPU detected during a call (bits of the device status word)."""
+
+    def __init__(self, what: str, bits: int):
+        names = [n for b, n in ((GNS_DEVST_NONFINITE, "non-finite output"),
+                                (GNS_DEVST_TIMEOUT, "a bounded wait timed out (results are incomplete)"))
+                 if bits & b]
+        super().__init__(f"{what}: device status {bits}: {', '.join(names) or 'unknown bits'}")
+        self.bits = bits
 
 
 def load(path: str = LIB_PATH) -> ctypes.CDLL:
@@ -98,6 +110,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.gns_frac_row_select.argtypes = [B, i32, vp, B, vp, sz, vp]
     lib.gns_gram_ns_batched_noalloc.restype = i32
     lib.gns_gram_ns_batched_noalloc.argtypes = [B, B, i32, i32, P(GnsNsParams), vp, vp]
+    lib.gns_selftest_bounded_wait.restype = i32
+    lib.gns_selftest_bounded_wait.argtypes = [vp, i32, ctypes.c_uint32, vp, vp, vp]
     lib.gns_profile_set.restype = i32
     lib.gns_profile_set.argtypes = [P(vp), i32]
     lib.gns_profile_query.restype = i32

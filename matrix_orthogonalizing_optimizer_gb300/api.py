@@ -16,7 +16,8 @@ from typing import Iterable, List, Optional, Sequence
 import torch
 
 from . import _lib
-from ._lib import GnsBatch, GnsMuonParams, GnsNsParams, check, load
+from ._lib import GnsBatch, GnsMuonParams, GnsNsParams, load
+from ._lib import check as check_rc
 
 # Fixed quintic of "Scaling Muon for Diffusion Transformers", appendix D.3.
 QUINTIC_FIXED = ((3.4445, -4.7750, 2.0315),) * 5
@@ -164,7 +165,84 @@ def _status_ptr(status: Optional[torch.Tensor]) -> Optional[int]:
     return status.data_ptr()
 
 
-def _ns_common(fn_name: str, op: int, xs, outs, ns, workspace, status, stream):
+# Device status words (include/gns.h: bit 0 non-finite output, bit 1 a bounded wait timed
+# out) owned by this module, one per device, for calls made without `status=`. The kernels OR
+# into them; a word is only cleared when its bits are reported, so nothing the GPU detects is
+# lost: a call that cannot check (check=False, or stream capture) leaves its bits for the next
+# checked call on the device, or for check_status().
+_OWNED_STATUS = {}
+
+
+def _device_index(device) -> int:
+    d = torch.device(device) if device is not None else torch.device("cuda")
+    return d.index if d.index is not None else torch.cuda.current_device()
+
+
+def _capturing(stream: Optional[torch.cuda.Stream]) -> bool:
+    if torch.cuda.is_current_stream_capturing():
+        return True
+    if stream is not None:
+        with torch.cuda.stream(stream):
+            return torch.cuda.is_current_stream_capturing()
+    return False
+
+
+def _owned_status(device) -> torch.Tensor:
+    idx = _device_index(device)
+    t = _OWNED_STATUS.get(idx)
+    if t is None:
+        if torch.cuda.is_current_stream_capturing():
+            raise ValueError("the first call on a device must run outside stream capture (or pass status=)")
+        t = torch.zeros(1, dtype=torch.int32, device=torch.device("cuda", idx))
+        _OWNED_STATUS[idx] = t
+    return t
+
+
+def _report(what: str, st: torch.Tensor) -> None:
+    v = int(st.cpu()[0])
+    if v:
+        st.zero_()
+        raise _lib.GnsDeviceError(what, v)
+
+
+class _CallStatus:
+    """The status word one call passes to the library: the caller's own (`status=`, read by
+    the caller, or by check_status(status)), else this module's word of the device, which is
+    checked after the call when `check` is set by synchronising the call's stream."""
+
+    def __init__(self, status: Optional[torch.Tensor], device, check: bool, stream):
+        self.owned = status is None
+        self.word = _owned_status(device) if self.owned else status
+        self.check = check
+        self.stream = stream
+        self.device = device
+
+    def ptr(self) -> int:
+        return _status_ptr(self.word)
+
+    def done(self, what: str) -> None:
+        if not self.owned or not self.check or _capturing(self.stream):
+            return
+        s = self.stream if self.stream is not None else torch.cuda.current_stream(self.device)
+        s.synchronize()
+        _report(what, self.word)
+
+
+def check_status(status: Optional[torch.Tensor] = None, device=None, what: str = "libgns") -> None:
+    """Synchronises the device and raises GnsDeviceError when the status word has bits set
+    (then clears it): the caller's `status` tensor, or, when None, this module's word for the
+    device, which collects the bits of every call made without `status=` (including calls
+    recorded into CUDA graphs and replayed)."""
+    if status is None:
+        idx = _device_index(device)
+        if idx not in _OWNED_STATUS:
+            return
+        status = _OWNED_STATUS[idx]
+    torch.cuda.synchronize(status.device)
+    _report(what, status)
+
+
+def _ns_common(fn_name: str, op: int, xs, outs, ns, workspace, status, stream, check_dev):
     xs = _as_list(xs)
     outs = [empty_padded(x.shape, x.dtype, x.device) for x in xs] if outs is None else _as_list(outs)
     ns = ns or NsParams()
@@ -174,55 +252,74 @@ def _ns_common(fn_name: str, op: int, xs, outs, ns, workspace, status, stream):
     oa, _ = _batches(outs)
     nsp = ns.c_struct()
     fn = getattr(load(), fn_name)
+    cs = _CallStatus(status, xs[0].device, check_dev, stream)
     rc = fn(xa, oa, len(xs), _dtype_code(xs[0]), ctypes.byref(nsp), ws.data_ptr(), ws.numel(),
-            _status_ptr(status), _stream_ptr(stream, xs[0].device))
-    check(rc, fn_name)
+            cs.ptr(), _stream_ptr(stream, xs[0].device))
+    check_rc(rc, fn_name)
+    cs.done(fn_name)
     return outs
 
 
-def gram_ns_batched(xs, outs=None, ns: Optional[NsParams] = None, workspace=None, status=None, stream=None):
+# Device status of every call below: with `status=` (a CUDA int32 tensor) the library ORs its
+# bits into that tensor and the call returns without synchronising (read it, or pass it to
+# check_status(), after the stream is done). Without it the call uses this module's status
+# word of the device and, when `check` is set (the default), synchronises the call's stream
+# and raises GnsDeviceError if the GPU flagged a non-finite output or a timed-out wait.
+
+
+def gram_ns_batched(xs, outs=None, ns: Optional[NsParams] = None, workspace=None, status=None, stream=None,
+                    check: bool = True):
     """Gram Newton-Schulz (Dion3 Algorithm 3) of every matrix in xs (tensor or list of
     tensors, one per shape group); returns the list of outputs."""
-    return _ns_common("gns_gram_ns_batched", _lib.GNS_OP_GRAM_NS, xs, outs, ns, workspace, status, stream)
+    return _ns_common("gns_gram_ns_batched", _lib.GNS_OP_GRAM_NS, xs, outs, ns, workspace, status, stream, check)
 
 
-def ns_standard_batched(xs, outs=None, ns: Optional[NsParams] = None, workspace=None, status=None, stream=None):
+def ns_standard_batched(xs, outs=None, ns: Optional[NsParams] = None, workspace=None, status=None, stream=None,
+                        check: bool = True):
     """Standard Newton-Schulz (Dion3 Algorithm 1 with symmetric products)."""
-    return _ns_common("gns_ns_standard_batched", _lib.GNS_OP_NS_STANDARD, xs, outs, ns, workspace, status, stream)
+    return _ns_common("gns_ns_standard_batched", _lib.GNS_OP_NS_STANDARD, xs, outs, ns, workspace, status, stream,
+                      check)
 
 
-def sym_gemm_xxt(x: torch.Tensor, c: torch.Tensor, alpha: float = 1.0, beta: float = 0.0, status=None, stream=None):
+def sym_gemm_xxt(x: torch.Tensor, c: torch.Tensor, alpha: float = 1.0, beta: float = 0.0, status=None, stream=None,
+                 check: bool = True):
     xb, cb = batch_of(x), batch_of(c)
+    cs = _CallStatus(status, x.device, check, stream)
     rc = load().gns_sym_gemm_xxt(ctypes.byref(xb), ctypes.byref(cb), float(alpha), float(beta), _dtype_code(x),
-                                 _status_ptr(status), _stream_ptr(stream, x.device))
-    check(rc, "gns_sym_gemm_xxt")
+                                 cs.ptr(), _stream_ptr(stream, x.device))
+    check_rc(rc, "gns_sym_gemm_xxt")
+    cs.done("gns_sym_gemm_xxt")
     return c
 
 
 def sym_gemm(a: torch.Tensor, b: torch.Tensor, c: Optional[torch.Tensor], d: torch.Tensor, alpha: float = 1.0,
-             beta: float = 0.0, status=None, stream=None):
+             beta: float = 0.0, status=None, stream=None, check: bool = True):
     ab, bb, db = batch_of(a), batch_of(b), batch_of(d)
     cb = batch_of(c) if c is not None else None
+    cs = _CallStatus(status, a.device, check, stream)
     rc = load().gns_sym_gemm(ctypes.byref(ab), ctypes.byref(bb), ctypes.byref(cb) if cb is not None else None,
-                             ctypes.byref(db), float(alpha), float(beta), _dtype_code(a), _status_ptr(status),
+                             ctypes.byref(db), float(alpha), float(beta), _dtype_code(a), cs.ptr(),
                              _stream_ptr(stream, a.device))
-    check(rc, "gns_sym_gemm")
+    check_rc(rc, "gns_sym_gemm")
+    cs.done("gns_sym_gemm")
     return d
 
 
 def sym_poly_update(R, Q, Z, RZ, q_scratch, a: float, b: float, c: float, q_is_identity: bool, skip_r: bool,
-                    status=None, stream=None):
+                    status=None, stream=None, check: bool = True):
     bs = [batch_of(t) for t in (R, Q, Z, RZ)]
     qs = batch_of(q_scratch) if q_scratch is not None else None
+    cs = _CallStatus(status, R.device, check, stream)
     rc = load().gns_sym_poly_update(*[ctypes.byref(x) for x in bs], ctypes.byref(qs) if qs is not None else None,
                                     float(a), float(b), float(c), int(bool(q_is_identity)), int(bool(skip_r)),
-                                    _dtype_code(R), _status_ptr(status), _stream_ptr(stream, R.device))
-    check(rc, "gns_sym_poly_update")
+                                    _dtype_code(R), cs.ptr(), _stream_ptr(stream, R.device))
+    check_rc(rc, "gns_sym_poly_update")
+    cs.done("gns_sym_poly_update")
 
 
 def muon_step(W, G, M, lr: Optional[float] = None, momentum: float = 0.95, weight_decay: float = 0.0, scale: float = 1.0,
               frac: float = 1.0, ns: Optional[NsParams] = None, workspace=None, status=None, stream=None,
-              V=None, params: Optional[MuonParams] = None):
+              V=None, params: Optional[MuonParams] = None, check: bool = True):
     """One optimizer step in place on W and M (and V): Muon (frac = 1), the Dion3 fractional
     update (frac < 1), or the flavour named in `params` (which then supplies every
     hyper-parameter). V: NorMuon second moments, fp32 tensors (count, 1, min(rows, cols)) or
@@ -243,9 +340,11 @@ def muon_step(W, G, M, lr: Optional[float] = None, momentum: float = 0.95, weigh
         va, _ = _batches(_as_list(V))
     nsp = ns.c_struct()
     mp = params.c_struct()
+    cs = _CallStatus(status, Ms[0].device, check, stream)
     rc = load().gns_muon_step(wa, ga, ma, va, len(Ms), ctypes.byref(mp), ctypes.byref(nsp), ws.data_ptr(),
-                              ws.numel(), _status_ptr(status), _stream_ptr(stream, Ms[0].device))
-    check(rc, "gns_muon_step")
+                              ws.numel(), cs.ptr(), _stream_ptr(stream, Ms[0].device))
+    check_rc(rc, "gns_muon_step")
+    cs.done("gns_muon_step")
 
 
 def frac_row_select(m: torch.Tensor, k: int, idx: Optional[torch.Tensor] = None, gathered=None, workspace=None,
@@ -263,7 +362,7 @@ def frac_row_select(m: torch.Tensor, k: int, idx: Optional[torch.Tensor] = None,
     rc = load().gns_frac_row_select(ctypes.byref(mb), int(k), idx.data_ptr(),
                                     ctypes.byref(gb) if gb is not None else None, ws.data_ptr(), ws.numel(),
                                     _stream_ptr(stream, m.device))
-    check(rc, "gns_frac_row_select")
+    check_rc(rc, "gns_frac_row_select")
     return idx
 
 

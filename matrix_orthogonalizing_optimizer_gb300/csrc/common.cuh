@@ -66,9 +66,10 @@ GNS_DEV bool mbar_try_wait(uint32_t bar_addr, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait until the phase with the given parity has completed. Returns false on timeout or
-// when another role of the CTA has already aborted.
-GNS_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* status) {
+// Wait until the phase with the given parity has completed. Returns false on timeout (after
+// limit_ns of waiting) or when another role of the CTA has already aborted.
+GNS_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* status,
+                       uint64_t limit_ns = GNS_WAIT_TIMEOUT_NS) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = global_timer_ns();
@@ -76,7 +77,7 @@ GNS_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
     if (mbar_try_wait(a, parity)) return true;
     if ((i & 63u) == 0u) {
       if (*abort_flag) return false;
-      if (global_timer_ns() - t0 > GNS_WAIT_TIMEOUT_NS) {
+      if (global_timer_ns() - t0 > limit_ns) {
         *abort_flag = 1;
         set_status(status, GNS_DEVST_TIMEOUT);
         return false;
@@ -266,8 +267,10 @@ GNS_DEV void red_release_gpu_add(int* p, int v) {
 }
 GNS_DEV void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
-// Spin (bounded) until *ctr >= target; then order later async-proxy (TMA) reads after it.
-GNS_DEV bool wait_counter(const int* ctr, int target, volatile int* abort_flag, int* status) {
+// Spin (bounded by limit_ns) until *ctr >= target; then order later async-proxy (TMA) reads
+// after it.
+GNS_DEV bool wait_counter(const int* ctr, int target, volatile int* abort_flag, int* status,
+                          uint64_t limit_ns = GNS_WAIT_TIMEOUT_NS) {
   if (ld_acquire_gpu(ctr) < target) {
     const uint64_t t0 = global_timer_ns();
     for (uint32_t i = 1;; ++i) {
@@ -275,7 +278,7 @@ GNS_DEV bool wait_counter(const int* ctr, int target, volatile int* abort_flag, 
       __nanosleep(64);
       if ((i & 15u) == 0u) {
         if (*abort_flag) return false;
-        if (global_timer_ns() - t0 > GNS_WAIT_TIMEOUT_NS) {
+        if (global_timer_ns() - t0 > limit_ns) {
           *abort_flag = 1;
           set_status(status, GNS_DEVST_TIMEOUT);
           return false;

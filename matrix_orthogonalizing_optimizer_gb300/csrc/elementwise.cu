@@ -1121,6 +1121,32 @@ static unsigned grid_1d(long long work, int threads) {
   return (unsigned)g;
 }
 
+// ---------------------------------------------------------------------------------------
+// failure detection without a fault: the bounded waits, made to run out
+
+// One thread waits, through the same bounded-wait helpers the GEMM kernel uses for its
+// cross-CTA completion counters and its mbarrier phases, first on *counter >= target and
+// then on the first phase of an mbarrier that nothing arrives on, each for at most limit_ns.
+// out[0] = nanoseconds spent in both waits, out[1] = bit 0 if the counter wait succeeded,
+// bit 1 if the mbarrier wait did (it cannot). A wait that runs out sets GNS_DEVST_TIMEOUT.
+__global__ void selftest_wait_kernel(const int* counter, int target, unsigned long long limit_ns, int* status,
+                                     unsigned long long* out) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  abort_flag = 0;
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  const uint64_t t0 = global_timer_ns();
+  const bool c_ok = wait_counter(counter, target, &abort_flag, status, limit_ns);
+  abort_flag = 0;  // the mbarrier wait then runs its own limit
+  const bool m_ok = mbar_wait(&bar, 0u, &abort_flag, status, limit_ns);
+  if (out) {
+    out[0] = global_timer_ns() - t0;
+    out[1] = (c_ok ? 1ull : 0ull) | (m_ok ? 2ull : 0ull);
+  }
+}
+
 int launch_sumsq(gns_dtype dt, const MatRef& X, int64_t count, float* partials, void* stream, std::string* err) {
   dim3 grid(NPART, (unsigned)count);
   if (dt == GNS_BF16)
@@ -1380,6 +1406,12 @@ int launch_copy(gns_dtype dt, const MatRef& D, const MatRef& Sr, int64_t count, 
                                                    static_cast<const float*>(Sr.ptr), Sr.ld, Sr.stride, (int)D.rows,
                                                    (int)D.cols);
   return check_launch("copy", err);
+}
+
+int launch_selftest_wait(const int* counter, int target, uint64_t limit_ns, int* status, unsigned long long* out,
+                         void* stream, std::string* err) {
+  selftest_wait_kernel<<<1, 32, 0, S(stream)>>>(counter, target, (unsigned long long)limit_ns, status, out);
+  return check_launch("selftest_wait", err);
 }
 
 }  // namespace gns

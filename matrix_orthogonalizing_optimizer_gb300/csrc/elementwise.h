@@ -59,5 +59,9 @@ int launch_rowscale_update(const MatRef& W, const MatRef& Y, const float* r, int
 int launch_cast_scaled(const MatRef& X16, const MatRef& M, const float* inv, int64_t count, void* stream,
                        std::string* err);
 int launch_copy(gns_dtype dt, const MatRef& D, const MatRef& S, int64_t count, void* stream, std::string* err);
+// One block whose bounded waits (a completion counter, then an mbarrier phase nothing
+// completes) run out after limit_ns each (gns_selftest_bounded_wait).
+int launch_selftest_wait(const int* counter, int target, uint64_t limit_ns, int* status, unsigned long long* out,
+                         void* stream, std::string* err);
 
 }  // namespace gns

@@ -744,11 +744,28 @@ static int plan_op(gns_op op, const gns_batch* x, int ngroups, gns_dtype dt, con
   return GNS_OK;
 }
 
+}  // extern "C"
+
+namespace gns {
+// Workspace bytes of a request in *need, returning the planner's status (and setting the last
+// error) when the request is invalid or unsupported.
+int plan_workspace(gns_op op, const gns_batch* x, int ngroups, gns_dtype dtype, const gns_ns_params* ns,
+                   const gns_muon_params* muon, size_t* need) {
+  Arena a;
+  *need = 0;
+  const int rc = plan_op(op, x, ngroups, dtype, ns, muon, a);
+  if (rc) return rc;
+  *need = a.off + 256;
+  return GNS_OK;
+}
+}  // namespace gns
+
+extern "C" {
+
 size_t gns_workspace_size(gns_op op, const gns_batch* x, int ngroups, gns_dtype dtype, const gns_ns_params* ns,
                           const gns_muon_params* muon) {
-  Arena a;
-  if (plan_op(op, x, ngroups, dtype, ns, muon, a)) return 0;
-  return a.off + 256;
+  size_t need = 0;
+  return plan_workspace(op, x, ngroups, dtype, ns, muon, &need) ? 0 : need;
 }
 
 static int check_ws(void* ws, size_t ws_bytes, size_t need) {
@@ -763,9 +780,10 @@ static int ns_common(bool gram, const gns_batch* x, const gns_batch* out, int ng
                      const gns_ns_params* ns, void* ws, size_t ws_bytes, int32_t* st, void* stream) {
   if (!out) return fail(GNS_ERR_INVALID, "null out");
   const gns_op op = gram ? GNS_OP_GRAM_NS : GNS_OP_NS_STANDARD;
-  size_t need = gns_workspace_size(op, x, ngroups, dt, ns, nullptr);
-  if (!need) return GNS_ERR_INVALID;
-  int rc = check_ws(ws, ws_bytes, need);
+  size_t need = 0;
+  int rc = plan_workspace(op, x, ngroups, dt, ns, nullptr, &need);
+  if (rc) return rc;
+  rc = check_ws(ws, ws_bytes, need);
   if (rc) return rc;
   for (int gi = 0; gi < ngroups; ++gi) {
     if ((rc = check_batch(&out[gi], dt, "out"))) return rc;
@@ -915,8 +933,8 @@ int gns_muon_step(const gns_batch* W, const gns_batch* G, const gns_batch* M, co
         return fail(GNS_ERR_INVALID, "V may not alias W, G or M");
     }
   }
-  size_t need = gns_workspace_size(GNS_OP_MUON_STEP, M, ngroups, GNS_BF16, ns, mp);
-  if (!need) return GNS_ERR_INVALID;
+  size_t need = 0;
+  if ((rc = plan_workspace(GNS_OP_MUON_STEP, M, ngroups, GNS_BF16, ns, mp, &need))) return rc;
   if ((rc = check_ws(ws, ws_bytes, need))) return rc;
   const gns_ns_params nse = effective_ns(*ns);
   ns = &nse;
@@ -1045,6 +1063,17 @@ int gns_muon_step(const gns_batch* W, const gns_batch* G, const gns_batch* M, co
       return fail(rc, err);
   }
   return GNS_OK;
+}
+
+int gns_selftest_bounded_wait(const int32_t* counter, int32_t target, uint32_t limit_us, int32_t* dev_status,
+                              uint64_t* out, void* stream) {
+  if (!counter || reinterpret_cast<uintptr_t>(counter) % 4) return fail(GNS_ERR_INVALID, "counter: null or unaligned");
+  if (out && reinterpret_cast<uintptr_t>(out) % 8) return fail(GNS_ERR_INVALID, "out: unaligned");
+  if (limit_us < 1 || limit_us > 2000000u) return fail(GNS_ERR_INVALID, "limit_us must be in [1, 2000000]");
+  std::string err;
+  int rc = launch_selftest_wait(counter, target, (uint64_t)limit_us * 1000ull, dev_status,
+                                reinterpret_cast<unsigned long long*>(out), stream, &err);
+  return rc ? fail(rc, err) : GNS_OK;
 }
 
 int gns_frac_row_select(const gns_batch* m, int k, int32_t* idx, const gns_batch* gathered, void* ws,

@@ -10,9 +10,13 @@
 //
 // The array lives in device global memory: every GPU on which the library's code is loaded
 // reserves GNS_NOALLOC_SCRATCH_BYTES for it until the process exits. In host code its name
-// is only a stand-in, not a device address, so its address is looked up once per device
-// (cudaGetSymbolAddress, with that device current) on the first call made on that device;
-// make that first call before any stream capture. All calls share the array and it keeps
+// is only a stand-in, not a device address, so every call outside stream capture looks its
+// address up (cudaGetSymbolAddress, with the call's device current) and remembers it per
+// device; a call recorded by stream capture, which may not make that query, uses the
+// remembered address, so the first call on a device must come before any capture (a first
+// call under capture is refused with a message saying so). Looking the address up again on
+// every uncaptured call keeps it valid after a cudaDeviceReset, which unloads the module and
+// may place the array elsewhere when it is loaded again. All calls share the array and it keeps
 // whatever the last call left there: the completion counters that must start at zero are
 // reset by every call (a memset on the stream), and every other scratch value is written
 // before it is read. Calls whose executions overlap on the GPU (different streams, or
@@ -38,14 +42,17 @@ void* g_scratch_ptr[kMaxDevices] = {nullptr};
 
 namespace gns {
 int set_error(int code, const std::string& msg);  // sets gns_last_error(); defined with the C ABI
+int plan_workspace(gns_op op, const gns_batch* x, int ngroups, gns_dtype dtype, const gns_ns_params* ns,
+                   const gns_muon_params* muon, size_t* need);
 }
 
 extern "C" {
 
 GNS_API int gns_gram_ns_batched_noalloc(const gns_batch* x, const gns_batch* out, int ngroups, gns_dtype dtype,
                                         const gns_ns_params* ns, int32_t* dev_status, void* stream) {
-  const size_t need = gns_workspace_size(GNS_OP_GRAM_NS, x, ngroups, dtype, ns, nullptr);
-  if (need == 0) return GNS_ERR_INVALID;  // argument error, message already set
+  size_t need = 0;
+  const int prc = gns::plan_workspace(GNS_OP_GRAM_NS, x, ngroups, dtype, ns, nullptr, &need);
+  if (prc) return prc;  // invalid or unsupported request, message already set
   if (need > kScratchBytes)
     return gns::set_error(GNS_ERR_WORKSPACE,
                           "gns_gram_ns_batched_noalloc: these batches need " + std::to_string(need) +
@@ -55,10 +62,13 @@ GNS_API int gns_gram_ns_batched_noalloc(const gns_batch* x, const gns_batch* out
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
     return gns::set_error(GNS_ERR_CUDA, "gns_gram_ns_batched_noalloc: no usable current device");
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &cap) != cudaSuccess)
+    return gns::set_error(GNS_ERR_CUDA, "gns_gram_ns_batched_noalloc: cudaStreamIsCapturing failed on the stream");
   void* scratch = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_mutex);
-    if (!g_scratch_ptr[dev]) {
+    if (cap == cudaStreamCaptureStatusNone) {
       void* p = nullptr;
       const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
       if (e != cudaSuccess || !p)
@@ -66,6 +76,10 @@ GNS_API int gns_gram_ns_batched_noalloc(const gns_batch* x, const gns_batch* out
                                                         "the scratch array failed: ") +
                                                 cudaGetErrorString(e));
       g_scratch_ptr[dev] = p;
+    } else if (!g_scratch_ptr[dev]) {
+      return gns::set_error(GNS_ERR_INVALID,
+                            "gns_gram_ns_batched_noalloc: the first call on a device must run outside stream "
+                            "capture (it looks up the scratch array's device address, which a capture cannot)");
     }
     scratch = g_scratch_ptr[dev];
   }

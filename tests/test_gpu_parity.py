@@ -256,6 +256,11 @@ def test_degenerate_inputs():
     gns.gram_ns_batched(bad, status=st)
     torch.cuda.synchronize()
     assert int(st.item()) & 1
+    # ... and, without a status word of the caller's, raised by the API after the call
+    with pytest.raises(gns.GnsDeviceError, match="non-finite"):
+        gns.gram_ns_batched(bad)
+    gns.check_status()   # the API's word was cleared when it was reported
+    gns.gram_ns_batched(bits_to_torch(bits))
 
 
 def test_argument_errors():
@@ -380,8 +385,10 @@ def test_frac_step_special_values(cols):
     Mb[2, 3, 10] = 0x7F80                                      # +Inf: the row's key is maximal
     Mb[2, 12, cols - 1] = 0xFF80                               # -Inf in a tail column
     Wt, Gt, Mt = bits_to_torch(Wb), bits_to_torch(Gb), bits_to_torch(Mb)
-    gns.muon_step(Wt, Gt, Mt, lr=0.02, momentum=mu, frac=frac)
+    st = _status()
+    gns.muon_step(Wt, Gt, Mt, lr=0.02, momentum=mu, frac=frac, status=st)
     torch.cuda.synchronize()
+    assert int(st.item()) == 1   # the Inf rows are selected: their update is flagged non-finite
     Mg = torch_to_bits(Mt)
     k = int(np.ceil(frac * rows))
     for b in range(count):
@@ -411,8 +418,10 @@ def test_frac_step_special_values_tall(rows, cols):
     Mb[2, 10, 3] = 0x7F80
     Mb[2, rows - 1, 12] = 0xFF80
     Wt, Gt, Mt = bits_to_torch(Wb), bits_to_torch(Gb), bits_to_torch(Mb)
-    gns.muon_step(Wt, Gt, Mt, lr=0.02, momentum=mu, frac=frac)
+    st = _status()
+    gns.muon_step(Wt, Gt, Mt, lr=0.02, momentum=mu, frac=frac, status=st)
     torch.cuda.synchronize()
+    assert int(st.item()) == 1
     Mg = torch_to_bits(Mt)
     k = int(np.ceil(frac * cols))
     for b in range(count):
