@@ -28,7 +28,10 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstdio>
+#include <cstdlib>
 #include <mutex>
+#include <vector>
 
 #include "common.cuh"
 #include "gemm.h"
@@ -96,7 +99,7 @@ struct Problem {
   int a_mn, b_mn;
   int kblocks;
   int tiles_m, tiles_n, sym;
-  int tile_begin, tiles_per_mat;
+  int tiles_per_mat;
   float alpha, beta, gamma;
   int alpha_pow, beta_pow;
   const float* scale;
@@ -110,12 +113,21 @@ struct Problem {
   int ctr_off;        // this problem's completion counters: counters[ctr_off + b]
 };
 
+// The launch's tiles form a sequence of segments, each the tiles of problem p for the
+// matrices b0 .. b0 + nb - 1 (matrix-major, then tile): seg_pb = p << 24 | b0, seg_tile =
+// index of its first tile (nb follows from the next segment's start). The host orders the
+// segments so that every tile depends only on tiles earlier in the sequence.
+constexpr int MAX_SEG = 640;
+
 struct Params {
   Problem prob[MAX_PROB];
   int nprob;
   int total_tiles;
+  int nseg;
   int* status;
   int* counters;  // per (problem, matrix): CTA-halves of tiles completed (zero at launch)
+  uint32_t seg_pb[MAX_SEG];
+  int seg_tile[MAX_SEG];
 };
 
 // Bounded wait until every problem this tile depends on has finished matrix b.
@@ -152,10 +164,6 @@ __device__ __forceinline__ bool wait_ready(volatile int* ready, int tile, volati
   return true;
 }
 
-struct TileCoord {
-  int p, b, I, J;
-};
-
 // Major-ness of the A (B) slice of 64-wide K block kb for tile row I (column J). An operand
 // that is the upper triangle of a symmetric matrix (256-blocks at or above the diagonal) is
 // read from the mirrored block, with the other major-ness, wherever the block it would read
@@ -187,17 +195,25 @@ __device__ __forceinline__ int b_major(const KLoop& pr, int J, int kb) {
   return pr.b_mn ^ ((pr.b_upper && lower) ? 1 : 0);
 }
 
-// p0: a problem index at or below the tile's (every role walks its tiles in increasing
-// order, so the previous tile's problem is a valid start).
-__device__ __forceinline__ TileCoord decode_tile(const Params& P, int tile, int p0 = 0) {
+struct TileCoord {
+  int p, b, I, J;
+};
+
+// s0: a segment index at or below the tile's (every role walks its tiles in increasing
+// order, so the previous tile's segment is a valid start); *seg receives the tile's.
+__device__ __forceinline__ TileCoord decode_tile(const Params& P, int tile, int* seg) {
   TileCoord tc;
-  int p = p0;
-  while (p + 1 < P.nprob && tile >= P.prob[p + 1].tile_begin) ++p;
+  int s = *seg;
+  while (s + 1 < P.nseg && tile >= P.seg_tile[s + 1]) ++s;
+  *seg = s;
+  const uint32_t pb = P.seg_pb[s];
+  const int p = (int)(pb >> 24);
   const Problem& pr = P.prob[p];
-  int t = tile - pr.tile_begin;
+  int t = tile - P.seg_tile[s];
   tc.p = p;
-  tc.b = t / pr.tiles_per_mat;
-  t -= tc.b * pr.tiles_per_mat;
+  const int bi = t / pr.tiles_per_mat;
+  tc.b = (int)(pb & 0xFFFFFFu) + bi;
+  t -= bi * pr.tiles_per_mat;
   if (pr.sym) {
     int i = 0;
     while (t >= pr.tiles_m - i) {
@@ -369,10 +385,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       int s = 0;
       uint32_t ph = 0;
       bool ok = true;
-      int last_p = 0;
+      int seg = 0;
       for (int tile = pair; ok && tile < P.total_tiles; tile += npairs) {
-        const TileCoord c = decode_tile(P, tile, last_p);
-        last_p = c.p;
+        const TileCoord c = decode_tile(P, tile, &seg);
         const Problem& pr = P.prob[c.p];
         const int m0 = c.I * 256 + (int)rank * TM;
         const int n0 = c.J * 256 + (int)rank * BN;
@@ -430,10 +445,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       uint32_t ph = 0;
       bool ok = true;
       int local = 0;
-      int last_p = 0;
+      int seg = 0;
       for (int tile = pair; ok && tile < P.total_tiles; tile += npairs, ++local) {
-        const TileCoord c = decode_tile(P, tile, last_p);
-        last_p = c.p;
+        const TileCoord c = decode_tile(P, tile, &seg);
         const Problem& pr = P.prob[c.p];
         const int acc = local & 1;
         const uint32_t aph = (local >> 1) & 1;
@@ -477,10 +491,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       // the completion counters of the problems each tile depends on, and publishes the
       // highest tile whose inputs are complete, so the L2 round trips of those checks stay
       // off the producer's path.
-      int last_p = 0;
+      int seg = 0;
       for (int tile = pair; tile < P.total_tiles; tile += npairs) {
-        const TileCoord c = decode_tile(P, tile, last_p);
-        last_p = c.p;
+        const TileCoord c = decode_tile(P, tile, &seg);
         const Problem& pr = P.prob[c.p];
         if (pr.dep_mask && !wait_deps(P, pr, c.b, abort_flag)) break;
         __threadfence_block();
@@ -492,10 +505,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       // Loads the C chunks of the next tile as soon as the epilogue releases each buffer,
       // a whole main loop ahead of their use.
       uint32_t qc = 0;  // C chunks loaded so far (ring slot and phase)
-      int last_p = 0;
+      int seg = 0;
       for (int tile = pair; tile < P.total_tiles; tile += npairs) {
-        const TileCoord c = decode_tile(P, tile, last_p);
-        last_p = c.p;
+        const TileCoord c = decode_tile(P, tile, &seg);
         const Problem& pr = P.prob[c.p];
         if (!pr.has_c) continue;
         const int m0 = c.I * 256 + (int)rank * TM;
@@ -528,10 +540,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     uint32_t qc = 0;  // C chunks consumed so far (ring slot and phase)
     uint32_t gc = 0;  // chunks stored so far (output staging buffers)
     int local = 0;
-    int last_p = 0;
+    int seg = 0;
     for (int tile = pair; tile < P.total_tiles; tile += npairs, ++local) {
-      const TileCoord c = decode_tile(P, tile, last_p);
-      last_p = c.p;
+      const TileCoord c = decode_tile(P, tile, &seg);
       const Problem& pr = P.prob[c.p];
       const int acc = local & 1;
       const uint32_t aph = (local >> 1) & 1;
@@ -786,9 +797,61 @@ static int resident_pairs(std::string* err) {
   return clusters;
 }
 
+struct Segment {
+  int p;
+  int64_t b0, nb;
+};
+
+// Order of the tiles of one launch. Independent products (no dependency masks), or products
+// over batches of different sizes, run problem after problem. A program of dependent
+// products over one batch of B matrices runs in waves of W matrices: segment (w, p) holds
+// the tiles of problem p for the matrices of wave w and is placed by the key p + D * w (ties
+// to the lower wave). D = 0 is stage-major across the waves (W = B: every stage over the
+// whole batch before the next one); D = nops runs wave after wave, every stage of a few
+// matrices at a time, whose n x n buffers then stay in L2; values in between overlap the
+// late stages of one wave with the early ones of the next. Every segment comes after the
+// segments of earlier problems for the same matrices, so each tile depends only on earlier
+// tiles. GNS_TILE_ORDER="W,D" in the environment overrides the default (a tuning knob).
+static void tile_order(const GemmOp* ops, int nops, bool dependent, std::vector<Segment>* out) {
+  out->clear();
+  bool same = true;
+  for (int i = 1; i < nops; ++i) same = same && ops[i].batch == ops[0].batch;
+  const int64_t B = ops[0].batch;
+  int64_t W = B;
+  int64_t D = 0;
+  if (dependent && same) {
+    const char* env = getenv("GNS_TILE_ORDER");
+    long w = 0, d = 0;
+    if (env && sscanf(env, "%ld,%ld", &w, &d) == 2 && w > 0 && d >= 0) {
+      W = std::min<int64_t>(w, B);
+      D = d;
+    }
+    // the segment list must fit the launch parameters
+    const int64_t max_waves = std::max<int64_t>(1, tc::MAX_SEG / nops);
+    if ((B + W - 1) / W > max_waves) W = (B + max_waves - 1) / max_waves;
+  }
+  if (!dependent || !same) {
+    for (int p = 0; p < nops; ++p) out->push_back({p, 0, ops[p].batch});
+    return;
+  }
+  const int64_t nw = (B + W - 1) / W;
+  struct Key {
+    int64_t key, w;
+    int p;
+  };
+  std::vector<Key> keys;
+  for (int64_t w = 0; w < nw; ++w)
+    for (int p = 0; p < nops; ++p) keys.push_back({p + D * w, w, p});
+  std::stable_sort(keys.begin(), keys.end(), [](const Key& a, const Key& b) {
+    return a.key != b.key ? a.key < b.key : a.w < b.w;
+  });
+  for (const Key& k : keys) out->push_back({k.p, k.w * W, std::min(W, B - k.w * W)});
+}
+
 int gemm_launch_tc(const GemmOp* ops, int nops, const uint32_t* dep_masks, int* counters, int32_t* dev_status,
                    void* stream, std::string* err) {
   using namespace tc;
+  static_assert(sizeof(Params) <= 32764, "kernel parameter space");
   if (nops < 1 || nops > MAX_PROB) {
     *err = "internal: bad number of products in one launch";
     return GNS_ERR_INVALID;
@@ -844,7 +907,6 @@ int gemm_launch_tc(const GemmOp* ops, int nops, const uint32_t* dep_masks, int* 
       return GNS_ERR_UNSUPPORTED;
     }
     pr.tiles_per_mat = (int)tpm;
-    pr.tile_begin = tiles;
     tiles += pr.tiles_per_mat * (int)o.batch;
     pr.alpha = o.alpha;
     pr.beta = o.beta;
@@ -866,6 +928,26 @@ int gemm_launch_tc(const GemmOp* ops, int nops, const uint32_t* dep_masks, int* 
   for (int i = 0; i < nops; ++i) {
     P.prob[i].ctr_off = off;
     off += (int)ops[i].batch;
+  }
+  // tile order: segments (problem, first matrix, matrices), see tile_order()
+  {
+    std::vector<Segment> segs;
+    tile_order(ops, nops, dep_masks != nullptr, &segs);
+    if (segs.empty() || (int)segs.size() > MAX_SEG) {
+      *err = "internal: tile order does not fit the launch parameters";
+      return GNS_ERR_INVALID;
+    }
+    int t = 0;
+    for (size_t i = 0; i < segs.size(); ++i) {
+      P.seg_pb[i] = ((uint32_t)segs[i].p << 24) | (uint32_t)segs[i].b0;
+      P.seg_tile[i] = t;
+      t += P.prob[segs[i].p].tiles_per_mat * (int)segs[i].nb;
+    }
+    P.nseg = (int)segs.size();
+    if (t != tiles) {
+      *err = "internal: tile order does not cover every tile once";
+      return GNS_ERR_INVALID;
+    }
   }
   P.nprob = nops;
   P.total_tiles = tiles;
