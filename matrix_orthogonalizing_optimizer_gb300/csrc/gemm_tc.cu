@@ -117,10 +117,25 @@ struct Problem {
 // matrices b0 .. b0 + nb - 1 (matrix-major, then tile): seg_pb = p << 24 | b0, seg_tile =
 // index of its first tile (nb follows from the next segment's start). The host orders the
 // segments so that every tile depends only on tiles earlier in the sequence.
-constexpr int MAX_SEG = 640;
+constexpr int MAX_SEG = 576;
+
+// A problem whose output rows go through a row map (the fractional update's
+// W[S] <- beta W[S] + alpha O): the epilogue threads read C and write D (the same matrix) with
+// plain 16-byte global accesses, row i of the product at row map[b * map_stride + i] of
+// matrix b, instead of TMA tiles. rows: valid product rows; cols: columns of D.
+struct RowMapOut {
+  int prob;  // -1: none
+  int map_stride;
+  const int32_t* map;
+  void* ptr;
+  long long ld, stride;
+  int rows, cols;
+  int has_c;
+};
 
 struct Params {
   Problem prob[MAX_PROB];
+  RowMapOut rmo;
   int nprob;
   int total_tiles;
   int nseg;
@@ -307,6 +322,45 @@ __device__ __forceinline__ void pack_h16x2(const float2 (&o)[16], uint32_t (&pk)
       const __nv_bfloat162 h = __float22bfloat162_rn(o[i]);
       pk[i] = *reinterpret_cast<const uint32_t*>(&h);
     }
+  }
+}
+
+// The 32 16-bit values of a row-mapped C row at columns [col, col + 32), two per word (zero
+// beyond `cols` or without a row); 16-byte loads when the whole range is inside the row.
+__device__ __forceinline__ void rowmap_load(uint32_t (&cw)[16], const uint16_t* row, int col, int cols) {
+  if (!row) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) cw[i] = 0u;
+  } else if (col + 32 <= cols) {
+    const uint4* p = reinterpret_cast<const uint4*>(row + col);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 w = p[q];
+      cw[4 * q] = w.x;
+      cw[4 * q + 1] = w.y;
+      cw[4 * q + 2] = w.z;
+      cw[4 * q + 3] = w.w;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t lo = col + 2 * i < cols ? row[col + 2 * i] : 0u;
+      const uint32_t hi = col + 2 * i + 1 < cols ? row[col + 2 * i + 1] : 0u;
+      cw[i] = lo | (hi << 16);
+    }
+  }
+}
+
+__device__ __forceinline__ void rowmap_store(uint16_t* row, int col, int cols, const uint32_t (&pk)[16]) {
+  if (!row) return;
+  if (col + 32 <= cols) {
+    uint4* p = reinterpret_cast<uint4*>(row + col);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) p[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (col + j < cols) row[col + j] = (uint16_t)(pk[j >> 1] >> (16 * (j & 1)));
   }
 }
 
@@ -562,6 +616,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       const float gamma = pr.gamma;
       const int m0 = c.I * 256 + (int)rank * TM;  // first row of this CTA's half
       const int n0 = c.J * 256;
+      // row-mapped output: this thread's row of D (= C), and its first C values, loaded
+      // before the accumulator is ready
+      const bool rowmap = c.p == P.rmo.prob;
+      uint16_t* rm_row = nullptr;
+      const int rm_cols = P.rmo.cols, rm_has_c = P.rmo.has_c;
+      uint32_t cw_next[16];
+      if (rowmap) {
+        if (m0 + r < P.rmo.rows) {
+          const long long wr = P.rmo.map[(long long)c.b * P.rmo.map_stride + m0 + r];
+          rm_row = static_cast<uint16_t*>(P.rmo.ptr) + (long long)c.b * P.rmo.stride + wr * P.rmo.ld;
+        }
+        rowmap_load(cw_next, rm_has_c ? rm_row : nullptr, n0 + half * 32, rm_cols);
+      }
       if (et == 0) *epi_flag = mbar_wait(&tfull[acc], aph, abort_flag, P.status) ? 1 : 0;
       named_bar_sync(1, EPI_THREADS);
       if (!*epi_flag) break;
@@ -570,7 +637,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       const bool diag_mine = want_diag && ((diag_col >> 5) & 1) == half;
       float dv = 0.f;
       bool bad = false;
-      for (int ch = 0; ch < NCHUNK; ++ch, ++gc) {
+      if (rowmap) {
+        // each thread reads, updates and writes its own row segment: no staging, no barriers
+        for (int ch = 0; ch < NCHUNK; ++ch) {
+          uint32_t cw[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) cw[i] = cw_next[i];
+          if (ch + 1 < NCHUNK) rowmap_load(cw_next, rm_has_c ? rm_row : nullptr, n0 + (ch + 1) * CHUNK + half * 32, rm_cols);
+          uint32_t v[32];
+          __syncwarp();
+          tmem_ld_32x32b_x32(tmem_base + acc * TN + ch * CHUNK + half * 32 + ((uint32_t)(quarter * 32) << 16), v);
+          tmem_ld_wait();
+          if (ch == NCHUNK - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(acc ? tempty_leader1 : tempty_leader0);
+          }
+          float2 o[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) o[i] = make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+          if (alpha != 1.f) {
+            const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) o[i] = __fmul2_rn(a2, o[i]);
+          }
+          if (rm_has_c) axpy_h16x2(o, cw, beta, d_f16);
+          if (check_finite) {
+            float2 z = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) z = __ffma2_rn(o[i], make_float2(0.f, 0.f), z);
+            bad |= !(z.x == 0.f && z.y == 0.f);
+          }
+          uint32_t pk[16];
+          pack_h16x2(o, pk, d_f16);
+          rowmap_store(rm_row, n0 + ch * CHUNK + half * 32, rm_cols, pk);
+        }
+        // the tile's stores are visible before its completion is published
+        __threadfence();
+        named_bar_sync(1, EPI_THREADS);
+      }
+      for (int ch = 0; ch < (rowmap ? 0 : NCHUNK); ++ch, ++gc) {
         uint8_t* sd = SD + (gc % OUT_BUFS) * CHUNK_BYTES;
         // the stores that last read these buffers are done
         if (et == 0) {
@@ -863,13 +969,26 @@ int gemm_launch_tc(const GemmOp* ops, int nops, const uint32_t* dep_masks, int* 
   Params P;
   memset(&P, 0, sizeof(P));
   int tiles = 0;
+  P.rmo.prob = -1;
   for (int i = 0; i < nops; ++i) {
     const GemmOp& o = ops[i];
-    if (o.row_map) {
-      *err = "internal: row-mapped outputs are not handled by the tensor-core GEMM";
-      return GNS_ERR_INVALID;
-    }
     Problem& pr = P.prob[i];
+    if (o.row_map) {
+      if (P.rmo.prob >= 0 || o.sym || o.d_trans || o.c_trans || o.D2.ptr || (o.C.ptr && o.C.ptr != o.D.ptr) ||
+          o.D.ld % 8 || reinterpret_cast<uintptr_t>(o.D.ptr) % 16 || (o.batch > 1 && o.D.stride % 8)) {
+        *err = "internal: unsupported row-mapped output";
+        return GNS_ERR_INVALID;
+      }
+      P.rmo.prob = i;
+      P.rmo.map = o.row_map;
+      P.rmo.map_stride = (int)o.row_map_stride;
+      P.rmo.ptr = o.D.ptr;
+      P.rmo.ld = o.D.ld;
+      P.rmo.stride = o.D.stride;
+      P.rmo.rows = (int)o.M;
+      P.rmo.cols = (int)o.N;
+      P.rmo.has_c = o.C.ptr != nullptr && o.beta != 0.f;
+    }
     const int dts[3] = {o.ab_dt, o.c_dt, o.d_dt};
     for (int t : dts)
       if (t != GNS_BF16 && t != GNS_F16) {
@@ -886,13 +1005,14 @@ int gemm_launch_tc(const GemmOp* ops, int nops, const uint32_t* dep_masks, int* 
     pr.mirror_out = o.upper_out ? 0 : 1;
     if (o.a_upper && !encode_map(&pr.tmA2, o.A, o.batch, o.a_mn ? 128 : 64, pr.ab_f16, err)) return GNS_ERR_CUDA;
     if (o.b_upper && !encode_map(&pr.tmB2, o.B, o.batch, o.b_mn ? 128 : 64, pr.ab_f16, err)) return GNS_ERR_CUDA;
-    pr.has_c = o.C.ptr != nullptr && o.beta != 0.f;
+    // a row-mapped output reads its C in the epilogue: the C loader skips the problem
+    pr.has_c = o.C.ptr != nullptr && o.beta != 0.f && !o.row_map;
     // one 128-row box per chunk where a map serves only direct chunks
     pr.c_mode = o.c_trans ? 1 : 2;
     const bool d_one_box = !o.d_trans && !(o.sym && !o.upper_out);
     pr.d_mode = d_one_box ? 2 : 0;
     if (pr.has_c && !encode_map(&pr.tmC, o.C, o.batch, o.c_trans ? 64 : 128, pr.c_f16, err)) return GNS_ERR_CUDA;
-    if (!encode_map(&pr.tmD, o.D, o.batch, d_one_box ? 128 : 64, pr.d_f16, err)) return GNS_ERR_CUDA;
+    if (!o.row_map && !encode_map(&pr.tmD, o.D, o.batch, d_one_box ? 128 : 64, pr.d_f16, err)) return GNS_ERR_CUDA;
     pr.has_d2 = o.D2.ptr != nullptr;
     if (pr.has_d2 && !encode_map(&pr.tmD2, o.D2, o.batch, d_one_box ? 128 : 64, pr.d_f16, err)) return GNS_ERR_CUDA;
     pr.a_mn = o.a_mn;

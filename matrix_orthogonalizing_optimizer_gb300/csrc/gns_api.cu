@@ -614,7 +614,9 @@ static void plan_muon(Arena& a, const GroupShape& sh, const gns_muon_params& mp,
   mb->nf = static_cast<int*>(a.take(sizeof(int) * n * B));
   mb->idx = static_cast<int*>(a.take(sizeof(int) * k * B));
   mb->xs = ws_mat(a, B, round_up(k, PAD), k, m, ldm, 2);
-  mb->os = ws_mat(a, B, k, k, m, ldm, 2);
+  // O gets its own buffer only where the update cannot ride on the last product's epilogue:
+  // NorMuon (its row statistics need O first) and the columns of a tall matrix
+  if (normuon || sh.trans) mb->os = ws_mat(a, B, k, k, m, ldm, 2);
   if (mb->nsdt == GNS_F16) mb->x16 = ws_mat(a, B, round_up(k, PAD), k, m, ldm, 2);
   plan_gram(a, B, k, m, mb->nsdt, ns, &mb->gb, true);
   if (normuon) {
@@ -1048,9 +1050,22 @@ int gns_muon_step(const gns_batch* W, const gns_batch* G, const gns_batch* M, co
       src.user = false;
     }
     Final fin;
-    fin.D = mb.os;
     fin.out_dt = GNS_BF16;
+    const bool fused = !normuon && !s.trans;
+    if (fused) {
+      // W[S] <- (1 - lr wd) W[S] - lr scale O in the last product's epilogue (Dion3 sec. 6,
+      // "Weight update"): rows of O go to the selected rows of W, fp32 arithmetic, one rounding
+      fin.D = wm;
+      fin.alpha = step_scale;
+      fin.beta = decay;
+      fin.has_c = true;
+      fin.row_map = mb.idx;
+      fin.rms = k;
+    } else {
+      fin.D = mb.os;
+    }
     if ((rc = run_gram(mb.nsdt, src, s.B, k, s.m, ns, mb.gb, mb.gb.inv, fin, dev_status, stream))) return rc;
+    if (fused) continue;
     // NorMuon flavour: second moments of the selected rows, scaling, rescale
     if (normuon) {
       if ((rc = launch_row_sumsq(mb.os, k, s.m, s.B, mb.s, stream, &err))) return fail(rc, err);

@@ -1,0 +1,94 @@
+"""Precision of the three storage types on spectra the stated tolerance does not cover
+evenly: one dominant singular value and the other n - 1 at ratio rho (X = U diag(1, rho, ...,
+rho) V^T with random orthonormal U, V), down to effectively rank-one inputs (rho <= 3e-3),
+plus the exactly rank-one single row. Errors are relative Frobenius errors against the fp64
+oracle of the same algorithm on the same rounded input.
+
+Measured on GB300 (max over three seeds; n x 4n... shapes 8 x 256, 64 x 512, 256 x 1024):
+  * fp32: at most 2.1e-5 everywhere (the 1e-4 validation bar holds on every class);
+  * fp16: at most 0.9 % except rho <= 3e-3 with 8 rows (3.8 %);
+  * bf16 Gram NS: 1-2.6 % for rho >= 0.01 with 64 or more rows, up to 5 % with 8 rows, and
+    3-22 % on effectively rank-one inputs; bf16 standard NS on the same kernels reaches 9 %
+    there. A model of Algorithm 3 with every stored matrix rounded to bf16 (storage_model)
+    shows the same errors, so they are the cost of bf16 storage, not of the kernels: before
+    the restart Q's eigenvalues spread ~10x between the weak directions (gain a^2) and the
+    dominant one, and bf16 rounding relative to Q's largest entries costs the dominant
+    direction several percent; with rho below bf16's resolution of R the weak directions
+    are lost outright.
+Bounds asserted per class (from those measurements, with margin): fp32 1e-4 everywhere;
+fp16 2e-2 except effectively rank-one with 8 rows (6e-2); bf16 at most 2x the storage
+model's error plus 1e-2 everywhere, 4e-2 for rho >= 0.01 with 64 or more rows, 8e-2 with 8
+rows, 4e-2 on the single row; the stated 2e-2 bf16 bar is asserted on the Gaussian inputs of
+the other parity tests, which is what the workloads look like.
+"""
+import numpy as np
+import pytest
+
+from matrix_orthogonalizing_optimizer_gb300 import inputs
+from oracle import muon as omuon
+from oracle import newton_schulz as ons
+from storage_model import gram_ns_stored, round_bf16
+from util import rel_fro
+
+torch = pytest.importorskip("torch")
+gns = pytest.importorskip("matrix_orthogonalizing_optimizer_gb300")
+
+pytestmark = pytest.mark.gpu
+
+
+def _spectrum(n, m, rho, seed):
+    g = np.random.default_rng(seed)
+    U, _ = np.linalg.qr(g.standard_normal((n, n)))
+    V, _ = np.linalg.qr(g.standard_normal((m, n)))
+    s = np.full(n, rho)
+    s[0] = 1.0
+    return (U * s) @ V.T / np.sqrt(m)
+
+
+def _run(x, dtype):
+    t = torch.from_numpy(np.ascontiguousarray(x)).cuda()[None].contiguous()
+    if dtype == torch.bfloat16:
+        bits = inputs.round_to_bf16_bits(x)
+        t = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()[None].contiguous()
+        xin = inputs.bf16_bits_to_f32(bits).astype(np.float64)
+    elif dtype == torch.float16:
+        x16 = x.astype(np.float16)
+        t = torch.from_numpy(x16).cuda()[None].contiguous()
+        xin = x16.astype(np.float64)
+    else:
+        x32 = x.astype(np.float32)
+        t = torch.from_numpy(x32).cuda()[None].contiguous()
+        xin = x32.astype(np.float64)
+    out = gns.gram_ns_batched(t)[0][0].double().cpu().numpy()
+    return rel_fro(out, omuon.orthogonalize(xin)), xin
+
+
+CASES = [(n, m, rho) for (n, m) in [(8, 256), (64, 512), (256, 1024)]
+         for rho in [1.0, 0.3, 0.1, 0.03, 0.01, 3e-3, 1e-3]]
+
+
+@pytest.mark.parametrize("n,m,rho", CASES)
+def test_precision_classes(n, m, rho):
+    rank_one = rho <= 3e-3
+    for seed in range(2):
+        x = _spectrum(n, m, rho, seed)
+        e32, _ = _run(x, torch.float32)
+        assert e32 < 1e-4, ("fp32", seed, e32)
+        e16, _ = _run(x, torch.float16)
+        assert e16 < (6e-2 if rank_one and n <= 8 else 2e-2), ("fp16", seed, e16)
+        ebf, xb = _run(x, torch.bfloat16)
+        model = rel_fro(gram_ns_stored(xb, ons.QUINTIC_FIXED, round_bf16), omuon.orthogonalize(xb))
+        assert ebf < 2.0 * model + 1e-2, ("bf16 vs storage model", seed, ebf, model)
+        if not rank_one:
+            assert ebf < (8e-2 if n <= 8 else 4e-2), ("bf16", seed, ebf)
+
+
+def test_single_row_rank_one():
+    """n = 1: every singular value at the top of [0, 1], where the stored bf16 Z ~ -2.74
+    cancels against a ~ 3.44 in Q (x3.9 amplification of its rounding): bf16 2.8 %, fp16
+    0.23 % measured."""
+    for seed in range(3):
+        x = inputs.gaussian(60 + seed, (1, 4096), 1.0 / 64)
+        assert _run(x, torch.bfloat16)[0] < 4e-2
+        assert _run(x, torch.float16)[0] < 2e-2
+        assert _run(x, torch.float32)[0] < 1e-4
