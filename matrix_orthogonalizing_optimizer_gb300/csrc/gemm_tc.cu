@@ -111,6 +111,7 @@ struct Problem {
   int c_mode, d_mode;        // chunk modes of the C loads and of the direct D / D2 stores
   uint32_t dep_mask;  // earlier problems whose tiles of the same matrix must be complete
   int ctr_off;        // this problem's completion counters: counters[ctr_off + b]
+  int publish;        // a later problem of the launch depends on this one: publish completions
 };
 
 // The launch's tiles form a sequence of segments, each the tiles of problem p for the
@@ -623,11 +624,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       const int rm_cols = P.rmo.cols, rm_has_c = P.rmo.has_c;
       uint32_t cw_next[16];
       if (rowmap) {
-        if (m0 + r < P.rmo.rows) {
-          const long long wr = P.rmo.map[(long long)c.b * P.rmo.map_stride + m0 + r];
+        // this tile's row and the next tile's (its row segments are fetched into L2 now, a
+        // whole tile before their loads: the epilogue of a row-mapped tile waits on them)
+        const int tn = tile + npairs;
+        int sn = seg;
+        const TileCoord nc = tn < P.total_tiles ? decode_tile(P, tn, &sn) : c;
+        const bool pf = tn < P.total_tiles && nc.p == c.p && nc.I * 256 + (int)rank * TM + r < P.rmo.rows;
+        long long wr = 0, wn = 0;
+        if (m0 + r < P.rmo.rows) wr = P.rmo.map[(long long)c.b * P.rmo.map_stride + m0 + r];
+        if (pf) wn = P.rmo.map[(long long)nc.b * P.rmo.map_stride + nc.I * 256 + (int)rank * TM + r];
+        if (m0 + r < P.rmo.rows)
           rm_row = static_cast<uint16_t*>(P.rmo.ptr) + (long long)c.b * P.rmo.stride + wr * P.rmo.ld;
-        }
         rowmap_load(cw_next, rm_has_c ? rm_row : nullptr, n0 + half * 32, rm_cols);
+        if (pf && rm_has_c) {
+          const uint16_t* nrow = static_cast<const uint16_t*>(P.rmo.ptr) + (long long)nc.b * P.rmo.stride + wn * P.rmo.ld;
+#pragma unroll
+          for (int ch = 0; ch < NCHUNK; ++ch) {
+            const int col = nc.J * 256 + ch * CHUNK + half * 32;
+            if (col < rm_cols) asm volatile("prefetch.global.L2 [%0];" ::"l"(nrow + col));
+          }
+        }
       }
       if (et == 0) *epi_flag = mbar_wait(&tfull[acc], aph, abort_flag, P.status) ? 1 : 0;
       named_bar_sync(1, EPI_THREADS);
@@ -672,17 +688,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           pack_h16x2(o, pk, d_f16);
           rowmap_store(rm_row, n0 + ch * CHUNK + half * 32, rm_cols, pk);
         }
-        // the tile's stores are visible before its completion is published
-        __threadfence();
-        named_bar_sync(1, EPI_THREADS);
+        if (pr.publish) {
+          // the tile's stores are visible before its completion is published
+          __threadfence();
+          named_bar_sync(1, EPI_THREADS);
+        }
       }
       for (int ch = 0; ch < (rowmap ? 0 : NCHUNK); ++ch, ++gc) {
         uint8_t* sd = SD + (gc % OUT_BUFS) * CHUNK_BYTES;
-        // the stores that last read these buffers are done
-        if (et == 0) {
-          if (OUT_BUFS == 2) bulk_wait_read<1>(); else bulk_wait_read<0>();
-        }
-        named_bar_sync(1, EPI_THREADS);
         uint32_t v[32];
         __syncwarp();
         tmem_ld_32x32b_x32(tmem_base + acc * TN + ch * CHUNK + half * 32 + ((uint32_t)(quarter * 32) << 16), v);
@@ -743,6 +756,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         }
         uint32_t pk[16];  // the row's 32 outputs rounded once, two per word
         pack_h16x2(o, pk, d_f16);
+        // the stores that last read the staging buffer are done (waited for only now, so that
+        // they drain while this chunk is loaded from tensor memory and computed)
+        if (et == 0) {
+          if (OUT_BUFS == 2) bulk_wait_read<1>(); else bulk_wait_read<0>();
+        }
+        named_bar_sync(1, EPI_THREADS);
         if (!d_trans) {
 #pragma unroll
           for (int q = 0; q < 4; ++q)
@@ -794,8 +813,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         }
       }
       if (bad) set_status(P.status, GNS_DEVST_NONFINITE);
-      if (et == 0 && P.counters) {
+      if (et == 0 && pr.publish) {
         // this CTA's half of the tile is in global memory: publish it to dependent tiles
+        // (products nothing in the launch depends on skip the wait for their stores)
         bulk_wait_all();
         fence_proxy_async_global();
         red_release_gpu_add(P.counters + pr.ctr_off + c.b, 1);
@@ -1043,6 +1063,10 @@ int gemm_launch_tc(const GemmOp* ops, int nops, const uint32_t* dep_masks, int* 
       *err = "internal: dependent products need completion counters";
       return GNS_ERR_INVALID;
     }
+    pr.publish = 0;
+    if (dep_masks && counters)
+      for (int j = i + 1; j < nops; ++j)
+        if (dep_masks[j] & (1u << i)) pr.publish = 1;
   }
   int off = 0;
   for (int i = 0; i < nops; ++i) {
