@@ -497,6 +497,39 @@ def run_ours(args, rank, world, dist):
     moe = moe_experts()
     moe_sq = moe_squares()
 
+    # ---- many small matrices (one call per batch; products of at most 128 rows take the
+    #      1-CTA 128 x 128 tile plan) and a batch-size sweep at 1024 x 4096 ----
+    def small_batches():
+        res = {}
+        for (count, n, m) in [(2048, 128, 512), (512, 256, 1024), (96, 512, 2048)]:
+            X = (torch.randn((count, n, m), generator=gen, device=dev, dtype=torch.float32) / m ** 0.5).to(
+                torch.bfloat16)
+            r = time_orth(X, gns.gram_ns_batched, _lib.GNS_OP_GRAM_NS, count * alg_flops_per_matrix(n, m))
+            std = time_orth(X, gns.ns_standard_batched, _lib.GNS_OP_NS_STANDARD, count * std_flops_per_matrix(n, m))
+            r["standard_ns_ms_per_call"] = std["ms_per_call"]
+            r["gram_vs_standard_speedup"] = std["ms_per_call"] / r["ms_per_call"]
+            r["tile_plan"] = "1-CTA 128 x 128" if n <= 128 else "2-CTA 256 x 256"
+            res[f"{count}x{n}x{m}"] = r
+            del X
+            torch.cuda.empty_cache()
+        return res
+
+    def batch_sweep():
+        res = {}
+        n, m = ROWS, COLS
+        for count in [1, 2, 4, 8, 16, 24, 32, 48, 64]:
+            X = (torch.randn((count, n, m), generator=gen, device=dev, dtype=torch.float32) / m ** 0.5).to(
+                torch.bfloat16)
+            r = time_orth(X, gns.gram_ns_batched, _lib.GNS_OP_GRAM_NS, count * alg_flops_per_matrix(n, m))
+            res[str(count)] = {k: r[k] for k in ("ms_per_call", "matrices_per_s", "gemm_tflops",
+                                                 "gemm_frac_of_burst_peak")}
+            del X
+            torch.cuda.empty_cache()
+        return res
+
+    small = small_batches()
+    sweep = batch_sweep()
+
     # ---- the fractional-update configuration: 32 x 4096 x 16384, f = 1/4 (k = 1024) ----
     def frac_config(rows=4096, cols=16384):
         count = 32
@@ -676,6 +709,8 @@ def run_ours(args, rank, world, dist):
         "flavors": flavors,
         "moe_experts_alpha4": moe,
         "moe_squares_7168": moe_sq,
+        "small_matrices": small,
+        "batch_sweep_1024x4096_gram_ns": sweep,
         "frac_quarter_4096x16384": frac_cfg,
         "frac_quarter_16384x4096_tall": frac_tall,
         "dense_layers_32": dense,

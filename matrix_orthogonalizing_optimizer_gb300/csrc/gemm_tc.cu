@@ -40,8 +40,7 @@ namespace gns {
 
 namespace tc {
 
-constexpr int TM = 128;                          // accumulator rows per CTA (256 per pair)
-constexpr int TN = 256;                          // tile columns
+constexpr int TM = 128;                          // accumulator rows per CTA
 constexpr int BN = 128;                          // B columns staged per CTA
 constexpr int TK = 64;                           // K slice per stage
 #ifndef GNS_TC_OUTBUFS
@@ -51,7 +50,6 @@ constexpr int OUT_BUFS = GNS_TC_OUTBUFS;         // staging buffers for output (
 constexpr int A_BYTES = TM * TK * 2;             // 16 KiB
 constexpr int STAGE_BYTES = (TM + BN) * TK * 2;  // 32 KiB per CTA
 constexpr int CHUNK = 64;                        // epilogue columns per chunk
-constexpr int NCHUNK = TN / CHUNK;
 constexpr int BOX_BYTES = 64 * 64 * 2;           // one 64 x 64 16-bit box, 128-byte swizzle
 constexpr int CHUNK_BYTES = 2 * BOX_BYTES;       // 128 x 64 (or 64 x 128) elements
 constexpr int C_WARP = 2;                        // loads the C tile ahead of the epilogue
@@ -64,7 +62,19 @@ constexpr int EPI_THREADS = 32 * EPI_WARPS;
 constexpr int PROD2_WARP = FIRST_EPI_WARP + EPI_WARPS;
 constexpr int NUM_THREADS = 32 * (FIRST_EPI_WARP + EPI_WARPS + 1);
 constexpr int MAX_PROB = 24;                     // stages of one launch
-constexpr int TMEM_COLS = 512;                   // two 256-column fp32 accumulators
+
+// Tile geometry of a CTA group: CG = 2 (a CTA pair, 2-CTA MMAs, 256 x 256 tiles) or CG = 1
+// (one CTA, 128 x 128 tiles, for products of at most 128 rows: a 256 x 256 tile would
+// compute 4x the useful work of an n <= 128 Gram product). Per CTA the operand staging is the
+// same (128 rows of A, 128 columns of B per 64-wide K slice); the accumulator is TILE
+// columns wide, two of them in tensor memory.
+template <int CG>
+struct Geo {
+  static constexpr int TILE = 128 * CG;             // tile rows = tile columns
+  static constexpr int NCH = TILE / CHUNK;          // epilogue chunks per tile
+  static constexpr int TMEM_COLS = 2 * TILE;        // two fp32 accumulators
+  static constexpr int KSH = CG == 2 ? 2 : 1;       // log2 of 64-wide K slices per tile edge
+};
 constexpr int BAR_BYTES = 512;
 
 // Shared-memory plan of a kernel with STAGES operand stages and a ring of C_BUFS C chunks.
@@ -147,13 +157,14 @@ struct Params {
 };
 
 // Bounded wait until every problem this tile depends on has finished matrix b.
+template <int CG>
 __device__ __forceinline__ bool wait_deps(const Params& P, const Problem& pr, int b, volatile int* abort_flag) {
   uint32_t m = pr.dep_mask;
   while (m) {
     const int d = __ffs(m) - 1;
     m &= m - 1;
     const Problem& pd = P.prob[d];
-    if (!wait_counter(P.counters + pd.ctr_off + b, 2 * pd.tiles_per_mat, abort_flag, P.status)) return false;
+    if (!wait_counter(P.counters + pd.ctr_off + b, CG * pd.tiles_per_mat, abort_flag, P.status)) return false;
   }
   return true;
 }
@@ -181,17 +192,18 @@ __device__ __forceinline__ bool wait_ready(volatile int* ready, int tile, volati
 }
 
 // Major-ness of the A (B) slice of 64-wide K block kb for tile row I (column J). An operand
-// that is the upper triangle of a symmetric matrix (256-blocks at or above the diagonal) is
+// that is the upper triangle of a symmetric matrix (tile blocks at or above the diagonal) is
 // read from the mirrored block, with the other major-ness, wherever the block it would read
 // lies below the diagonal.
 // The per-product fields a K loop reads, copied into registers once per tile: the loops'
 // inline assembly clobbers memory, which would otherwise reload them from the parameter
 // block at every K slice.
 struct KLoop {
-  int kblocks, a_mn, b_mn, a_upper, b_upper, ab_f16;
+  int kblocks, a_mn, b_mn, a_upper, b_upper, ab_f16, ksh;
 };
-__device__ __forceinline__ KLoop kloop_of(const Problem& pr) {
+__device__ __forceinline__ KLoop kloop_of(const Problem& pr, int ksh) {
   KLoop k;
+  k.ksh = ksh;
   k.kblocks = pr.kblocks;
   k.a_mn = pr.a_mn;
   k.b_mn = pr.b_mn;
@@ -201,12 +213,12 @@ __device__ __forceinline__ KLoop kloop_of(const Problem& pr) {
   return k;
 }
 __device__ __forceinline__ int a_major(const KLoop& pr, int I, int kb) {
-  const int kbl = kb >> 2;
+  const int kbl = kb >> pr.ksh;
   const bool lower = pr.a_mn ? (kbl > I) : (I > kbl);
   return pr.a_mn ^ ((pr.a_upper && lower) ? 1 : 0);
 }
 __device__ __forceinline__ int b_major(const KLoop& pr, int J, int kb) {
-  const int kbl = kb >> 2;
+  const int kbl = kb >> pr.ksh;
   const bool lower = pr.b_mn ? (kbl > J) : (J > kbl);
   return pr.b_mn ^ ((pr.b_upper && lower) ? 1 : 0);
 }
@@ -326,6 +338,31 @@ __device__ __forceinline__ void pack_h16x2(const float2 (&o)[16], uint32_t (&pk)
   }
 }
 
+// One operand box of a K slice into this CTA's stage; completion is signalled on the stage
+// barrier at shared::cluster address bar (the pair leader's for CG = 2, with .cta_group::2).
+template <int CG>
+__device__ __forceinline__ void op_load(void* dst, const CUtensorMap* map, uint32_t bar, int c0, int c1, int c2) {
+  if constexpr (CG == 2) {
+    tma_load_3d_pair(dst, map, bar, c0, c1, c2);
+  } else {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+  }
+}
+
+// Releases an accumulator to the group's MMA issuer: a remote arrival on the leader's barrier
+// for a CTA pair, a local one for a single CTA.
+template <int CG>
+__device__ __forceinline__ void acc_release(uint32_t bar) {
+  if constexpr (CG == 2)
+    mbar_arrive_cluster(bar);
+  else
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
 // The 32 16-bit values of a row-mapped C row at columns [col, col + 32), two per word (zero
 // beyond `cols` or without a row); 16-byte loads when the whole range is inside the row.
 __device__ __forceinline__ void rowmap_load(uint32_t (&cw)[16], const uint16_t* row, int col, int cols) {
@@ -365,9 +402,11 @@ __device__ __forceinline__ void rowmap_store(uint16_t* row, int col, int cols, c
   }
 }
 
-template <class L>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
-    gemm_kernel(const __grid_constant__ Params P) {
+template <class L, int CG>
+__global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_constant__ Params P) {
+  constexpr int TT = Geo<CG>::TILE;
+  constexpr int NCHUNK = Geo<CG>::NCH;
+  constexpr int TMEM_COLS = Geo<CG>::TMEM_COLS;
   constexpr int STAGES = L::STAGES;
   constexpr int C_BUFS = L::C_BUFS;
   constexpr int OFF_SC = L::OFF_SC;
@@ -392,9 +431,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank();
-  const int pair = blockIdx.x >> 1;
-  const int npairs = gridDim.x >> 1;
+  // a "pair" is the CTA group of one tile: two CTAs of a cluster, or one CTA
+  const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;
+  const int pair = blockIdx.x / CG;
+  const int npairs = gridDim.x / CG;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -403,7 +443,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 2 * EPI_WARPS);  // one arrival per epilogue warp of both CTAs
+      mbar_init(&tempty[a], CG * EPI_WARPS);  // one arrival per epilogue warp of the group
     }
     for (int q = 0; q < C_BUFS; ++q) {
       mbar_init(&cfull[q], 1);
@@ -421,12 +461,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     }
   }
   if (warp == 1) {
-    tmem_alloc2(tmem_slot, TMEM_COLS);
-    tmem_relinquish2();
+    if constexpr (CG == 2) {
+      tmem_alloc2(tmem_slot, TMEM_COLS);
+      tmem_relinquish2();
+    } else {
+      tmem_alloc(tmem_slot, TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync_all();  // the peer's barriers are initialised before any remote arrival
+  if constexpr (CG == 2) cluster_sync_all();  // the peer's barriers are initialised before any remote arrival
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -435,7 +480,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       // ---------------- TMA producers (both CTAs): even K slices / odd K slices ----------------
       const int pid = warp == 0 ? 0 : 1;
       int* const status = P.status;
-      const uint32_t full0 = mapa_shared(smem_u32(&full[0]), 0);  // stage barriers in the leader
+      // stage barriers: the leader's for a CTA pair
+      const uint32_t full0 = CG == 2 ? mapa_shared(smem_u32(&full[0]), 0) : smem_u32(&full[0]);
       uint32_t g = 0;  // K slices of this pair so far: producer g & 1 takes slice g
       int s = 0;
       uint32_t ph = 0;
@@ -444,9 +490,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       for (int tile = pair; ok && tile < P.total_tiles; tile += npairs) {
         const TileCoord c = decode_tile(P, tile, &seg);
         const Problem& pr = P.prob[c.p];
-        const int m0 = c.I * 256 + (int)rank * TM;
-        const int n0 = c.J * 256 + (int)rank * BN;
-        const KLoop kl = kloop_of(pr);
+        const int m0 = c.I * TT + (int)rank * TM;
+        const int n0 = c.J * TT + (int)rank * BN;
+        const KLoop kl = kloop_of(pr, Geo<CG>::KSH);
         const CUtensorMap* const tmA = &pr.tmA;
         const CUtensorMap* const tmA2 = &pr.tmA2;
         const CUtensorMap* const tmB = &pr.tmB;
@@ -464,7 +510,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             ok = false;
             break;
           }
-          if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * STAGE_BYTES);
+          if (rank == 0) mbar_arrive_expect_tx(&full[s], CG * STAGE_BYTES);
           const uint32_t fb = full0 + 8u * (uint32_t)s;
           uint8_t* sa = stages + s * STAGE_BYTES;
           uint8_t* sb = sa + A_BYTES;
@@ -473,16 +519,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           const CUtensorMap* ma = amn == kl.a_mn ? tmA : tmA2;
           const CUtensorMap* mb = bmn == kl.b_mn ? tmB : tmB2;
           if (!amn) {
-            tma_load_3d_pair(sa, ma, fb, k0, m0, c.b);
+            op_load<CG>(sa, ma, fb, k0, m0, c.b);
           } else {
-            tma_load_3d_pair(sa, ma, fb, m0, k0, c.b);
-            tma_load_3d_pair(sa + BOX_BYTES, ma, fb, m0 + 64, k0, c.b);
+            op_load<CG>(sa, ma, fb, m0, k0, c.b);
+            op_load<CG>(sa + BOX_BYTES, ma, fb, m0 + 64, k0, c.b);
           }
           if (!bmn) {
-            tma_load_3d_pair(sb, mb, fb, k0, n0, c.b);
+            op_load<CG>(sb, mb, fb, k0, n0, c.b);
           } else {
-            tma_load_3d_pair(sb, mb, fb, n0, k0, c.b);
-            tma_load_3d_pair(sb + BOX_BYTES, mb, fb, n0 + 64, k0, c.b);
+            op_load<CG>(sb, mb, fb, n0, k0, c.b);
+            op_load<CG>(sb + BOX_BYTES, mb, fb, n0 + 64, k0, c.b);
           }
           if (++s == STAGES) {
             s = 0;
@@ -508,11 +554,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         const uint32_t aph = (local >> 1) & 1;
         if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, status)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * TN;
-        const KLoop kl = kloop_of(pr);
+        const uint32_t d_tmem = tmem_base + acc * TT;
+        const KLoop kl = kloop_of(pr, Geo<CG>::KSH);
         for (int kb = 0; kb < kl.kblocks; ++kb) {
           const int amn = a_major(kl, c.I, kb), bmn = b_major(kl, c.J, kb);
-          const uint32_t idesc = idesc_f16kind_f32(2 * TM, TN, amn, bmn, kl.ab_f16);
+          const uint32_t idesc = idesc_f16kind_f32(TT, TT, amn, bmn, kl.ab_f16);
           if (!mbar_wait(&full[s], ph, abort_flag, status)) {
             ok = false;
             break;
@@ -528,15 +574,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           const uint64_t astep = amn ? 2048 / 16 : 32 / 16;
           const uint64_t bstep = bmn ? 2048 / 16 : 32 / 16;
 #pragma unroll
-          for (int kk = 0; kk < TK / 16; ++kk)
-            umma2_f16kind(d_tmem, ad0 + astep * kk, bd0 + bstep * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
-          umma2_commit_multicast(&empty[s], 0x3);
+          for (int kk = 0; kk < TK / 16; ++kk) {
+            if constexpr (CG == 2)
+              umma2_f16kind(d_tmem, ad0 + astep * kk, bd0 + bstep * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+            else
+              umma_f16kind(d_tmem, ad0 + astep * kk, bd0 + bstep * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          if constexpr (CG == 2)
+            umma2_commit_multicast(&empty[s], 0x3);
+          else
+            umma_commit(&empty[s]);
           if (++s == STAGES) {
             s = 0;
             ph ^= 1u;
           }
         }
-        if (ok) umma2_commit_multicast(&tfull[acc], 0x3);
+        if (ok) {
+          if constexpr (CG == 2)
+            umma2_commit_multicast(&tfull[acc], 0x3);
+          else
+            umma_commit(&tfull[acc]);
+        }
       }
     }
   } else if (warp == C_WARP) {
@@ -550,7 +608,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       for (int tile = pair; tile < P.total_tiles; tile += npairs) {
         const TileCoord c = decode_tile(P, tile, &seg);
         const Problem& pr = P.prob[c.p];
-        if (pr.dep_mask && !wait_deps(P, pr, c.b, abort_flag)) break;
+        if (pr.dep_mask && !wait_deps<CG>(P, pr, c.b, abort_flag)) break;
         __threadfence_block();
         *ready_tile = tile;
       }
@@ -565,8 +623,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         const TileCoord c = decode_tile(P, tile, &seg);
         const Problem& pr = P.prob[c.p];
         if (!pr.has_c) continue;
-        const int m0 = c.I * 256 + (int)rank * TM;
-        const int n0 = c.J * 256;
+        const int m0 = c.I * TT + (int)rank * TM;
+        const int n0 = c.J * TT;
         if (pr.dep_mask && !wait_ready(ready_tile, tile, abort_flag, P.status)) break;
         bool ok = true;
         const CUtensorMap* const tmC = &pr.tmC;
@@ -590,8 +648,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     const int quarter = warp & 3;  // TMEM lanes this warp may read
     const int half = ew >> 2;      // which 32 of a chunk's 64 columns
     const int r = quarter * 32 + lane;
-    const uint32_t tempty_leader0 = mapa_shared(smem_u32(&tempty[0]), 0);
-    const uint32_t tempty_leader1 = mapa_shared(smem_u32(&tempty[1]), 0);
+    // the accumulator barriers the epilogue releases: the leader's for a CTA pair
+    const uint32_t tempty_leader0 = CG == 2 ? mapa_shared(smem_u32(&tempty[0]), 0) : smem_u32(&tempty[0]);
+    const uint32_t tempty_leader1 = CG == 2 ? mapa_shared(smem_u32(&tempty[1]), 0) : smem_u32(&tempty[1]);
     uint32_t qc = 0;  // C chunks consumed so far (ring slot and phase)
     uint32_t gc = 0;  // chunks stored so far (output staging buffers)
     int local = 0;
@@ -615,8 +674,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       const int d_mode = d_trans ? 1 : pr.d_mode;
       const int check_finite = pr.check_finite, has_d2 = pr.has_d2, diag_limit = pr.diag_limit;
       const float gamma = pr.gamma;
-      const int m0 = c.I * 256 + (int)rank * TM;  // first row of this CTA's half
-      const int n0 = c.J * 256;
+      const int m0 = c.I * TT + (int)rank * TM;  // first row of this CTA's half
+      const int n0 = c.J * TT;
       // row-mapped output: this thread's row of D (= C), and its first C values, loaded
       // before the accumulator is ready
       const bool rowmap = c.p == P.rmo.prob;
@@ -629,10 +688,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         const int tn = tile + npairs;
         int sn = seg;
         const TileCoord nc = tn < P.total_tiles ? decode_tile(P, tn, &sn) : c;
-        const bool pf = tn < P.total_tiles && nc.p == c.p && nc.I * 256 + (int)rank * TM + r < P.rmo.rows;
+        const bool pf = tn < P.total_tiles && nc.p == c.p && nc.I * TT + (int)rank * TM + r < P.rmo.rows;
         long long wr = 0, wn = 0;
         if (m0 + r < P.rmo.rows) wr = P.rmo.map[(long long)c.b * P.rmo.map_stride + m0 + r];
-        if (pf) wn = P.rmo.map[(long long)nc.b * P.rmo.map_stride + nc.I * 256 + (int)rank * TM + r];
+        if (pf) wn = P.rmo.map[(long long)nc.b * P.rmo.map_stride + nc.I * TT + (int)rank * TM + r];
         if (m0 + r < P.rmo.rows)
           rm_row = static_cast<uint16_t*>(P.rmo.ptr) + (long long)c.b * P.rmo.stride + wr * P.rmo.ld;
         rowmap_load(cw_next, rm_has_c ? rm_row : nullptr, n0 + half * 32, rm_cols);
@@ -640,7 +699,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           const uint16_t* nrow = static_cast<const uint16_t*>(P.rmo.ptr) + (long long)nc.b * P.rmo.stride + wn * P.rmo.ld;
 #pragma unroll
           for (int ch = 0; ch < NCHUNK; ++ch) {
-            const int col = nc.J * 256 + ch * CHUNK + half * 32;
+            const int col = nc.J * TT + ch * CHUNK + half * 32;
             if (col < rm_cols) asm volatile("prefetch.global.L2 [%0];" ::"l"(nrow + col));
           }
         }
@@ -662,12 +721,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           if (ch + 1 < NCHUNK) rowmap_load(cw_next, rm_has_c ? rm_row : nullptr, n0 + (ch + 1) * CHUNK + half * 32, rm_cols);
           uint32_t v[32];
           __syncwarp();
-          tmem_ld_32x32b_x32(tmem_base + acc * TN + ch * CHUNK + half * 32 + ((uint32_t)(quarter * 32) << 16), v);
+          tmem_ld_32x32b_x32(tmem_base + acc * TT + ch * CHUNK + half * 32 + ((uint32_t)(quarter * 32) << 16), v);
           tmem_ld_wait();
           if (ch == NCHUNK - 1) {
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(acc ? tempty_leader1 : tempty_leader0);
+            if (lane == 0) acc_release<CG>(acc ? tempty_leader1 : tempty_leader0);
           }
           float2 o[16];
 #pragma unroll
@@ -698,13 +757,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         uint8_t* sd = SD + (gc % OUT_BUFS) * CHUNK_BYTES;
         uint32_t v[32];
         __syncwarp();
-        tmem_ld_32x32b_x32(tmem_base + acc * TN + ch * CHUNK + half * 32 + ((uint32_t)(quarter * 32) << 16), v);
+        tmem_ld_32x32b_x32(tmem_base + acc * TT + ch * CHUNK + half * 32 + ((uint32_t)(quarter * 32) << 16), v);
         tmem_ld_wait();
         if (ch == NCHUNK - 1) {
           // the accumulator has been read: release it to the leader's MMA issuer
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(acc ? tempty_leader1 : tempty_leader0);
+          if (lane == 0) acc_release<CG>(acc ? tempty_leader1 : tempty_leader0);
         }
         float2 o[16];  // the row's 32 values, in pairs
 #pragma unroll
@@ -830,10 +889,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  cluster_sync_all();  // no remote arrival or peer MMA can still target this CTA
+  if constexpr (CG == 2) cluster_sync_all();  // no remote arrival or peer MMA can still target this CTA
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc2(tmem_base, TMEM_COLS);
+    if constexpr (CG == 2)
+      tmem_dealloc2(tmem_base, TMEM_COLS);
+    else
+      tmem_dealloc(tmem_base, TMEM_COLS);
   }
 }
 
@@ -895,32 +957,52 @@ int device_sm_count() {
   return cached[dev];
 }
 
-// Number of CTA pairs of the GEMM kernel that can be resident at once (and the one-time
-// shared-memory opt-in).
-template <class L>
-static int resident_pairs(std::string* err) {
+// Number of CTA groups (pairs for CG = 2, single CTAs for CG = 1) of the GEMM kernel that can
+// be resident at once, and the one-time shared-memory opt-in. A persistent launch never asks
+// for more: its groups wait on one another's completion counters.
+template <class L, int CG>
+static int resident_groups(std::string* err) {
   static int cached[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) dev = 0;
   if (cached[dev]) return cached[dev];
-  cudaError_t e = cudaFuncSetAttribute(tc::gemm_kernel<L>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_BYTES);
+  cudaError_t e =
+      cudaFuncSetAttribute(tc::gemm_kernel<L, CG>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_BYTES);
   if (e != cudaSuccess) {
     *err = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e);
     return 0;
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * (device_sm_count() / 2), 1, 1);
-  cfg.blockDim = dim3(tc::NUM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = L::SMEM_BYTES;
-  int clusters = 0;
-  e = cudaOccupancyMaxActiveClusters(&clusters, tc::gemm_kernel<L>, &cfg);
-  if (e != cudaSuccess || clusters < 1) {
-    (void)cudaGetLastError();
-    clusters = device_sm_count() / 2;
+  int groups = 0;
+  if constexpr (CG == 2) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * (device_sm_count() / 2), 1, 1);
+    cfg.blockDim = dim3(tc::NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = L::SMEM_BYTES;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaOccupancyMaxActiveClusters(&groups, tc::gemm_kernel<L, CG>, &cfg);
+    if (e != cudaSuccess || groups < 1) {
+      (void)cudaGetLastError();
+      groups = device_sm_count() / 2;
+    }
+  } else {
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tc::gemm_kernel<L, CG>, tc::NUM_THREADS,
+                                                      L::SMEM_BYTES);
+    if (e != cudaSuccess || per_sm < 1) {
+      (void)cudaGetLastError();
+      per_sm = 1;
+    }
+    groups = per_sm * device_sm_count();
   }
-  cached[dev] = clusters;
-  return clusters;
+  cached[dev] = groups;
+  return groups;
 }
 
 struct Segment {
@@ -982,10 +1064,16 @@ int gemm_launch_tc(const GemmOp* ops, int nops, const uint32_t* dep_masks, int* 
     *err = "internal: bad number of products in one launch";
     return GNS_ERR_INVALID;
   }
-  const int pairs_deep = resident_pairs<DeepPlan>(err);
-  if (pairs_deep < 1) return GNS_ERR_CUDA;
-  const int pairs_shallow = resident_pairs<ShallowPlan>(err);
-  if (pairs_shallow < 1) return GNS_ERR_CUDA;
+  // CTA-group size: single CTAs with 128 x 128 tiles when every product has at most 128
+  // rows (GNS_CTA_GROUP=1 or 2 in the environment overrides, a tuning knob)
+  int64_t max_m = 0;
+  for (int i = 0; i < nops; ++i) max_m = std::max<int64_t>(max_m, ops[i].M);
+  int cg = max_m <= 128 ? 1 : 2;
+  if (const char* env = getenv("GNS_CTA_GROUP")) {
+    if (env[0] == '1' && env[1] == 0) cg = 1;
+    if (env[0] == '2' && env[1] == 0) cg = 2;
+  }
+  const int tile = 128 * cg;
   Params P;
   memset(&P, 0, sizeof(P));
   int tiles = 0;
@@ -1038,8 +1126,8 @@ int gemm_launch_tc(const GemmOp* ops, int nops, const uint32_t* dep_masks, int* 
     pr.a_mn = o.a_mn;
     pr.b_mn = o.b_mn;
     pr.kblocks = (int)((o.K + TK - 1) / TK);
-    pr.tiles_m = (int)((o.M + 255) / 256);
-    pr.tiles_n = (int)((o.N + 255) / 256);
+    pr.tiles_m = (int)((o.M + tile - 1) / tile);
+    pr.tiles_n = (int)((o.N + tile - 1) / tile);
     pr.sym = o.sym;
     const long long tpm = o.sym ? (long long)pr.tiles_m * (pr.tiles_m + 1) / 2 : (long long)pr.tiles_m * pr.tiles_n;
     if (tpm * o.batch + tiles > (long long)INT32_MAX) {
@@ -1109,14 +1197,28 @@ int gemm_launch_tc(const GemmOp* ops, int nops, const uint32_t* dep_masks, int* 
   for (int i = 0; i < nops; ++i)
     slices += (long long)P.prob[i].kblocks * P.prob[i].tiles_per_mat * ops[i].batch;
   const bool deep = slices <= (long long)DEEP_MAX_SLICES_PER_TILE * tiles;
-  const int pairs = std::min(tiles, deep ? pairs_deep : pairs_shallow);
+  const int resident = cg == 2 ? (deep ? resident_groups<DeepPlan, 2>(err) : resident_groups<ShallowPlan, 2>(err))
+                                : (deep ? resident_groups<DeepPlan, 1>(err) : resident_groups<ShallowPlan, 1>(err));
+  if (resident < 1) return GNS_ERR_CUDA;
+  const int groups = std::min(tiles, resident);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(cg * groups, 1, 1);
   cfg.blockDim = dim3(NUM_THREADS, 1, 1);
   cfg.dynamicSmemBytes = deep ? DeepPlan::SMEM_BYTES : ShallowPlan::SMEM_BYTES;
   cfg.stream = static_cast<cudaStream_t>(stream);
-  cudaError_t e = deep ? cudaLaunchKernelEx(&cfg, gemm_kernel<DeepPlan>, P)
-                       : cudaLaunchKernelEx(&cfg, gemm_kernel<ShallowPlan>, P);
+  if (cg == 2) {
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  cudaError_t e = cg == 2 ? (deep ? cudaLaunchKernelEx(&cfg, gemm_kernel<DeepPlan, 2>, P)
+                                  : cudaLaunchKernelEx(&cfg, gemm_kernel<ShallowPlan, 2>, P))
+                          : (deep ? cudaLaunchKernelEx(&cfg, gemm_kernel<DeepPlan, 1>, P)
+                                  : cudaLaunchKernelEx(&cfg, gemm_kernel<ShallowPlan, 1>, P));
   if (e != cudaSuccess) {
     *err = std::string("tcgen05 GEMM launch: ") + cudaGetErrorString(e);
     return GNS_ERR_CUDA;
