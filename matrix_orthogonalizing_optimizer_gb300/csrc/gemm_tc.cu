@@ -75,7 +75,8 @@ struct Geo {
   static constexpr int TMEM_COLS = 2 * TILE;        // two fp32 accumulators
   static constexpr int KSH = CG == 2 ? 2 : 1;       // log2 of 64-wide K slices per tile edge
 };
-constexpr int BAR_BYTES = 512;
+constexpr int BAR_BYTES = 1024;
+constexpr int RM_IDX_OFF = 512;  // in the barrier area: W row of each tile row (row-mapped outputs)
 
 // Shared-memory plan of a kernel with STAGES operand stages and a ring of C_BUFS C chunks.
 // Two plans are compiled: a deep operand ring (6 stages, 1 C chunk) pays on launches of
@@ -91,7 +92,8 @@ struct Plan {
   static constexpr int OFF_BAR = OFF_SD + OUT_BUFS * CHUNK_BYTES;
   static constexpr int SMEM_BYTES = 1024 + OFF_BAR + BAR_BYTES;
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-  static_assert((2 * STAGES + 4 + 2 * C_BUFS) * 8 + 16 <= BAR_BYTES, "barrier area");
+  static_assert((2 * STAGES + 4 + 2 * C_BUFS) * 8 + 16 <= RM_IDX_OFF, "barrier area");
+  static_assert(RM_IDX_OFF + TM * 4 <= BAR_BYTES, "row-map area");
 };
 using DeepPlan = Plan<6, 1>;
 using ShallowPlan = Plan<4, 4>;
@@ -363,42 +365,60 @@ __device__ __forceinline__ void acc_release(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-// The 32 16-bit values of a row-mapped C row at columns [col, col + 32), two per word (zero
-// beyond `cols` or without a row); 16-byte loads when the whole range is inside the row.
-__device__ __forceinline__ void rowmap_load(uint32_t (&cw)[16], const uint16_t* row, int col, int cols) {
-  if (!row) {
+// Row-mapped chunks: 128 rows x 64 columns of W whose rows are rm_idx[0..127] (-1: none).
+// Thread t of the 256 epilogue threads moves the 16-byte vectors v = t + 256 i (i < 4): row
+// v / 8, columns 8 (v % 8) .. +7 of the chunk, so a warp covers four whole 128-byte row
+// segments per access. Vectors past the matrix's columns are partial (zero filled on load,
+// not written on store).
+__device__ __forceinline__ void rowmap_chunk_load(uint4 (&cv)[4], const uint16_t* base, long long ld,
+                                                  const int* rm_idx, int t, int col0, int cols) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) cw[i] = 0u;
-  } else if (col + 32 <= cols) {
-    const uint4* p = reinterpret_cast<const uint4*>(row + col);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint4 w = p[q];
-      cw[4 * q] = w.x;
-      cw[4 * q + 1] = w.y;
-      cw[4 * q + 2] = w.z;
-      cw[4 * q + 3] = w.w;
+  for (int i = 0; i < 4; ++i) {
+    const int v = t + 256 * i;
+    const int row = v >> 3;
+    const int col = col0 + (v & 7) * 8;
+    const int wr = rm_idx[row];
+    uint4 w = make_uint4(0u, 0u, 0u, 0u);
+    if (wr >= 0 && col < cols) {
+      const uint16_t* q = base + (long long)wr * ld + col;
+      if (col + 8 <= cols) {
+        w = *reinterpret_cast<const uint4*>(q);
+      } else {
+        uint32_t e[4] = {0u, 0u, 0u, 0u};
+        for (int j = 0; j < 8 && col + j < cols; ++j) e[j >> 1] |= (uint32_t)q[j] << (16 * (j & 1));
+        w = make_uint4(e[0], e[1], e[2], e[3]);
+      }
     }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const uint32_t lo = col + 2 * i < cols ? row[col + 2 * i] : 0u;
-      const uint32_t hi = col + 2 * i + 1 < cols ? row[col + 2 * i + 1] : 0u;
-      cw[i] = lo | (hi << 16);
-    }
+    cv[i] = w;
   }
 }
 
-__device__ __forceinline__ void rowmap_store(uint16_t* row, int col, int cols, const uint32_t (&pk)[16]) {
-  if (!row) return;
-  if (col + 32 <= cols) {
-    uint4* p = reinterpret_cast<uint4*>(row + col);
+__device__ __forceinline__ void rowmap_chunk_stage(uint8_t* sd, const uint4 (&cv)[4], int t) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) p[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-  } else {
+  for (int i = 0; i < 4; ++i) {
+    const int v = t + 256 * i;
+    *reinterpret_cast<uint4*>(sd + off_direct(v >> 3, (v & 7) * 8)) = cv[i];
+  }
+}
+
+__device__ __forceinline__ void rowmap_chunk_store(const uint8_t* sd, void* ptr, long long boff, long long ld,
+                                                   const int* rm_idx, int t, int col0, int cols) {
+  uint16_t* const base = static_cast<uint16_t*>(ptr) + boff;
 #pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (col + j < cols) row[col + j] = (uint16_t)(pk[j >> 1] >> (16 * (j & 1)));
+  for (int i = 0; i < 4; ++i) {
+    const int v = t + 256 * i;
+    const int row = v >> 3;
+    const int col = col0 + (v & 7) * 8;
+    const int wr = rm_idx[row];
+    if (wr < 0 || col >= cols) continue;
+    const uint4 w = *reinterpret_cast<const uint4*>(sd + off_direct(row, (v & 7) * 8));
+    uint16_t* q = base + (long long)wr * ld + col;
+    if (col + 8 <= cols) {
+      *reinterpret_cast<uint4*>(q) = w;
+    } else {
+      const uint32_t e[4] = {w.x, w.y, w.z, w.w};
+      for (int j = 0; j < 8 && col + j < cols; ++j) q[j] = (uint16_t)(e[j >> 1] >> (16 * (j & 1)));
+    }
   }
 }
 
@@ -676,31 +696,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
       const float gamma = pr.gamma;
       const int m0 = c.I * TT + (int)rank * TM;  // first row of this CTA's half
       const int n0 = c.J * TT;
-      // row-mapped output: this thread's row of D (= C), and its first C values, loaded
-      // before the accumulator is ready
+      // row-mapped output: the W rows of this tile's rows go to shared memory (the staging
+      // buffer is free once the previous stores have read it), the first chunk's W loads are
+      // issued, and the rows of this CTA's next tile are fetched into L2
       const bool rowmap = c.p == P.rmo.prob;
-      uint16_t* rm_row = nullptr;
       const int rm_cols = P.rmo.cols, rm_has_c = P.rmo.has_c;
-      uint32_t cw_next[16];
+      int* const rm_idx = reinterpret_cast<int*>(smem + OFF_BAR + RM_IDX_OFF);
+      const uint16_t* const rm_base =
+          rowmap ? static_cast<const uint16_t*>(P.rmo.ptr) + (long long)c.b * P.rmo.stride : nullptr;
+      uint4 cvec[4];  // this thread's four 16-byte vectors of the next chunk's C
       if (rowmap) {
-        // this tile's row and the next tile's (its row segments are fetched into L2 now, a
-        // whole tile before their loads: the epilogue of a row-mapped tile waits on them)
+        if (et == 0) bulk_wait_read<0>();
+        if (et < TM) rm_idx[et] = m0 + et < P.rmo.rows ? P.rmo.map[(long long)c.b * P.rmo.map_stride + m0 + et] : -1;
+        named_bar_sync(1, EPI_THREADS);
+        if (rm_has_c) rowmap_chunk_load(cvec, rm_base, P.rmo.ld, rm_idx, et, n0, rm_cols);
         const int tn = tile + npairs;
         int sn = seg;
-        const TileCoord nc = tn < P.total_tiles ? decode_tile(P, tn, &sn) : c;
-        const bool pf = tn < P.total_tiles && nc.p == c.p && nc.I * TT + (int)rank * TM + r < P.rmo.rows;
-        long long wr = 0, wn = 0;
-        if (m0 + r < P.rmo.rows) wr = P.rmo.map[(long long)c.b * P.rmo.map_stride + m0 + r];
-        if (pf) wn = P.rmo.map[(long long)nc.b * P.rmo.map_stride + nc.I * TT + (int)rank * TM + r];
-        if (m0 + r < P.rmo.rows)
-          rm_row = static_cast<uint16_t*>(P.rmo.ptr) + (long long)c.b * P.rmo.stride + wr * P.rmo.ld;
-        rowmap_load(cw_next, rm_has_c ? rm_row : nullptr, n0 + half * 32, rm_cols);
-        if (pf && rm_has_c) {
-          const uint16_t* nrow = static_cast<const uint16_t*>(P.rmo.ptr) + (long long)nc.b * P.rmo.stride + wn * P.rmo.ld;
-#pragma unroll
-          for (int ch = 0; ch < NCHUNK; ++ch) {
-            const int col = nc.J * TT + ch * CHUNK + half * 32;
-            if (col < rm_cols) asm volatile("prefetch.global.L2 [%0];" ::"l"(nrow + col));
+        if (rm_has_c && tn < P.total_tiles) {
+          const TileCoord nc = decode_tile(P, tn, &sn);
+          const int nrow = nc.I * TT + (int)rank * TM + (et >> 1);
+          if (nc.p == c.p && nrow < P.rmo.rows) {
+            const long long wn = P.rmo.map[(long long)nc.b * P.rmo.map_stride + nrow];
+            const uint16_t* q = static_cast<const uint16_t*>(P.rmo.ptr) + (long long)nc.b * P.rmo.stride +
+                                wn * P.rmo.ld + nc.J * TT + (et & 1) * (TT / 2);
+            for (int o = 0; o < TT / 2 && nc.J * TT + (et & 1) * (TT / 2) + o < rm_cols; o += 64)
+              asm volatile("prefetch.global.L2 [%0];" ::"l"(q + o));
           }
         }
       }
@@ -713,12 +733,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
       float dv = 0.f;
       bool bad = false;
       if (rowmap) {
-        // each thread reads, updates and writes its own row segment: no staging, no barriers
+        // per chunk: W rows staged in shared memory by whole-row 16-byte loads, every thread
+        // updates its own row segment there (fp32, one rounding), whole-row stores back to W
         for (int ch = 0; ch < NCHUNK; ++ch) {
-          uint32_t cw[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) cw[i] = cw_next[i];
-          if (ch + 1 < NCHUNK) rowmap_load(cw_next, rm_has_c ? rm_row : nullptr, n0 + (ch + 1) * CHUNK + half * 32, rm_cols);
+          const int col0 = n0 + ch * CHUNK;
+          if (rm_has_c) {
+            rowmap_chunk_stage(SD, cvec, et);
+            named_bar_sync(1, EPI_THREADS);
+            if (ch + 1 < NCHUNK) rowmap_chunk_load(cvec, rm_base, P.rmo.ld, rm_idx, et, col0 + CHUNK, rm_cols);
+          }
           uint32_t v[32];
           __syncwarp();
           tmem_ld_32x32b_x32(tmem_base + acc * TT + ch * CHUNK + half * 32 + ((uint32_t)(quarter * 32) << 16), v);
@@ -736,7 +759,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
 #pragma unroll
             for (int i = 0; i < 16; ++i) o[i] = __fmul2_rn(a2, o[i]);
           }
-          if (rm_has_c) axpy_h16x2(o, cw, beta, d_f16);
+          if (rm_has_c) {
+            uint32_t cw[16];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const uint4 w = *reinterpret_cast<const uint4*>(SD + off_direct(r, half * 32 + q * 8));
+              cw[4 * q] = w.x;
+              cw[4 * q + 1] = w.y;
+              cw[4 * q + 2] = w.z;
+              cw[4 * q + 3] = w.w;
+            }
+            axpy_h16x2(o, cw, beta, d_f16);
+          }
           if (check_finite) {
             float2 z = make_float2(0.f, 0.f);
 #pragma unroll
@@ -745,7 +779,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
           }
           uint32_t pk[16];
           pack_h16x2(o, pk, d_f16);
-          rowmap_store(rm_row, n0 + ch * CHUNK + half * 32, rm_cols, pk);
+          // each thread overwrites exactly the values it read
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4*>(SD + off_direct(r, half * 32 + q * 8)) =
+                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          named_bar_sync(1, EPI_THREADS);
+          rowmap_chunk_store(SD, P.rmo.ptr, (long long)c.b * P.rmo.stride, P.rmo.ld, rm_idx, et, col0, rm_cols);
+          named_bar_sync(1, EPI_THREADS);  // the buffer is free for the next chunk
         }
         if (pr.publish) {
           // the tile's stores are visible before its completion is published

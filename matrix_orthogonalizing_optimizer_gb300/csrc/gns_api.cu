@@ -107,10 +107,26 @@ int gemm_program(gns_dtype dt, const GemmOp* ops, int nops, int* counters, int32
   for (int base = 0; base < nops; base += kMaxProgramOps) {
     const int n = std::min(kMaxProgramOps, nops - base);
     uint32_t masks[kMaxProgramOps];
+    uint32_t closure[kMaxProgramOps];  // every op an op waits for, directly or through others
     for (int j = 0; j < n; ++j) {
       masks[j] = 0;
       for (int i = 0; i < j; ++i)
         if (op_conflict(ops[base + i], ops[base + j])) masks[j] |= 1u << i;
+      closure[j] = masks[j];
+      for (int i = 0; i < j; ++i)
+        if ((masks[j] >> i) & 1u) closure[j] |= closure[i];
+      // transitive reduction: when op k (waited for) has itself waited for op i, op i's
+      // completion for the same matrix is implied and need not be checked again
+      uint32_t red = masks[j];
+      for (int i = 0; i < j; ++i) {
+        if (!((masks[j] >> i) & 1u)) continue;
+        for (int k = i + 1; k < j; ++k)
+          if (((masks[j] >> k) & 1u) && ((closure[k] >> i) & 1u)) {
+            red &= ~(1u << i);
+            break;
+          }
+      }
+      masks[j] = red;
     }
     profile_gemm_begin(stream);
     int rc = gemm_launch_tc(ops + base, n, masks, counters, dev_status, stream, err);
