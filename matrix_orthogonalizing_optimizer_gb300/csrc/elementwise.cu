@@ -154,6 +154,27 @@ __global__ void momentum_kernel(bf16* M, long long ldm, long long sm, const bf16
   }
 }
 
+// inv[b] = 1 / (sqrt(sum of the npart partials) + eps) for many partials, one block of 256
+// threads per matrix: thread t sums a contiguous run of partials in order (fp64), the runs
+// are combined by a fixed tree.
+__global__ void __launch_bounds__(256) finalize_norm_many_kernel(const float* partials, int npart, float eps,
+                                                                 float* inv) {
+  __shared__ double ws[8];
+  const int b = blockIdx.x;
+  const int per = (npart + 255) / 256;
+  const int p0 = threadIdx.x * per;
+  double s = 0.0;
+  for (int p = p0; p < p0 + per && p < npart; ++p) s += (double)partials[(long long)b * npart + p];
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if ((threadIdx.x & 31) == 0) ws[threadIdx.x >> 5] = s;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double t = 0.0;
+    for (int w = 0; w < 8; ++w) t += ws[w];
+    inv[b] = (float)(1.0 / (sqrt(t) + (double)eps));
+  }
+}
+
 // inv[b] = 1 / (sqrt(sum of partials) + eps), partials summed in order in fp64.
 __global__ void finalize_norm_kernel(const float* partials, int npart, int count, float eps, float* inv) {
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
@@ -701,11 +722,13 @@ __global__ void gather_rows_kernel(bf16* M, long long ldm, long long sm, const i
 constexpr int COL_TILE_ROWS = 64;
 
 // X[b][i][j] = M[b][j][idx[b*k + i]] (columns of M become rows of X), with the decay
-// M[b][j][idx[i]] = bf16(mu * M) when asked; 32 x TJ tiles staged in shared memory.
+// M[b][j][idx[i]] = bf16(mu * M) when asked; 32 x TJ tiles staged in shared memory. With
+// bpart, each block also stores the sum of squares of the values it gathered, in a fixed
+// order (per thread, then the fixed block tree), at bpart[b * blocks + its index].
 template <int TJ>
 __global__ void __launch_bounds__(256) gather_cols_kernel(bf16* M, long long ldm, long long sm, const int* idx, int k,
                                                           int rows, bf16* X, long long ldx, long long sx, int decay,
-                                                          float mu) {
+                                                          float mu, float* bpart) {
   // 32 selected columns x TJ rows per block: each thread issues its TJ / 8 loads before
   // using any of them
   __shared__ bf16 tile[TJ][33];
@@ -728,6 +751,14 @@ __global__ void __launch_bounds__(256) gather_cols_kernel(bf16* M, long long ldm
     const int j = j0 + ty + 8 * r;
     if (decay && iv && j < rows) col[(long long)j * ldm] = f_to_bf16(__fmul_rn(mu, bf16_to_f(v[r])));
     tile[ty + 8 * r][tx] = v[r];
+  }
+  if (bpart) {
+    float q = 0.f;
+#pragma unroll
+    for (int r = 0; r < R; ++r) q = fmaf(bf16_to_f(v[r]), bf16_to_f(v[r]), q);
+    q = block_sum_256(q);
+    if (threadIdx.x == 0)
+      bpart[(long long)b * gridDim.x * gridDim.y + (long long)blockIdx.y * gridDim.x + blockIdx.x] = q;
   }
   __syncthreads();
   for (int ii = ty; ii < 32; ii += 8) {
@@ -841,6 +872,38 @@ __global__ void __launch_bounds__(256) scatter_update_cols_kernel(bf16* W, long 
   for (int r = 0; r < R; ++r) {
     const int j = j0 + ty + 8 * r;
     if (j < len) col[(long long)j * ldw] = f_to_bf16(fmaf(alpha, tile[tx][ty + 8 * r], beta * bf16_to_f(w[r])));
+  }
+}
+
+// The same update from the transpose of O (OT[j][i] = O[i][j], len x k): W[j][idx[i]] =
+// bf16(beta W + alpha OT[j][i]). A block covers 32 selected columns x TJ rows; a warp reads
+// 32 consecutive entries of an OT row and the 32 selected entries of the same W row, and
+// each thread issues all its loads of W and OT before its first update.
+template <int TJ>
+__global__ void __launch_bounds__(256) scatter_update_cols_t_kernel(bf16* W, long long ldw, long long sw,
+                                                                    const bf16* OT, long long ldo, long long so,
+                                                                    const int* idx, int k, int len, float alpha,
+                                                                    float beta) {
+  constexpr int R = TJ / 8;
+  const int b = blockIdx.z;
+  const int i = blockIdx.x * 32 + (threadIdx.x & 31);
+  const int j0 = blockIdx.y * TJ + (threadIdx.x >> 5);
+  if (i >= k) return;
+  bf16* col = W + (long long)b * sw + idx[(long long)b * k + i];
+  const bf16* oc = OT + (long long)b * so + i;
+  bf16 w[R], o[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int j = j0 + 8 * r;
+    if (j < len) {
+      w[r] = col[(long long)j * ldw];
+      o[r] = oc[(long long)j * ldo];
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int j = j0 + 8 * r;
+    if (j < len) col[(long long)j * ldw] = f_to_bf16(fmaf(alpha, bf16_to_f(o[r]), beta * bf16_to_f(w[r])));
   }
 }
 
@@ -1170,9 +1233,18 @@ int launch_momentum(const MatRef& M, const MatRef& G, int64_t count, float mu, i
   return check_launch("momentum", err);
 }
 
-int launch_finalize_norm(const float* partials, int64_t count, float eps, float* inv, void* stream, std::string* err) {
-  finalize_norm_kernel<<<(unsigned)((count + 127) / 128), 128, 0, S(stream)>>>(partials, NPART, (int)count, eps, inv);
+int launch_finalize_norm(const float* partials, int64_t count, float eps, float* inv, void* stream, std::string* err,
+                         int64_t npart) {
+  if (npart <= NPART)
+    finalize_norm_kernel<<<(unsigned)((count + 127) / 128), 128, 0, S(stream)>>>(partials, (int)npart, (int)count,
+                                                                                  eps, inv);
+  else
+    finalize_norm_many_kernel<<<(unsigned)count, 256, 0, S(stream)>>>(partials, (int)npart, eps, inv);
   return check_launch("finalize_norm", err);
+}
+
+int64_t gather_cols_blocks(int64_t k, int64_t rows) {
+  return ((k + 31) / 32) * ((rows + COL_TILE_ROWS - 1) / COL_TILE_ROWS);
 }
 
 int launch_frac_add_keys(const MatRef& M, const MatRef& G, int64_t count, int trans, unsigned long long* keys,
@@ -1243,7 +1315,7 @@ int launch_select_topk(unsigned long long* keys, const int* nf, int64_t n, int64
 }
 
 int launch_gather(const MatRef& M, int64_t count, int trans, const int* idx, int64_t k, const MatRef& X,
-                  float* partials, void* stream, std::string* err, bool decay, float mu) {
+                  float* partials, void* stream, std::string* err, bool decay, float mu, float* bpart) {
   if (!trans) {
     dim3 grid(NPART, (unsigned)count);
     gather_rows_kernel<<<grid, 256, 0, S(stream)>>>(static_cast<bf16*>(M.ptr), M.ld, M.stride, idx, (int)k,
@@ -1253,8 +1325,8 @@ int launch_gather(const MatRef& M, int64_t count, int trans, const int* idx, int
     dim3 grid((unsigned)((k + 31) / 32), (unsigned)((M.rows + COL_TILE_ROWS - 1) / COL_TILE_ROWS), (unsigned)count);
     gather_cols_kernel<COL_TILE_ROWS><<<grid, 256, 0, S(stream)>>>(static_cast<bf16*>(M.ptr), M.ld, M.stride, idx, (int)k,
                                                     (int)M.rows, static_cast<bf16*>(X.ptr), X.ld, X.stride,
-                                                    decay ? 1 : 0, mu);
-    if (partials) {
+                                                    decay ? 1 : 0, mu, bpart);
+    if (partials && !bpart) {
       MatRef xs = X;
       xs.rows = k;
       xs.cols = M.rows;
@@ -1294,6 +1366,16 @@ int launch_scatter_update(const MatRef& W, const MatRef& O, int64_t count, int t
                                                             (int)k, (int)len, alpha, beta);
   }
   return check_launch("scatter_update", err);
+}
+
+int launch_scatter_update_cols_t(const MatRef& W, const MatRef& OT, int64_t count, const int* idx, int64_t k,
+                                 float alpha, float beta, void* stream, std::string* err) {
+  const int64_t len = OT.rows;
+  dim3 grid((unsigned)((k + 31) / 32), (unsigned)((len + COL_TILE_ROWS - 1) / COL_TILE_ROWS), (unsigned)count);
+  scatter_update_cols_t_kernel<COL_TILE_ROWS><<<grid, 256, 0, S(stream)>>>(
+      static_cast<bf16*>(W.ptr), W.ld, W.stride, static_cast<const bf16*>(OT.ptr), OT.ld, OT.stride, idx, (int)k,
+      (int)len, alpha, beta);
+  return check_launch("scatter_update_cols_t", err);
 }
 
 int launch_row_sumsq(const MatRef& X, int64_t k, int64_t cols, int64_t count, float* s, void* stream,

@@ -16,7 +16,12 @@ constexpr int MAX_SELECT_N = 65536; // largest selection dimension (shared-memor
 int launch_sumsq(gns_dtype dt, const MatRef& X, int64_t count, float* partials, void* stream, std::string* err);
 int launch_momentum(const MatRef& M, const MatRef& G, int64_t count, float mu, int mode, float* partials,
                     void* stream, std::string* err);
-int launch_finalize_norm(const float* partials, int64_t count, float eps, float* inv, void* stream, std::string* err);
+// npart: partials per matrix (NPART, or a gather's per-block sums, gather_cols_blocks).
+int launch_finalize_norm(const float* partials, int64_t count, float eps, float* inv, void* stream, std::string* err,
+                         int64_t npart = NPART);
+// Blocks per matrix of the column gather of a tall matrix (k selected columns, rows rows):
+// the per-block sums of squares it stores with bpart.
+int64_t gather_cols_blocks(int64_t k, int64_t rows);
 int launch_frac_add_keys(const MatRef& M, const MatRef& G, int64_t count, int trans, unsigned long long* keys,
                          int* nf, void* stream, std::string* err);
 int launch_keys_only(const MatRef& M, int64_t count, int trans, unsigned long long* keys, int* nf, void* stream,
@@ -24,14 +29,22 @@ int launch_keys_only(const MatRef& M, int64_t count, int trans, unsigned long lo
 int launch_select_topk(unsigned long long* keys, const int* nf, int64_t n, int64_t k, int64_t count, int* idx,
                        void* stream, std::string* err);
 // decay: also M[S] <- bf16(mu * M[S]) in the same pass (Algorithm 4's error feedback).
+// Columns of a tall M (trans): with bpart (gather_cols_blocks(k, rows) floats per matrix) the
+// gather stores its per-block sums of squares there instead of filling partials by a second
+// pass over X.
 int launch_gather(const MatRef& M, int64_t count, int trans, const int* idx, int64_t k, const MatRef& X,
-                  float* partials, void* stream, std::string* err, bool decay = false, float mu = 1.f);
+                  float* partials, void* stream, std::string* err, bool decay = false, float mu = 1.f,
+                  float* bpart = nullptr);
 // flags: count * n ints of scratch (n = rows, or cols when trans).
 int launch_scale_unselected(const MatRef& W, int64_t count, int trans, const int* idx, int64_t k, float factor,
                             int* flags, void* stream, std::string* err);
 // rs (nullable): per-row scale of O (NorMuon); idx NULL: every row, in order.
 int launch_scatter_update(const MatRef& W, const MatRef& O, int64_t count, int trans, const int* idx, int64_t k,
                           float alpha, float beta, void* stream, std::string* err, const float* rs = nullptr);
+// Columns idx of a tall W from the transpose of O (OT: len x k, len = rows of W):
+// W[j][idx[i]] <- bf16(beta W + alpha OT[j][i]).
+int launch_scatter_update_cols_t(const MatRef& W, const MatRef& OT, int64_t count, const int* idx, int64_t k,
+                                 float alpha, float beta, void* stream, std::string* err);
 // y_dt: type of Y when it differs from W's (bf16 W with fp16 Y); -1 = dt.
 int launch_axpby(gns_dtype dt, const MatRef& W, const MatRef& Y, int64_t count, float alpha, float beta, void* stream,
                  std::string* err, gns_dtype y_dt = (gns_dtype)-1);

@@ -593,6 +593,8 @@ struct MuonBufs {
   float* s = nullptr;                  // NorMuon / RowNorm: row sums of squares
   float* r = nullptr;                  // and row scales
   float* part = nullptr;               // RowNorm of a tall matrix: column partial sums
+  float* colpart = nullptr;            // frac, tall: per-block sums of squares of the column gather
+  int64_t ncolpart = 0;
 };
 
 static void plan_muon(Arena& a, const GroupShape& sh, const gns_muon_params& mp, const gns_ns_params* ns,
@@ -629,10 +631,18 @@ static void plan_muon(Arena& a, const GroupShape& sh, const gns_muon_params& mp,
   mb->keys = static_cast<unsigned long long*>(a.take(sizeof(unsigned long long) * KEY_DIGITS * n * B));
   mb->nf = static_cast<int*>(a.take(sizeof(int) * n * B));
   mb->idx = static_cast<int*>(a.take(sizeof(int) * k * B));
+  if (sh.trans) {
+    mb->ncolpart = gather_cols_blocks(k, sh.rows);
+    mb->colpart = static_cast<float*>(a.take(sizeof(float) * B * mb->ncolpart));
+  }
   mb->xs = ws_mat(a, B, round_up(k, PAD), k, m, ldm, 2);
   // O gets its own buffer only where the update cannot ride on the last product's epilogue:
-  // NorMuon (its row statistics need O first) and the columns of a tall matrix
-  if (normuon || sh.trans) mb->os = ws_mat(a, B, k, k, m, ldm, 2);
+  // NorMuon (its row statistics need O first) and the columns of a tall matrix, where the
+  // Muon flavour stores O transposed (m x k) for the column scatter
+  if (normuon)
+    mb->os = ws_mat(a, B, k, k, m, ldm, 2);
+  else if (sh.trans)
+    mb->os = ws_mat(a, B, m, m, k, round_up(k, 8), 2);
   if (mb->nsdt == GNS_F16) mb->x16 = ws_mat(a, B, round_up(k, PAD), k, m, ldm, 2);
   plan_gram(a, B, k, m, mb->nsdt, ns, &mb->gb, true);
   if (normuon) {
@@ -1050,9 +1060,11 @@ int gns_muon_step(const gns_batch* W, const gns_batch* G, const gns_batch* M, co
     if ((rc = launch_select_topk(mb.keys, mb.nf, s.n, k, s.B, mb.idx, stream, &err))) return fail(rc, err);
     // gather M[S, :] and its Frobenius norm; the error feedback (M[S] <- mu M[S]) rides
     // on the same pass: M[S] is not read again
-    if ((rc = launch_gather(mm, s.B, s.trans, mb.idx, k, mb.xs, mb.gb.partials, stream, &err, true, mu)))
+    if ((rc = launch_gather(mm, s.B, s.trans, mb.idx, k, mb.xs, mb.gb.partials, stream, &err, true, mu, mb.colpart)))
       return fail(rc, err);
-    if ((rc = launch_finalize_norm(mb.gb.partials, s.B, ns->eps, mb.gb.inv, stream, &err))) return fail(rc, err);
+    if ((rc = s.trans ? launch_finalize_norm(mb.colpart, s.B, ns->eps, mb.gb.inv, stream, &err, mb.ncolpart)
+                      : launch_finalize_norm(mb.gb.partials, s.B, ns->eps, mb.gb.inv, stream, &err)))
+      return fail(rc, err);
     // weight decay on the rows that are not updated below
     if (decay != 1.f && (rc = launch_scale_unselected(wm, s.B, s.trans, mb.idx, k, decay, mb.nf, stream, &err)))
       return fail(rc, err);
@@ -1079,9 +1091,16 @@ int gns_muon_step(const gns_batch* W, const gns_batch* G, const gns_batch* M, co
       fin.rms = k;
     } else {
       fin.D = mb.os;
+      fin.d_trans = normuon ? 0 : 1;  // the tall Muon flavour's column scatter reads O transposed
     }
     if ((rc = run_gram(mb.nsdt, src, s.B, k, s.m, ns, mb.gb, mb.gb.inv, fin, dev_status, stream))) return rc;
     if (fused) continue;
+    if (!normuon) {
+      // W[:, S] <- (1 - lr wd) W[:, S] - lr scale O^T, one rounding
+      if ((rc = launch_scatter_update_cols_t(wm, mb.os, s.B, mb.idx, k, step_scale, decay, stream, &err)))
+        return fail(rc, err);
+      continue;
+    }
     // NorMuon flavour: second moments of the selected rows, scaling, rescale
     if (normuon) {
       if ((rc = launch_row_sumsq(mb.os, k, s.m, s.B, mb.s, stream, &err))) return fail(rc, err);

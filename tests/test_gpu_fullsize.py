@@ -127,9 +127,12 @@ def test_fullsize_moe_experts_and_squares_gram_vs_standard():
         _properties(torch_to_f64(sq[b]), torch_to_f64(out_g[1][b]), seed=10 + b)
 
 
-def test_fullsize_fractional_quarter():
+@pytest.mark.parametrize("shape", [(32, 4096, 16384), (32, 16384, 4096)])
+def test_fullsize_fractional_quarter(shape):
+    """f = 1/4 at full size, wide (rows selected; the update in the last product's epilogue)
+    and tall (columns selected; O written transposed for the column scatter)."""
     g = _gen(303)
-    s = (32, 4096, 16384)
+    s = shape
     W = _randn(g, s, 1.0 / np.sqrt(s[2]))
     G = _randn(g, s, 1.0 / np.sqrt(s[2]))
     M = _randn(g, s, 1.0 / np.sqrt(s[2]))
@@ -144,5 +147,8 @@ def test_fullsize_fractional_quarter():
         assert len(S) == 1024
         assert np.array_equal(torch_to_bits(M[b]), M_or), "selection and error feedback bit-exact"
         dW = np.zeros_like(W_or)
-        dW[S] = 0.02 * O
+        if s[1] <= s[2]:
+            dW[S] = 0.02 * O
+        else:
+            dW[:, S] = 0.02 * O.T
         assert _w_ok(torch_to_f64(W[b]), W_or, dW) < TOL_BF16
