@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libgns.so")
-SOURCES = ["gemm_tc.cu", "gemm_simt.cu", "elementwise.cu", "gns_api.cu", "noalloc.cu"]
+SOURCES = ["gemm_tc.cu", "chain_small.cu", "gemm_simt.cu", "elementwise.cu", "gns_api.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

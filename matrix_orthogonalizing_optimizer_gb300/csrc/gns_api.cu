@@ -11,6 +11,7 @@
 #include <vector>
 
 #include "../../include/gns.h"
+#include "chain_small.h"
 #include "elementwise.h"
 #include "gemm.h"
 
@@ -271,6 +272,42 @@ struct Final {
   int check_finite = 1;
 };
 
+// Groups of small matrices (oriented X at most 128 x 512) run whole in the on-chip chain
+// kernel (chain_small.cu): one CTA per matrix, every product on one SM.
+static bool chain_ok(bool gram, gns_dtype dt, const Src& src, int64_t n, int64_t m, const gns_ns_params* ns,
+                     const Final& fin) {
+  return fin.row_map == nullptr && chain_supported(gram, dt, n, m, src.trans, ns);
+}
+
+// inv: per-matrix 1/(||X||_F + eps), or null to have the kernel sum the norm itself
+static int run_chain(bool gram, gns_dtype dt, const Src& src, int64_t B, int64_t n, int64_t m,
+                     const gns_ns_params* ns, const float* inv, const Final& fin, int32_t* st, void* stream) {
+  ChainCall c;
+  c.gram = gram;
+  c.dt = dt;
+  c.x = src.mat;
+  c.xt = src.trans;
+  c.x_user = src.user;
+  c.B = B;
+  c.n = n;
+  c.m = m;
+  c.ns = ns;
+  c.inv = src.user ? inv : nullptr;
+  c.eps = ns->eps;
+  c.D = fin.D;
+  c.d_f16 = (fin.out_dt < 0 ? dt : (gns_dtype)fin.out_dt) == GNS_F16;
+  c.d_trans = fin.d_trans;
+  c.alpha = fin.alpha;
+  c.beta = fin.beta;
+  c.has_c = fin.has_c;
+  c.check_finite = fin.check_finite;
+  c.status = st;
+  c.stream = stream;
+  std::string err;
+  const int rc = launch_chain(c, &err);
+  return rc ? fail(rc, err) : GNS_OK;
+}
+
 struct GramBufs {
   float* partials = nullptr;
   float* inv = nullptr;
@@ -358,6 +395,7 @@ static GemmOp sym_op(const MatRef& A, int a_mn, const MatRef& Bm, int b_mn, int6
 // 1/(||X||_F + eps) already computed on the stream.
 static int run_gram(gns_dtype dt, const Src& src, int64_t B, int64_t n, int64_t m, const gns_ns_params* ns,
                     const GramBufs& g, const float* inv, const Final& fin, int32_t* st, void* stream) {
+  if (chain_ok(true, dt, src, n, m, ns, fin)) return run_chain(true, dt, src, B, n, m, ns, inv, fin, st, stream);
   std::string err;
   const int64_t np = g.np;
   std::vector<GemmOp> prog;  // the whole sequence, in program order
@@ -831,7 +869,13 @@ static int ns_common(bool gram, const gns_batch* x, const gns_batch* out, int ng
     Final fin;
     fin.D = to_ref(out[gi]);
     fin.d_trans = s.trans;
-    if (gram && s.n != s.m) {
+    const bool g_alg = gram && s.n != s.m;
+    if (chain_ok(g_alg, dt, src, s.n, s.m, ns, fin)) {
+      // the norm is summed inside the kernel, from the X it holds on chip
+      if ((rc = run_chain(g_alg, dt, src, s.B, s.n, s.m, ns, nullptr, fin, st, stream))) return rc;
+      continue;
+    }
+    if (g_alg) {
       GramBufs gb;
       plan_gram(a, s.B, s.n, s.m, dt, ns, &gb, true);
       if ((rc = launch_sumsq(dt, src.mat, s.B, gb.partials, stream, &err))) return fail(rc, err);
@@ -1026,7 +1070,17 @@ int gns_muon_step(const gns_batch* W, const gns_batch* G, const gns_batch* M, co
         fin.beta = decay;
         fin.has_c = true;
       }
-      if (mb.use_std) {
+      Final fs = fin;  // the standard-NS flavour's final write
+      if (mb.use_std && !normuon) {
+        fs.D = wm;
+        fs.d_trans = s.trans;
+        fs.alpha = step_scale;
+        fs.beta = decay;
+        fs.has_c = true;
+      }
+      if (mb.use_std && chain_ok(false, mb.nsdt, src, s.n, s.m, ns, fs)) {
+        if ((rc = run_chain(false, mb.nsdt, src, s.B, s.n, s.m, ns, inv, fs, dev_status, stream))) return rc;
+      } else if (mb.use_std) {
         MatRef xt;
         if ((rc = run_std(mb.nsdt, src, s.B, s.n, s.m, ns, mb.sb, inv, normuon ? &fin : nullptr, &xt, dev_status,
                           stream)))

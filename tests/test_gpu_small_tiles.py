@@ -21,16 +21,23 @@ TOL_BF16 = 2e-2
 TOL_PRODUCT = 1e-2
 
 
-def _with_group(g, fn):
-    old = os.environ.get("GNS_CTA_GROUP")
-    os.environ["GNS_CTA_GROUP"] = str(g)
+def _with_env(env, fn):
+    old = {k: os.environ.get(k) for k in env}
+    os.environ.update(env)
     try:
         return fn()
     finally:
-        if old is None:
-            del os.environ["GNS_CTA_GROUP"]
-        else:
-            os.environ["GNS_CTA_GROUP"] = old
+        for k, v in old.items():
+            if v is None:
+                del os.environ[k]
+            else:
+                os.environ[k] = v
+
+
+def _with_group(g, fn):
+    # the tile plans themselves: groups the on-chip chain kernel would take stay on the
+    # batched tile path here
+    return _with_env({"GNS_CTA_GROUP": str(g), "GNS_CHAIN_SMALL": "0"}, fn)
 
 
 @pytest.mark.parametrize("count,n,K", [(3, 128, 512), (2, 100, 72), (2, 200, 328), (1, 384, 256), (4, 8, 24)])
@@ -66,15 +73,15 @@ def test_gram_ns_both_plans(count, rows, cols):
 
 
 def test_muon_step_small_matrices_plan1():
-    """Full Muon step (momentum, Gram NS, update in the last epilogue) on 128 x 512 matrices,
-    which take the 1-CTA plan by default."""
+    """Full Muon step (momentum, Gram NS, update in the last epilogue) on 128 x 512 matrices
+    on the 1-CTA tile plan (the chain kernel turned off)."""
     count, rows, cols = 16, 128, 512
     s = 1.0 / np.sqrt(cols)
     Wb, _ = bf16_input(72, (count, rows, cols), s, stream=0)
     Gb, _ = bf16_input(72, (count, rows, cols), s, stream=1)
     Mb, _ = bf16_input(72, (count, rows, cols), s, stream=2)
     Wt, Gt, Mt = bits_to_torch(Wb), bits_to_torch(Gb), bits_to_torch(Mb)
-    gns.muon_step(Wt, Gt, Mt, lr=0.02, momentum=0.95)
+    _with_env({"GNS_CHAIN_SMALL": "0"}, lambda: gns.muon_step(Wt, Gt, Mt, lr=0.02, momentum=0.95))
     torch.cuda.synchronize()
     Mg, Wg = torch_to_bits(Mt), torch_to_f64(Wt)
     for b in range(count):
