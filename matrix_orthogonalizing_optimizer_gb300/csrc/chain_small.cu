@@ -250,11 +250,6 @@ __device__ __forceinline__ void nn_chunks(const Ctx& x, const Op o, int g, const
   }
   const float2 k2 = make_float2(k, k), p0 = make_float2(o.p0, o.p0), p1 = make_float2(o.p1, o.p1);
   const bool qinit = EPI == E_POLY && (o.flags & F_QINIT) != 0;
-  // Q = Z + a I: the diagonal entry (r, r) gets the fp32 value plus a, rounded once (Dion3
-  // appendix B.2.3: adding a_t I to an already rounded Z would lose a_t's low bits); rows
-  // at and beyond n stay zero. Column r is local column (r mod 32) of group r / 32.
-  const bool diag_here = qinit && g == (r >> 5) && r < x.n;
-  const int dj = (r & 31) >> 3, dw = (r & 7) >> 1, dh = r & 1;
 #pragma unroll
   for (int jj = 0; jj < 4; ++jj) {
     const uint32_t cu[4] = {cw[jj].x, cw[jj].y, cw[jj].z, cw[jj].w};
@@ -273,23 +268,26 @@ __device__ __forceinline__ void nn_chunks(const Ctx& x, const Op o, int g, const
     }
     const uint32_t off = chunk_off(r, jb + jj);
     *reinterpret_cast<uint4*>(dp + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-    if (qinit) {
-      if (diag_here && jj == dj) {
+    if (qinit) *reinterpret_cast<uint4*>(qp + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  }
+  // Q = Z + a I: the diagonal entry (r, r) gets the fp32 value of Z plus a, rounded once
+  // (Dion3 appendix B.2.3: adding a_t I to an already rounded Z would lose a_t's low bits);
+  // rows at and beyond n stay zero. Column r is local column lane of group r / 32, i.e. of
+  // this group in the warps of lane quarter g (a warp-uniform test).
+  if (qinit && g == (r >> 5)) {
+    float ad = 0.f;
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          if (i == dw) {
-            const float yd = dh ? y[i].y : y[i].x;
-            const uint32_t hv = f_to_h16(yd + o.p2, F16);
-            pk[i] = dh ? ((pk[i] & 0xFFFFu) | (hv << 16)) : ((pk[i] & 0xFFFF0000u) | hv);
-          }
-      }
-      *reinterpret_cast<uint4*>(qp + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-    }
+    for (int k2i = 0; k2i < 32; ++k2i)
+      if (k2i == x.lane) ad = v[k2i];
+    const uint32_t doff = (uint32_t)(r * 128 + (((jb + (x.lane >> 3)) ^ (r & 7)) << 4) + (x.lane & 7) * 2);
+    const float zd = fmaf(o.p0, h16_to_f(*reinterpret_cast<const uint16_t*>(cp + doff), F16), o.p1 * ad);
+    if (r < x.n) *reinterpret_cast<uint16_t*>(qp + doff) = f_to_h16(zd + o.p2, F16);
   }
 }
 
 // All of this warp's 32-column groups of an n x n product (G = g, g + NG, ...). sc scales
-// the accumulator of E_SCALE (s^2 for the Gram product of the user's X, else 1).
+// the accumulator of E_SCALE (s^2 for the Gram product of the user's X, else 1). (Both
+// groups' TMEM loads in flight together spill registers at this kernel's budget.)
 template <bool F16>
 __device__ __forceinline__ void epi_nn(const Ctx& x, const Op o, float sc) {
 #pragma unroll 1
@@ -388,10 +386,10 @@ __device__ __forceinline__ bool epi_ax(const Ctx& x, const Op o, float s, int& n
     if (x.d_tma) {
       // D = alpha su acc, rounded once, staged as this warp's 32 x 32 block of 16-bit values
       // (64-byte rows, chunk c of row i at c ^ ((i / 2) mod 4): the TMA 64-byte swizzle) in one
-      // of two 2 KiB buffers, and written by one TMA store (rows and columns outside D are
+      // of four 2 KiB buffers, and written by one TMA store (rows and columns outside D are
       // dropped by the copy itself)
-      uint8_t* blk = x.sm + OFF_R + (2 * x.ew + (nblk & 1)) * 2048;
-      if (lane == 0 && nblk >= 2) bulk_wait_read<1>();  // the store of two groups ago has read it
+      uint8_t* blk = x.sm + OFF_R + (4 * x.ew + (nblk & 3)) * 2048;
+      if (lane == 0 && nblk >= 4) bulk_wait_read<3>();  // the store of four groups ago has read it
       __syncwarp();
       const float2 k2 = make_float2(kout, kout);
       float2 z = make_float2(0.f, 0.f);
