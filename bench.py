@@ -220,6 +220,78 @@ def run_ours(args, rank, world, dist):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    def time_orth(X, fn, op, flops):
+        """One batched orthogonalization call (warm-up, then 3 timed calls): call time and the
+        GEMM launches' time from the library's event hooks."""
+        Xo = torch.empty_like(X)
+        ws_m = gns.alloc_workspace(gns.workspace_size(op, X, ns), dev)
+        # the bench's status word: the calls run back to back without a host synchronisation
+        # after each (the word is checked once the timed calls are done)
+        fn(X, outs=[Xo], ns=ns, workspace=ws_m, stream=stream, status=status)
+        torch.cuda.synchronize()
+        reps = 3
+        evm = [torch.cuda.Event(enable_timing=True) for _ in range(2 * reps)]
+        for e in evm:
+            e.record(stream)
+        hm = (ctypes.c_void_p * (2 * reps))(*[ctypes.c_void_p(e.cuda_event) for e in evm])
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        lib.gns_profile_set(hm, reps)
+        a.record(stream)
+        for _ in range(reps):
+            fn(X, outs=[Xo], ns=ns, workspace=ws_m, stream=stream, status=status)
+        b.record(stream)
+        torch.cuda.synchronize()
+        gns.check_status(status, what="bench orthogonalization")
+        lib.gns_profile_set(None, 0)
+        call_ms = a.elapsed_time(b) / reps
+        g_ms = sum(evm[2 * i].elapsed_time(evm[2 * i + 1]) for i in range(reps)) / reps
+        del Xo, ws_m
+        torch.cuda.empty_cache()
+        tf = flops / (g_ms / 1000.0) / 1e12
+        return {"ms_per_call": call_ms, "matrices_per_s": X.shape[0] / (call_ms / 1000.0), "gemm_ms": g_ms,
+                "gemm_tflops": tf, "gemm_frac_of_burst_peak": tf / load_peaks()[0],
+                "gemm_frac_of_sustained_peak": tf / load_peaks()[1]}
+
+    def small_batches():
+        """Groups of small matrices: the on-chip chain kernel (one CTA per matrix, oriented X
+        at most 128 x 512) where it applies, else the batched tile path; for chain-kernel
+        shapes the tile path is timed beside it (GNS_CHAIN_SMALL=0)."""
+        res = {}
+        for (count, n, m) in [(2048, 128, 512), (4096, 64, 256), (512, 256, 1024), (96, 512, 2048)]:
+            X = (torch.randn((count, n, m), generator=gen, device=dev, dtype=torch.float32) / m ** 0.5).to(
+                torch.bfloat16)
+            r = time_orth(X, gns.gram_ns_batched, _lib.GNS_OP_GRAM_NS, count * alg_flops_per_matrix(n, m))
+            std = time_orth(X, gns.ns_standard_batched, _lib.GNS_OP_NS_STANDARD, count * std_flops_per_matrix(n, m))
+            r["standard_ns_ms_per_call"] = std["ms_per_call"]
+            r["gram_vs_standard_speedup"] = std["ms_per_call"] / r["ms_per_call"]
+            chain = n <= 128 and m <= 512
+            r["path"] = ("on-chip chain kernel, one CTA per matrix" if chain else
+                         "batched tiles, 1-CTA 128 x 128" if n <= 128 else "batched tiles, 2-CTA 256 x 256")
+            if chain:
+                os.environ["GNS_CHAIN_SMALL"] = "0"
+                try:
+                    tg = time_orth(X, gns.gram_ns_batched, _lib.GNS_OP_GRAM_NS, count * alg_flops_per_matrix(n, m))
+                    ts = time_orth(X, gns.ns_standard_batched, _lib.GNS_OP_NS_STANDARD,
+                                   count * std_flops_per_matrix(n, m))
+                finally:
+                    del os.environ["GNS_CHAIN_SMALL"]
+                r["tile_path"] = {"gram_ns_ms_per_call": tg["ms_per_call"], "standard_ns_ms_per_call": ts["ms_per_call"],
+                                  "chain_speedup_gram": tg["ms_per_call"] / r["ms_per_call"],
+                                  "chain_speedup_standard": ts["ms_per_call"] / std["ms_per_call"]}
+            res[f"{count}x{n}x{m}"] = r
+            del X
+            torch.cuda.empty_cache()
+        return res
+
+    if args.small_only:
+        # the small-matrix section alone (for profiling the chain kernel): one JSON line
+        if rank == 0:
+            print(json.dumps({"small_matrices": small_batches(),
+                              "note": "--small-only: the small-matrix section alone, not a bench line"}), flush=True)
+        return 0
+
+
     def step(g):
         gns.muon_step(W, g, M, lr=LR, momentum=MU, ns=ns, workspace=ws, status=status, stream=stream)
 
@@ -441,36 +513,6 @@ def run_ours(args, rank, world, dist):
         return step_ms, g_ms
 
     # ---- the MoE-expert alpha = 4 batch: Gram NS alone on 256 x 2048 x 8192 ----
-    def time_orth(X, fn, op, flops):
-        """One batched orthogonalization call (warm-up, then 3 timed calls): call time and the
-        GEMM launches' time from the library's event hooks."""
-        Xo = torch.empty_like(X)
-        ws_m = gns.alloc_workspace(gns.workspace_size(op, X, ns), dev)
-        fn(X, outs=[Xo], ns=ns, workspace=ws_m, stream=stream)
-        torch.cuda.synchronize()
-        reps = 3
-        evm = [torch.cuda.Event(enable_timing=True) for _ in range(2 * reps)]
-        for e in evm:
-            e.record(stream)
-        hm = (ctypes.c_void_p * (2 * reps))(*[ctypes.c_void_p(e.cuda_event) for e in evm])
-        torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        lib.gns_profile_set(hm, reps)
-        a.record(stream)
-        for _ in range(reps):
-            fn(X, outs=[Xo], ns=ns, workspace=ws_m, stream=stream)
-        b.record(stream)
-        torch.cuda.synchronize()
-        lib.gns_profile_set(None, 0)
-        call_ms = a.elapsed_time(b) / reps
-        g_ms = sum(evm[2 * i].elapsed_time(evm[2 * i + 1]) for i in range(reps)) / reps
-        del Xo, ws_m
-        torch.cuda.empty_cache()
-        tf = flops / (g_ms / 1000.0) / 1e12
-        return {"ms_per_call": call_ms, "matrices_per_s": X.shape[0] / (call_ms / 1000.0), "gemm_ms": g_ms,
-                "gemm_tflops": tf, "gemm_frac_of_burst_peak": tf / load_peaks()[0],
-                "gemm_frac_of_sustained_peak": tf / load_peaks()[1]}
-
     def moe_experts():
         count, n, m = 256, 2048, 8192
         X = (torch.randn((count, n, m), generator=gen, device=dev, dtype=torch.float32) / m ** 0.5).to(torch.bfloat16)
@@ -499,21 +541,6 @@ def run_ours(args, rank, world, dist):
 
     # ---- many small matrices (one call per batch; products of at most 128 rows take the
     #      1-CTA 128 x 128 tile plan) and a batch-size sweep at 1024 x 4096 ----
-    def small_batches():
-        res = {}
-        for (count, n, m) in [(2048, 128, 512), (512, 256, 1024), (96, 512, 2048)]:
-            X = (torch.randn((count, n, m), generator=gen, device=dev, dtype=torch.float32) / m ** 0.5).to(
-                torch.bfloat16)
-            r = time_orth(X, gns.gram_ns_batched, _lib.GNS_OP_GRAM_NS, count * alg_flops_per_matrix(n, m))
-            std = time_orth(X, gns.ns_standard_batched, _lib.GNS_OP_NS_STANDARD, count * std_flops_per_matrix(n, m))
-            r["standard_ns_ms_per_call"] = std["ms_per_call"]
-            r["gram_vs_standard_speedup"] = std["ms_per_call"] / r["ms_per_call"]
-            r["tile_plan"] = "1-CTA 128 x 128" if n <= 128 else "2-CTA 256 x 256"
-            res[f"{count}x{n}x{m}"] = r
-            del X
-            torch.cuda.empty_cache()
-        return res
-
     def batch_sweep():
         res = {}
         n, m = ROWS, COLS
@@ -732,6 +759,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--metric-only", action="store_true",
                     help="time the metric step alone and print a short line (for profiling runs)")
+    ap.add_argument("--small-only", action="store_true",
+                    help="time the small-matrix section alone and print it (for profiling runs)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
