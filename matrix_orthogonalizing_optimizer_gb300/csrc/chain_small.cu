@@ -80,7 +80,9 @@ enum : uint8_t {
   E_OUT = 5     // D = alpha s (acc [+ p0 X]) + beta D   (the result)
 };
 // op flags
-enum : uint8_t { F_QINIT = 1, F_USER = 2, F_XT = 4, F_ADDX = 8 };
+// F_XIN: the op reads the X region while it still holds the input as stored (a tall
+// matrix's storage is X transposed: the products read it the other way)
+enum : uint8_t { F_QINIT = 1, F_USER = 2, F_XIN = 4, F_ADDX = 8 };
 
 struct Op {
   uint8_t kind, epi;
@@ -93,24 +95,40 @@ struct Op {
   float p0, p1, p2;
 };
 
-struct Params {
-  CUtensorMap tmX;
-  CUtensorMap tmD;    // the result, 32 x 32 boxes, 64-byte swizzle (used when d_tma)
-  Op ops[MAX_OPS];
-  int nops;
-  int B, n, m, mp;    // count, rows, columns, columns padded to 64
-  int xt;             // the user's X is stored transposed (m x n)
-  int ab_f16;         // products in fp16 (else bf16)
-  int norm_mode;      // 0: s = 1; 1: s = inv[b]; 2: summed here
-  const float* inv;
-  float eps;
+constexpr int MAX_GROUPS = 8;  // shape groups one launch carries
+
+// One shape group of a launch: its matrices are the launch's matrices first .. first+count-1.
+struct Group {
+  CUtensorMap tmX;  // X: rows of the n x m operand (box 64 x 128), or a tall matrix's m x n
+                    // storage (box 64 x 64); zero fill outside the matrix
+  CUtensorMap tmD;  // the result, 32 x 32 boxes, 64-byte swizzle (used when d_tma)
   void* D;
+  const float* inv;  // per-matrix 1/(||X||_F + eps) (norm_mode 1)
   long long ldd, sd;
-  int d_f16, d_trans, has_c, check_finite;
-  int d_tma;          // the result goes out by TMA stores (no addend to read)
+  int first, count, n, m, mp;  // mp: m padded to 64
+  int xt;                      // the input X is stored transposed (m x n)
+  int d_f16, d_trans, has_c;
+  int d_tma;  // the result goes out by TMA stores (no addend to read)
   float alpha, beta;
+};
+
+struct Params {
+  Group grp[MAX_GROUPS];
+  Op ops[MAX_OPS];  // one list for every group (X <- Q X and Q X take all four accumulators)
+  int nops, ngroups, total;
+  int ab_f16;     // products in fp16 (else bf16)
+  int norm_mode;  // 0: s = 1; 1: s = inv[b]; 2: from the trace of the first Gram product
+  int check_finite;
+  float eps;
   int32_t* status;
 };
+
+// the group of launch matrix i (groups are in order of their first matrix)
+__device__ __forceinline__ int group_of(const Params& P, int i) {
+  int g = 0;
+  while (g + 1 < P.ngroups && i >= P.grp[g + 1].first) ++g;
+  return g;
+}
 
 __host__ __device__ inline uint32_t buf_off(int buf) {
   return buf == BUF_R ? OFF_R : buf == BUF_Z ? OFF_Z : buf == BUF_Q ? OFF_Q : 0u;
@@ -140,8 +158,8 @@ __device__ __forceinline__ void load_acc32(uint32_t trow, int col, float (&v)[32
 // inside its 64-column panel; an MN-major one advances 16 rows (2048 bytes), its 64-wide
 // MN blocks lbo bytes apart.
 
-__device__ __forceinline__ void issue_op(const Op o, int mp, int ab, uint32_t s, uint32_t tmem) {
-  const bool xt = (o.flags & F_XT) != 0;
+__device__ __forceinline__ void issue_op(const Op o, int mp, int ab, bool xt_in, uint32_t s, uint32_t tmem) {
+  const bool xt = xt_in && (o.flags & F_XIN) != 0;
   if (o.kind == K_GRAM) {
     // X X^T: A(i,k) = B(i,k) = X[i][k]
     const uint32_t d = tmem + 128u * o.slot;
@@ -507,12 +525,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) chain_kernel(const __grid_cons
   if (warp == 0) {
     // ---- X loads
     if (lane == 0) {
-      tma_prefetch_desc(&P.tmX);
-      const uint32_t xbytes = (uint32_t)(P.mp * 256);
       int it = 0;
       bool issued = false;
       uint32_t ipar = 0;
-      for (int b = blockIdx.x; b < P.B; b += gridDim.x, ++it) {
+      for (int i = blockIdx.x; i < P.total; i += gridDim.x, ++it) {
+        const Group& gr = P.grp[group_of(P, i)];
+        const int b = i - gr.first, mp = gr.mp;
+        const uint32_t xbytes = (uint32_t)(mp * 256);
         if (it > 0) {
           // the region is free once the last product (and, when its epilogue reads X, that
           // epilogue) of the previous matrix is done
@@ -520,12 +539,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) chain_kernel(const __grid_cons
           if (!mbar_wait(wb, (uint32_t)((it - 1) & 1), abortv, P.status)) break;
         }
         mbar_arrive_expect_tx(bar_x, xbytes);
-        if (!P.xt) {
-          for (int p = 0; p < P.mp / 64; ++p) tma_load_3d(sm + p * PANEL_BYTES, &P.tmX, bar_x, 64 * p, 0, b);
+        if (!gr.xt) {
+          for (int p = 0; p < mp / 64; ++p) tma_load_3d(sm + p * PANEL_BYTES, &gr.tmX, bar_x, 64 * p, 0, b);
         } else {
           for (int ib = 0; ib < 2; ++ib)
-            for (int kb = 0; kb < P.mp / 64; ++kb)
-              tma_load_3d(sm + ib * (P.mp * 128) + kb * 8192, &P.tmX, bar_x, 64 * ib, 64 * kb, b);
+            for (int kb = 0; kb < mp / 64; ++kb)
+              tma_load_3d(sm + ib * (mp * 128) + kb * 8192, &gr.tmX, bar_x, 64 * ib, 64 * kb, b);
         }
         issued = true;
         ipar = (uint32_t)(it & 1);
@@ -539,12 +558,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) chain_kernel(const __grid_cons
   } else if (warp == 1) {
     // ---- MMA issue
     if (lane == 0) {
-      const int mp = P.mp, ab = P.ab_f16;
+      const int ab = P.ab_f16;
       int it = 0, last = -1;
       uint32_t last_par = 0;
       bool ok = true;
-      for (int b = blockIdx.x; ok && b < P.B; b += gridDim.x, ++it) {
+      for (int mi = blockIdx.x; ok && mi < P.total; mi += gridDim.x, ++it) {
         const uint32_t par = (uint32_t)(it & 1);
+        const Group& gr = P.grp[group_of(P, mi)];
+        const int mp = gr.mp;
+        const bool xt_in = gr.xt != 0;
         for (int i = 0; i < nops; ++i) {
           const Op o = P.ops[i];
           if (i == 0) {
@@ -554,7 +576,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) chain_kernel(const __grid_cons
           }
           if (o.dep >= 0 && !(ok = mbar_wait(&bar_epi[o.dep], par, abortv, P.status))) break;
           tc_fence_after();
-          issue_op(o, mp, ab, sbase, tmem);
+          issue_op(o, mp, ab, xt_in, sbase, tmem);
           umma_commit(&bar_acc[i]);
           last = i;
           last_par = par;
@@ -579,18 +601,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) chain_kernel(const __grid_cons
     cx.g = g;
     cx.ew = ew;
     cx.lane = lane;
-    cx.n = P.n;
-    cx.m = P.m;
-    cx.mp = P.mp;
     const bool f16 = P.ab_f16 != 0;
-    cx.d_f16 = P.d_f16;
-    cx.d_trans = P.d_trans;
-    cx.has_c = P.has_c;
-    cx.alpha = P.alpha;
-    cx.beta = P.beta;
-    cx.ldd = P.ldd;
-    cx.d_tma = P.d_tma;
-    cx.tmD = &P.tmD;
     int nblk = 0;  // TMA-stored result blocks of this warp
     const int norm_mode = P.norm_mode;
     const float eps = P.eps;
@@ -598,12 +609,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) chain_kernel(const __grid_cons
     // takes the whole warp out of the loop together (the TMEM loads are warp-collective)
     int it = 0;
     bool ok = true, bad = false;
-    for (int b = blockIdx.x; ok && b < P.B; b += gridDim.x, ++it) {
+    for (int mi = blockIdx.x; ok && mi < P.total; mi += gridDim.x, ++it) {
       const uint32_t par = (uint32_t)(it & 1);
-      cx.D = static_cast<uint16_t*>(P.D) + (long long)b * P.sd;
+      const Group& gr = P.grp[group_of(P, mi)];
+      const int b = mi - gr.first;
+      cx.n = gr.n;
+      cx.m = gr.m;
+      cx.mp = gr.mp;
+      cx.d_f16 = gr.d_f16;
+      cx.d_trans = gr.d_trans;
+      cx.has_c = gr.has_c;
+      cx.alpha = gr.alpha;
+      cx.beta = gr.beta;
+      cx.ldd = gr.ldd;
+      cx.d_tma = gr.d_tma;
+      cx.tmD = &gr.tmD;
+      cx.D = static_cast<uint16_t*>(gr.D) + (long long)b * gr.sd;
       cx.b = b;
       float s = 1.f;
-      if (norm_mode == 1) s = P.inv[b];
+      if (norm_mode == 1) s = gr.inv[b];
       // X has landed (the epilogues of X <- a X + B X and of the standard-NS result read it)
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_x, par, abortv, P.status)))) break;
       for (int i = 0; i < nops; ++i) {
@@ -714,9 +738,10 @@ Op make_op(uint8_t kind, uint8_t epi) {
 // iteration Z = b R + c R^2 (Q = Z + a I while Q is the identity), RZ = R Z + a R,
 // Q_t = Q Z + a Q, R_t = Z RZ + a RZ (R only where it is read again); a restart after
 // iteration i forms X <- Q X, R <- X X^T, Q <- I; the result is Q_T X.
-void build_gram(Builder& bd, const gns_ns_params& ns, bool user, bool xt) {
+void build_gram(Builder& bd, const gns_ns_params& ns, bool user) {
   using namespace chain;
-  auto fl = [&]() { return (uint8_t)((user ? F_USER : 0) | (xt ? F_XT : 0)); };
+  bool xin = true;  // the region holds the input X (until the first restart overwrites it)
+  auto fl = [&]() { return (uint8_t)((user ? F_USER : 0) | (xin ? F_XIN : 0)); };
   Op g = make_op(K_GRAM, E_SCALE);
   g.d = BUF_R;
   g.flags = fl();
@@ -731,7 +756,7 @@ void build_gram(Builder& bd, const gns_ns_params& ns, bool user, bool xt) {
       x.flags = fl();
       bd.add(x, {BUF_Q, BUF_X}, {BUF_X});
       user = false;
-      xt = false;
+      xin = false;
       Op r = make_op(K_GRAM, E_SCALE);
       r.d = BUF_R;
       bd.add(r, {BUF_X}, {BUF_R});
@@ -818,7 +843,7 @@ void build_std(Builder& bd, const gns_ns_params& ns, bool user) {
 int count_ops(bool gram, const gns_ns_params& ns) {
   Builder bd;
   if (gram)
-    build_gram(bd, ns, true, false);
+    build_gram(bd, ns, true);
   else
     build_std(bd, ns, true);
   return (int)bd.ops.size();
@@ -850,79 +875,40 @@ bool chain_supported(bool gram, gns_dtype dt, int64_t n, int64_t m, int xt, cons
   return count_ops(gram, *ns) <= chain::MAX_OPS;
 }
 
-int launch_chain(const ChainCall& c, std::string* err) {
-  using namespace chain;
-  if (!chain_supported(c.gram, c.dt, c.n, c.m, c.xt, c.ns)) {
-    *err = "chain kernel: unsupported group";
-    return GNS_ERR_UNSUPPORTED;
-  }
-  static Params P;  // large (tensor map + op list): built in static storage, copied at launch
-  std::memset(&P, 0, sizeof(P));
-  Builder bd;
-  const int64_t mp = (c.m + 63) / 64 * 64;
-  bd.ax_slots = (int)((mp + 127) / 128);
-  if (c.gram)
-    build_gram(bd, *c.ns, c.x_user, c.xt != 0);
-  else
-    build_std(bd, *c.ns, c.x_user);
-  P.nops = (int)bd.ops.size();
-  for (int i = 0; i < P.nops; ++i) P.ops[i] = bd.ops[i];
-  P.B = (int)c.B;
-  P.n = (int)c.n;
-  P.m = (int)c.m;
-  P.mp = (int)mp;
-  P.xt = c.xt;
-  P.ab_f16 = c.dt == GNS_F16;
-  P.norm_mode = !c.x_user ? 0 : c.inv ? 1 : 2;
-  P.inv = c.inv;
-  P.eps = c.eps;
-  P.D = c.D.ptr;
-  P.ldd = c.D.ld;
-  P.sd = c.B > 1 ? c.D.stride : 0;
-  P.d_f16 = c.d_f16;
-  P.d_trans = c.d_trans;
-  P.has_c = c.has_c;
-  P.check_finite = c.check_finite;
-  P.alpha = c.alpha;
-  P.beta = c.beta;
-  P.status = c.status;
-
-  // X: rows of the n x m operand (box 64 columns x 128 rows), or for a tall matrix its
-  // m x n storage (box 64 x 64); zero fill outside the matrix
+// Tensor map of a batch of 16-bit row-major matrices: dims {cols, rows, count} of the storage.
+static bool encode16(CUtensorMap* map, const MatRef& mref, int64_t count, uint32_t box_cols, uint32_t box_rows,
+                     int f16, CUtensorMapSwizzle swz, std::string* err) {
   auto fn = encode_fn(err);
-  if (!fn) return GNS_ERR_CUDA;
-  const MatRef& x = c.x;
-  int64_t st_b = (c.B > 1 ? x.stride : x.rows * x.ld) * 2;
+  if (!fn) return false;
+  int64_t st_b = (count > 1 ? mref.stride : mref.rows * mref.ld) * 2;
   st_b = std::max<int64_t>((st_b + 15) / 16 * 16, 16);
-  cuuint64_t dims[3] = {(cuuint64_t)x.cols, (cuuint64_t)x.rows, (cuuint64_t)c.B};
-  cuuint64_t strides[2] = {(cuuint64_t)(x.ld * 2), (cuuint64_t)st_b};
-  cuuint32_t box[3] = {64u, c.xt ? 64u : 128u, 1u};
+  cuuint64_t dims[3] = {(cuuint64_t)mref.cols, (cuuint64_t)mref.rows, (cuuint64_t)count};
+  cuuint64_t strides[2] = {(cuuint64_t)(mref.ld * 2), (cuuint64_t)st_b};
+  cuuint32_t box[3] = {box_cols, box_rows, 1u};
   cuuint32_t estr[3] = {1u, 1u, 1u};
-  CUresult r = fn(&P.tmX, P.ab_f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, x.ptr,
-                  dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const CUresult r = fn(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, mref.ptr,
+                        dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     *err = "cuTensorMapEncodeTiled failed (code " + std::to_string((int)r) + ")";
-    return GNS_ERR_CUDA;
+    return false;
   }
+  return true;
+}
 
-  // D (when no addend is read): dims {cols, rows, count} of its storage, box 32 x 32
-  P.d_tma = !c.has_c;
-  if (P.d_tma) {
-    const MatRef& d = c.D;
-    int64_t sd_b = (c.B > 1 ? d.stride : d.rows * d.ld) * 2;
-    sd_b = std::max<int64_t>((sd_b + 15) / 16 * 16, 16);
-    cuuint64_t ddims[3] = {(cuuint64_t)d.cols, (cuuint64_t)d.rows, (cuuint64_t)c.B};
-    cuuint64_t dstr[2] = {(cuuint64_t)(d.ld * 2), (cuuint64_t)sd_b};
-    cuuint32_t dbox[3] = {32u, 32u, 1u};
-    r = fn(&P.tmD, c.d_f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, d.ptr, ddims,
-           dstr, dbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) {
-      *err = "cuTensorMapEncodeTiled (result) failed (code " + std::to_string((int)r) + ")";
-      return GNS_ERR_CUDA;
+int launch_chain(const ChainCall& c, std::string* err) {
+  using namespace chain;
+  if (c.groups.empty()) return GNS_OK;
+  for (const ChainGroup& g : c.groups)
+    if (!chain_supported(c.gram, c.dt, g.n, g.m, g.xt, c.ns) || (c.x_user && (g.inv == nullptr) != (c.groups[0].inv == nullptr))) {
+      *err = "chain kernel: unsupported group";
+      return GNS_ERR_UNSUPPORTED;
     }
-  }
+  Builder bd;  // one op list for every group: X <- Q X and Q X take all four accumulators
+  if (c.gram)
+    build_gram(bd, *c.ns, c.x_user);
+  else
+    build_std(bd, *c.ns, c.x_user);
 
   static bool attr_set[64] = {false};
   int dev = 0;
@@ -936,14 +922,63 @@ int launch_chain(const ChainCall& c, std::string* err) {
     }
     attr_set[dev] = true;
   }
-  const int grid = (int)std::min<int64_t>(c.B, device_sm_count());
-  profile_gemm_begin(c.stream);
-  chain_kernel<<<grid, NUM_THREADS, SMEM_BYTES, static_cast<cudaStream_t>(c.stream)>>>(P);
-  const cudaError_t e = cudaGetLastError();
-  profile_gemm_end(c.stream);
-  if (e != cudaSuccess) {
-    *err = std::string("chain_kernel launch: ") + cudaGetErrorString(e);
-    return GNS_ERR_CUDA;
+
+  // up to MAX_GROUPS groups per launch; the launch's matrices are the groups' matrices in order
+  thread_local Params P;  // a few KB (tensor maps, op list): built per calling thread, copied at launch
+  const int f16 = c.dt == GNS_F16;
+  for (size_t g0 = 0; g0 < c.groups.size(); g0 += MAX_GROUPS) {
+    std::memset(&P, 0, sizeof(P));
+    P.nops = (int)bd.ops.size();
+    for (int i = 0; i < P.nops; ++i) P.ops[i] = bd.ops[i];
+    P.ab_f16 = f16;
+    P.norm_mode = !c.x_user ? 0 : c.groups[0].inv ? 1 : 2;
+    P.eps = c.eps;
+    P.check_finite = c.check_finite;
+    P.status = c.status;
+    int64_t total = 0;
+    const size_t g1 = std::min(c.groups.size(), g0 + MAX_GROUPS);
+    for (size_t gi = g0; gi < g1; ++gi) {
+      const ChainGroup& cg = c.groups[gi];
+      Group& G = P.grp[P.ngroups++];
+      G.first = (int)total;
+      G.count = (int)cg.B;
+      total += cg.B;
+      G.n = (int)cg.n;
+      G.m = (int)cg.m;
+      G.mp = (int)((cg.m + 63) / 64 * 64);
+      G.xt = cg.xt;
+      G.inv = cg.inv;
+      G.D = cg.D.ptr;
+      G.ldd = cg.D.ld;
+      G.sd = cg.B > 1 ? cg.D.stride : 0;
+      G.d_f16 = cg.d_f16;
+      G.d_trans = cg.d_trans;
+      G.has_c = cg.has_c;
+      G.alpha = cg.alpha;
+      G.beta = cg.beta;
+      // X: rows of the n x m operand (box 64 columns x 128 rows), or for a tall matrix its
+      // m x n storage (box 64 x 64); zero fill outside the matrix
+      if (!encode16(&G.tmX, cg.x, cg.B, 64u, cg.xt ? 64u : 128u, f16, CU_TENSOR_MAP_SWIZZLE_128B, err))
+        return GNS_ERR_CUDA;
+      // the result, when no addend is read: 32 x 32 boxes of its storage
+      G.d_tma = !cg.has_c;
+      if (G.d_tma && !encode16(&G.tmD, cg.D, cg.B, 32u, 32u, cg.d_f16, CU_TENSOR_MAP_SWIZZLE_64B, err))
+        return GNS_ERR_CUDA;
+    }
+    if (total > INT32_MAX) {
+      *err = "chain kernel: too many matrices in one launch";
+      return GNS_ERR_UNSUPPORTED;
+    }
+    P.total = (int)total;
+    const int grid = (int)std::min<int64_t>(total, device_sm_count());
+    profile_gemm_begin(c.stream);
+    chain_kernel<<<grid, NUM_THREADS, SMEM_BYTES, static_cast<cudaStream_t>(c.stream)>>>(P);
+    const cudaError_t e = cudaGetLastError();
+    profile_gemm_end(c.stream);
+    if (e != cudaSuccess) {
+      *err = std::string("chain_kernel launch: ") + cudaGetErrorString(e);
+      return GNS_ERR_CUDA;
+    }
   }
   return GNS_OK;
 }

@@ -279,33 +279,59 @@ static bool chain_ok(bool gram, gns_dtype dt, const Src& src, int64_t n, int64_t
   return fin.row_map == nullptr && chain_supported(gram, dt, n, m, src.trans, ns);
 }
 
-// inv: per-matrix 1/(||X||_F + eps), or null to have the kernel sum the norm itself
+// One chain-kernel group: X as the source describes it, the result as the final write does.
+// inv: per-matrix 1/(||X||_F + eps), or null to have the kernel sum the norm itself.
+static ChainGroup chain_group(gns_dtype dt, const Src& src, int64_t B, int64_t n, int64_t m, const float* inv,
+                              const Final& fin) {
+  ChainGroup g;
+  g.x = src.mat;
+  g.xt = src.trans;
+  g.B = B;
+  g.n = n;
+  g.m = m;
+  g.inv = src.user ? inv : nullptr;
+  g.D = fin.D;
+  g.d_f16 = (fin.out_dt < 0 ? dt : (gns_dtype)fin.out_dt) == GNS_F16;
+  g.d_trans = fin.d_trans;
+  g.alpha = fin.alpha;
+  g.beta = fin.beta;
+  g.has_c = fin.has_c;
+  return g;
+}
+
+// Chain-kernel groups collected over a call and launched together (one launch carries up to
+// eight groups, so a small group's tail does not leave the chip idle until the next group's
+// launch): one list per (algorithm, product type).
+struct ChainBatch {
+  ChainCall calls[2][2];  // [gram][fp16]
+  void add(bool gram, gns_dtype dt, bool user, const gns_ns_params* ns, const ChainGroup& g) {
+    ChainCall& c = calls[gram ? 1 : 0][dt == GNS_F16 ? 1 : 0];
+    c.gram = gram;
+    c.dt = dt;
+    c.x_user = user;
+    c.ns = ns;
+    c.eps = ns->eps;
+    c.groups.push_back(g);
+  }
+  int launch(int32_t* st, void* stream) {
+    for (auto& row : calls)
+      for (ChainCall& c : row) {
+        if (c.groups.empty()) continue;
+        c.status = st;
+        c.stream = stream;
+        std::string err;
+        const int rc = launch_chain(c, &err);
+        if (rc) return fail(rc, err);
+      }
+    return GNS_OK;
+  }
+};
+
 static int run_chain(bool gram, gns_dtype dt, const Src& src, int64_t B, int64_t n, int64_t m,
                      const gns_ns_params* ns, const float* inv, const Final& fin, int32_t* st, void* stream) {
-  ChainCall c;
-  c.gram = gram;
-  c.dt = dt;
-  c.x = src.mat;
-  c.xt = src.trans;
-  c.x_user = src.user;
-  c.B = B;
-  c.n = n;
-  c.m = m;
-  c.ns = ns;
-  c.inv = src.user ? inv : nullptr;
-  c.eps = ns->eps;
-  c.D = fin.D;
-  c.d_f16 = (fin.out_dt < 0 ? dt : (gns_dtype)fin.out_dt) == GNS_F16;
-  c.d_trans = fin.d_trans;
-  c.alpha = fin.alpha;
-  c.beta = fin.beta;
-  c.has_c = fin.has_c;
-  c.check_finite = fin.check_finite;
-  c.status = st;
-  c.stream = stream;
-  std::string err;
-  const int rc = launch_chain(c, &err);
-  return rc ? fail(rc, err) : GNS_OK;
+  ChainBatch cb;
+  cb.add(gram, dt, src.user, ns, chain_group(dt, src, B, n, m, inv, fin));
+  return cb.launch(st, stream);
 }
 
 struct GramBufs {
@@ -861,6 +887,7 @@ static int ns_common(bool gram, const gns_batch* x, const gns_batch* out, int ng
   std::string err;
   const gns_ns_params nse = effective_ns(*ns);
   ns = &nse;
+  ChainBatch chains;
   for (int gi = 0; gi < ngroups; ++gi) {
     GroupShape s = shape_of(x[gi]);
     Src src;
@@ -871,8 +898,9 @@ static int ns_common(bool gram, const gns_batch* x, const gns_batch* out, int ng
     fin.d_trans = s.trans;
     const bool g_alg = gram && s.n != s.m;
     if (chain_ok(g_alg, dt, src, s.n, s.m, ns, fin)) {
-      // the norm is summed inside the kernel, from the X it holds on chip
-      if ((rc = run_chain(g_alg, dt, src, s.B, s.n, s.m, ns, nullptr, fin, st, stream))) return rc;
+      // launched with the call's other small groups below; the norm is summed inside the
+      // kernel, from the X it holds on chip
+      chains.add(g_alg, dt, true, ns, chain_group(dt, src, s.B, s.n, s.m, nullptr, fin));
       continue;
     }
     if (g_alg) {
@@ -889,7 +917,7 @@ static int ns_common(bool gram, const gns_batch* x, const gns_batch* out, int ng
       if ((rc = run_std(dt, src, s.B, s.n, s.m, ns, sb, sb.inv, &fin, nullptr, st, stream))) return rc;
     }
   }
-  return GNS_OK;
+  return chains.launch(st, stream);
 }
 
 int gns_gram_ns_batched(const gns_batch* x, const gns_batch* out, int ngroups, gns_dtype dtype,
@@ -1016,6 +1044,7 @@ int gns_muon_step(const gns_batch* W, const gns_batch* G, const gns_batch* M, co
   const float lr = mp->lr, mu = mp->momentum;
   const float decay = 1.f - mp->lr * mp->weight_decay;
   const float step_scale = -lr * mp->scale;
+  ChainBatch chains;
   for (int gi = 0; gi < ngroups; ++gi) {
     GroupShape s = shape_of(M[gi]);
     MatRef mm = to_ref(M[gi]), gm = to_ref(G[gi]), wm = to_ref(W[gi]);
@@ -1077,6 +1106,16 @@ int gns_muon_step(const gns_batch* W, const gns_batch* G, const gns_batch* M, co
         fs.alpha = step_scale;
         fs.beta = decay;
         fs.has_c = true;
+      }
+      if (!normuon) {
+        const bool g_alg = !mb.use_std;
+        const Final& ff = g_alg ? fin : fs;
+        if (chain_ok(g_alg, mb.nsdt, src, s.n, s.m, ns, ff)) {
+          // the orthogonalization and update of this small group run in the chain kernel,
+          // launched once for all such groups of the call after the loop
+          chains.add(g_alg, mb.nsdt, src.user, ns, chain_group(mb.nsdt, src, s.B, s.n, s.m, inv, ff));
+          continue;
+        }
       }
       if (mb.use_std && chain_ok(false, mb.nsdt, src, s.n, s.m, ns, fs)) {
         if ((rc = run_chain(false, mb.nsdt, src, s.B, s.n, s.m, ns, inv, fs, dev_status, stream))) return rc;
@@ -1166,7 +1205,7 @@ int gns_muon_step(const gns_batch* W, const gns_batch* G, const gns_batch* M, co
                                     normuon ? mb.r : nullptr)))
       return fail(rc, err);
   }
-  return GNS_OK;
+  return chains.launch(dev_status, stream);
 }
 
 int gns_selftest_bounded_wait(const int32_t* counter, int32_t target, uint32_t limit_us, int32_t* dev_status,

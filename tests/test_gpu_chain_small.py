@@ -225,3 +225,58 @@ def test_chain_many_matrices_per_cta():
         assert rel_fro(torch_to_f64(out[b]), want) < TOL_BF16, b
         want_s = ons.ns_standard(torch_to_f64(X[b]), ons.QUINTIC_FIXED)
         assert rel_fro(torch_to_f64(outs[b]), want_s) < TOL_BF16, b
+
+
+def test_chain_several_groups_one_launch():
+    """Several shape groups in one call: the chain kernel carries all Gram groups in one launch
+    (wide, ragged, tall, a single-row group), square groups (standard NS) in a second, and
+    more than eight groups in further launches of eight."""
+    shapes = [(40, 128, 512), (17, 96, 300), (33, 400, 72), (5, 1, 64), (9, 64, 64)]
+    xs, refs = [], []
+    for i, (c, r, k) in enumerate(shapes):
+        bits, x = bf16_input(88, (c, r, k), stream=i)
+        xs.append(bits_to_torch(bits))
+        refs.append(x)
+    st = _status()
+    outs, n_gemm, n_all = _launches(lambda: gns.gram_ns_batched(xs, status=st))
+    assert int(st.item()) == 0
+    assert (n_gemm, n_all) == (2, 2)  # the four Gram groups, then the square group
+    for (c, r, k), out, x in zip(shapes, outs, refs):
+        got = torch_to_f64(out)
+        for b in sorted({0, c // 2, c - 1}):
+            want = (ons.ns_standard(x[b], ons.QUINTIC_FIXED) if r == k else omuon.orthogonalize(x[b]))
+            tol = TOL_RANK1 if min(r, k) == 1 else TOL_BF16
+            assert rel_fro(got[b], want) < tol, (r, k, b)
+    # ten groups: two launches (eight, then two)
+    xs10 = [xs[0][:3].clone() for _ in range(10)]
+    outs10, n_gemm, _ = _launches(lambda: gns.gram_ns_batched(xs10))
+    assert n_gemm == 2
+    for o in outs10:
+        assert torch.equal(o, outs10[0])
+
+
+def test_chain_muon_step_several_groups():
+    """A Muon step over small groups (chain kernel, one launch after their momentum passes)
+    and a larger group (batched tile path), each against the oracle."""
+    shapes = [(12, 128, 512), (7, 384, 96), (5, 256, 1024)]
+    Ws, Gs, Ms, raw = [], [], [], []
+    for i, (c, r, k) in enumerate(shapes):
+        s = 1.0 / np.sqrt(k)
+        Wb, _ = bf16_input(89, (c, r, k), s, stream=3 * i)
+        Gb, _ = bf16_input(89, (c, r, k), s, stream=3 * i + 1)
+        Mb, _ = bf16_input(89, (c, r, k), s, stream=3 * i + 2)
+        Ws.append(bits_to_torch(Wb))
+        Gs.append(bits_to_torch(Gb))
+        Ms.append(bits_to_torch(Mb))
+        raw.append((Wb, Gb, Mb))
+    _, n_gemm, _ = _launches(lambda: gns.muon_step(Ws, Gs, Ms, lr=0.02, momentum=0.95))
+    assert n_gemm == 2  # one chain launch for the two small groups, one tile-path launch
+    for (c, r, k), Wt, Mt, (Wb, Gb, Mb) in zip(shapes, Ws, Ms, raw):
+        Mg, Wg = torch_to_bits(Mt), torch_to_f64(Wt)
+        for b in sorted({0, c - 1}):
+            W_or, M_or, O = omuon.muon_step(Wb[b], Gb[b], Mb[b], lr=0.02, mu=0.95)
+            assert np.array_equal(Mg[b], M_or)
+            dW = Wg[b] - W_or
+            mag = np.maximum(np.maximum(np.abs(Wg[b]), np.abs(W_or)), 2.0 ** -126)
+            excess = np.maximum(np.abs(dW) - 0.5 * 2.0 ** (np.floor(np.log2(mag)) - 7), 0.0)
+            assert np.linalg.norm(excess) / np.linalg.norm(0.02 * O) < TOL_BF16, (r, k, b)
