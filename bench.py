@@ -282,6 +282,41 @@ def run_ours(args, rank, world, dist):
             res[f"{count}x{n}x{m}"] = r
             del X
             torch.cuda.empty_cache()
+        # several small shape groups in one call (one chain-kernel launch carries them all)
+        # against one call per group
+        shapes = [(1024, 128, 512), (600, 96, 384), (300, 64, 256), (150, 128, 256), (77, 112, 448)]
+        Xs = [(torch.randn((c, n, m), generator=gen, device=dev, dtype=torch.float32) / m ** 0.5).to(torch.bfloat16)
+              for (c, n, m) in shapes]
+        Os = [torch.empty_like(X) for X in Xs]
+        ws_all = gns.alloc_workspace(gns.workspace_size(_lib.GNS_OP_GRAM_NS, Xs, ns), dev)
+
+        def one_call():
+            gns.gram_ns_batched(Xs, outs=Os, ns=ns, workspace=ws_all, stream=stream, status=status)
+
+        def per_group():
+            for X, O in zip(Xs, Os):
+                gns.gram_ns_batched(X, outs=[O], ns=ns, workspace=ws_all, stream=stream, status=status)
+
+        def t_call(fn, reps=5):
+            fn()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(reps):
+                fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            return a.elapsed_time(b) / reps
+        t1, tg = t_call(one_call), t_call(per_group)
+        gns.check_status(status, what="bench mixed groups")
+        fl = sum(c * alg_flops_per_matrix(n, m) for (c, n, m) in shapes)
+        res["mixed_groups_one_call"] = {
+            "groups": [f"{c}x{n}x{m}" for (c, n, m) in shapes], "matrices": sum(c for c, _, _ in shapes),
+            "one_call_ms": t1, "one_call_per_group_ms": tg, "speedup": tg / t1,
+            "tflops_one_call": fl / (t1 / 1000.0) / 1e12,
+            "what": "Gram NS of five small shape groups: one call (one chain-kernel launch) vs one call per group"}
+        del Xs, Os, ws_all
+        torch.cuda.empty_cache()
         return res
 
     if args.small_only:
