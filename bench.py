@@ -258,7 +258,7 @@ def run_ours(args, rank, world, dist):
         at most 128 x 512) where it applies, else the batched tile path; for chain-kernel
         shapes the tile path is timed beside it (GNS_CHAIN_SMALL=0)."""
         res = {}
-        for (count, n, m) in [(2048, 128, 512), (4096, 64, 256), (512, 256, 1024), (96, 512, 2048)]:
+        for (count, n, m) in [(2048, 128, 512), (4096, 64, 256), (8192, 32, 128), (512, 256, 1024), (96, 512, 2048)]:
             X = (torch.randn((count, n, m), generator=gen, device=dev, dtype=torch.float32) / m ** 0.5).to(
                 torch.bfloat16)
             r = time_orth(X, gns.gram_ns_batched, _lib.GNS_OP_GRAM_NS, count * alg_flops_per_matrix(n, m))
@@ -266,7 +266,8 @@ def run_ours(args, rank, world, dist):
             r["standard_ns_ms_per_call"] = std["ms_per_call"]
             r["gram_vs_standard_speedup"] = std["ms_per_call"] / r["ms_per_call"]
             chain = n <= 128 and m <= 512
-            r["path"] = ("on-chip chain kernel, one CTA per matrix" if chain else
+            pack = 4 if n <= 32 else 2 if n <= 64 else 1
+            r["path"] = (f"on-chip chain kernel, {pack} matrices per CTA chain" if chain else
                          "batched tiles, 1-CTA 128 x 128" if n <= 128 else "batched tiles, 2-CTA 256 x 256")
             if chain:
                 os.environ["GNS_CHAIN_SMALL"] = "0"

@@ -105,8 +105,9 @@ struct Group {
   void* D;
   const float* inv;  // per-matrix 1/(||X||_F + eps) (norm_mode 1)
   long long ldd, sd;
-  int first, count, n, m, mp;  // mp: m padded to 64
+  int first, count, n, m, mp;  // first: the group's first job of the launch; mp: m padded to 64
   int xt;                      // the input X is stored transposed (m x n)
+  int pack, nb;                // matrices per 128-row chain (1, 2 or 4) and rows per block (128 / pack)
   int d_f16, d_trans, has_c;
   int d_tma;  // the result goes out by TMA stores (no addend to read)
   float alpha, beta;
@@ -227,10 +228,14 @@ struct Ctx {
   int r, g, ew, lane, n, m, mp;
   int d_f16, d_trans, has_c, d_tma;
   float alpha, beta;
-  uint16_t* D;  // this matrix's output
+  uint16_t* D;  // the output of this thread's row block's matrix
   long long ldd;
   const CUtensorMap* tmD;
-  int b;        // this matrix's index
+  int b;        // that matrix's index in its group
+  int nb, kb;   // rows per block (128 / pack) and this thread's block (rows kb*nb .. +nb-1)
+  int rl;       // this thread's row within its block
+  bool valid;   // the block holds a matrix (the last job of a group may have fewer)
+  bool badrow;  // the block's matrix is not finite: its X rows are kept at zero
 };
 
 // two 16-bit values of one word (the first in the low half) as fp32, and back (nearest even)
@@ -255,7 +260,7 @@ __device__ __forceinline__ uint32_t pack2(float2 y) {
 // anything is stored: C may be the output buffer itself (the in-place updates), and a load
 // placed after a store to it could not start before it.
 template <bool F16, int EPI>
-__device__ __forceinline__ void nn_chunks(const Ctx& x, const Op o, int g, const float (&v)[32], float k) {
+__device__ __forceinline__ void nn_chunks(const Ctx& x, const Op o, int g, const float (&v)[32], float k, bool keep) {
   const int r = x.r;
   const int pb = (g >> 1) * PANEL_BYTES, jb = 4 * (g & 1);
   uint8_t* __restrict__ dp = x.sm + buf_off(o.d) + pb;
@@ -282,7 +287,9 @@ __device__ __forceinline__ void nn_chunks(const Ctx& x, const Op o, int g, const
         y[i] = __ffma2_rn(p0, unpack2<F16>(cu[i]), __fmul2_rn(p1, a));
       else
         y[i] = __ffma2_rn(p0, unpack2<F16>(cu[i]), a);
-      pk[i] = pack2<F16>(y[i]);
+      // packed chains: entries outside the diagonal blocks are exact zeros (selected, so that
+      // a non-finite block cannot leak into the others)
+      pk[i] = keep ? pack2<F16>(y[i]) : 0u;
     }
     const uint32_t off = chunk_off(r, jb + jj);
     *reinterpret_cast<uint4*>(dp + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
@@ -290,7 +297,7 @@ __device__ __forceinline__ void nn_chunks(const Ctx& x, const Op o, int g, const
   }
   // Q = Z + a I: the diagonal entry (r, r) gets the fp32 value of Z plus a, rounded once
   // (Dion3 appendix B.2.3: adding a_t I to an already rounded Z would lose a_t's low bits);
-  // rows at and beyond n stay zero. Column r is local column lane of group r / 32, i.e. of
+  // rows at and beyond n (of the row's block) stay zero. Column r is local column lane of group r / 32, i.e. of
   // this group in the warps of lane quarter g (a warp-uniform test).
   if (qinit && g == (r >> 5)) {
     float ad = 0.f;
@@ -299,7 +306,7 @@ __device__ __forceinline__ void nn_chunks(const Ctx& x, const Op o, int g, const
       if (k2i == x.lane) ad = v[k2i];
     const uint32_t doff = (uint32_t)(r * 128 + (((jb + (x.lane >> 3)) ^ (r & 7)) << 4) + (x.lane & 7) * 2);
     const float zd = fmaf(o.p0, h16_to_f(*reinterpret_cast<const uint16_t*>(cp + doff), F16), o.p1 * ad);
-    if (r < x.n) *reinterpret_cast<uint16_t*>(qp + doff) = f_to_h16(zd + o.p2, F16);
+    if (x.rl < x.n) *reinterpret_cast<uint16_t*>(qp + doff) = f_to_h16(zd + o.p2, F16);
   }
 }
 
@@ -312,12 +319,13 @@ __device__ __forceinline__ void epi_nn(const Ctx& x, const Op o, float sc) {
   for (int G = x.g; G < 4; G += NG) {
     float v[32];
     load_acc32(x.trow, 128 * o.slot + 32 * G, v);
+    const bool keep = (32 * G) / x.nb == x.kb;  // the group lies in this row's block
     if (o.epi == E_SCALE)
-      nn_chunks<F16, E_SCALE>(x, o, G, v, sc);
+      nn_chunks<F16, E_SCALE>(x, o, G, v, sc, keep);
     else if (o.epi == E_POLY)
-      nn_chunks<F16, E_POLY>(x, o, G, v, 1.f);
+      nn_chunks<F16, E_POLY>(x, o, G, v, 1.f, keep);
     else
-      nn_chunks<F16, E_AXPY>(x, o, G, v, 1.f);
+      nn_chunks<F16, E_AXPY>(x, o, G, v, 1.f, keep);
   }
 }
 
@@ -395,12 +403,19 @@ __device__ __forceinline__ bool epi_ax(const Ctx& x, const Op o, float s, int& n
         uint32_t pk[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-          pk[i] = pack2<F16>(__fmul2_rn(su2, make_float2(v[8 * jj + 2 * i], v[8 * jj + 2 * i + 1])));
+          pk[i] = x.badrow ? 0u : pack2<F16>(__fmul2_rn(su2, make_float2(v[8 * jj + 2 * i], v[8 * jj + 2 * i + 1])));
         *reinterpret_cast<uint4*>(xp + chunk_off(r, jb + jj)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
       continue;
     }
-    const int col_g = 32 * G, row_q = r & ~31;
+    // this warp's 32 rows lie in one block: rows row_q .. row_q + 31 of its matrix
+    const int col_g = 32 * G, row_q = (r & ~31) % x.nb;
+    if (x.badrow) {
+      // a packed block whose input was not finite: its result is marked not finite (its
+      // zeroed rows would otherwise give finite zeros after a restart)
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = __int_as_float(0x7fc00000);
+    }
     if (x.d_tma) {
       // D = alpha su acc, rounded once, staged as this warp's 32 x 32 block of 16-bit values
       // (64-byte rows, chunk c of row i at c ^ ((i / 2) mod 4): the TMA 64-byte swizzle) in one
@@ -437,11 +452,11 @@ __device__ __forceinline__ bool epi_ax(const Ctx& x, const Op o, float s, int& n
           *reinterpret_cast<uint16_t*>(blk + (c + 1) * 64 + o1) = (uint16_t)(pk >> 16);
         }
       }
-      bad |= !(z.x == 0.f && z.y == 0.f) && r < x.n;
+      bad |= !(z.x == 0.f && z.y == 0.f) && x.rl < x.n && x.valid;
       fence_proxy_async_smem();
       __syncwarp();
-      // (blocks wholly outside D are not stored; the others start inside it)
-      if (lane == 0 && row_q < x.n && col_g < x.m) {
+      // (blocks wholly outside D, or of a job's missing matrices, are not stored)
+      if (lane == 0 && x.valid && row_q < x.n && col_g < x.m) {
         if (!x.d_trans)
           tma_store_3d(x.tmD, blk, col_g, row_q, x.b);
         else
@@ -464,7 +479,7 @@ __device__ __forceinline__ bool epi_ax(const Ctx& x, const Op o, float s, int& n
         const int rl = 4 * k + (lane >> 3), c = lane & 7;
         const int row = row_q + rl, col = col_g + 4 * c;
         const float4 y = *reinterpret_cast<const float4*>(stg + rl * 128 + ((c ^ (rl & 7)) << 4));
-        if (row < x.n && col < x.m)
+        if (x.valid && row < x.n && col < x.m)
           bad |= out4(x, x.D + (long long)row * x.ldd + col, y, kout, col + 4 <= x.m, x.m - col);
       }
     } else {
@@ -530,7 +545,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) chain_kernel(const __grid_cons
       uint32_t ipar = 0;
       for (int i = blockIdx.x; i < P.total; i += gridDim.x, ++it) {
         const Group& gr = P.grp[group_of(P, i)];
-        const int b = i - gr.first, mp = gr.mp;
+        const int b = (i - gr.first) * gr.pack, mp = gr.mp, nb = gr.nb;
         const uint32_t xbytes = (uint32_t)(mp * 256);
         if (it > 0) {
           // the region is free once the last product (and, when its epilogue reads X, that
@@ -540,7 +555,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) chain_kernel(const __grid_cons
         }
         mbar_arrive_expect_tx(bar_x, xbytes);
         if (!gr.xt) {
-          for (int p = 0; p < mp / 64; ++p) tma_load_3d(sm + p * PANEL_BYTES, &gr.tmX, bar_x, 64 * p, 0, b);
+          // the job's matrices b .. b + pack - 1 in row blocks of nb rows (a matrix index past
+          // the group's last reads as zeros)
+          for (int p = 0; p < mp / 64; ++p)
+            for (int k = 0; k < gr.pack; ++k)
+              tma_load_3d(sm + p * PANEL_BYTES + k * nb * 128, &gr.tmX, bar_x, 64 * p, 0, b + k);
         } else {
           for (int ib = 0; ib < 2; ++ib)
             for (int kb = 0; kb < mp / 64; ++kb)
@@ -612,7 +631,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) chain_kernel(const __grid_cons
     for (int mi = blockIdx.x; ok && mi < P.total; mi += gridDim.x, ++it) {
       const uint32_t par = (uint32_t)(it & 1);
       const Group& gr = P.grp[group_of(P, mi)];
-      const int b = mi - gr.first;
+      const int pack = gr.pack, nb = gr.nb;
+      cx.nb = nb;
+      cx.kb = r / nb;
+      cx.rl = r - cx.kb * nb;
+      const int b = (mi - gr.first) * pack + cx.kb;  // this row block's matrix
+      cx.valid = b < gr.count;
+      cx.badrow = false;
       cx.n = gr.n;
       cx.m = gr.m;
       cx.mp = gr.mp;
@@ -624,10 +649,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) chain_kernel(const __grid_cons
       cx.ldd = gr.ldd;
       cx.d_tma = gr.d_tma;
       cx.tmD = &gr.tmD;
-      cx.D = static_cast<uint16_t*>(gr.D) + (long long)b * gr.sd;
+      cx.D = static_cast<uint16_t*>(gr.D) + (long long)(cx.valid ? b : 0) * gr.sd;
       cx.b = b;
       float s = 1.f;
-      if (norm_mode == 1) s = gr.inv[b];
+      if (norm_mode == 1 && cx.valid) s = gr.inv[b];
       // X has landed (the epilogues of X <- a X + B X and of the standard-NS result read it)
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_x, par, abortv, P.status)))) break;
       for (int i = 0; i < nops; ++i) {
@@ -642,9 +667,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) chain_kernel(const __grid_cons
             __syncwarp();
           }
         } else {
-          if ((o.flags & F_USER) && norm_mode == 2) {
+          if (i == 0 && (norm_mode == 2 || pack > 1)) {
             // ||X||_F^2 = trace(X X^T): the diagonal of this accumulator (row r = 32 q + lane,
-            // column r: local column lane of group q), summed in a fixed order
+            // column r: local column lane of group q), summed per row block (one matrix each)
+            // in a fixed order; a block whose sum is not finite has its X rows zeroed, so that
+            // the products of a packed chain keep it from the other blocks
             float d = 0.f;
             if ((q % NG) == g) {
               float v[32];
@@ -662,8 +689,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) chain_kernel(const __grid_cons
             // microseconds
             float t = 0.f;
 #pragma unroll
-            for (int w = 0; w < EPI_WARPS; ++w) t += part[par * EPI_WARPS + w];
-            s = 1.f / (sqrtf(t) + eps);
+            for (int w = 0; w < EPI_WARPS; ++w)
+              if ((32 * ((FIRST_EPI_WARP + w) & 3)) / nb == cx.kb) t += part[par * EPI_WARPS + w];
+            if (norm_mode == 2 && (o.flags & F_USER)) s = 1.f / (sqrtf(t) + eps);
+            if (pack > 1 && !isfinite(t)) {
+              cx.badrow = true;
+              for (int p = 0; p < cx.mp / 64; ++p)
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                  *reinterpret_cast<uint4*>(sm + p * PANEL_BYTES + chunk_off(r, j)) = make_uint4(0u, 0u, 0u, 0u);
+            }
           }
           const float sc = (o.flags & F_USER) ? s * s : 1.f;
           if (f16)
@@ -940,9 +975,15 @@ int launch_chain(const ChainCall& c, std::string* err) {
     for (size_t gi = g0; gi < g1; ++gi) {
       const ChainGroup& cg = c.groups[gi];
       Group& G = P.grp[P.ngroups++];
+      // wide matrices of at most 64 (32) rows go two (four) to a 128-row chain, each in a
+      // diagonal block of the iterates (GNS_CHAIN_PACK=0 turns this off)
+      const char* penv = std::getenv("GNS_CHAIN_PACK");
+      const bool pack_ok = !cg.xt && !(penv && penv[0] == '0');
+      G.pack = pack_ok && cg.n <= 32 ? 4 : pack_ok && cg.n <= 64 ? 2 : 1;
+      G.nb = NP / G.pack;
       G.first = (int)total;
       G.count = (int)cg.B;
-      total += cg.B;
+      total += (cg.B + G.pack - 1) / G.pack;
       G.n = (int)cg.n;
       G.m = (int)cg.m;
       G.mp = (int)((cg.m + 63) / 64 * 64);
@@ -958,7 +999,7 @@ int launch_chain(const ChainCall& c, std::string* err) {
       G.beta = cg.beta;
       // X: rows of the n x m operand (box 64 columns x 128 rows), or for a tall matrix its
       // m x n storage (box 64 x 64); zero fill outside the matrix
-      if (!encode16(&G.tmX, cg.x, cg.B, 64u, cg.xt ? 64u : 128u, f16, CU_TENSOR_MAP_SWIZZLE_128B, err))
+      if (!encode16(&G.tmX, cg.x, cg.B, 64u, cg.xt ? 64u : (uint32_t)G.nb, f16, CU_TENSOR_MAP_SWIZZLE_128B, err))
         return GNS_ERR_CUDA;
       // the result, when no addend is read: 32 x 32 boxes of its storage
       G.d_tma = !cg.has_c;

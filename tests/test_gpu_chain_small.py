@@ -280,3 +280,84 @@ def test_chain_muon_step_several_groups():
             mag = np.maximum(np.maximum(np.abs(Wg[b]), np.abs(W_or)), 2.0 ** -126)
             excess = np.maximum(np.abs(dW) - 0.5 * 2.0 ** (np.floor(np.log2(mag)) - 7), 0.0)
             assert np.linalg.norm(excess) / np.linalg.norm(0.02 * O) < TOL_BF16, (r, k, b)
+
+
+def _pack_off(fn):
+    old = os.environ.get("GNS_CHAIN_PACK")
+    os.environ["GNS_CHAIN_PACK"] = "0"
+    try:
+        return fn()
+    finally:
+        if old is None:
+            del os.environ["GNS_CHAIN_PACK"]
+        else:
+            os.environ["GNS_CHAIN_PACK"] = old
+
+
+# Gaussian matrices of at most 64 rows: bf16 storage costs 1.3-3.2 % on every path (the
+# packed and unpacked chains and the batched tile path give the same errors to three digits)
+TOL_SMALL_N = 4e-2
+
+
+@pytest.mark.parametrize("count,rows,cols", [(5, 64, 200), (7, 32, 96), (6, 48, 320), (9, 20, 64), (3, 1, 24),
+                                            (6, 64, 64), (4, 33, 512)])
+def test_chain_packed(count, rows, cols):
+    """Wide matrices of at most 64 (32) rows packed two (four) to a 128-row chain in diagonal
+    blocks: bit-identical to the same group unpacked (GNS_CHAIN_PACK=0), each matrix against
+    the oracle (standard NS for a square group), groups whose last chain is partly empty."""
+    bits, x = bf16_input(92, (count, rows, cols))
+    xt = bits_to_torch(bits)
+    fn = gns.ns_standard_batched if rows == cols else gns.gram_ns_batched
+    st = _status()
+    got = fn(xt, status=st)[0]
+    unpacked = _pack_off(lambda: fn(xt))[0]
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(got, unpacked)
+    got = torch_to_f64(got)
+    tol = TOL_RANK1 if rows == 1 else TOL_SMALL_N
+    for b in range(count):
+        want = ons.ns_standard(x[b], ons.QUINTIC_FIXED) if rows == cols else omuon.orthogonalize(x[b])
+        assert rel_fro(got[b], want) < tol, b
+
+
+def test_chain_packed_muon_step():
+    """A Muon step over packed chains: momentum bit-exact, the weight update against the oracle."""
+    count, rows, cols = 11, 64, 256
+    s = 1.0 / np.sqrt(cols)
+    Wb, _ = bf16_input(93, (count, rows, cols), s, stream=0)
+    Gb, _ = bf16_input(93, (count, rows, cols), s, stream=1)
+    Mb, _ = bf16_input(93, (count, rows, cols), s, stream=2)
+    Wt, Gt, Mt = bits_to_torch(Wb), bits_to_torch(Gb), bits_to_torch(Mb)
+    gns.muon_step(Wt, Gt, Mt, lr=0.02, momentum=0.95, weight_decay=0.1)
+    torch.cuda.synchronize()
+    Mg, Wg = torch_to_bits(Mt), torch_to_f64(Wt)
+    for b in range(count):
+        W_or, M_or, O = omuon.muon_step(Wb[b], Gb[b], Mb[b], lr=0.02, mu=0.95, weight_decay=0.1)
+        assert np.array_equal(Mg[b], M_or)
+        dW = Wg[b] - W_or
+        mag = np.maximum(np.maximum(np.abs(Wg[b]), np.abs(W_or)), 2.0 ** -126)
+        excess = np.maximum(np.abs(dW) - 0.5 * 2.0 ** (np.floor(np.log2(mag)) - 7), 0.0)
+        assert np.linalg.norm(excess) / np.linalg.norm(0.02 * O) < TOL_BF16, b
+
+
+@pytest.mark.parametrize("rows,cols,bad", [(64, 200, 2), (32, 96, 5), (64, 64, 1)])
+def test_chain_packed_nonfinite_isolated(rows, cols, bad):
+    """A non-finite entry in one matrix of a packed chain: reported, that matrix's result not
+    finite, and the matrices packed with it bit-identical to the same call without it (their
+    rows never meet its values)."""
+    count = 8
+    bits, x = bf16_input(94, (count, rows, cols))
+    clean = bits_to_torch(bits)
+    dirty = clean.clone()
+    dirty[bad, 3, 7] = float("inf")
+    fn = gns.ns_standard_batched if rows == cols else gns.gram_ns_batched
+    ref = fn(clean)[0]
+    st = _status()
+    out = fn(dirty, status=st)[0]
+    torch.cuda.synchronize()
+    assert int(st.item()) & 1
+    assert not torch.isfinite(out[bad]).all()
+    for b in range(count):
+        if b != bad:
+            assert torch.equal(out[b], ref[b]), b
