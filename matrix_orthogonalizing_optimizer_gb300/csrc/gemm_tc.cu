@@ -1107,9 +1107,20 @@ int gemm_launch_tc(const GemmOp* ops, int nops, const uint32_t* dep_masks, int* 
   }
   // CTA-group size: single CTAs with 128 x 128 tiles when every product has at most 128
   // rows (GNS_CTA_GROUP=1 or 2 in the environment overrides, a tuning knob)
-  int64_t max_m = 0;
-  for (int i = 0; i < nops; ++i) max_m = std::max<int64_t>(max_m, ops[i].M);
-  int cg = max_m <= 128 ? 1 : 2;
+  int64_t max_m = 0, sym_pair_tiles = 0;
+  for (int i = 0; i < nops; ++i) {
+    max_m = std::max<int64_t>(max_m, ops[i].M);
+    if (ops[i].sym) {
+      const int64_t t = (ops[i].M + 255) / 256;
+      sym_pair_tiles = std::max<int64_t>(sym_pair_tiles, ops[i].batch * t * (t + 1) / 2);
+    }
+  }
+  // 1-CTA 128 x 128 tiles for products of at most 256 rows (a 256 x 256 tile of an n = 256
+  // product has 4 K slices), and for small batches of n <= 1024 whose largest symmetric stage
+  // has at most 48 pair tiles, which would leave most of the chip's 76 CTA pairs idle
+  // (measured: 1-4 matrices of 1024 x 4096 and 16 of 512 x 2048 run 3-13 % faster on 1-CTA
+  // tiles, 8 or more of 1024 x 4096 10-40 % slower)
+  int cg = max_m <= 256 || (max_m <= 1024 && sym_pair_tiles > 0 && sym_pair_tiles <= 48) ? 1 : 2;
   if (const char* env = getenv("GNS_CTA_GROUP")) {
     if (env[0] == '1' && env[1] == 0) cg = 1;
     if (env[0] == '2' && env[1] == 0) cg = 2;
