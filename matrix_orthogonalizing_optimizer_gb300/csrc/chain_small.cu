@@ -91,7 +91,8 @@ struct Op {
   uint8_t slot;  // first 128-column accumulator
   uint8_t flags;
   int16_t dep;   // wait for this op's epilogue before issuing (-1: none)
-  int16_t pad;
+  int8_t half;   // K_AX: the half of the columns it computes (0 or 1), or -1: all
+  uint8_t pad;
   float p0, p1, p2;
 };
 
@@ -117,6 +118,8 @@ struct Params {
   Group grp[MAX_GROUPS];
   Op ops[MAX_OPS];  // one list for every group (X <- Q X and Q X take all four accumulators)
   int nops, ngroups, total;
+  int op0_prev;   // the last op of a matrix that uses accumulator 0: the next matrix's first
+                  // product waits for its epilogue
   int ab_f16;     // products in fp16 (else bf16)
   int norm_mode;  // 0: s = 1; 1: s = inv[b]; 2: from the trace of the first Gram product
   int check_finite;
@@ -153,6 +156,10 @@ __device__ __forceinline__ void load_acc32(uint32_t trow, int col, float (&v)[32
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(u[i]);
 }
+
+// The columns of the first half of a split A X product: mp / 2 rounded up to a whole 64-column
+// panel (the operand descriptors start on panel boundaries), at most 256 (one MMA).
+__host__ __device__ __forceinline__ int ax_split(int mp) { return min(256, (mp / 2 + 63) & ~63); }
 
 // ------------------------------------------------------------------------------------
 // MMA issue (one thread). Descriptors: a K-major operand advances 32 bytes per K = 16 step
@@ -194,18 +201,22 @@ __device__ __forceinline__ void issue_op(const Op o, int mp, int ab, bool xt_in,
     }
   } else {
     // A X, n x m: B(j,k) = X[k][j], MN-major from the row layout, K-major from the
-    // transposed one; N = 256 columns per MMA group
+    // transposed one. Columns [c0, c0 + N) go to TMEM columns from 256 hh: the whole
+    // product in N = 256 pieces, or the op's half (the first ax_split(mp) columns, or the rest)
     const uint32_t A = s + buf_off(o.a);
-    for (int hh = 0; hh * 256 < mp; ++hh) {
-      const int N = min(256, mp - 256 * hh);
+    const int h0 = o.half < 0 ? 0 : o.half, h1 = o.half < 0 ? 2 : o.half + 1;
+    for (int hh = h0; hh < h1; ++hh) {
+      const int c0 = o.half < 0 ? 256 * hh : (hh == 0 ? 0 : ax_split(mp));
+      const int N = o.half < 0 ? min(256, mp - c0) : (hh == 0 ? ax_split(mp) : mp - c0);
+      if (N <= 0) continue;
       const uint32_t idesc = idesc_f16kind_f32(128, N, 0, xt ? 0 : 1, ab);
       const uint32_t d = tmem + 256u * hh;
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
         const uint64_t ad = sdesc_sw128(A + (ks >> 2) * PANEL_BYTES + (ks & 3) * 32, 16, 1024);
         const uint64_t bd =
-            xt ? sdesc_sw128(s + (ks >> 2) * (mp * 128) + (ks & 3) * 32 + hh * 256 * 128, 16, 1024)
-               : sdesc_sw128(s + 4 * hh * PANEL_BYTES + ks * 2048, PANEL_BYTES, 1024);
+            xt ? sdesc_sw128(s + (ks >> 2) * (mp * 128) + (ks & 3) * 32 + c0 * 128, 16, 1024)
+               : sdesc_sw128(s + (c0 / 64) * PANEL_BYTES + ks * 2048, PANEL_BYTES, 1024);
         umma_f16kind(d, ad, bd, idesc, ks != 0 ? 1u : 0u);
       }
     }
@@ -375,7 +386,12 @@ __device__ __forceinline__ bool epi_ax(const Ctx& x, const Op o, float s, int& n
   const float kout = x.alpha * su;  // E_OUT: D = alpha su (acc [+ p0 X]) + beta D
   bool bad = false;
   uint8_t* __restrict__ stg = x.sm + OFF_R + x.ew * 4096;  // EPI_WARPS x 4 KiB <= R and Z
-  for (int G = x.g; G < x.mp / 32; G += NG) {
+  // the op's 32-column groups [g0, g1): all, or one half, whose columns from ax_split(mp) lie
+  // in TMEM from column 256 (tshift)
+  const int gs = ax_split(x.mp) / 32;
+  const int g0 = o.half == 1 ? gs : 0, g1 = o.half == 0 ? gs : x.mp / 32;
+  const int tshift = o.half == 1 ? 256 - 32 * gs : 0;
+  for (int G = g0 + x.g; G < g1; G += NG) {
     uint8_t* __restrict__ xp = x.sm + (G >> 1) * PANEL_BYTES;
     const int jb = 4 * (G & 1);
     uint4 cw[4];
@@ -384,7 +400,7 @@ __device__ __forceinline__ bool epi_ax(const Ctx& x, const Op o, float s, int& n
       for (int jj = 0; jj < 4; ++jj) cw[jj] = *reinterpret_cast<const uint4*>(xp + chunk_off(r, jb + jj));
     }
     float v[32];
-    load_acc32(x.trow, 32 * G, v);
+    load_acc32(x.trow, 32 * G + tshift, v);
     if (rdx) {
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj) {
@@ -589,8 +605,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) chain_kernel(const __grid_cons
         for (int i = 0; i < nops; ++i) {
           const Op o = P.ops[i];
           if (i == 0) {
-            // the previous matrix's last epilogue has read every accumulator; X has landed
-            if (it > 0 && !(ok = mbar_wait(&bar_epi[nops - 1], par ^ 1u, abortv, P.status))) break;
+            // the previous matrix's last user of accumulator 0 has read it (later epilogues of
+            // that matrix come before this one's in the epilogue warps' order); X has landed
+            if (it > 0 && !(ok = mbar_wait(&bar_epi[P.op0_prev], par ^ 1u, abortv, P.status))) break;
             if (!(ok = mbar_wait(bar_x, par, abortv, P.status))) break;
           }
           if (o.dep >= 0 && !(ok = mbar_wait(&bar_epi[o.dep], par, abortv, P.status))) break;
@@ -662,18 +679,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) chain_kernel(const __grid_cons
         if (o.kind == K_AX) {
           bad |= f16 ? epi_ax<true>(cx, o, s, nblk) : epi_ax<false>(cx, o, s, nblk);
           // the staging blocks lie in the R and Z buffers, which the next epilogues rewrite
-          if (o.epi == E_OUT && cx.d_tma) {
+          // (a first half is followed by the second, which stages in the same blocks in turn)
+          if (o.epi == E_OUT && cx.d_tma && o.half != 0) {
             if (lane == 0) bulk_wait_read<0>();
             __syncwarp();
           }
         } else {
-          if (i == 0 && (norm_mode == 2 || pack > 1)) {
+          if (i == 0) {
             // ||X||_F^2 = trace(X X^T): the diagonal of this accumulator (row r = 32 q + lane,
             // column r: local column lane of group q), summed per row block (one matrix each)
             // in a fixed order; a block whose sum is not finite has its X rows zeroed, so that
-            // the products of a packed chain keep it from the other blocks
+            // the products of a packed chain keep it from the other blocks. The exchange is
+            // also the point from which every warp has finished the previous matrix (its
+            // result staging in R and Z, read by its stores), before any warp writes R.
+            const bool need = norm_mode == 2 || pack > 1;
             float d = 0.f;
-            if ((q % NG) == g) {
+            if (need && (q % NG) == g) {
               float v[32];
               load_acc32(cx.trow, 128 * o.slot + 32 * q, v);
 #pragma unroll
@@ -746,7 +767,10 @@ struct Builder {
     int dep = -1;
     for (int bf : reads) dep = std::max(dep, last_w[bf]);
     int s0 = 0, ns = ax_slots;
-    if (o.kind != chain::K_AX) {
+    if (o.kind == chain::K_AX && o.half >= 0) {
+      s0 = 2 * o.half;
+      ns = 2;
+    } else if (o.kind != chain::K_AX) {
       s0 = next_slot;
       ns = 1;
       next_slot = (next_slot + 1) & 3;
@@ -766,6 +790,7 @@ Op make_op(uint8_t kind, uint8_t epi) {
   std::memset(&o, 0, sizeof(o));
   o.kind = kind;
   o.epi = epi;
+  o.half = -1;
   return o;
 }
 
@@ -836,10 +861,16 @@ void build_gram(Builder& bd, const gns_ns_params& ns, bool user) {
     }
     q_id = false;
   }
-  Op out = make_op(K_AX, E_OUT);
-  out.a = BUF_Q;
-  out.flags = fl();
-  bd.add(out, {BUF_Q, BUF_X}, {});
+  // the result in two column halves: the first half's epilogue runs under the second half's
+  // products, and the next matrix's first product (accumulator 0) under the second half's
+  // epilogue (the result writes nothing the products read)
+  for (int h = 0; h < 2; ++h) {
+    Op out = make_op(K_AX, E_OUT);
+    out.a = BUF_Q;
+    out.flags = fl();
+    out.half = (int8_t)h;
+    bd.add(out, {BUF_Q, BUF_X}, {});
+  }
 }
 
 // Dion3 Algorithm 1 with the same products: A = X X^T, B = b A + c A^2, X <- a X + B X.
@@ -965,6 +996,7 @@ int launch_chain(const ChainCall& c, std::string* err) {
     std::memset(&P, 0, sizeof(P));
     P.nops = (int)bd.ops.size();
     for (int i = 0; i < P.nops; ++i) P.ops[i] = bd.ops[i];
+    P.op0_prev = bd.last_slot[0];
     P.ab_f16 = f16;
     P.norm_mode = !c.x_user ? 0 : c.groups[0].inv ? 1 : 2;
     P.eps = c.eps;
