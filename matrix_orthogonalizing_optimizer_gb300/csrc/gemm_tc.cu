@@ -75,8 +75,14 @@ struct Geo {
   static constexpr int TMEM_COLS = 2 * TILE;        // two fp32 accumulators
   static constexpr int KSH = CG == 2 ? 2 : 1;       // log2 of 64-wide K slices per tile edge
 };
-constexpr int BAR_BYTES = 1024;
+constexpr int BAR_BYTES = 2048;
 constexpr int RM_IDX_OFF = 512;  // in the barrier area: W row of each tile row (row-mapped outputs)
+// In the barrier area: a ring of the epilogue's per-tile parameters (TileInfo), filled ahead by
+// one lane of the C-loader warp, and its full / empty barriers.
+constexpr int INFO_RING = 8;
+constexpr int INFO_OFF = 1024;
+constexpr int INFO_BAR_OFF = INFO_OFF + INFO_RING * 32;
+static_assert(INFO_BAR_OFF + 2 * INFO_RING * 8 <= BAR_BYTES, "tile-info ring");
 
 // Shared-memory plan of a kernel with STAGES operand stages and a ring of C_BUFS C chunks.
 // Two plans are compiled: a deep operand ring (6 stages, 1 C chunk) pays on launches of
@@ -93,7 +99,7 @@ struct Plan {
   static constexpr int SMEM_BYTES = 1024 + OFF_BAR + BAR_BYTES;
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert((2 * STAGES + 4 + 2 * C_BUFS) * 8 + 16 <= RM_IDX_OFF, "barrier area");
-  static_assert(RM_IDX_OFF + TM * 4 <= BAR_BYTES, "row-map area");
+  static_assert(RM_IDX_OFF + TM * 4 <= INFO_OFF, "row-map area");
 };
 using DeepPlan = Plan<6, 1>;
 using ShallowPlan = Plan<4, 4>;
@@ -228,6 +234,25 @@ __device__ __forceinline__ int b_major(const KLoop& pr, int J, int kb) {
 struct TileCoord {
   int p, b, I, J;
 };
+
+// What the epilogue needs of one tile, decoded and scaled ahead of it: decoding reads the
+// parameter block with tile-dependent indices, and the per-matrix scale is a global load, so
+// done at the top of each tile they kept the epilogue (the launch's bottleneck on tiles of
+// few K slices) waiting between tiles.
+enum : uint32_t {
+  TI_HAS_C = 1u << 8, TI_MIRROR = 1u << 9, TI_DIAG = 1u << 10, TI_C_TRANS = 1u << 11, TI_C_F16 = 1u << 12,
+  TI_D_TRANS = 1u << 13, TI_D_F16 = 1u << 14, TI_CHECK = 1u << 15, TI_HAS_D2 = 1u << 16, TI_PUBLISH = 1u << 17,
+  TI_ROWMAP = 1u << 18, TI_DMODE_SHIFT = 19  // bits 0-7: the problem; 19-20: the D chunk mode
+};
+struct TileInfo {
+  uint32_t pf;     // problem and flags
+  int b;           // matrix
+  uint32_t ij;     // tile row I (low half) and column J (high half)
+  int ctr_off;     // the problem's completion counters
+  float alpha, beta, gamma;
+  int diag_limit;
+};
+static_assert(sizeof(TileInfo) == 32, "tile-info entry");
 
 // s0: a segment index at or below the tile's (every role walks its tiles in increasing
 // order, so the previous tile's segment is a valid start); *seg receives the tile's.
@@ -448,6 +473,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* epi_flag = abort_flag + 1;
   volatile int* ready_tile = abort_flag + 2;  // highest tile of this pair whose inputs are complete
+  TileInfo* const info = reinterpret_cast<TileInfo*>(smem + OFF_BAR + INFO_OFF);
+  uint64_t* const info_full = reinterpret_cast<uint64_t*>(smem + OFF_BAR + INFO_BAR_OFF);
+  uint64_t* const info_empty = info_full + INFO_RING;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -468,6 +496,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
     for (int q = 0; q < C_BUFS; ++q) {
       mbar_init(&cfull[q], 1);
       mbar_init(&cempty[q], EPI_WARPS);
+    }
+    for (int q = 0; q < INFO_RING; ++q) {
+      mbar_init(&info_full[q], 1);
+      mbar_init(&info_empty[q], 1);
     }
     *abort_flag = 0;
     *epi_flag = 1;
@@ -633,6 +665,47 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         *ready_tile = tile;
       }
     }
+    if (lane == 2) {
+      // ---------------- tile-info lane (both CTAs) ----------------
+      // Decodes this pair's tiles and the epilogue's per-tile parameters into the TileInfo
+      // ring, up to INFO_RING tiles ahead of the epilogue.
+      int seg = 0, local = 0;
+      for (int tile = pair; tile < P.total_tiles; tile += npairs, ++local) {
+        const int slot = local % INFO_RING;
+        if (!mbar_wait(&info_empty[slot], ((local / INFO_RING) & 1u) ^ 1u, abort_flag, P.status)) break;
+        const TileCoord c = decode_tile(P, tile, &seg);
+        const Problem& pr = P.prob[c.p];
+        float alpha = pr.alpha, beta = pr.beta;
+        if (pr.scale) {
+          const float sc = pr.scale[c.b];
+          alpha *= powi(sc, pr.alpha_pow);
+          beta *= powi(sc, pr.beta_pow);
+        }
+        uint32_t pf = (uint32_t)c.p;
+        if (pr.has_c) pf |= TI_HAS_C;
+        if (pr.sym && c.I != c.J && pr.mirror_out) pf |= TI_MIRROR;
+        if (pr.has_d2 && c.I == c.J) pf |= TI_DIAG;
+        if (pr.c_trans) pf |= TI_C_TRANS;
+        if (pr.c_f16) pf |= TI_C_F16;
+        if (pr.d_trans) pf |= TI_D_TRANS;
+        if (pr.d_f16) pf |= TI_D_F16;
+        if (pr.check_finite) pf |= TI_CHECK;
+        if (pr.has_d2) pf |= TI_HAS_D2;
+        if (pr.publish) pf |= TI_PUBLISH;
+        if (c.p == P.rmo.prob) pf |= TI_ROWMAP;
+        pf |= (uint32_t)(pr.d_trans ? 1 : pr.d_mode) << TI_DMODE_SHIFT;
+        TileInfo& e = info[slot];
+        e.pf = pf;
+        e.b = c.b;
+        e.ij = (uint32_t)c.I | ((uint32_t)c.J << 16);
+        e.ctr_off = pr.ctr_off;
+        e.alpha = alpha;
+        e.beta = beta;
+        e.gamma = pr.gamma;
+        e.diag_limit = pr.diag_limit;
+        mbar_arrive(&info_full[slot]);  // release: the entry is visible to the epilogue's wait
+      }
+    }
     if (lane == 0) {
       // ---------------- C-tile loader (both CTAs) ----------------
       // Loads the C chunks of the next tile as soon as the epilogue releases each buffer,
@@ -676,30 +749,43 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
     int local = 0;
     int seg = 0;
     for (int tile = pair; tile < P.total_tiles; tile += npairs, ++local) {
-      const TileCoord c = decode_tile(P, tile, &seg);
-      const Problem& pr = P.prob[c.p];
       const int acc = local & 1;
       const uint32_t aph = (local >> 1) & 1;
-      float alpha = pr.alpha, beta = pr.beta;
-      if (pr.scale) {
-        const float sc = pr.scale[c.b];
-        alpha *= powi(sc, pr.alpha_pow);
-        beta *= powi(sc, pr.beta_pow);
+      const int islot = local % INFO_RING;
+      // the tile's parameters (decoded ahead by the tile-info lane); then, unless the tile's
+      // output is row-mapped (whose setup comes first), its accumulator
+      if (et == 0) {
+        bool okw = mbar_wait(&info_full[islot], (local / INFO_RING) & 1u, abort_flag, P.status);
+        if (okw && !(info[islot].pf & TI_ROWMAP)) okw = mbar_wait(&tfull[acc], aph, abort_flag, P.status);
+        *epi_flag = okw ? 1 : 0;
       }
-      const bool has_c = pr.has_c != 0;
-      const bool mirror = pr.sym && c.I != c.J && pr.mirror_out;
-      const bool want_diag = pr.has_d2 && c.I == c.J;
+      named_bar_sync(1, EPI_THREADS);
+      if (!*epi_flag) break;
+      TileCoord c;
+      const TileInfo ti = info[islot];
+      c.p = (int)(ti.pf & 0xFFu);
+      c.b = ti.b;
+      c.I = (int)(ti.ij & 0xFFFFu);
+      c.J = (int)(ti.ij >> 16);
+      const Problem& pr = P.prob[c.p];
+      const float alpha = ti.alpha, beta = ti.beta;
+      const bool has_c = (ti.pf & TI_HAS_C) != 0;
+      const bool mirror = (ti.pf & TI_MIRROR) != 0;
+      const bool want_diag = (ti.pf & TI_DIAG) != 0;
       // per-product fields used inside the chunk loop, in registers (see KLoop)
-      const int c_trans = pr.c_trans, c_f16 = pr.c_f16, d_trans = pr.d_trans, d_f16 = pr.d_f16;
-      const int d_mode = d_trans ? 1 : pr.d_mode;
-      const int check_finite = pr.check_finite, has_d2 = pr.has_d2, diag_limit = pr.diag_limit;
-      const float gamma = pr.gamma;
+      const int c_trans = (ti.pf & TI_C_TRANS) != 0, c_f16 = (ti.pf & TI_C_F16) != 0;
+      const int d_trans = (ti.pf & TI_D_TRANS) != 0, d_f16 = (ti.pf & TI_D_F16) != 0;
+      const int d_mode = (int)((ti.pf >> TI_DMODE_SHIFT) & 3u);
+      const int check_finite = (ti.pf & TI_CHECK) != 0, has_d2 = (ti.pf & TI_HAS_D2) != 0;
+      const int diag_limit = ti.diag_limit;
+      const bool publish = (ti.pf & TI_PUBLISH) != 0;
+      const float gamma = ti.gamma;
       const int m0 = c.I * TT + (int)rank * TM;  // first row of this CTA's half
       const int n0 = c.J * TT;
       // row-mapped output: the W rows of this tile's rows go to shared memory (the staging
       // buffer is free once the previous stores have read it), the first chunk's W loads are
       // issued, and the rows of this CTA's next tile are fetched into L2
-      const bool rowmap = c.p == P.rmo.prob;
+      const bool rowmap = (ti.pf & TI_ROWMAP) != 0;
       const int rm_cols = P.rmo.cols, rm_has_c = P.rmo.has_c;
       int* const rm_idx = reinterpret_cast<int*>(smem + OFF_BAR + RM_IDX_OFF);
       const uint16_t* const rm_base =
@@ -711,9 +797,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         named_bar_sync(1, EPI_THREADS);
         if (rm_has_c) rowmap_chunk_load(cvec, rm_base, P.rmo.ld, rm_idx, et, n0, rm_cols);
         const int tn = tile + npairs;
-        int sn = seg;
         if (rm_has_c && tn < P.total_tiles) {
-          const TileCoord nc = decode_tile(P, tn, &sn);
+          // (segment search from the last one this loop found: tiles only increase)
+          const TileCoord nc = decode_tile(P, tn, &seg);
           const int nrow = nc.I * TT + (int)rank * TM + (et >> 1);
           if (nc.p == c.p && nrow < P.rmo.rows) {
             const long long wn = P.rmo.map[(long long)nc.b * P.rmo.map_stride + nrow];
@@ -723,10 +809,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
               asm volatile("prefetch.global.L2 [%0];" ::"l"(q + o));
           }
         }
+        if (et == 0) *epi_flag = mbar_wait(&tfull[acc], aph, abort_flag, P.status) ? 1 : 0;
+        named_bar_sync(1, EPI_THREADS);
+        if (!*epi_flag) break;
       }
-      if (et == 0) *epi_flag = mbar_wait(&tfull[acc], aph, abort_flag, P.status) ? 1 : 0;
-      named_bar_sync(1, EPI_THREADS);
-      if (!*epi_flag) break;
       tc_fence_after();
       const int diag_col = (int)rank * TM + r;  // tile column of this row's diagonal element
       const bool diag_mine = want_diag && ((diag_col >> 5) & 1) == half;
@@ -788,7 +874,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
           rowmap_chunk_store(SD, P.rmo.ptr, (long long)c.b * P.rmo.stride, P.rmo.ld, rm_idx, et, col0, rm_cols);
           named_bar_sync(1, EPI_THREADS);  // the buffer is free for the next chunk
         }
-        if (pr.publish) {
+        if (publish) {
           // the tile's stores are visible before its completion is published
           __threadfence();
           named_bar_sync(1, EPI_THREADS);
@@ -913,14 +999,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         }
       }
       if (bad) set_status(P.status, GNS_DEVST_NONFINITE);
-      if (et == 0 && pr.publish) {
+      if (et == 0 && publish) {
         // this CTA's half of the tile is in global memory: publish it to dependent tiles
         // (products nothing in the launch depends on skip the wait for their stores)
         bulk_wait_all();
         fence_proxy_async_global();
-        red_release_gpu_add(P.counters + pr.ctr_off + c.b, 1);
+        red_release_gpu_add(P.counters + ti.ctr_off + c.b, 1);
       }
       named_bar_sync(1, EPI_THREADS);
+      if (et == 0) mbar_arrive(&info_empty[islot]);  // every thread has read the tile's entry
       if (!*epi_flag) break;
     }
     if (et == 0) bulk_wait_all();
@@ -1180,6 +1267,10 @@ int gemm_launch_tc(const GemmOp* ops, int nops, const uint32_t* dep_masks, int* 
     pr.kblocks = (int)((o.K + TK - 1) / TK);
     pr.tiles_m = (int)((o.M + tile - 1) / tile);
     pr.tiles_n = (int)((o.N + tile - 1) / tile);
+    if (pr.tiles_m > 65535 || pr.tiles_n > 65535) {  // tile coordinates travel as 16-bit fields
+      *err = "a product of more than 65535 tiles along one dimension";
+      return GNS_ERR_UNSUPPORTED;
+    }
     pr.sym = o.sym;
     const long long tpm = o.sym ? (long long)pr.tiles_m * (pr.tiles_m + 1) / 2 : (long long)pr.tiles_m * pr.tiles_n;
     if (tpm * o.batch + tiles > (long long)INT32_MAX) {
