@@ -78,11 +78,13 @@ struct Geo {
 constexpr int BAR_BYTES = 2048;
 constexpr int RM_IDX_OFF = 512;  // in the barrier area: W row of each tile row (row-mapped outputs)
 // In the barrier area: a ring of the epilogue's per-tile parameters (TileInfo), filled ahead by
-// one lane of the C-loader warp, and its full / empty barriers.
+// one lane of the C-loader warp, and its barriers: full (the entry is written), stored (the
+// epilogue's stores of the tile have landed) and empty (the epilogue and the publishing lane
+// are done with the entry).
 constexpr int INFO_RING = 8;
 constexpr int INFO_OFF = 1024;
 constexpr int INFO_BAR_OFF = INFO_OFF + INFO_RING * 32;
-static_assert(INFO_BAR_OFF + 2 * INFO_RING * 8 <= BAR_BYTES, "tile-info ring");
+static_assert(INFO_BAR_OFF + 3 * INFO_RING * 8 <= BAR_BYTES, "tile-info ring");
 
 // Shared-memory plan of a kernel with STAGES operand stages and a ring of C_BUFS C chunks.
 // Two plans are compiled: a deep operand ring (6 stages, 1 C chunk) pays on launches of
@@ -476,6 +478,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
   TileInfo* const info = reinterpret_cast<TileInfo*>(smem + OFF_BAR + INFO_OFF);
   uint64_t* const info_full = reinterpret_cast<uint64_t*>(smem + OFF_BAR + INFO_BAR_OFF);
   uint64_t* const info_empty = info_full + INFO_RING;
+  uint64_t* const info_stored = info_empty + INFO_RING;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -499,7 +502,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
     }
     for (int q = 0; q < INFO_RING; ++q) {
       mbar_init(&info_full[q], 1);
-      mbar_init(&info_empty[q], 1);
+      mbar_init(&info_empty[q], 2);
+      mbar_init(&info_stored[q], 1);
     }
     *abort_flag = 0;
     *epi_flag = 1;
@@ -704,6 +708,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         e.gamma = pr.gamma;
         e.diag_limit = pr.diag_limit;
         mbar_arrive(&info_full[slot]);  // release: the entry is visible to the epilogue's wait
+      }
+    }
+    if (lane == 3) {
+      // ---------------- publishing lane (both CTAs) ----------------
+      // Publishes each tile's completion to the dependent tiles once the epilogue has seen its
+      // stores land: the release at GPU scope waits for the CTA's earlier writes to become
+      // visible device-wide, which kept every epilogue thread waiting at the tile's last
+      // barrier when the storing thread did it itself.
+      int local = 0;
+      for (int tile = pair; tile < P.total_tiles; tile += npairs, ++local) {
+        const int slot = local % INFO_RING;
+        const uint32_t ph = (local / INFO_RING) & 1u;
+        if (!mbar_wait(&info_full[slot], ph, abort_flag, P.status)) break;
+        const uint32_t pf = info[slot].pf;
+        const int ctr = info[slot].ctr_off + info[slot].b;
+        if (!mbar_wait(&info_stored[slot], ph, abort_flag, P.status)) break;
+        if (pf & TI_PUBLISH) red_release_gpu_add(P.counters + ctr, 1);
+        mbar_arrive(&info_empty[slot]);
       }
     }
     if (lane == 0) {
@@ -999,12 +1021,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         }
       }
       if (bad) set_status(P.status, GNS_DEVST_NONFINITE);
-      if (et == 0 && publish) {
-        // this CTA's half of the tile is in global memory: publish it to dependent tiles
-        // (products nothing in the launch depends on skip the wait for their stores)
-        bulk_wait_all();
-        fence_proxy_async_global();
-        red_release_gpu_add(P.counters + ti.ctr_off + c.b, 1);
+      if (et == 0) {
+        // this CTA's half of the tile is in global memory (products nothing in the launch
+        // depends on skip the wait): the publishing lane announces it to dependent tiles
+        if (publish) {
+          bulk_wait_all();
+          fence_proxy_async_global();
+        }
+        mbar_arrive(&info_stored[islot]);
       }
       named_bar_sync(1, EPI_THREADS);
       if (et == 0) mbar_arrive(&info_empty[islot]);  // every thread has read the tile's entry
