@@ -83,7 +83,7 @@ constexpr int RM_IDX_OFF = 512;  // in the barrier area: W row of each tile row 
 // are done with the entry).
 constexpr int INFO_RING = 8;
 constexpr int INFO_OFF = 1024;
-constexpr int INFO_BAR_OFF = INFO_OFF + INFO_RING * 32;
+constexpr int INFO_BAR_OFF = INFO_OFF + INFO_RING * 48;
 static_assert(INFO_BAR_OFF + 3 * INFO_RING * 8 <= BAR_BYTES, "tile-info ring");
 
 // Shared-memory plan of a kernel with STAGES operand stages and a ring of C_BUFS C chunks.
@@ -206,22 +206,10 @@ __device__ __forceinline__ bool wait_ready(volatile int* ready, int tile, volati
 // read from the mirrored block, with the other major-ness, wherever the block it would read
 // lies below the diagonal.
 // The per-product fields a K loop reads, copied into registers once per tile: the loops'
-// inline assembly clobbers memory, which would otherwise reload them from the parameter
-// block at every K slice.
+// inline assembly clobbers memory, which would otherwise reload them at every K slice.
 struct KLoop {
   int kblocks, a_mn, b_mn, a_upper, b_upper, ab_f16, ksh;
 };
-__device__ __forceinline__ KLoop kloop_of(const Problem& pr, int ksh) {
-  KLoop k;
-  k.ksh = ksh;
-  k.kblocks = pr.kblocks;
-  k.a_mn = pr.a_mn;
-  k.b_mn = pr.b_mn;
-  k.a_upper = pr.a_upper;
-  k.b_upper = pr.b_upper;
-  k.ab_f16 = pr.ab_f16;
-  return k;
-}
 __device__ __forceinline__ int a_major(const KLoop& pr, int I, int kb) {
   const int kbl = kb >> pr.ksh;
   const bool lower = pr.a_mn ? (kbl > I) : (I > kbl);
@@ -237,15 +225,17 @@ struct TileCoord {
   int p, b, I, J;
 };
 
-// What the epilogue needs of one tile, decoded and scaled ahead of it: decoding reads the
+// What the roles need of one tile, decoded and scaled ahead of them: decoding reads the
 // parameter block with tile-dependent indices, and the per-matrix scale is a global load, so
-// done at the top of each tile they kept the epilogue (the launch's bottleneck on tiles of
-// few K slices) waiting between tiles.
+// done at the top of each tile they kept the epilogue and the MMA issuer waiting between
+// tiles (the launch's bottleneck on tiles of few K slices).
 enum : uint32_t {
   TI_HAS_C = 1u << 8, TI_MIRROR = 1u << 9, TI_DIAG = 1u << 10, TI_C_TRANS = 1u << 11, TI_C_F16 = 1u << 12,
   TI_D_TRANS = 1u << 13, TI_D_F16 = 1u << 14, TI_CHECK = 1u << 15, TI_HAS_D2 = 1u << 16, TI_PUBLISH = 1u << 17,
   TI_ROWMAP = 1u << 18, TI_DMODE_SHIFT = 19  // bits 0-7: the problem; 19-20: the D chunk mode
 };
+enum : uint32_t { KF_A_MN = 1u, KF_B_MN = 2u, KF_A_UPPER = 4u, KF_B_UPPER = 8u, KF_AB_F16 = 16u, KF_DEP = 32u,
+                  KF_CMODE_SHIFT = 6 };
 struct TileInfo {
   uint32_t pf;     // problem and flags
   int b;           // matrix
@@ -253,8 +243,11 @@ struct TileInfo {
   int ctr_off;     // the problem's completion counters
   float alpha, beta, gamma;
   int diag_limit;
+  int kblocks;     // K slices
+  uint32_t kf;     // operand major-ness and types, dependencies, C chunk mode
+  int pad[2];
 };
-static_assert(sizeof(TileInfo) == 32, "tile-info entry");
+static_assert(sizeof(TileInfo) == 48, "tile-info entry");
 
 // s0: a segment index at or below the tile's (every role walks its tiles in increasing
 // order, so the previous tile's segment is a valid start); *seg receives the tile's.
@@ -284,6 +277,31 @@ __device__ __forceinline__ TileCoord decode_tile(const Params& P, int tile, int*
     tc.J = t - tc.I * pr.tiles_n;
   }
   return tc;
+}
+
+// A tile's coordinates and K loop from its TileInfo entry (copied out of shared memory once).
+struct TileHead {
+  TileCoord c;
+  KLoop kl;
+  uint32_t pf, kf;
+};
+__device__ __forceinline__ TileHead tile_head(const TileInfo* e, int ksh) {
+  TileHead h;
+  h.pf = e->pf;
+  h.kf = e->kf;
+  const uint32_t ij = e->ij;
+  h.c.p = (int)(h.pf & 0xFFu);
+  h.c.b = e->b;
+  h.c.I = (int)(ij & 0xFFFFu);
+  h.c.J = (int)(ij >> 16);
+  h.kl.ksh = ksh;
+  h.kl.kblocks = e->kblocks;
+  h.kl.a_mn = (h.kf & KF_A_MN) != 0;
+  h.kl.b_mn = (h.kf & KF_B_MN) != 0;
+  h.kl.a_upper = (h.kf & KF_A_UPPER) != 0;
+  h.kl.b_upper = (h.kf & KF_B_UPPER) != 0;
+  h.kl.ab_f16 = (h.kf & KF_AB_F16) != 0;
+  return h;
 }
 
 __device__ __forceinline__ float powi(float s, int p) { return p == 0 ? 1.f : (p == 1 ? s : s * s); }
@@ -542,18 +560,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
       int s = 0;
       uint32_t ph = 0;
       bool ok = true;
-      int seg = 0;
-      for (int tile = pair; ok && tile < P.total_tiles; tile += npairs) {
-        const TileCoord c = decode_tile(P, tile, &seg);
-        const Problem& pr = P.prob[c.p];
+      int local = 0;
+      for (int tile = pair; ok && tile < P.total_tiles; tile += npairs, ++local) {
+        const int islot = local % INFO_RING;
+        if (!mbar_wait(&info_full[islot], (local / INFO_RING) & 1u, abort_flag, status)) break;
+        const TileHead h = tile_head(&info[islot], Geo<CG>::KSH);
+        const TileCoord c = h.c;
+        const KLoop kl = h.kl;
+        const Problem& pr = P.prob[c.p];  // (tensor-map addresses only)
         const int m0 = c.I * TT + (int)rank * TM;
         const int n0 = c.J * TT + (int)rank * BN;
-        const KLoop kl = kloop_of(pr, Geo<CG>::KSH);
         const CUtensorMap* const tmA = &pr.tmA;
         const CUtensorMap* const tmA2 = &pr.tmA2;
         const CUtensorMap* const tmB = &pr.tmB;
         const CUtensorMap* const tmB2 = &pr.tmB2;
-        if (pr.dep_mask && !wait_ready(ready_tile, tile, abort_flag, status)) break;
+        if ((h.kf & KF_DEP) && !wait_ready(ready_tile, tile, abort_flag, status)) break;
         for (int kb = 0; kb < kl.kblocks; ++kb) {
           if ((g++ & 1u) != (uint32_t)pid) {  // the other producer's slice
             if (++s == STAGES) {
@@ -602,16 +623,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
       uint32_t ph = 0;
       bool ok = true;
       int local = 0;
-      int seg = 0;
       for (int tile = pair; ok && tile < P.total_tiles; tile += npairs, ++local) {
-        const TileCoord c = decode_tile(P, tile, &seg);
-        const Problem& pr = P.prob[c.p];
+        const int islot = local % INFO_RING;
+        if (!mbar_wait(&info_full[islot], (local / INFO_RING) & 1u, abort_flag, status)) break;
+        const TileHead h = tile_head(&info[islot], Geo<CG>::KSH);
+        const TileCoord c = h.c;
+        const KLoop kl = h.kl;
         const int acc = local & 1;
         const uint32_t aph = (local >> 1) & 1;
         if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * TT;
-        const KLoop kl = kloop_of(pr, Geo<CG>::KSH);
         for (int kb = 0; kb < kl.kblocks; ++kb) {
           const int amn = a_major(kl, c.I, kb), bmn = b_major(kl, c.J, kb);
           const uint32_t idesc = idesc_f16kind_f32(TT, TT, amn, bmn, kl.ab_f16);
@@ -707,6 +729,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         e.beta = beta;
         e.gamma = pr.gamma;
         e.diag_limit = pr.diag_limit;
+        e.kblocks = pr.kblocks;
+        e.kf = (pr.a_mn ? KF_A_MN : 0u) | (pr.b_mn ? KF_B_MN : 0u) | (pr.a_upper ? KF_A_UPPER : 0u) |
+               (pr.b_upper ? KF_B_UPPER : 0u) | (pr.ab_f16 ? KF_AB_F16 : 0u) | (pr.dep_mask ? KF_DEP : 0u) |
+               ((uint32_t)pr.c_mode << KF_CMODE_SHIFT);
         mbar_arrive(&info_full[slot]);  // release: the entry is visible to the epilogue's wait
       }
     }
@@ -733,17 +759,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
       // Loads the C chunks of the next tile as soon as the epilogue releases each buffer,
       // a whole main loop ahead of their use.
       uint32_t qc = 0;  // C chunks loaded so far (ring slot and phase)
-      int seg = 0;
-      for (int tile = pair; tile < P.total_tiles; tile += npairs) {
-        const TileCoord c = decode_tile(P, tile, &seg);
-        const Problem& pr = P.prob[c.p];
-        if (!pr.has_c) continue;
+      int local = 0;
+      for (int tile = pair; tile < P.total_tiles; tile += npairs, ++local) {
+        const int islot = local % INFO_RING;
+        if (!mbar_wait(&info_full[islot], (local / INFO_RING) & 1u, abort_flag, P.status)) break;
+        const TileHead h = tile_head(&info[islot], Geo<CG>::KSH);
+        if (!(h.pf & TI_HAS_C)) continue;
+        const TileCoord c = h.c;
+        const Problem& pr = P.prob[c.p];  // (tensor-map address only)
         const int m0 = c.I * TT + (int)rank * TM;
         const int n0 = c.J * TT;
-        if (pr.dep_mask && !wait_ready(ready_tile, tile, abort_flag, P.status)) break;
+        if ((h.kf & KF_DEP) && !wait_ready(ready_tile, tile, abort_flag, P.status)) break;
         bool ok = true;
         const CUtensorMap* const tmC = &pr.tmC;
-        const int c_mode = pr.c_mode;
+        const int c_mode = (int)((h.kf >> KF_CMODE_SHIFT) & 3u);
         for (int ch = 0; ch < NCHUNK; ++ch, ++qc) {
           const uint32_t q = qc % C_BUFS;
           if (!mbar_wait(&cempty[q], ((qc / C_BUFS) & 1u) ^ 1u, abort_flag, P.status)) {
