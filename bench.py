@@ -267,8 +267,12 @@ def run_ours(args, rank, world, dist):
             r["gram_vs_standard_speedup"] = std["ms_per_call"] / r["ms_per_call"]
             chain = n <= 128 and m <= 512
             pack = 4 if n <= 32 else 2 if n <= 64 else 1
+            # the library's tile plan: 1-CTA 128 x 128 tiles for products of at most 256 rows and
+            # for n <= 1024 batches whose largest symmetric stage has at most 48 pair tiles
+            t = (n + 255) // 256
+            one_cta = n <= 256 or (n <= 1024 and count * t * (t + 1) // 2 <= 48)
             r["path"] = (f"on-chip chain kernel, {pack} matrices per CTA chain" if chain else
-                         "batched tiles, 1-CTA 128 x 128" if n <= 128 else "batched tiles, 2-CTA 256 x 256")
+                         "batched tiles, 1-CTA 128 x 128" if one_cta else "batched tiles, 2-CTA 256 x 256")
             if chain:
                 os.environ["GNS_CHAIN_SMALL"] = "0"
                 try:
