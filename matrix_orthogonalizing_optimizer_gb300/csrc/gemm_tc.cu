@@ -44,9 +44,11 @@ constexpr int TM = 128;                          // accumulator rows per CTA
 constexpr int BN = 128;                          // B columns staged per CTA
 constexpr int TK = 64;                           // K slice per stage
 #ifndef GNS_TC_OUTBUFS
-#define GNS_TC_OUTBUFS 1
+#define GNS_TC_OUTBUFS 2
 #endif
-constexpr int OUT_BUFS = GNS_TC_OUTBUFS;         // staging buffers for output (and mirror) chunks
+// staging buffers for output (and mirror) chunks: with two, a chunk's stores drain while the
+// next chunk is staged
+constexpr int OUT_BUFS = GNS_TC_OUTBUFS;
 constexpr int A_BYTES = TM * TK * 2;             // 16 KiB
 constexpr int STAGE_BYTES = (TM + BN) * TK * 2;  // 32 KiB per CTA
 constexpr int CHUNK = 64;                        // epilogue columns per chunk
