@@ -692,19 +692,32 @@ __global__ void gather_rows_kernel(bf16* M, long long ldm, long long sm, const i
     bf16* src = M + (long long)b * sm + (long long)r * ldm;
     bf16* dst = X + (long long)b * sx + (long long)i * ldx;
     const int cvec = cols & ~7;
-    for (int c = threadIdx.x * 8; c < cvec; c += blockDim.x * 8) {
-      const uint4 u = *reinterpret_cast<const uint4*>(src + c);
-      *reinterpret_cast<uint4*>(dst + c) = u;
-      const bf16* e = reinterpret_cast<const bf16*>(&u);
-      uint4 dv;
-      bf16* de = reinterpret_cast<bf16*>(&dv);
+    // GV vectors of the row per thread are loaded before the first store (a store to M or X
+    // may alias the next load as far as the compiler knows, so a load after it would wait)
+    constexpr int GV = 8;
+    for (int c0 = threadIdx.x * 8; c0 < cvec; c0 += GV * blockDim.x * 8) {
+      uint4 u[GV];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float f = bf16_to_f(e[q]);
-        acc = fmaf(f, f, acc);
-        de[q] = f_to_bf16(__fmul_rn(mu, f));
+      for (int j = 0; j < GV; ++j) {
+        const int c = c0 + j * blockDim.x * 8;
+        u[j] = c < cvec ? *reinterpret_cast<const uint4*>(src + c) : make_uint4(0u, 0u, 0u, 0u);
       }
-      if (decay) *reinterpret_cast<uint4*>(src + c) = dv;
+#pragma unroll
+      for (int j = 0; j < GV; ++j) {
+        const int c = c0 + j * blockDim.x * 8;
+        if (c >= cvec) break;
+        *reinterpret_cast<uint4*>(dst + c) = u[j];
+        const bf16* e = reinterpret_cast<const bf16*>(&u[j]);
+        uint4 dv;
+        bf16* de = reinterpret_cast<bf16*>(&dv);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float f = bf16_to_f(e[q]);
+          acc = fmaf(f, f, acc);
+          de[q] = f_to_bf16(__fmul_rn(mu, f));
+        }
+        if (decay) *reinterpret_cast<uint4*>(src + c) = dv;
+      }
     }
     for (int c = cvec + threadIdx.x; c < cols; c += blockDim.x) {
       const bf16 v = src[c];
