@@ -445,6 +445,33 @@ struct ColKeys8 {
     asm("shf.l.wrap.b32 %0, %1, %2, %3;" : "=r"(hi) : "r"(mant), "r"(0u), "r"(q));
     cur[e] += (static_cast<uint64_t>(hi) << 32) | lo;
   }
+  // The same for columns e and e + 1 from one word of two bf16 values (e in the low half):
+  // the exponent and mantissa fields of both are formed with 32-bit operations on the pair
+  // (no carry or borrow crosses the halves: mant <= 255, q <= 256, E >= min(E, 1)).
+  __device__ __forceinline__ void add2(int e, uint32_t w, unsigned long long* key) {
+    const uint32_t E2 = (w >> 7) & 0x00FF00FFu;
+    const uint32_t h2 = ((E2 + 0x00FF00FFu) >> 8) & 0x00010001u;  // min(E, 1): E + 255 reaches bit 8 iff E > 0
+    const uint32_t mant2 = (w & 0x007F007Fu) + (h2 << 7);
+    const uint32_t q2 = E2 - h2 + 0x00020002u;
+    step(e, mant2 & 0xFFFFu, q2 & 0xFFFFu, key);
+    step(e + 1, mant2 >> 16, q2 >> 16, key + KEY_DIGITS);
+  }
+  __device__ __forceinline__ void step(int e, uint32_t mant, uint32_t q, unsigned long long* key) {
+    const uint32_t d = mant ? (q >> 5) : dcur[e];
+    if (d != dcur[e]) {
+      if (d > 7u) {
+        nonfinite |= 1u << e;
+      } else {
+        if (cur[e]) atomicAdd(key + dcur[e], (unsigned long long)cur[e]);
+        cur[e] = 0;
+        dcur[e] = d;
+      }
+    }
+    uint32_t lo, hi;
+    asm("shf.l.wrap.b32 %0, %1, %2, %3;" : "=r"(lo) : "r"(0u), "r"(mant), "r"(q));
+    asm("shf.l.wrap.b32 %0, %1, %2, %3;" : "=r"(hi) : "r"(mant), "r"(0u), "r"(q));
+    cur[e] += (static_cast<uint64_t>(hi) << 32) | lo;
+  }
 };
 
 __global__ void __launch_bounds__(256) frac_add_keys_cols8_kernel(bf16* M, long long ldm, long long sm,
@@ -479,8 +506,7 @@ __global__ void __launch_bounds__(256) frac_add_keys_cols8_kernel(bf16* M, long 
     *reinterpret_cast<uint4*>(Mb + (long long)r * ldm) = mv;
     const uint32_t w[4] = {mv.x, mv.y, mv.z, mv.w};
 #pragma unroll
-    for (int e = 0; e < 8; ++e)
-      ka.add(e, (w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu, kb + (long long)e * KEY_DIGITS);
+    for (int e = 0; e < 8; e += 2) ka.add2(e, w[e >> 1], kb + (long long)e * KEY_DIGITS);
     mv = mn;
     gv = gn;
   }
