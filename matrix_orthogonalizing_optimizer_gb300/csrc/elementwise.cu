@@ -425,28 +425,8 @@ struct ColKeys8 {
     }
     nonfinite = 0;
   }
-  __device__ __forceinline__ void add(int e, uint32_t u, unsigned long long* key) {
-    const uint32_t E = (u >> 7) & 0xFFu, f = u & 0x7Fu;
-    const uint32_t h = min(E, 1u);
-    const uint32_t mant = f + (h << 7);
-    const uint32_t q = E - h + 2u;
-    const uint32_t d = mant ? (q >> 5) : dcur[e];
-    if (d != dcur[e]) {
-      if (d > 7u) {
-        nonfinite |= 1u << e;  // the column's key is replaced; what is added no longer matters
-      } else {
-        if (cur[e]) atomicAdd(key + dcur[e], (unsigned long long)cur[e]);
-        cur[e] = 0;
-        dcur[e] = d;
-      }
-    }
-    uint32_t lo, hi;
-    asm("shf.l.wrap.b32 %0, %1, %2, %3;" : "=r"(lo) : "r"(0u), "r"(mant), "r"(q));
-    asm("shf.l.wrap.b32 %0, %1, %2, %3;" : "=r"(hi) : "r"(mant), "r"(0u), "r"(q));
-    cur[e] += (static_cast<uint64_t>(hi) << 32) | lo;
-  }
-  // The same for columns e and e + 1 from one word of two bf16 values (e in the low half):
-  // the exponent and mantissa fields of both are formed with 32-bit operations on the pair
+  // Columns e and e + 1 from one word of two bf16 values (e in the low half): the exponent and
+  // mantissa fields of both are formed with 32-bit operations on the pair
   // (no carry or borrow crosses the halves: mant <= 255, q <= 256, E >= min(E, 1)).
   __device__ __forceinline__ void add2(int e, uint32_t w, unsigned long long* key) {
     const uint32_t E2 = (w >> 7) & 0x00FF00FFu;
@@ -456,6 +436,8 @@ struct ColKeys8 {
     step(e, mant2 & 0xFFFFu, q2 & 0xFFFFu, key);
     step(e + 1, mant2 >> 16, q2 >> 16, key + KEY_DIGITS);
   }
+  // One value of column e: a change of digit window adds the finished window sum into the
+  // key; window 8 (Inf / NaN) flags the column, whose key is then replaced.
   __device__ __forceinline__ void step(int e, uint32_t mant, uint32_t q, unsigned long long* key) {
     const uint32_t d = mant ? (q >> 5) : dcur[e];
     if (d != dcur[e]) {
