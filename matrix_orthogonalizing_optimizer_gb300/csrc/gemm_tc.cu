@@ -78,13 +78,14 @@ struct Geo {
   static constexpr int KSH = CG == 2 ? 2 : 1;       // log2 of 64-wide K slices per tile edge
 };
 constexpr int BAR_BYTES = 2048;
-constexpr int RM_IDX_OFF = 512;  // in the barrier area: W row of each tile row (row-mapped outputs)
-// In the barrier area: a ring of the epilogue's per-tile parameters (TileInfo), filled ahead by
-// one lane of the C-loader warp, and its barriers: full (the entry is written), stored (the
-// epilogue's stores of the tile have landed) and empty (the epilogue and the publishing lane
-// are done with the entry).
+// In the barrier area: for row-mapped outputs, two buffers (by tile parity) of the W row of
+// each tile row, the next tile's written during the current one; then a ring of the
+// epilogue's per-tile parameters (TileInfo), filled ahead by one lane of the C-loader warp, and
+// its barriers: full (the entry is written), stored (the epilogue's stores of the tile have
+// landed) and empty (the epilogue and the publishing lane are done with the entry).
+constexpr int RM_IDX_OFF = 256;
 constexpr int INFO_RING = 8;
-constexpr int INFO_OFF = 1024;
+constexpr int INFO_OFF = RM_IDX_OFF + 2 * TM * 4;
 constexpr int INFO_BAR_OFF = INFO_OFF + INFO_RING * 48;
 static_assert(INFO_BAR_OFF + 3 * INFO_RING * 8 <= BAR_BYTES, "tile-info ring");
 
@@ -106,7 +107,6 @@ struct Plan {
   static constexpr int SMEM_BYTES = 1024 + OFF_BAR + BAR_BYTES;
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert((2 * STAGES + 4 + 2 * C_BUFS) * 8 + 16 <= RM_IDX_OFF, "barrier area");
-  static_assert(RM_IDX_OFF + TM * 4 <= INFO_OFF, "row-map area");
 };
 using DeepPlan = Plan<5, 2>;
 using ShallowPlan = Plan<4, 4>;
@@ -421,42 +421,34 @@ __device__ __forceinline__ void acc_release(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-// Row-mapped chunks: 128 rows x 64 columns of W whose rows are rm_idx[0..127] (-1: none).
-// Thread t of the 256 epilogue threads moves the 16-byte vectors v = t + 256 i (i < 4): row
-// v / 8, columns 8 (v % 8) .. +7 of the chunk, so a warp covers four whole 128-byte row
-// segments per access. Vectors past the matrix's columns are partial (zero filled on load,
-// not written on store).
-__device__ __forceinline__ void rowmap_chunk_load(uint4 (&cv)[4], const uint16_t* base, long long ld,
-                                                  const int* rm_idx, int t, int col0, int cols) {
+// The addend of one epilogue thread's row segment of a row-mapped chunk: W row wr (-1: none),
+// columns col .. col + 31, as four 16-byte vectors (zeros past the matrix's columns). Loaded
+// straight into the registers the epilogue adds it from, a chunk ahead: a warp reads 32 rows'
+// 64-byte segments, whole 32-byte sectors.
+__device__ __forceinline__ void rowmap_own_load(uint4 (&cv)[4], const uint16_t* base, long long ld, int wr, int col,
+                                                int cols) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int v = t + 256 * i;
-    const int row = v >> 3;
-    const int col = col0 + (v & 7) * 8;
-    const int wr = rm_idx[row];
+  for (int q = 0; q < 4; ++q) {
+    const int c = col + 8 * q;
     uint4 w = make_uint4(0u, 0u, 0u, 0u);
-    if (wr >= 0 && col < cols) {
-      const uint16_t* q = base + (long long)wr * ld + col;
-      if (col + 8 <= cols) {
-        w = *reinterpret_cast<const uint4*>(q);
+    if (wr >= 0 && c < cols) {
+      const uint16_t* p = base + (long long)wr * ld + c;
+      if (c + 8 <= cols) {
+        w = *reinterpret_cast<const uint4*>(p);
       } else {
         uint32_t e[4] = {0u, 0u, 0u, 0u};
-        for (int j = 0; j < 8 && col + j < cols; ++j) e[j >> 1] |= (uint32_t)q[j] << (16 * (j & 1));
+        for (int j = 0; j < 8 && c + j < cols; ++j) e[j >> 1] |= (uint32_t)p[j] << (16 * (j & 1));
         w = make_uint4(e[0], e[1], e[2], e[3]);
       }
     }
-    cv[i] = w;
+    cv[q] = w;
   }
 }
 
-__device__ __forceinline__ void rowmap_chunk_stage(uint8_t* sd, const uint4 (&cv)[4], int t) {
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int v = t + 256 * i;
-    *reinterpret_cast<uint4*>(sd + off_direct(v >> 3, (v & 7) * 8)) = cv[i];
-  }
-}
-
+// Row-mapped chunks: 128 rows x 64 columns of W whose rows are rm_idx[0..127] (-1: none).
+// Thread t of the 256 epilogue threads stores the 16-byte vectors v = t + 256 i (i < 4): row
+// v / 8, columns 8 (v % 8) .. +7 of the chunk, so a warp covers four whole 128-byte row
+// segments per access. Vectors past the matrix's columns are partial (not written).
 __device__ __forceinline__ void rowmap_chunk_store(const uint8_t* sd, void* ptr, long long boff, long long ld,
                                                    const int* rm_idx, int t, int col0, int cols) {
   uint16_t* const base = static_cast<uint16_t*>(ptr) + boff;
@@ -808,17 +800,44 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
     const uint32_t tempty_leader1 = CG == 2 ? mapa_shared(smem_u32(&tempty[1]), 0) : smem_u32(&tempty[1]);
     uint32_t qc = 0;  // C chunks consumed so far (ring slot and phase)
     uint32_t gc = 0;  // chunks stored so far (output staging buffers)
+    // Row-mapped outputs: the W row of each of a tile's rows (-1 past the valid product rows)
+    // is written to the tile's row buffer during the previous tile's first chunk (its map entry
+    // loaded at that tile's start), and the tile's first chunk of W rows is loaded into cvec at
+    // the previous tile's end, so that neither wait is on the tile's own path.
+    int* const rm_idx_all = reinterpret_cast<int*>(smem + OFF_BAR + RM_IDX_OFF);  // [2][TM]
+    const int rm_cols = P.rmo.cols, rm_has_c = P.rmo.has_c;
+    auto rm_row = [&](const TileInfo& e, int i) {
+      const int prow = (int)(e.ij & 0xFFFFu) * TT + (int)rank * TM + i;
+      return prow < P.rmo.rows ? P.rmo.map[(long long)e.b * P.rmo.map_stride + prow] : -1;
+    };
+    auto rm_base = [&](const TileInfo& e) {
+      return static_cast<const uint16_t*>(P.rmo.ptr) + (long long)e.b * P.rmo.stride;
+    };
+    uint4 cvec[4];  // this thread's row segment of the next row-mapped chunk's W
+    if (pair < P.total_tiles) {
+      if (et == 0) *epi_flag = mbar_wait(&info_full[0], 0u, abort_flag, P.status) ? 1 : 0;
+      named_bar_sync(1, EPI_THREADS);
+      if (*epi_flag && (info[0].pf & TI_ROWMAP)) {
+        if (et < TM) rm_idx_all[et] = rm_row(info[0], et);
+        named_bar_sync(1, EPI_THREADS);
+        if (rm_has_c)
+          rowmap_own_load(cvec, rm_base(info[0]), P.rmo.ld, rm_idx_all[r], (int)(info[0].ij >> 16) * TT + half * 32,
+                          rm_cols);
+      }
+    }
     int local = 0;
-    int seg = 0;
     for (int tile = pair; tile < P.total_tiles; tile += npairs, ++local) {
       const int acc = local & 1;
       const uint32_t aph = (local >> 1) & 1;
-      const int islot = local % INFO_RING;
-      // the tile's parameters (decoded ahead by the tile-info lane); then, unless the tile's
-      // output is row-mapped (whose setup comes first), its accumulator
+      const int islot = local % INFO_RING, nslot = (local + 1) % INFO_RING;
+      const bool has_next = tile + npairs < P.total_tiles;
+      // the tile's parameters and the next tile's (decoded ahead by the tile-info lane), then
+      // the accumulator; before a row-mapped tile's staging, every TMA store has read its buffer
       if (et == 0) {
         bool okw = mbar_wait(&info_full[islot], (local / INFO_RING) & 1u, abort_flag, P.status);
-        if (okw && !(info[islot].pf & TI_ROWMAP)) okw = mbar_wait(&tfull[acc], aph, abort_flag, P.status);
+        if (okw && has_next) okw = mbar_wait(&info_full[nslot], ((local + 1) / INFO_RING) & 1u, abort_flag, P.status);
+        if (okw) okw = mbar_wait(&tfull[acc], aph, abort_flag, P.status);
+        if (okw && (info[islot].pf & TI_ROWMAP)) bulk_wait_read<0>();
         *epi_flag = okw ? 1 : 0;
       }
       named_bar_sync(1, EPI_THREADS);
@@ -844,37 +863,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
       const float gamma = ti.gamma;
       const int m0 = c.I * TT + (int)rank * TM;  // first row of this CTA's half
       const int n0 = c.J * TT;
-      // row-mapped output: the W rows of this tile's rows go to shared memory (the staging
-      // buffer is free once the previous stores have read it), the first chunk's W loads are
-      // issued, and the rows of this CTA's next tile are fetched into L2
       const bool rowmap = (ti.pf & TI_ROWMAP) != 0;
-      const int rm_cols = P.rmo.cols, rm_has_c = P.rmo.has_c;
-      int* const rm_idx = reinterpret_cast<int*>(smem + OFF_BAR + RM_IDX_OFF);
-      const uint16_t* const rm_base =
-          rowmap ? static_cast<const uint16_t*>(P.rmo.ptr) + (long long)c.b * P.rmo.stride : nullptr;
-      uint4 cvec[4];  // this thread's four 16-byte vectors of the next chunk's C
-      if (rowmap) {
-        if (et == 0) bulk_wait_read<0>();
-        if (et < TM) rm_idx[et] = m0 + et < P.rmo.rows ? P.rmo.map[(long long)c.b * P.rmo.map_stride + m0 + et] : -1;
-        named_bar_sync(1, EPI_THREADS);
-        if (rm_has_c) rowmap_chunk_load(cvec, rm_base, P.rmo.ld, rm_idx, et, n0, rm_cols);
-        const int tn = tile + npairs;
-        if (rm_has_c && tn < P.total_tiles) {
-          // (segment search from the last one this loop found: tiles only increase)
-          const TileCoord nc = decode_tile(P, tn, &seg);
-          const int nrow = nc.I * TT + (int)rank * TM + (et >> 1);
-          if (nc.p == c.p && nrow < P.rmo.rows) {
-            const long long wn = P.rmo.map[(long long)nc.b * P.rmo.map_stride + nrow];
-            const uint16_t* q = static_cast<const uint16_t*>(P.rmo.ptr) + (long long)nc.b * P.rmo.stride +
-                                wn * P.rmo.ld + nc.J * TT + (et & 1) * (TT / 2);
-            for (int o = 0; o < TT / 2 && nc.J * TT + (et & 1) * (TT / 2) + o < rm_cols; o += 64)
-              asm volatile("prefetch.global.L2 [%0];" ::"l"(q + o));
-          }
-        }
-        if (et == 0) *epi_flag = mbar_wait(&tfull[acc], aph, abort_flag, P.status) ? 1 : 0;
-        named_bar_sync(1, EPI_THREADS);
-        if (!*epi_flag) break;
-      }
+      const int* const rows_mine = rm_idx_all + (local & 1) * TM;
+      int* const rows_next = rm_idx_all + ((local + 1) & 1) * TM;
+      const bool next_rowmap = has_next && (info[nslot].pf & TI_ROWMAP) != 0;
+      const TileInfo* const nti = &info[nslot];
+      int next_row = -1;  // (its map entry: the load's latency passes under this tile's first chunk)
+      if (next_rowmap && et < TM) next_row = rm_row(*nti, et);
       tc_fence_after();
       const int diag_col = (int)rank * TM + r;  // tile column of this row's diagonal element
       const bool diag_mine = want_diag && ((diag_col >> 5) & 1) == half;
@@ -883,13 +878,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
       if (rowmap) {
         // per chunk: W rows staged in shared memory by whole-row 16-byte loads, every thread
         // updates its own row segment there (fp32, one rounding), whole-row stores back to W
-        for (int ch = 0; ch < NCHUNK; ++ch) {
+        const uint16_t* const base_mine = rm_base(ti);
+        const int wr_mine = rows_mine[r];  // this thread's W row
+        for (int ch = 0; ch < NCHUNK; ++ch, ++gc) {
+          // chunks alternate between the two staging buffers, so that a chunk's staging does not
+          // wait for the previous chunk's stores to have read theirs
+          uint8_t* const sd = SD + (gc % OUT_BUFS) * CHUNK_BYTES;
           const int col0 = n0 + ch * CHUNK;
-          if (rm_has_c) {
-            rowmap_chunk_stage(SD, cvec, et);
-            named_bar_sync(1, EPI_THREADS);
-            if (ch + 1 < NCHUNK) rowmap_chunk_load(cvec, rm_base, P.rmo.ld, rm_idx, et, col0 + CHUNK, rm_cols);
-          }
+          if (ch == 0 && next_rowmap && et < TM) rows_next[et] = next_row;
           uint32_t v[32];
           __syncwarp();
           tmem_ld_32x32b_x32(tmem_base + acc * TT + ch * CHUNK + half * 32 + ((uint32_t)(quarter * 32) << 16), v);
@@ -911,13 +907,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
             uint32_t cw[16];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              const uint4 w = *reinterpret_cast<const uint4*>(SD + off_direct(r, half * 32 + q * 8));
-              cw[4 * q] = w.x;
-              cw[4 * q + 1] = w.y;
-              cw[4 * q + 2] = w.z;
-              cw[4 * q + 3] = w.w;
+              cw[4 * q] = cvec[q].x;
+              cw[4 * q + 1] = cvec[q].y;
+              cw[4 * q + 2] = cvec[q].z;
+              cw[4 * q + 3] = cvec[q].w;
             }
             axpy_h16x2(o, cw, beta, d_f16);
+            // the next chunk's (or the next row-mapped tile's first chunk's) segment
+            if (ch + 1 < NCHUNK)
+              rowmap_own_load(cvec, base_mine, P.rmo.ld, wr_mine, col0 + CHUNK + half * 32, rm_cols);
+            else if (next_rowmap)
+              rowmap_own_load(cvec, rm_base(*nti), P.rmo.ld, rows_next[r], (int)(nti->ij >> 16) * TT + half * 32,
+                              rm_cols);
           }
           if (check_finite) {
             float2 z = make_float2(0.f, 0.f);
@@ -930,11 +931,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
           // each thread overwrites exactly the values it read
 #pragma unroll
           for (int q = 0; q < 4; ++q)
-            *reinterpret_cast<uint4*>(SD + off_direct(r, half * 32 + q * 8)) =
+            *reinterpret_cast<uint4*>(sd + off_direct(r, half * 32 + q * 8)) =
                 make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
           named_bar_sync(1, EPI_THREADS);
-          rowmap_chunk_store(SD, P.rmo.ptr, (long long)c.b * P.rmo.stride, P.rmo.ld, rm_idx, et, col0, rm_cols);
-          named_bar_sync(1, EPI_THREADS);  // the buffer is free for the next chunk
+          rowmap_chunk_store(sd, P.rmo.ptr, (long long)c.b * P.rmo.stride, P.rmo.ld, rows_mine, et, col0, rm_cols);
+          // (the buffer is staged again two chunks on, after every thread has passed the next
+          // chunk's barriers, and so finished these stores)
         }
         if (publish) {
           // the tile's stores are visible before its completion is published
@@ -1009,6 +1011,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         if (et == 0) {
           if (OUT_BUFS == 2) bulk_wait_read<1>(); else bulk_wait_read<0>();
         }
+        if (ch == 0 && next_rowmap && et < TM) rows_next[et] = next_row;
         named_bar_sync(1, EPI_THREADS);
         if (!d_trans) {
 #pragma unroll
@@ -1060,6 +1063,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
           }
         }
       }
+      // a row-mapped next tile's first chunk of W rows (a row-mapped tile issued it in its
+      // last chunk)
+      if (!rowmap && next_rowmap && rm_has_c)
+        rowmap_own_load(cvec, rm_base(*nti), P.rmo.ld, rows_next[r], (int)(nti->ij >> 16) * TT + half * 32, rm_cols);
       if (bad) set_status(P.status, GNS_DEVST_NONFINITE);
       if (et == 0) {
         // this CTA's half of the tile is in global memory (products nothing in the launch
