@@ -267,6 +267,13 @@ GNS_DEV void red_release_gpu_add(int* p, int v) {
 }
 GNS_DEV void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
+// Programmatic dependent launch. A kernel launched with programmatic stream serialization may
+// start while the kernel ahead of it on the stream is still running; grid_dep_wait() returns
+// once that kernel has completed and its memory operations are visible (at once after an
+// ordinary launch). grid_dep_launch() lets such a kernel behind this one begin to launch.
+GNS_DEV void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+GNS_DEV void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Spin (bounded by limit_ns) until *ctr >= target; then order later async-proxy (TMA) reads
 // after it.
 GNS_DEV bool wait_counter(const int* ctr, int target, volatile int* abort_flag, int* status,

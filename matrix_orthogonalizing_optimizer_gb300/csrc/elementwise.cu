@@ -72,10 +72,19 @@ __device__ __forceinline__ __half from_f<__half>(float v) {
 
 // Rows start on 16-byte boundaries (ld and the base are 16-byte aligned), so each thread
 // reads 16-byte vectors of VEC elements; a scalar tail covers cols % VEC.
+// Both kernels below may also zero `nzero` ints at `zero` (the completion counters of the GEMM
+// launch that follows them on the stream), and let that launch begin while they finish.
+__device__ __forceinline__ void zero_and_release(int* zero, int nzero) {
+  grid_dep_launch();
+  if (zero && blockIdx.x == 0 && blockIdx.y == 0)
+    for (int i = threadIdx.x; i < nzero; i += blockDim.x) zero[i] = 0;
+}
+
 template <typename T>
 __global__ void sumsq_kernel(const T* X, long long ld, long long stride, int rows, int cols, int npart,
-                             float* partials) {
+                             float* partials, int* zero, int nzero) {
   constexpr int VEC = 16 / sizeof(T);
+  zero_and_release(zero, nzero);
   const int b = blockIdx.y, part = blockIdx.x;
   const int rp = (rows + npart - 1) / npart;
   const int r0 = part * rp, r1 = min(rows, r0 + rp);
@@ -116,7 +125,9 @@ __device__ __forceinline__ float mom(float m, float g, float mu, int mode) {
 }
 
 __global__ void momentum_kernel(bf16* M, long long ldm, long long sm, const bf16* G, long long ldg, long long sg,
-                                int rows, int cols, float mu, int mode, int npart, float* partials) {
+                                int rows, int cols, float mu, int mode, int npart, float* partials, int* zero,
+                                int nzero) {
+  zero_and_release(zero, nzero);
   const int b = blockIdx.y, part = blockIdx.x;
   const int rp = (rows + npart - 1) / npart;
   const int r0 = part * rp, r1 = min(rows, r0 + rp);
@@ -1231,26 +1242,27 @@ __global__ void selftest_wait_kernel(const int* counter, int target, unsigned lo
   }
 }
 
-int launch_sumsq(gns_dtype dt, const MatRef& X, int64_t count, float* partials, void* stream, std::string* err) {
+int launch_sumsq(gns_dtype dt, const MatRef& X, int64_t count, float* partials, void* stream, std::string* err,
+                 int* zero, int nzero) {
   dim3 grid(NPART, (unsigned)count);
   if (dt == GNS_BF16)
     sumsq_kernel<bf16><<<grid, 256, 0, S(stream)>>>(static_cast<const bf16*>(X.ptr), X.ld, X.stride, (int)X.rows,
-                                                   (int)X.cols, NPART, partials);
+                                                   (int)X.cols, NPART, partials, zero, nzero);
   else if (dt == GNS_F16)
     sumsq_kernel<__half><<<grid, 256, 0, S(stream)>>>(static_cast<const __half*>(X.ptr), X.ld, X.stride, (int)X.rows,
-                                                     (int)X.cols, NPART, partials);
+                                                     (int)X.cols, NPART, partials, zero, nzero);
   else
     sumsq_kernel<float><<<grid, 256, 0, S(stream)>>>(static_cast<const float*>(X.ptr), X.ld, X.stride, (int)X.rows,
-                                                    (int)X.cols, NPART, partials);
+                                                    (int)X.cols, NPART, partials, zero, nzero);
   return check_launch("sumsq", err);
 }
 
 int launch_momentum(const MatRef& M, const MatRef& G, int64_t count, float mu, int mode, float* partials,
-                    void* stream, std::string* err) {
+                    void* stream, std::string* err, int* zero, int nzero) {
   dim3 grid(NPART, (unsigned)count);
   momentum_kernel<<<grid, 256, 0, S(stream)>>>(static_cast<bf16*>(M.ptr), M.ld, M.stride,
                                                static_cast<const bf16*>(G.ptr), G.ld, G.stride, (int)M.rows,
-                                               (int)M.cols, mu, mode, NPART, partials);
+                                               (int)M.cols, mu, mode, NPART, partials, zero, nzero);
   return check_launch("momentum", err);
 }
 

@@ -13,9 +13,12 @@ constexpr int NPART = 32;           // parts per matrix of a deterministic reduc
 constexpr int KEY_DIGITS = 10;      // base-2^32 digits of an exact l1 key (320 bits)
 constexpr int MAX_SELECT_N = 65536; // largest selection dimension (shared-memory state)
 
-int launch_sumsq(gns_dtype dt, const MatRef& X, int64_t count, float* partials, void* stream, std::string* err);
+// zero / nzero (optional): ints the kernel sets to 0 (the completion counters of the GEMM launch
+// enqueued right after it, which then skips its own reset).
+int launch_sumsq(gns_dtype dt, const MatRef& X, int64_t count, float* partials, void* stream, std::string* err,
+                 int* zero = nullptr, int nzero = 0);
 int launch_momentum(const MatRef& M, const MatRef& G, int64_t count, float mu, int mode, float* partials,
-                    void* stream, std::string* err);
+                    void* stream, std::string* err, int* zero = nullptr, int nzero = 0);
 // npart: partials per matrix (NPART, or a gather's per-block sums, gather_cols_blocks).
 int launch_finalize_norm(const float* partials, int64_t count, float eps, float* inv, void* stream, std::string* err,
                          int64_t npart = NPART);

@@ -7,6 +7,10 @@
 //     B(j,k) = b_mn ? B[k][j] : B[j][k]
 // so an ordinary product A * Bmat is b_mn = 1 with B = Bmat, and X X^T is A = B = X with
 // a_mn = b_mn = 0. alpha' = alpha * scale[b]^alpha_pow, beta' = beta * scale[b]^beta_pow.
+// With scale_part set instead (tensor-core kernel only), scale[b] = 1 / (sqrt(s) + scale_eps),
+// s the sum of the scale_npart = 32 partial sums scale_part[b * 32 + p] (16-byte aligned) by a
+// fixed pairwise tree in fp32 (fp64 where that overflows): the Frobenius-norm scale, formed by
+// the GEMM from the norm pass's partial sums.
 // C and D are read / written at (i, j) (or at (j, i) when c_trans / d_trans), with the
 // row index i replaced by row_map[b * row_map_stride + i] when row_map is set.
 // sym: M == N and only tiles with tile_row <= tile_col are computed; each off-diagonal tile
@@ -45,6 +49,9 @@ struct GemmOp {
   float alpha = 1.f, beta = 0.f, gamma = 0.f;
   int alpha_pow = 0, beta_pow = 0;
   const float* scale = nullptr;
+  const float* scale_part = nullptr;
+  int scale_npart = 0;
+  float scale_eps = 0.f;
   MatRef C;
   int c_trans = 0;
   MatRef D;
@@ -76,10 +83,13 @@ inline std::vector<GemmOp> with_types(gns_dtype dt, const GemmOp* ops, int nops)
 // Enqueues ops as ONE launch. dep_masks[i] (nullable) names earlier ops of the same launch
 // whose tiles of the same matrix must be complete before a tile of op i starts (the
 // tensor-core kernel waits on per-(op, matrix) completion counters: `counters`, at least
-// sum(batch) ints of device memory, reset by the launch). Without masks the ops must be
-// mutually independent. Returns GNS_OK or an error status with *err set.
+// sum(batch) ints of device memory, reset by the launch unless counters_zeroed: then the
+// kernel enqueued just before it on the stream has zeroed them). Without masks the ops must be
+// mutually independent. The launch may begin while the kernel before it on the stream ends
+// (programmatic dependent launch): it reads and writes global memory only after that kernel
+// has completed. Returns GNS_OK or an error status with *err set.
 int gemm_launch_tc(const GemmOp* ops, int nops, const uint32_t* dep_masks, int* counters, int32_t* dev_status,
-                   void* stream, std::string* err);
+                   void* stream, std::string* err, bool counters_zeroed = false);
 int gemm_launch_f32(const GemmOp* ops, int nops, const uint32_t* dep_masks, int* counters, int32_t* dev_status,
                     void* stream, std::string* err);
 
@@ -105,9 +115,10 @@ constexpr int kMaxProgramOps = 24;
 // A sequence of ops in program order (op j may read what op i < j wrote, or overwrite what
 // it read). bf16 / fp16: as few launches as possible, dependencies between ops found from
 // the buffers they read (A, B, C) and write (D, D2) and enforced per matrix inside the
-// launch; fp32: one launch per op, ordered by the stream. `counters`: kMaxProgramOps * batch ints.
+// launch; fp32: one launch per op, ordered by the stream. `counters`: kMaxProgramOps * batch ints,
+// already zero when counters_zeroed (see gemm_launch_tc).
 int gemm_program(gns_dtype dt, const GemmOp* ops, int nops, int* counters, int32_t* dev_status, void* stream,
-                 std::string* err);
+                 std::string* err, bool counters_zeroed = false);
 
 // Number of SMs of the current device (cached per device).
 int device_sm_count();

@@ -190,6 +190,10 @@ int gemm_launch_f32(const GemmOp* ops, int nops, const uint32_t* dep_masks, int*
   int tiles = 0;
   for (int i = 0; i < nops; ++i) {
     const GemmOp& o = ops[i];
+    if (o.scale_part) {
+      *err = "internal: the fp32 path takes the norm scale as a finished array";
+      return GNS_ERR_UNSUPPORTED;
+    }
     Problem& pr = P.prob[i];
     pr.A = static_cast<const float*>(o.A.ptr);
     pr.lda = o.A.ld;

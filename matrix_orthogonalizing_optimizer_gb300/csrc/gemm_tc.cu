@@ -119,6 +119,9 @@ constexpr int DEEP_MAX_SLICES_PER_TILE = 24;
 constexpr int DEEP_SMALL_BATCH = 32;
 constexpr int DEEP_MAX_SLICES_SMALL_BATCH = 96;
 
+// Partial sums per matrix a problem's norm scale is formed from (scale_part).
+constexpr int SCALE_NPART = 32;
+
 struct Problem {
   CUtensorMap tmA;
   CUtensorMap tmB;
@@ -134,6 +137,8 @@ struct Problem {
   float alpha, beta, gamma;
   int alpha_pow, beta_pow;
   const float* scale;
+  const float* scale_part;  // per-matrix partial sums of squares (SCALE_NPART, 16-byte aligned)
+  float scale_eps;
   int has_c, c_trans, d_trans, has_d2;
   int diag_limit;
   int check_finite;
@@ -551,6 +556,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
   if constexpr (CG == 2) cluster_sync_all();  // the peer's barriers are initialised before any remote arrival
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // everything above touches only this CTA pair's shared memory and TMEM: with a programmatic
+  // launch it overlaps the end of the kernel ahead, whose results are read from here on
+  grid_dep_wait();
 
   if (warp == 0 || warp == PROD2_WARP) {
     if (lane == 0) {
@@ -699,13 +707,46 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
       // Decodes this pair's tiles and the epilogue's per-tile parameters into the TileInfo
       // ring, up to INFO_RING tiles ahead of the epilogue.
       int seg = 0, local = 0;
+      const float* sc_part = nullptr;  // the last scale formed from partial sums, and its matrix
+      int sc_b = -1;
+      float sc_last = 0.f;
       for (int tile = pair; tile < P.total_tiles; tile += npairs, ++local) {
         const int slot = local % INFO_RING;
         if (!mbar_wait(&info_empty[slot], ((local / INFO_RING) & 1u) ^ 1u, abort_flag, P.status)) break;
         const TileCoord c = decode_tile(P, tile, &seg);
         const Problem& pr = P.prob[c.p];
         float alpha = pr.alpha, beta = pr.beta;
-        if (pr.scale) {
+        if (pr.scale_part) {
+          if (pr.scale_part != sc_part || c.b != sc_b) {
+            // 1 / (||X_b||_F + eps) from the matrix's 32 partial sums, added by a fixed pairwise
+            // tree in fp32 (fp64 arithmetic on this lane stalls the C loader and publishing lanes
+            // of its warp); in fp64 only when the fp32 sum overflows
+            const float4* pp = reinterpret_cast<const float4*>(pr.scale_part + (long long)c.b * SCALE_NPART);
+            float4 v[SCALE_NPART / 4];
+#pragma unroll
+            for (int q = 0; q < SCALE_NPART / 4; ++q) v[q] = pp[q];
+            float u[SCALE_NPART / 4];
+#pragma unroll
+            for (int q = 0; q < SCALE_NPART / 4; ++q) u[q] = (v[q].x + v[q].y) + (v[q].z + v[q].w);
+#pragma unroll
+            for (int w = SCALE_NPART / 8; w >= 1; w /= 2)
+#pragma unroll
+              for (int q = 0; q < w; ++q) u[q] = u[2 * q] + u[2 * q + 1];
+            const float t = u[0];
+            if (t <= 3.0e38f) {
+              sc_last = __fdiv_rn(1.f, __fadd_rn(__fsqrt_rn(t), pr.scale_eps));
+            } else {
+              double d = 0.0;
+#pragma unroll
+              for (int q = 0; q < SCALE_NPART / 4; ++q) d += ((double)v[q].x + v[q].y) + ((double)v[q].z + v[q].w);
+              sc_last = (float)(1.0 / (sqrt(d) + (double)pr.scale_eps));
+            }
+            sc_part = pr.scale_part;
+            sc_b = c.b;
+          }
+          alpha *= powi(sc_last, pr.alpha_pow);
+          beta *= powi(sc_last, pr.beta_pow);
+        } else if (pr.scale) {
           const float sc = pr.scale[c.b];
           alpha *= powi(sc, pr.alpha_pow);
           beta *= powi(sc, pr.beta_pow);
@@ -1256,7 +1297,7 @@ static void tile_order(const GemmOp* ops, int nops, bool dependent, std::vector<
 }
 
 int gemm_launch_tc(const GemmOp* ops, int nops, const uint32_t* dep_masks, int* counters, int32_t* dev_status,
-                   void* stream, std::string* err) {
+                   void* stream, std::string* err, bool counters_zeroed) {
   using namespace tc;
   static_assert(sizeof(Params) <= 32764, "kernel parameter space");
   if (nops < 1 || nops > MAX_PROB) {
@@ -1356,6 +1397,12 @@ int gemm_launch_tc(const GemmOp* ops, int nops, const uint32_t* dep_masks, int* 
     pr.alpha_pow = o.alpha_pow;
     pr.beta_pow = o.beta_pow;
     pr.scale = o.scale;
+    if (o.scale_part && (o.scale_npart != SCALE_NPART || reinterpret_cast<uintptr_t>(o.scale_part) % 16 != 0)) {
+      *err = "internal: a norm scale formed from other than 32 aligned partial sums per matrix";
+      return GNS_ERR_UNSUPPORTED;
+    }
+    pr.scale_part = o.scale_part;
+    pr.scale_eps = o.scale_eps;
     pr.c_trans = o.c_trans;
     pr.d_trans = o.d_trans;
     pr.diag_limit = (int)o.diag_limit;
@@ -1399,7 +1446,7 @@ int gemm_launch_tc(const GemmOp* ops, int nops, const uint32_t* dep_masks, int* 
   P.total_tiles = tiles;
   P.status = dev_status;
   P.counters = counters;
-  if (counters && tiles > 0) {
+  if (counters && tiles > 0 && !counters_zeroed) {
     cudaError_t me = cudaMemsetAsync(counters, 0, sizeof(int) * off, static_cast<cudaStream_t>(stream));
     if (me != cudaSuccess) {
       *err = std::string("counter reset: ") + cudaGetErrorString(me);
@@ -1420,19 +1467,20 @@ int gemm_launch_tc(const GemmOp* ops, int nops, const uint32_t* dep_masks, int* 
   if (resident < 1) return GNS_ERR_CUDA;
   const int groups = std::min(tiles, resident);
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];
+  // the kernel waits (grid_dep_wait) for the kernel ahead of it before it touches global memory
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.gridDim = dim3(cg * groups, 1, 1);
   cfg.blockDim = dim3(NUM_THREADS, 1, 1);
   cfg.dynamicSmemBytes = deep ? DeepPlan::SMEM_BYTES : ShallowPlan::SMEM_BYTES;
   cfg.stream = static_cast<cudaStream_t>(stream);
-  if (cg == 2) {
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-  }
+  cfg.attrs = attr;
+  cfg.numAttrs = cg == 2 ? 2 : 1;
   cudaError_t e = cg == 2 ? (deep ? cudaLaunchKernelEx(&cfg, gemm_kernel<DeepPlan, 2>, P)
                                   : cudaLaunchKernelEx(&cfg, gemm_kernel<ShallowPlan, 2>, P))
                           : (deep ? cudaLaunchKernelEx(&cfg, gemm_kernel<DeepPlan, 1>, P)

@@ -82,7 +82,7 @@ static bool op_conflict(const GemmOp& first, const GemmOp& later) {
 }
 
 int gemm_program(gns_dtype dt, const GemmOp* ops, int nops, int* counters, int32_t* dev_status, void* stream,
-                 std::string* err) {
+                 std::string* err, bool counters_zeroed) {
   if (dt == GNS_F32) {
     for (int i = 0; i < nops; ++i) {
       int rc = gemm_launch(dt, ops + i, 1, dev_status, stream, err);
@@ -130,7 +130,7 @@ int gemm_program(gns_dtype dt, const GemmOp* ops, int nops, int* counters, int32
       masks[j] = red;
     }
     profile_gemm_begin(stream);
-    int rc = gemm_launch_tc(ops + base, n, masks, counters, dev_status, stream, err);
+    int rc = gemm_launch_tc(ops + base, n, masks, counters, dev_status, stream, err, counters_zeroed && base == 0);
     profile_gemm_end(stream);
     if (rc) return rc;
   }
@@ -419,9 +419,32 @@ static GemmOp sym_op(const MatRef& A, int a_mn, const MatRef& Bm, int b_mn, int6
 
 // Dion3 Algorithm 3 on one group (B matrices, oriented X = n x m). inv: per-matrix
 // 1/(||X||_F + eps) already computed on the stream.
+// The Frobenius-norm scale 1 / (||X_b||_F + eps) of a group's products: the finished array
+// (inv), or the per-matrix partial sums of squares the tensor-core GEMM forms it from (part),
+// in which case the kernel that wrote them also zeroed the GEMM's completion counters.
+struct NormScale {
+  const float* inv = nullptr;
+  const float* part = nullptr;
+  float eps = 0.f;
+  bool counters_zeroed = false;  // the group's GEMM completion counters are already zero
+};
+
+static void set_scale(GemmOp* o, const NormScale& sc) {
+  o->scale = sc.inv;
+  if (sc.part) {
+    o->scale_part = sc.part;
+    o->scale_npart = NPART;
+    o->scale_eps = sc.eps;
+  }
+}
+
 static int run_gram(gns_dtype dt, const Src& src, int64_t B, int64_t n, int64_t m, const gns_ns_params* ns,
-                    const GramBufs& g, const float* inv, const Final& fin, int32_t* st, void* stream) {
-  if (chain_ok(true, dt, src, n, m, ns, fin)) return run_chain(true, dt, src, B, n, m, ns, inv, fin, st, stream);
+                    const GramBufs& g, const NormScale& sc, const Final& fin, int32_t* st, void* stream) {
+  const float* inv = sc.inv;
+  if (chain_ok(true, dt, src, n, m, ns, fin)) {
+    if (!inv) return fail(GNS_ERR_UNSUPPORTED, "internal: the chain kernel takes the norm scale as an array");
+    return run_chain(true, dt, src, B, n, m, ns, inv, fin, st, stream);
+  }
   std::string err;
   const int64_t np = g.np;
   std::vector<GemmOp> prog;  // the whole sequence, in program order
@@ -436,7 +459,8 @@ static int run_gram(gns_dtype dt, const Src& src, int64_t B, int64_t n, int64_t 
     MatRef xa;
     int mn;
     as_rows(X, &xa, &mn);
-    GemmOp o = sym_op(xa, mn, xa, mn, m, np, B, 1.f, X.user ? 2 : 0, inv, nullptr, 0.f, g.R);
+    GemmOp o = sym_op(xa, mn, xa, mn, m, np, B, 1.f, X.user ? 2 : 0, nullptr, nullptr, 0.f, g.R);
+    if (X.user) set_scale(&o, sc);
     if ((rc = launch(&o, 1))) return rc;
   }
   bool q_id = true;
@@ -461,7 +485,7 @@ static int run_gram(gns_dtype dt, const Src& src, int64_t B, int64_t n, int64_t 
       o.batch = B;
       o.alpha = 1.f;
       o.alpha_pow = X.user ? 1 : 0;
-      o.scale = inv;
+      if (X.user) set_scale(&o, sc);
       MatRef xd = g.X[nx & 1];
       o.D = xd;
       if ((rc = launch(&o, 1))) return rc;
@@ -518,7 +542,7 @@ static int run_gram(gns_dtype dt, const Src& src, int64_t B, int64_t n, int64_t 
     o.batch = B;
     o.alpha = fin.alpha;
     o.alpha_pow = X.user ? 1 : 0;
-    o.scale = inv;
+    if (X.user) set_scale(&o, sc);
     o.D = fin.D;
     o.d_trans = fin.d_trans;
     o.c_dt = o.d_dt = fin.out_dt;
@@ -533,7 +557,7 @@ static int run_gram(gns_dtype dt, const Src& src, int64_t B, int64_t n, int64_t 
     if ((rc = launch(&o, 1))) return rc;
   }
   for (GemmOp& o : prog) o.upper_out = o.sym;  // internal symmetric buffers: upper tiles only
-  rc = gemm_program(dt, prog.data(), (int)prog.size(), g.counters, st, stream, &err);
+  rc = gemm_program(dt, prog.data(), (int)prog.size(), g.counters, st, stream, &err, sc.counters_zeroed);
   return rc ? fail(rc, err) : GNS_OK;
 }
 
@@ -906,9 +930,20 @@ static int ns_common(bool gram, const gns_batch* x, const gns_batch* out, int ng
     if (g_alg) {
       GramBufs gb;
       plan_gram(a, s.B, s.n, s.m, dt, ns, &gb, true);
-      if ((rc = launch_sumsq(dt, src.mat, s.B, gb.partials, stream, &err))) return fail(rc, err);
-      if ((rc = launch_finalize_norm(gb.partials, s.B, ns->eps, gb.inv, stream, &err))) return fail(rc, err);
-      if ((rc = run_gram(dt, src, s.B, s.n, s.m, ns, gb, gb.inv, fin, st, stream))) return rc;
+      NormScale sc;
+      if (dt != GNS_F32) {
+        // the GEMM forms the scale from the partial sums; their kernel zeroes its counters
+        sc.part = gb.partials;
+        sc.eps = ns->eps;
+        sc.counters_zeroed = true;
+        if ((rc = launch_sumsq(dt, src.mat, s.B, gb.partials, stream, &err, gb.counters, kMaxProgramOps * (int)s.B)))
+          return fail(rc, err);
+      } else {
+        sc.inv = gb.inv;
+        if ((rc = launch_sumsq(dt, src.mat, s.B, gb.partials, stream, &err))) return fail(rc, err);
+        if ((rc = launch_finalize_norm(gb.partials, s.B, ns->eps, gb.inv, stream, &err))) return fail(rc, err);
+      }
+      if ((rc = run_gram(dt, src, s.B, s.n, s.m, ns, gb, sc, fin, st, stream))) return rc;
     } else {
       StdBufs sb;
       plan_std(a, s.B, s.n, s.m, dt, &sb, true);
@@ -1077,17 +1112,9 @@ int gns_muon_step(const gns_batch* W, const gns_batch* G, const gns_batch* M, co
       // Muon, eq. (1) (NorMuon, eq. (2)): M <- mu M + G; O = polar(M); W <- (1 - lr wd) W - lr scale O
       float* partials = mb.use_std ? mb.sb.partials : mb.gb.partials;
       float* inv = mb.use_std ? mb.sb.inv : mb.gb.inv;
-      if ((rc = launch_momentum(mm, gm, s.B, mu, 0, partials, stream, &err))) return fail(rc, err);
-      if ((rc = launch_finalize_norm(partials, s.B, ns->eps, inv, stream, &err))) return fail(rc, err);
       Src src;
       src.mat = mm;
       src.trans = s.trans;
-      if (mb.nsdt == GNS_F16) {
-        // Dion3 Algorithm 3, normalise then cast: the normalised momentum, rounded once to float16
-        if ((rc = launch_cast_scaled(mb.x16, mm, inv, s.B, stream, &err))) return fail(rc, err);
-        src.mat = mb.x16;
-        src.user = false;
-      }
       Final fin;
       fin.out_dt = GNS_BF16;
       if (normuon) {
@@ -1106,6 +1133,19 @@ int gns_muon_step(const gns_batch* W, const gns_batch* G, const gns_batch* M, co
         fs.alpha = step_scale;
         fs.beta = decay;
         fs.has_c = true;
+      }
+      // bf16 Gram NS on the tile path: the GEMM forms the norm scale from the momentum pass's
+      // partial sums (no finalize launch), and that pass zeroes the GEMM's completion counters
+      const bool part_scale = !mb.use_std && mb.nsdt == GNS_BF16 && !chain_ok(true, mb.nsdt, src, s.n, s.m, ns, fin);
+      if ((rc = launch_momentum(mm, gm, s.B, mu, 0, partials, stream, &err, part_scale ? mb.gb.counters : nullptr,
+                                part_scale ? kMaxProgramOps * (int)s.B : 0)))
+        return fail(rc, err);
+      if (!part_scale && (rc = launch_finalize_norm(partials, s.B, ns->eps, inv, stream, &err))) return fail(rc, err);
+      if (mb.nsdt == GNS_F16) {
+        // Dion3 Algorithm 3, normalise then cast: the normalised momentum, rounded once to float16
+        if ((rc = launch_cast_scaled(mb.x16, mm, inv, s.B, stream, &err))) return fail(rc, err);
+        src.mat = mb.x16;
+        src.user = false;
       }
       if (!normuon) {
         const bool g_alg = !mb.use_std;
@@ -1131,7 +1171,15 @@ int gns_muon_step(const gns_batch* W, const gns_batch* G, const gns_batch* M, co
             return fail(rc, err);
         }
       } else {
-        if ((rc = run_gram(mb.nsdt, src, s.B, s.n, s.m, ns, mb.gb, inv, fin, dev_status, stream))) return rc;
+        NormScale sc;
+        if (part_scale) {
+          sc.part = partials;
+          sc.eps = ns->eps;
+          sc.counters_zeroed = true;
+        } else {
+          sc.inv = inv;
+        }
+        if ((rc = run_gram(mb.nsdt, src, s.B, s.n, s.m, ns, mb.gb, sc, fin, dev_status, stream))) return rc;
       }
       if (normuon) {
         // eq. (2): second moments of the rows of O, row scaling, Frobenius rescale, update
@@ -1186,7 +1234,9 @@ int gns_muon_step(const gns_batch* W, const gns_batch* G, const gns_batch* M, co
       fin.D = mb.os;
       fin.d_trans = normuon ? 0 : 1;  // the tall Muon flavour's column scatter reads O transposed
     }
-    if ((rc = run_gram(mb.nsdt, src, s.B, k, s.m, ns, mb.gb, mb.gb.inv, fin, dev_status, stream))) return rc;
+    NormScale sc;
+    sc.inv = mb.gb.inv;
+    if ((rc = run_gram(mb.nsdt, src, s.B, k, s.m, ns, mb.gb, sc, fin, dev_status, stream))) return rc;
     if (fused) continue;
     if (!normuon) {
       // W[:, S] <- (1 - lr wd) W[:, S] - lr scale O^T, one rounding
