@@ -429,6 +429,12 @@ struct NormScale {
   bool counters_zeroed = false;  // the group's GEMM completion counters are already zero
 };
 
+// Smallest oriented row count n whose groups take the scale from the partial sums: the GEMM
+// forms it per scaled tile (a 128-byte line of partial sums per matrix); on smaller matrices,
+// whose products are one short tile per matrix, that costs more than the finalize launch it
+// saves (measured: the 1-CTA tile paths of n = 32 .. 256 slower by a few per cent).
+constexpr int64_t kPartScaleMinN = 512;
+
 static void set_scale(GemmOp* o, const NormScale& sc) {
   o->scale = sc.inv;
   if (sc.part) {
@@ -931,7 +937,7 @@ static int ns_common(bool gram, const gns_batch* x, const gns_batch* out, int ng
       GramBufs gb;
       plan_gram(a, s.B, s.n, s.m, dt, ns, &gb, true);
       NormScale sc;
-      if (dt != GNS_F32) {
+      if (dt != GNS_F32 && s.n >= kPartScaleMinN) {
         // the GEMM forms the scale from the partial sums; their kernel zeroes its counters
         sc.part = gb.partials;
         sc.eps = ns->eps;
@@ -1134,9 +1140,11 @@ int gns_muon_step(const gns_batch* W, const gns_batch* G, const gns_batch* M, co
         fs.beta = decay;
         fs.has_c = true;
       }
-      // bf16 Gram NS on the tile path: the GEMM forms the norm scale from the momentum pass's
-      // partial sums (no finalize launch), and that pass zeroes the GEMM's completion counters
-      const bool part_scale = !mb.use_std && mb.nsdt == GNS_BF16 && !chain_ok(true, mb.nsdt, src, s.n, s.m, ns, fin);
+      // bf16 Gram NS on the tile path (n >= kPartScaleMinN): the GEMM forms the norm scale from
+      // the momentum pass's partial sums (no finalize launch), and that pass zeroes the GEMM's
+      // completion counters
+      const bool part_scale = !mb.use_std && mb.nsdt == GNS_BF16 && s.n >= kPartScaleMinN &&
+                              !chain_ok(true, mb.nsdt, src, s.n, s.m, ns, fin);
       if ((rc = launch_momentum(mm, gm, s.B, mu, 0, partials, stream, &err, part_scale ? mb.gb.counters : nullptr,
                                 part_scale ? kMaxProgramOps * (int)s.B : 0)))
         return fail(rc, err);

@@ -285,7 +285,8 @@ def _w_update_ok(W_gpu, W_or, dW_or, tol=TOL_BF16):
     return np.linalg.norm(excess) <= tol * np.linalg.norm(dW_or), np.linalg.norm(excess) / np.linalg.norm(dW_or)
 
 
-@pytest.mark.parametrize("count,rows,cols", [(3, 256, 1024), (2, 700, 200), (2, 384, 384)])
+@pytest.mark.parametrize("count,rows,cols", [(3, 256, 1024), (2, 700, 200), (2, 384, 384), (2, 512, 1536),
+                                            (2, 1600, 640)])
 def test_muon_step_dense(count, rows, cols):
     Wb, W = bf16_input(13, (count, rows, cols), 1.0 / np.sqrt(cols))
     Gb, _ = bf16_input(14, (count, rows, cols), 1.0 / np.sqrt(cols))
@@ -302,6 +303,36 @@ def test_muon_step_dense(count, rows, cols):
         assert np.array_equal(Mg[b], M_or), "momentum must match bit for bit"
         ok, err = _w_update_ok(Wg[b], W_or, 0.02 * 1.5 * O)
         assert ok, err
+
+
+def test_muon_step_two_launches():
+    """Groups of at least 512 oriented rows: the Muon step is two libgns launches, the momentum
+    pass (which also zeroes the GEMM's completion counters) and one GEMM launch that forms the
+    Frobenius scale from the pass's 32 partial sums per matrix; smaller groups keep the
+    finalize launch. Both stay within the update bar of the oracle."""
+    import ctypes
+    from matrix_orthogonalizing_optimizer_gb300 import _lib
+    lib = _lib.load()
+    for rows, cols, want in ((512, 1024, 2), (1024, 600, 2), (256, 1024, 3)):
+        Wb, _ = bf16_input(61, (2, rows, cols), 1.0 / np.sqrt(cols))
+        Gb, _ = bf16_input(62, (2, rows, cols), 1.0 / np.sqrt(cols))
+        Mb, _ = bf16_input(63, (2, rows, cols), 1.0 / np.sqrt(cols))
+        Wt, Gt, Mt = bits_to_torch(Wb), bits_to_torch(Gb), bits_to_torch(Mb)
+        st = _status()
+        torch.cuda.synchronize()
+        lib.gns_profile_set(None, 0)
+        gns.muon_step(Wt, Gt, Mt, lr=0.02, momentum=0.95, status=st)
+        torch.cuda.synchronize()
+        g, a = ctypes.c_int(0), ctypes.c_int(0)
+        lib.gns_profile_query(ctypes.byref(g), ctypes.byref(a))
+        assert (g.value, a.value) == (1, want), (rows, cols, g.value, a.value)
+        assert int(st.item()) == 0
+        Mg, Wg = torch_to_bits(Mt), torch_to_f64(Wt)
+        for b in range(2):
+            W_or, M_or, O = omuon.muon_step(Wb[b], Gb[b], Mb[b], lr=0.02, mu=0.95)
+            assert np.array_equal(Mg[b], M_or)
+            ok, err = _w_update_ok(Wg[b], W_or, 0.02 * O)
+            assert ok, (rows, cols, err)
 
 
 def _frac_case(seed, count, rows, cols, frac, ties=False):
