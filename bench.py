@@ -58,7 +58,8 @@ GEMM_TRAFFIC = {"a08be551760510ae": 2.300315e9, "afb81c60e8a2853b": 2.295040e9, 
                 "4ff1ba1d442b50cd": 2.308916e9,
                 "76c725126f780dc2": 2.303400e9,
                 "16ba07df5e30b2f1": 2.298324e9,
-                "bbd40895ad2357b8": 2.303989e9}
+                "bbd40895ad2357b8": 2.303989e9,
+                "cbd268b695867624": 2.297286e9}
 
 
 def gemm_source_hash():

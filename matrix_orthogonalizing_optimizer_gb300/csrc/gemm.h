@@ -85,9 +85,10 @@ inline std::vector<GemmOp> with_types(gns_dtype dt, const GemmOp* ops, int nops)
 // tensor-core kernel waits on per-(op, matrix) completion counters: `counters`, at least
 // sum(batch) ints of device memory, reset by the launch unless counters_zeroed: then the
 // kernel enqueued just before it on the stream has zeroed them). Without masks the ops must be
-// mutually independent. The launch may begin while the kernel before it on the stream ends
-// (programmatic dependent launch): it reads and writes global memory only after that kernel
-// has completed. Returns GNS_OK or an error status with *err set.
+// mutually independent. A launch with an op that forms its scale from partial sums
+// (scale_part) is a programmatic dependent launch: it may begin while the kernel before it on
+// the stream ends, and reads and writes global memory only after that kernel has completed.
+// Returns GNS_OK or an error status with *err set.
 int gemm_launch_tc(const GemmOp* ops, int nops, const uint32_t* dep_masks, int* counters, int32_t* dev_status,
                    void* stream, std::string* err, bool counters_zeroed = false);
 int gemm_launch_f32(const GemmOp* ops, int nops, const uint32_t* dep_masks, int* counters, int32_t* dev_status,

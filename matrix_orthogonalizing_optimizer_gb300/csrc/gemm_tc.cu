@@ -137,8 +137,6 @@ struct Problem {
   float alpha, beta, gamma;
   int alpha_pow, beta_pow;
   const float* scale;
-  const float* scale_part;  // per-matrix partial sums of squares (SCALE_NPART, 16-byte aligned)
-  float scale_eps;
   int has_c, c_trans, d_trans, has_d2;
   int diag_limit;
   int check_finite;
@@ -148,7 +146,12 @@ struct Problem {
   uint32_t dep_mask;  // earlier problems whose tiles of the same matrix must be complete
   int ctr_off;        // this problem's completion counters: counters[ctr_off + b]
   int publish;        // a later problem of the launch depends on this one: publish completions
+  int scale_part;     // scale holds SCALE_NPART partial sums per matrix (16-byte aligned), not scales
 };
+// (the parameter block holds up to MAX_PROB of these: kept at 1024 bytes, the size of the
+// seven 64-byte-aligned tensor maps and the fields that fit beside them, as launches of many
+// short tiles measured slower with a larger block)
+static_assert(sizeof(Problem) == 1024, "Problem size");
 
 // The launch's tiles form a sequence of segments, each the tiles of problem p for the
 // matrices b0 .. b0 + nb - 1 (matrix-major, then tile): seg_pb = p << 24 | b0, seg_tile =
@@ -173,6 +176,7 @@ struct RowMapOut {
 struct Params {
   Problem prob[MAX_PROB];
   RowMapOut rmo;
+  float scale_eps;  // the eps of every scale formed from partial sums in the launch
   int nprob;
   int total_tiles;
   int nseg;
@@ -475,7 +479,10 @@ __device__ __forceinline__ void rowmap_chunk_store(const uint8_t* sd, void* ptr,
   }
 }
 
-template <class L, int CG>
+// PS: the launch forms scales from partial sums (scale_part) and is a programmatic dependent
+// launch. Launches without either run an instance without that code: on launches of many short
+// tiles, where the tile-info lane is on the critical path, it measured a few per cent slower.
+template <class L, int CG, bool PS>
 __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_constant__ Params P) {
   constexpr int TT = Geo<CG>::TILE;
   constexpr int NCHUNK = Geo<CG>::NCH;
@@ -558,7 +565,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
   const uint32_t tmem_base = *tmem_slot;
   // everything above touches only this CTA pair's shared memory and TMEM: with a programmatic
   // launch it overlaps the end of the kernel ahead, whose results are read from here on
-  grid_dep_wait();
+  if constexpr (PS) grid_dep_wait();
 
   if (warp == 0 || warp == PROD2_WARP) {
     if (lane == 0) {
@@ -716,12 +723,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         const TileCoord c = decode_tile(P, tile, &seg);
         const Problem& pr = P.prob[c.p];
         float alpha = pr.alpha, beta = pr.beta;
-        if (pr.scale_part) {
-          if (pr.scale_part != sc_part || c.b != sc_b) {
+        if (PS && pr.scale_part) {
+          if (pr.scale != sc_part || c.b != sc_b) {
             // 1 / (||X_b||_F + eps) from the matrix's 32 partial sums, added by a fixed pairwise
             // tree in fp32 (fp64 arithmetic on this lane stalls the C loader and publishing lanes
             // of its warp); in fp64 only when the fp32 sum overflows
-            const float4* pp = reinterpret_cast<const float4*>(pr.scale_part + (long long)c.b * SCALE_NPART);
+            const float4* pp = reinterpret_cast<const float4*>(pr.scale + (long long)c.b * SCALE_NPART);
             float4 v[SCALE_NPART / 4];
 #pragma unroll
             for (int q = 0; q < SCALE_NPART / 4; ++q) v[q] = pp[q];
@@ -734,14 +741,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
               for (int q = 0; q < w; ++q) u[q] = u[2 * q] + u[2 * q + 1];
             const float t = u[0];
             if (t <= 3.0e38f) {
-              sc_last = __fdiv_rn(1.f, __fadd_rn(__fsqrt_rn(t), pr.scale_eps));
+              sc_last = __fdiv_rn(1.f, __fadd_rn(__fsqrt_rn(t), P.scale_eps));
             } else {
               double d = 0.0;
 #pragma unroll
               for (int q = 0; q < SCALE_NPART / 4; ++q) d += ((double)v[q].x + v[q].y) + ((double)v[q].z + v[q].w);
-              sc_last = (float)(1.0 / (sqrt(d) + (double)pr.scale_eps));
+              sc_last = (float)(1.0 / (sqrt(d) + (double)P.scale_eps));
             }
-            sc_part = pr.scale_part;
+            sc_part = pr.scale;
             sc_b = c.b;
           }
           alpha *= powi(sc_last, pr.alpha_pow);
@@ -1200,7 +1207,7 @@ int device_sm_count() {
 // Number of CTA groups (pairs for CG = 2, single CTAs for CG = 1) of the GEMM kernel that can
 // be resident at once, and the one-time shared-memory opt-in. A persistent launch never asks
 // for more: its groups wait on one another's completion counters.
-template <class L, int CG>
+template <class L, int CG, bool PS>
 static int resident_groups(std::string* err) {
   static int cached[64] = {0};
   int dev = 0;
@@ -1208,7 +1215,7 @@ static int resident_groups(std::string* err) {
   if (dev < 0 || dev >= 64) dev = 0;
   if (cached[dev]) return cached[dev];
   cudaError_t e =
-      cudaFuncSetAttribute(tc::gemm_kernel<L, CG>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_BYTES);
+      cudaFuncSetAttribute(tc::gemm_kernel<L, CG, PS>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_BYTES);
   if (e != cudaSuccess) {
     *err = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e);
     return 0;
@@ -1226,14 +1233,14 @@ static int resident_groups(std::string* err) {
     cfg.dynamicSmemBytes = L::SMEM_BYTES;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaOccupancyMaxActiveClusters(&groups, tc::gemm_kernel<L, CG>, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&groups, tc::gemm_kernel<L, CG, PS>, &cfg);
     if (e != cudaSuccess || groups < 1) {
       (void)cudaGetLastError();
       groups = device_sm_count() / 2;
     }
   } else {
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tc::gemm_kernel<L, CG>, tc::NUM_THREADS,
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tc::gemm_kernel<L, CG, PS>, tc::NUM_THREADS,
                                                       L::SMEM_BYTES);
     if (e != cudaSuccess || per_sm < 1) {
       (void)cudaGetLastError();
@@ -1329,6 +1336,7 @@ int gemm_launch_tc(const GemmOp* ops, int nops, const uint32_t* dep_masks, int* 
   memset(&P, 0, sizeof(P));
   int tiles = 0;
   P.rmo.prob = -1;
+  bool have_eps = false;  // a problem forms its scale from partial sums (their eps)
   for (int i = 0; i < nops; ++i) {
     const GemmOp& o = ops[i];
     Problem& pr = P.prob[i];
@@ -1397,12 +1405,18 @@ int gemm_launch_tc(const GemmOp* ops, int nops, const uint32_t* dep_masks, int* 
     pr.alpha_pow = o.alpha_pow;
     pr.beta_pow = o.beta_pow;
     pr.scale = o.scale;
-    if (o.scale_part && (o.scale_npart != SCALE_NPART || reinterpret_cast<uintptr_t>(o.scale_part) % 16 != 0)) {
-      *err = "internal: a norm scale formed from other than 32 aligned partial sums per matrix";
-      return GNS_ERR_UNSUPPORTED;
+    if (o.scale_part) {
+      if (o.scale_npart != SCALE_NPART || reinterpret_cast<uintptr_t>(o.scale_part) % 16 != 0 ||
+          (have_eps && o.scale_eps != P.scale_eps)) {
+        *err = "internal: a norm scale formed from other than 32 aligned partial sums per matrix, or with "
+               "another eps than the launch's";
+        return GNS_ERR_UNSUPPORTED;
+      }
+      pr.scale = o.scale_part;
+      pr.scale_part = 1;
+      P.scale_eps = o.scale_eps;
+      have_eps = true;
     }
-    pr.scale_part = o.scale_part;
-    pr.scale_eps = o.scale_eps;
     pr.c_trans = o.c_trans;
     pr.d_trans = o.d_trans;
     pr.diag_limit = (int)o.diag_limit;
@@ -1462,13 +1476,21 @@ int gemm_launch_tc(const GemmOp* ops, int nops, const uint32_t* dep_masks, int* 
   }
   const bool deep = slices <= (long long)DEEP_MAX_SLICES_PER_TILE * tiles ||
                     (max_batch <= DEEP_SMALL_BATCH && slices <= (long long)DEEP_MAX_SLICES_SMALL_BATCH * tiles);
-  const int resident = cg == 2 ? (deep ? resident_groups<DeepPlan, 2>(err) : resident_groups<ShallowPlan, 2>(err))
-                                : (deep ? resident_groups<DeepPlan, 1>(err) : resident_groups<ShallowPlan, 1>(err));
+  const bool ps = have_eps;
+  const int resident = cg == 2 ? (deep ? (ps ? resident_groups<DeepPlan, 2, true>(err)
+                                             : resident_groups<DeepPlan, 2, false>(err))
+                                       : (ps ? resident_groups<ShallowPlan, 2, true>(err)
+                                             : resident_groups<ShallowPlan, 2, false>(err)))
+                               : (deep ? (ps ? resident_groups<DeepPlan, 1, true>(err)
+                                             : resident_groups<DeepPlan, 1, false>(err))
+                                       : (ps ? resident_groups<ShallowPlan, 1, true>(err)
+                                             : resident_groups<ShallowPlan, 1, false>(err)));
   if (resident < 1) return GNS_ERR_CUDA;
   const int groups = std::min(tiles, resident);
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
-  // the kernel waits (grid_dep_wait) for the kernel ahead of it before it touches global memory
+  // PS instances wait (grid_dep_wait) for the kernel ahead of them before they touch global
+  // memory: only they are programmatic dependent launches
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   attr[1].id = cudaLaunchAttributeClusterDimension;
@@ -1479,12 +1501,24 @@ int gemm_launch_tc(const GemmOp* ops, int nops, const uint32_t* dep_masks, int* 
   cfg.blockDim = dim3(NUM_THREADS, 1, 1);
   cfg.dynamicSmemBytes = deep ? DeepPlan::SMEM_BYTES : ShallowPlan::SMEM_BYTES;
   cfg.stream = static_cast<cudaStream_t>(stream);
-  cfg.attrs = attr;
-  cfg.numAttrs = cg == 2 ? 2 : 1;
-  cudaError_t e = cg == 2 ? (deep ? cudaLaunchKernelEx(&cfg, gemm_kernel<DeepPlan, 2>, P)
-                                  : cudaLaunchKernelEx(&cfg, gemm_kernel<ShallowPlan, 2>, P))
-                          : (deep ? cudaLaunchKernelEx(&cfg, gemm_kernel<DeepPlan, 1>, P)
-                                  : cudaLaunchKernelEx(&cfg, gemm_kernel<ShallowPlan, 1>, P));
+  cfg.attrs = ps ? attr : attr + 1;
+  cfg.numAttrs = (ps ? 1 : 0) + (cg == 2 ? 1 : 0);
+  cudaError_t e;
+  if (cg == 2) {
+    if (deep)
+      e = ps ? cudaLaunchKernelEx(&cfg, gemm_kernel<DeepPlan, 2, true>, P)
+             : cudaLaunchKernelEx(&cfg, gemm_kernel<DeepPlan, 2, false>, P);
+    else
+      e = ps ? cudaLaunchKernelEx(&cfg, gemm_kernel<ShallowPlan, 2, true>, P)
+             : cudaLaunchKernelEx(&cfg, gemm_kernel<ShallowPlan, 2, false>, P);
+  } else {
+    if (deep)
+      e = ps ? cudaLaunchKernelEx(&cfg, gemm_kernel<DeepPlan, 1, true>, P)
+             : cudaLaunchKernelEx(&cfg, gemm_kernel<DeepPlan, 1, false>, P);
+    else
+      e = ps ? cudaLaunchKernelEx(&cfg, gemm_kernel<ShallowPlan, 1, true>, P)
+             : cudaLaunchKernelEx(&cfg, gemm_kernel<ShallowPlan, 1, false>, P);
+  }
   if (e != cudaSuccess) {
     *err = std::string("tcgen05 GEMM launch: ") + cudaGetErrorString(e);
     return GNS_ERR_CUDA;
