@@ -175,6 +175,12 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
+def bench_config(world):
+    """The workload both arms name in their line's config."""
+    return {"workload": WORKLOAD, "matrices": COUNT, "rows": ROWS, "cols": COLS,
+            "l2": "inputs larger than L2 (W, G, M: 604 MB per rank)", "parallelism": f"replicas x{world}"}
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return 0
@@ -188,7 +194,7 @@ def run_reference(args, rank, world):
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1000.0 * total / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD},
+            "config": bench_config(world),
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": sample},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -758,8 +764,7 @@ def run_ours(args, rank, world, dist):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "matrices": COUNT, "rows": ROWS, "cols": COLS,
-                   "l2": "inputs larger than L2 (W, G, M: 604 MB per rank)", "parallelism": f"replicas x{world}"},
+        "config": bench_config(world),
         "tflops": tflops, "tflops_frac_of_peak": tflops / peak_burst,
         "e2e": {"value": whole_job_rate(world, COUNT, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": bytes_step,
                 "d2h_bytes_per_step": bytes_step, "ms_per_step": e2e_ms,
