@@ -41,7 +41,9 @@
  *     result is mapped back (Dion3 Algorithm 1 assumes n <= m); no transposed copy is made.
  *   Streams. Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default stream)
  *     and returns without synchronising the host. The enqueued work is kernels and memsets
- *     only, so a call may be recorded by stream capture into a CUDA graph and replayed; make
+ *     only (a GEMM launch that follows the library's own norm pass may be a programmatic
+ *     dependent launch: it starts its setup early and waits on the device for that pass),
+ *     so a call may be recorded by stream capture into a CUDA graph and replayed; make
  *     one call on the device outside capture first (it looks up and caches the device's
  *     launch limits and the driver's tensor-map encoder).
  *   Workspace. Calls that need scratch take a caller-owned device buffer `ws` of at least

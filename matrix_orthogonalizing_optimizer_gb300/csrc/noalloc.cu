@@ -18,8 +18,8 @@
 // every uncaptured call keeps it valid after a cudaDeviceReset, which unloads the module and
 // may place the array elsewhere when it is loaded again. All calls share the array and it keeps
 // whatever the last call left there: the completion counters that must start at zero are
-// reset by every call (a memset on the stream), and every other scratch value is written
-// before it is read. Calls whose executions overlap on the GPU (different streams, or
+// reset by every call (a memset on the stream, or the norm pass enqueued just before the
+// GEMM), and every other scratch value is written before it is read. Calls whose executions overlap on the GPU (different streams, or
 // different host threads) race on the array and give wrong results: serialise them.
 #include <cuda_runtime.h>
 
