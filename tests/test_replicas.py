@@ -70,3 +70,7 @@ def test_reference_arm_under_torchrun_world2():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+    # the same workload description as the GPU arm's line
+    sys.path.insert(0, ROOT)
+    import bench
+    assert d["config"] == bench.bench_config(2)
