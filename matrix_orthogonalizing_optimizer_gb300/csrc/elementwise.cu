@@ -70,16 +70,17 @@ __device__ __forceinline__ __half from_f<__half>(float v) {
 // ---------------------------------------------------------------------------------------
 // sum of squares per matrix (read only), partials[b * npart + part]
 
-// Rows start on 16-byte boundaries (ld and the base are 16-byte aligned), so each thread
-// reads 16-byte vectors of VEC elements; a scalar tail covers cols % VEC.
-// Both kernels below may also zero `nzero` ints at `zero` (the completion counters of the GEMM
-// launch that follows them on the stream), and let that launch begin while they finish.
+// The norm pass (sumsq_kernel, momentum_kernel) may also zero `nzero` ints at `zero` (the
+// completion counters of the GEMM launch that follows it on the stream), and lets that launch
+// begin while it finishes.
 __device__ __forceinline__ void zero_and_release(int* zero, int nzero) {
   grid_dep_launch();
   if (zero && blockIdx.x == 0 && blockIdx.y == 0)
     for (int i = threadIdx.x; i < nzero; i += blockDim.x) zero[i] = 0;
 }
 
+// Rows start on 16-byte boundaries (ld and the base are 16-byte aligned), so each thread
+// reads 16-byte vectors of VEC elements; a scalar tail covers cols % VEC.
 template <typename T>
 __global__ void sumsq_kernel(const T* X, long long ld, long long stride, int rows, int cols, int npart,
                              float* partials, int* zero, int nzero) {

@@ -148,9 +148,8 @@ struct Problem {
   int publish;        // a later problem of the launch depends on this one: publish completions
   int scale_part;     // scale holds SCALE_NPART partial sums per matrix (16-byte aligned), not scales
 };
-// (the parameter block holds up to MAX_PROB of these: kept at 1024 bytes, the size of the
-// seven 64-byte-aligned tensor maps and the fields that fit beside them, as launches of many
-// short tiles measured slower with a larger block)
+// (the parameter block holds up to MAX_PROB of these: the fields fit in the 1024 bytes that
+// the seven 64-byte-aligned tensor maps round the struct up to)
 static_assert(sizeof(Problem) == 1024, "Problem size");
 
 // The launch's tiles form a sequence of segments, each the tiles of problem p for the

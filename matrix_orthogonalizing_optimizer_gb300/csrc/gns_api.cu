@@ -417,8 +417,6 @@ static GemmOp sym_op(const MatRef& A, int a_mn, const MatRef& Bm, int b_mn, int6
   return o;
 }
 
-// Dion3 Algorithm 3 on one group (B matrices, oriented X = n x m). inv: per-matrix
-// 1/(||X||_F + eps) already computed on the stream.
 // The Frobenius-norm scale 1 / (||X_b||_F + eps) of a group's products: the finished array
 // (inv), or the per-matrix partial sums of squares the tensor-core GEMM forms it from (part),
 // in which case the kernel that wrote them also zeroed the GEMM's completion counters.
@@ -444,6 +442,8 @@ static void set_scale(GemmOp* o, const NormScale& sc) {
   }
 }
 
+// Dion3 Algorithm 3 on one group (B matrices, oriented X = n x m). sc: the norm scale of X
+// (user data), already computed on the stream or to be formed by the GEMM.
 static int run_gram(gns_dtype dt, const Src& src, int64_t B, int64_t n, int64_t m, const gns_ns_params* ns,
                     const GramBufs& g, const NormScale& sc, const Final& fin, int32_t* st, void* stream) {
   const float* inv = sc.inv;
