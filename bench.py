@@ -773,8 +773,9 @@ def run_ours(args, rank, world, dist):
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_burst, "unit": "TFLOP/s",
                      "frac": achieved / peak_burst, "traffic": gemm_traffic() if per_step == 1 else None,
                      "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch, captured on "
-                                       f"this kernel source ({gemm_source_hash()}) by bench.py --metric-only; "
-                                       "null when no capture of this source is on record",
+                                       f"this kernel code ({gemm_source_hash()}: the sources' sha256 prefix with "
+                                       "comments removed) by bench.py --metric-only; null when no capture of this "
+                                       "code is on record",
                      "kernel": f"gns::tc::gemm_kernel (tcgen05 bf16 GEMM; {per_step} launch(es) per step carry the 17 products)",
                      "peak_kind": f"dense bf16 burst, {peak_src}",
                      "frac_of_sustained": achieved / peak_sus,
